@@ -1,0 +1,380 @@
+"""Pins the fp64 oracle to things other than itself (CPU only).
+
+Each pin is chosen so that a plausible slip in the oracle fails it:
+  * number formats: torch's float->bf16 rounding, hand-picked ties, a double-rounding trap;
+  * RoPE: complex multiplication by e^{i*angle} (numpy), norm, relative-position invariance;
+  * decode: two 3-token cases worked out in closed form, and special cases that reduce to
+    torch's scaled_dot_product_attention (Shared KV = M_h = I with no positional slice,
+    plain GQA, the key materialised from the page's K_h = V_g M_h);
+  * head->group map, split-T invariance, ragged tails, the paged layout and the
+    cache-size closed form against the figures the pages print.
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+import torch.nn.functional as F
+
+from compact_kv_cache_gva_b300 import synth
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def bf16_bits(x):
+    return torch.tensor(np.asarray(x, dtype=np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def bits_to_f(bits):
+    return torch.tensor(np.asarray(bits, dtype=np.uint16).view(np.int16)).view(torch.bfloat16).float().numpy().astype(np.float64)
+
+
+# ---------------------------------------------------------------- number formats
+
+def test_bf16_encode_matches_torch_on_f32_values(oracle_mod):
+    rng = np.random.default_rng(1)
+    x = np.concatenate([rng.standard_normal(4000), rng.standard_normal(1000) * 1e-30,
+                        rng.standard_normal(1000) * 1e30]).astype(np.float32)
+    want = bf16_bits(x)
+    got = np.array([oracle_mod.double_to_bf16(float(v)) for v in x], dtype=np.uint16)
+    assert np.array_equal(got, want)
+
+
+def test_bf16_ties_and_double_rounding(oracle_mod):
+    # ties go to the even significand
+    assert oracle_mod.double_to_bf16(1.0) == 0x3F80
+    assert oracle_mod.double_to_bf16(1.0 + 2.0 ** -8) == 0x3F80       # tie, even is down
+    assert oracle_mod.double_to_bf16(1.0 + 3 * 2.0 ** -8) == 0x3F82   # tie, even is up
+    assert oracle_mod.double_to_bf16(-(1.0 + 3 * 2.0 ** -8)) == 0xBF82
+    # just above a tie: must round up; a detour through binary32 would land on the tie
+    # (2^-30 is below half a binary32 ulp at 1.0) and round down to even
+    assert oracle_mod.double_to_bf16(1.0 + 2.0 ** -8 + 2.0 ** -30) == 0x3F81
+    assert oracle_mod.double_to_bf16(0.0) == 0x0000
+    assert oracle_mod.double_to_bf16(-0.0) == 0x8000
+    assert oracle_mod.double_to_bf16(1e39) == 0x7F80
+
+
+def test_bf16_decode_matches_torch(oracle_mod):
+    bits = np.arange(0, 65536, 7, dtype=np.uint16)
+    want = bits_to_f(bits)
+    got = np.array([oracle_mod.bf16_to_double(int(b)) for b in bits])
+    finite = np.isfinite(want)
+    assert np.array_equal(got[finite], want[finite])
+    assert np.array_equal(np.isnan(got), np.isnan(want))
+
+
+# ---------------------------------------------------------------- RoPE
+
+@pytest.mark.parametrize("d_r", [2, 16, 24])
+def test_rope_is_complex_rotation(oracle_mod, d_r):
+    rng = np.random.default_rng(d_r)
+    x = rng.standard_normal(d_r)
+    for pos in [0, 1, 7, 4095, 131071]:
+        y = oracle_mod.rope(x, pos)
+        i = np.arange(d_r // 2)
+        ang = pos * 10000.0 ** (-2.0 * i / d_r)
+        z = (x[0::2] + 1j * x[1::2]) * np.exp(1j * ang)
+        assert np.allclose(y[0::2], z.real, atol=1e-12) and np.allclose(y[1::2], z.imag, atol=1e-12)
+
+
+def test_rope_norm_and_relative_position(oracle_mod):
+    rng = np.random.default_rng(3)
+    d_r = 16
+    q, k = rng.standard_normal(d_r), rng.standard_normal(d_r)
+    for p, j, shift in [(5, 2, 11), (1000, 0, 77), (300, 299, 100000)]:
+        base_dot = oracle_mod.rope(q, p) @ oracle_mod.rope(k, j)
+        shifted = oracle_mod.rope(q, p + shift) @ oracle_mod.rope(k, j + shift)
+        assert abs(base_dot - shifted) < 1e-9
+        assert abs(np.linalg.norm(oracle_mod.rope(k, j)) - np.linalg.norm(k)) < 1e-12
+
+
+# ---------------------------------------------------------------- hand cases
+
+def _one_group_pool(vals, krs, dtype=np.float32):
+    """Tiny cache with one block: V rows `vals` [T,d_v], rotated keys `krs` [T,d_r]."""
+    T, d_v = vals.shape
+    d_r = krs.shape[1] if krs is not None else 0
+    vp = np.zeros((1, 1, 64, d_v), dtype=dtype)
+    vp[0, 0, :T] = vals
+    kp = np.zeros((1, 64, max(d_r, 1)), dtype=dtype)[:, :, :d_r].copy()
+    if d_r:
+        kp[0, :T] = krs
+    return vp, kp
+
+
+def test_hand_case_A_no_positional_term(oracle_mod):
+    # H=G=1, d_v=d_n=2, d_r=2, M=I, scale 1/sqrt(4); v_j=(j,0); q_c=(1,0); q_r=0; query at 2
+    vals = np.array([[0, 0], [1, 0], [2, 0]], dtype=np.float64)
+    vp, kp = _one_group_pool(vals, np.zeros((3, 2)))
+    q_abs, q_rot = oracle_mod.absorb(np.array([[[1.0, 0.0]]]), np.zeros((1, 1, 2)), [2], np.eye(2)[None])
+    out = oracle_mod.decode(q_abs, q_rot, vp, kp, np.array([[0]]), [3], G=1, d_n=2)
+    s = np.array([0.0, 0.5, 1.0])
+    p = np.exp(s) / np.exp(s).sum()
+    assert np.allclose(p, [0.186323723226, 0.307195885718, 0.506480391056], atol=1e-12)
+    assert abs(out[0, 0, 0] - (p[1] + 2 * p[2])) < 1e-14 and out[0, 0, 1] == 0.0
+    assert abs(out[0, 0, 0] - 1.320156667830) < 1e-11
+
+
+def test_hand_case_B_positional_term(oracle_mod):
+    # as A, plus q_r=(1,0) and every raw k_r=(1,0) written at its own position by append;
+    # with theta_0 = 1 the positional term of key j is cos(2 - j)
+    d_v, d_r = 2, 2
+    vals = np.array([[[0, 0]], [[1, 0]], [[2, 0]]], dtype=np.float32)[None]  # [1,3,1,2]
+    kr_raw = np.tile(np.array([1.0, 0.0], dtype=np.float32), (1, 3, 1))
+    vp = np.zeros((1, 1, 64, d_v), dtype=np.float32)
+    kp = np.zeros((1, 64, d_r), dtype=np.float32)
+    oracle_mod.append(vals, kr_raw, [0], np.array([[0]]), vp, kp)
+    q_abs, q_rot = oracle_mod.absorb(np.array([[[1.0, 0.0]]]), np.array([[[1.0, 0.0]]]), [2], np.eye(2)[None])
+    out = oracle_mod.decode(q_abs, q_rot, vp, kp, np.array([[0]]), [3], G=1, d_n=2)
+    s = 0.5 * (np.array([0.0, 1.0, 2.0]) + np.cos(2.0 - np.arange(3)))
+    assert np.allclose(s, [-0.208073418274, 0.770151152934, 1.5], atol=1e-12)
+    p = np.exp(s) / np.exp(s).sum()
+    assert np.allclose(p, [0.108955610521, 0.289792493605, 0.601251895873], atol=1e-9)
+    # keys were rotated to positions 0,1,2 and rounded to f32 in the cache
+    assert abs(out[0, 0, 0] - (p[1] + 2 * p[2])) < 1e-7
+    assert abs(out[0, 0, 0] - 1.492296285352) < 1e-7
+
+
+# ---------------------------------------------------------------- special cases vs library
+
+def _sdpa(q, k, v, scale):
+    """torch fp64 attention of one query row against keys/values [T, d]."""
+    q = torch.tensor(q, dtype=torch.float64)[None, None, None, :]
+    k = torch.tensor(k, dtype=torch.float64)[None, None]
+    v = torch.tensor(v, dtype=torch.float64)[None, None]
+    return F.scaled_dot_product_attention(q, k, v, scale=scale)[0, 0, 0].numpy()
+
+
+def _rand_cache(w, seed=0, lens=None):
+    inp = synth.decode_inputs(w, seed=seed, lens=lens)
+    return inp, synth.pool_bits(inp.v_pool), synth.pool_bits(inp.kr_pool)
+
+
+def _gather_rows(pool_np, table, b, T, g=None):
+    """Rows 0..T-1 of sequence b, read through the block table with numpy fancy indexing."""
+    j = np.arange(T)
+    blk = table[b, j // 64]
+    if g is None:
+        rows = pool_np[blk, j % 64]
+    else:
+        rows = pool_np[blk, g, j % 64]
+    if rows.dtype == np.uint16:
+        rows = bits_to_f(rows.reshape(-1)).reshape(rows.shape)
+    return rows.astype(np.float64)
+
+
+def test_shared_kv_special_case_is_plain_attention(oracle_mod):
+    # Shared KV (K = V): M_h = I and no positional slice -> textbook attention over V
+    w = synth.custom(dtype="bf16", B=2, H=4, G=2, d_v=32, d_r=0, T=200)
+    inp, vp, kp = _rand_cache(w)
+    table = inp.block_table.numpy()
+    q_c = inp.q_abs.double().numpy()
+    q_abs, q_rot = oracle_mod.absorb(q_c, np.zeros((2, 4, 0)), [199, 199], np.tile(np.eye(32), (4, 1, 1)))
+    out = oracle_mod.decode(q_abs, q_rot, vp, kp, table, inp.seq_lens.numpy(), G=2)
+    for b in range(2):
+        for h in range(4):
+            V = _gather_rows(vp, table, b, 200, g=h // 2)
+            ref = _sdpa(q_c[b, h], V, V, 1 / math.sqrt(32))
+            assert np.abs(out[b, h] - ref).max() < 1e-12
+
+
+def test_head_to_group_map_and_positional_term(oracle_mod):
+    # full decode vs attention over explicit keys [q'.v + q_r.k_r] built per head from group h // r
+    w = synth.custom(dtype="bf16", B=2, H=8, G=2, d_v=32, d_r=16, T=130)
+    inp, vp, kp = _rand_cache(w, seed=4)
+    table = inp.block_table.numpy()
+    qa, qr = inp.q_abs.double().numpy(), inp.q_rot.double().numpy()
+    out = oracle_mod.decode(qa, qr, vp, kp, table, inp.seq_lens.numpy(), G=2)
+    scale = 1 / math.sqrt(32 + 16)
+    for b in range(2):
+        KR = _gather_rows(kp, table, b, 130)
+        for h in range(8):
+            V = _gather_rows(vp, table, b, 130, g=h // 4)
+            ref = _sdpa(np.concatenate([qa[b, h], qr[b, h]]), np.concatenate([V, KR], 1), V, scale)
+            assert np.abs(out[b, h] - ref).max() < 1e-12
+    # a wrong map (h mod G) gives a different answer on this input
+    V_wrong = _gather_rows(vp, table, 0, 130, g=1 % 2)
+    KR = _gather_rows(kp, table, 0, 130)
+    wrong = _sdpa(np.concatenate([qa[0, 1], qr[0, 1]]), np.concatenate([V_wrong, KR], 1), V_wrong, scale)
+    assert np.abs(out[0, 1] - wrong).max() > 1e-3
+
+
+def test_absorbed_equals_unabsorbed_and_materialised_key(oracle_mod):
+    w = synth.custom(dtype="bf16", B=2, H=4, G=2, d_v=16, d_n=24, d_r=8, T=70)
+    lens = synth.seq_lens(w)
+    table, nb = synth.block_table(w, lens)
+    raw = synth.raw_inputs(w, lens, n_new=70, seed=5, pos_new=[0, 0])
+    vp = np.zeros((nb, 2, 64, 16), dtype=np.uint16)
+    kp = np.zeros((nb, 64, 8), dtype=np.uint16)
+    oracle_mod.append(synth.pool_bits(raw.v_new), synth.pool_bits(raw.kr_new), raw.pos_new.numpy(),
+                      table.numpy(), vp, kp)
+    q_c, q_r, M = raw.q_c.double().numpy(), raw.q_r.double().numpy(), raw.M.double().numpy()
+    pos_q = raw.pos_q.numpy()
+    qa, qr = oracle_mod.absorb(q_c, q_r, pos_q, M)
+    absorbed = oracle_mod.decode(qa, qr, vp, kp, table.numpy(), lens.numpy(), G=2, d_n=24)
+    unabsorbed = oracle_mod.decode_unabsorbed(q_c, q_r, pos_q, M, vp, kp, table.numpy(), lens.numpy(), G=2)
+    assert np.abs(absorbed - unabsorbed).max() < 1e-12
+    # library check of the page's formula: K_h = V_g M_h (row form), full key [K_h ; k~_r]
+    scale = 1 / math.sqrt(24 + 8)
+    for b in range(2):
+        KR = _gather_rows(kp, table.numpy(), b, 70)
+        for h in range(4):
+            V = _gather_rows(vp, table.numpy(), b, 70, g=h // 2)
+            K = V @ M[h]
+            qrot = oracle_mod.rope(q_r[b, h], pos_q[b])
+            ref = _sdpa(np.concatenate([q_c[b, h], qrot]), np.concatenate([K, KR], 1), V, scale)
+            assert np.abs(absorbed[b, h] - ref).max() < 1e-12
+    # and the transposed map (q' = M^T q_c) is detectably wrong
+    qa_t = np.einsum("hki,bhk->bhi", M.transpose(0, 2, 1), q_c) if M.shape[1] == M.shape[2] else None
+    assert qa_t is None or np.abs(qa_t - qa).max() > 1e-3
+
+
+def test_single_token_zero_query_and_constant_values(oracle_mod):
+    w = synth.custom(dtype="f32", B=1, H=2, G=1, d_v=8, d_r=4, T=100)
+    inp, vp, kp = _rand_cache(w, seed=6)
+    table = inp.block_table.numpy()
+    qa, qr = inp.q_abs.double().numpy(), inp.q_rot.double().numpy()
+    # T = 1 -> o = v_0 exactly
+    out = oracle_mod.decode(qa, qr, vp, kp, table, [1], G=1)
+    assert np.array_equal(out[0, 0], vp[table[0, 0], 0, 0].astype(np.float64))
+    # zero query -> uniform weights -> mean of the value rows
+    out = oracle_mod.decode(np.zeros_like(qa), np.zeros_like(qr), vp, kp, table, [100], G=1)
+    V = _gather_rows(vp, table, 0, 100, g=0)
+    assert np.abs(out[0, 1] - V.mean(0)).max() < 1e-13
+    # all value rows equal -> output is that row whatever the weights
+    vc = vp.copy()
+    vc[:] = np.float32(0.375)
+    out = oracle_mod.decode(qa, qr, vc, kp, table, [100], G=1)
+    assert np.abs(out - 0.375).max() < 1e-14
+
+
+def test_split_invariance(oracle_mod):
+    w = synth.custom(dtype="bf16", B=2, H=4, G=2, d_v=32, d_r=16, T=0, T_range=(70, 300))
+    inp, vp, kp = _rand_cache(w, seed=7)
+    table = inp.block_table.numpy()
+    lens = inp.seq_lens.numpy()
+    qa, qr = inp.q_abs.double().numpy(), inp.q_rot.double().numpy()
+    for b in range(2):
+        for h in range(4):
+            ref = oracle_mod.decode_one(qa, qr, vp, kp, table, lens, G=2, b=b, h=h)
+            for S in [1, 2, 3, 7, int(lens[b])]:
+                got = oracle_mod.decode_split(qa, qr, vp, kp, table, lens, G=2, b=b, h=h, S=S)
+                assert np.abs(got - ref).max() < 1e-12
+
+
+def test_ragged_tail_ignores_slots_past_length(oracle_mod):
+    w = synth.custom(dtype="bf16", B=1, H=2, G=1, d_v=16, d_r=8, T=77)
+    inp, vp, kp = _rand_cache(w, seed=8)
+    table = inp.block_table.numpy()
+    qa, qr = inp.q_abs.double().numpy(), inp.q_rot.double().numpy()
+    ref = oracle_mod.decode(qa, qr, vp, kp, table, [77], G=1)
+    vp2, kp2 = vp.copy(), kp.copy()
+    last = table[0, 1]
+    vp2[last, :, 77 - 64:] = 0x7FC0  # NaN in every slot past the end
+    kp2[last, 77 - 64:] = 0x7FC0
+    got = oracle_mod.decode(qa, qr, vp2, kp2, table, [77], G=1)
+    assert np.array_equal(got, ref)
+
+
+def test_gqa_oracle_is_plain_attention(oracle_mod):
+    w = synth.custom(dtype="bf16", B=2, H=4, G=2, d_v=32, d_r=0, T=150)
+    inp = synth.decode_inputs(w, seed=9, k_pool=True)
+    table = inp.block_table.numpy()
+    kp, vp = synth.pool_bits(inp.extra["k_pool"]), synth.pool_bits(inp.v_pool)
+    q = inp.extra["q"].double().numpy()
+    for b in range(2):
+        for h in range(4):
+            got = oracle_mod.gqa_decode_one(q, kp, vp, table, inp.seq_lens.numpy(), G=2, b=b, h=h)
+            K = _gather_rows(kp, table, b, 150, g=h // 2)
+            V = _gather_rows(vp, table, b, 150, g=h // 2)
+            assert np.abs(got - _sdpa(q[b, h], K, V, 1 / math.sqrt(32))).max() < 1e-12
+
+
+# ---------------------------------------------------------------- paged layout and append
+
+def test_layout_offsets_by_hand(oracle_mod):
+    # G=4, d_v=64: block 2, group 3, slot 6, element 5 -> ((2*4+3)*64+6)*64+5
+    assert oracle_mod.v_offset(4, 64, 2, 3, 6, 5) == ((2 * 4 + 3) * 64 + 6) * 64 + 5 == 45445
+    assert oracle_mod.kr_offset(16, 2, 6, 5) == (2 * 64 + 6) * 16 + 5 == 2149
+
+
+def test_append_is_a_bijection_onto_used_slots(oracle_mod):
+    w = synth.custom(dtype="bf16", B=3, H=4, G=2, d_v=16, d_r=8, T=0, T_range=(10, 200), shuffled=True)
+    lens = synth.seq_lens(w, seed_lens=3)
+    table, nb = synth.block_table(w, lens, seed_lens=3, spare_blocks=2)
+    n = int(lens.max())
+    raw = synth.raw_inputs(w, lens, n_new=n, seed=10, pos_new=[0, 0, 0])
+    sentinel = np.uint16(0xFFFF)  # a NaN pattern that no finite value takes
+    vp = np.full((nb, 2, 64, 16), sentinel, dtype=np.uint16)
+    kp = np.full((nb, 64, 8), sentinel, dtype=np.uint16)
+    # per-sequence appends of exactly T_b tokens
+    for b in range(3):
+        T = int(lens[b])
+        st = oracle_mod.append(synth.pool_bits(raw.v_new[b:b + 1, :T]), synth.pool_bits(raw.kr_new[b:b + 1, :T]),
+                               [0], table[b:b + 1].numpy(), vp, kp)
+        assert st == 0
+    written = (vp != sentinel).reshape(nb, 2, 64, 16).all(axis=(1, 3))
+    untouched = (vp == sentinel).reshape(nb, 2, 64, 16).all(axis=(1, 3))
+    assert np.array_equal(written, ~untouched)   # slots are written whole or not at all
+    assert written.sum() == int(lens.sum())     # one slot per token
+    tb = table.numpy()
+    for b in range(3):
+        for p in [0, int(lens[b]) - 1, int(lens[b]) // 2]:
+            blk, o = tb[b, p // 64], p % 64
+            assert written[blk, o]
+            assert np.array_equal(vp[blk, :, o], synth.pool_bits(raw.v_new[b, p]))  # bit copy
+            want = oracle_mod.rope(bits_to_f(synth.pool_bits(raw.kr_new[b, p])), p)
+            assert np.array_equal(kp[blk, o], np.array([oracle_mod.double_to_bf16(x) for x in want], np.uint16))
+    # spare blocks stay untouched
+    used = set(tb[tb >= 0].tolist())
+    for blk in range(nb):
+        if blk not in used:
+            assert untouched[blk].all()
+
+
+def test_append_rejects_positions_beyond_table(oracle_mod):
+    w = synth.custom(dtype="f32", B=1, H=2, G=1, d_v=8, d_r=4, T=64)
+    vp = np.zeros((1, 1, 64, 8), np.float32)
+    kp = np.zeros((1, 64, 4), np.float32)
+    st = oracle_mod.append(np.ones((1, 1, 1, 8), np.float32), np.ones((1, 1, 4), np.float32), [64],
+                           np.array([[0]]), vp, kp, raise_on_index=False)
+    assert st == 5 and not vp.any() and not kp.any()
+    st = oracle_mod.append(np.ones((1, 1, 1, 8), np.float32), np.ones((1, 1, 4), np.float32), [3],
+                           np.array([[7]]), vp, kp, raise_on_index=False)  # block id beyond the pool
+    assert st == 5 and not vp.any()
+
+
+def _golden_savings():
+    rows = []
+    with open(os.path.join(GOLDEN, "cache_saving.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                d_r, save, remain, exact = line.split()
+                rows.append((int(d_r), int(save), int(remain), exact == "yes"))
+    return rows
+
+
+def test_cache_ratio_closed_form_matches_pages(oracle_mod):
+    G, d_v = 4, 64
+    for d_r, save, remain, exact in _golden_savings():
+        ratio = oracle_mod.cache_ratio(G, d_v, d_r)
+        assert ratio == (G * d_v + d_r) / (2 * G * d_v)
+        if exact:
+            assert ratio == 0.5
+        assert round(100 * (1 - ratio)) == save and round(100 * ratio) == remain
+    assert oracle_mod.cache_ratio(2, 32, 16) == 0.625
+    assert oracle_mod.cache_ratio(8, 128, 24) == 0.51171875
+
+
+def test_cache_ratio_equals_counted_pool_scalars(oracle_mod):
+    # count the scalars one appended token occupies in the oracle's pools vs a K+V cache
+    for G, d_v, d_r in [(4, 64, 16), (4, 64, 24), (8, 128, 24)]:
+        vp = np.full((1, G, 64, d_v), 0xFFFF, np.uint16)
+        kp = np.full((1, 64, d_r), 0xFFFF, np.uint16)
+        oracle_mod.append(np.zeros((1, 1, G, d_v), np.uint16), np.zeros((1, 1, d_r), np.uint16), [5],
+                          np.array([[0]]), vp, kp)
+        used = int((vp != 0xFFFF).sum() + (kp != 0xFFFF).sum())
+        gqa = 2 * G * d_v  # key and value rows for each of the G groups
+        assert used / gqa == oracle_mod.cache_ratio(G, d_v, d_r)
