@@ -1,0 +1,461 @@
+"""Benchmark of the GVA decode hot path on B300: one step = absorb + append + decode.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 4] [--path auto|fma|mma]
+    python bench.py --impl reference ...     # the fp64 CPU oracle on a bounded sample
+
+Prints ONE JSON line (rank 0).  `value` is the cache bytes the step's decode attention must
+read (algorithmic: sum_b T_b * (G*d_v + d_r) * elem bytes) divided by the device time of the
+whole step, with every input resident in HBM.  `e2e` is the same metric through the same
+C-ABI calls when each step's inputs start in pinned host memory and its output returns to
+the host.  `roofline` is for the decode attention call (split-T partial kernel + combine).
+Under torchrun every rank runs its own replica of the workload (sequences are independent;
+no collective on the data path) and the line reports the total over ranks (weak scaling).
+"""
+import argparse
+import json
+import math
+import os
+import sys
+import threading
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from compact_kv_cache_gva_b300 import gva, synth  # noqa: E402
+from compact_kv_cache_gva_b300.layer import GVADecodeLayer  # noqa: E402
+
+METRIC = "GVA decode-attention cache-read GB/s (% of B300 HBM peak) and context tokens/s"
+L2_BYTES = 126 * 1024 * 1024
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+NVML_REASONS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap", 0x8: "hw_slowdown",
+                0x10: "sync_boost", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+                0x80: "hw_power_brake_slowdown", 0x100: "display_clock_setting"}
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=2000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--workload", type=int, default=4, choices=sorted(synth.WORKLOADS))
+    p.add_argument("--path", default="auto", choices=["auto", "fma", "mma"])
+    p.add_argument("--split-tokens", type=int, default=0)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-gqa", action="store_true")
+    p.add_argument("--e2e-steps", type=int, default=200)
+    p.add_argument("--cpu-sample-seqs", type=int, default=0, help="sequences in the CPU sample (0 = auto)")
+    return p.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ----------------------------------------------------------------------------- distributed
+
+def dist_setup(n):
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    if ws > 1:
+        import torch.distributed as dist
+        rank = int(os.environ["RANK"])
+        local = int(os.environ.get("LOCAL_RANK", rank))
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend=backend)
+        return rank, ws
+    return 0, 1
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, ws):
+    """Largest value of x over ranks (timing is the slowest rank's)."""
+    if ws == 1:
+        return float(x)
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64,
+                     device="cuda" if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job(per_rank_units, ws, seconds):
+    """Units processed by all ranks per second of the slowest rank (weak scaling)."""
+    return per_rank_units * ws / seconds
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """Samples SM clock and clock-event reasons through NVML while the timed region runs."""
+
+    def __init__(self, period_s=0.01):
+        self.period = period_s
+        self.samples = []
+        self.max_mhz = None
+        self.ok = False
+        self._stop = threading.Event()
+        try:
+            import pynvml
+            pynvml.nvmlInit()
+            self.nv = pynvml
+            h = None
+            try:
+                uuid = str(torch.cuda.get_device_properties(torch.cuda.current_device()).uuid)
+                h = pynvml.nvmlDeviceGetHandleByUUID(("GPU-" + uuid) if not uuid.startswith("GPU-") else uuid)
+            except Exception:
+                h = pynvml.nvmlDeviceGetHandleByIndex(torch.cuda.current_device())
+            self.h = h
+            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(h, pynvml.NVML_CLOCK_SM)
+            self.ok = True
+        except Exception as e:  # no NVML: report that instead of guessing
+            self.err = repr(e)
+
+    def _run(self):
+        nv = self.nv
+        while not self._stop.is_set():
+            try:
+                sm = nv.nvmlDeviceGetClockInfo(self.h, nv.NVML_CLOCK_SM)
+                try:
+                    reasons = nv.nvmlDeviceGetCurrentClocksEventReasons(self.h)
+                except Exception:
+                    reasons = nv.nvmlDeviceGetCurrentClocksThrottleReasons(self.h)
+                self.samples.append((sm, int(reasons)))
+            except Exception:
+                pass
+            time.sleep(self.period)
+
+    def __enter__(self):
+        if self.ok:
+            self.t = threading.Thread(target=self._run, daemon=True)
+            self.t.start()
+        return self
+
+    def __exit__(self, *a):
+        if self.ok:
+            self._stop.set()
+            self.t.join()
+
+    def summary(self):
+        if not self.ok:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "note": "NVML unavailable"}
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": [], "samples": 0}
+        mhz = sorted(s for s, _ in self.samples)
+        bits = 0
+        for _, r in self.samples:
+            bits |= r
+        names = [n for b, n in NVML_REASONS.items() if bits & b and n != "gpu_idle"]
+        return {"sm_mhz": mhz[len(mhz) // 2], "sm_max_mhz": self.max_mhz, "reasons": names,
+                "samples": len(self.samples)}
+
+
+# ----------------------------------------------------------------------------- workload
+
+class Setup:
+    """A resident workload: cache, block table, lengths, step inputs, layer buffers."""
+
+    def __init__(self, w, seed, path, split_tokens, device="cuda"):
+        self.w = w
+        self.inp = synth.decode_inputs(w, seed=seed, device=device)
+        self.lens_cpu = self.inp.seq_lens.cpu()
+        # the step appends the current token at T_b - 1 and attends 0..T_b-1 (the token itself
+        # included), so every step has the same work
+        self.raw = synth.raw_inputs(w, self.lens_cpu, n_new=1, seed=seed + 1000, device=device)
+        self.layer = GVADecodeLayer(w.H, w.G, w.d_v, w.d_n, w.d_r, w.dtype, w.B, w.max_seq_len, device=device,
+                                    split_tokens=split_tokens,
+                                    path={"auto": gva.GVA_PATH_AUTO, "fma": gva.GVA_PATH_FMA,
+                                          "mma": gva.GVA_PATH_MMA}[path])
+        self.sum_T = int(self.lens_cpu.sum())
+        self.bytes_per_token = (w.G * w.d_v + w.d_r) * w.elem_bytes
+        self.cache_bytes = self.sum_T * self.bytes_per_token
+        # algorithmic bytes of the decode call: cache + queries + output + lengths + table rows used
+        used_blocks = int(((self.lens_cpu + 63) // 64).sum())
+        self.decode_bytes = (self.cache_bytes + w.B * w.H * (w.d_v + w.d_r) * 4 + w.B * w.H * w.d_v * 4 +
+                             w.B * 4 + used_blocks * 4)
+        self.decode_flops = self.sum_T * w.H * (2 * (w.d_v + w.d_r) + 2 * w.d_v)
+
+    def step(self, stream=None):
+        r, i = self.raw, self.inp
+        return self.layer.step(r.q_c, r.q_r, r.pos_q, r.M, r.v_new, r.kr_new, r.pos_new, i.block_table,
+                               i.seq_lens, i.v_pool, i.kr_pool, stream)
+
+    def timed_step(self, ev):
+        """Same step with events between the three calls: (start, after absorb, after append, end)."""
+        r, i, L = self.raw, self.inp, self.layer
+        ev[0].record()
+        L.absorb(r.q_c, r.q_r, r.pos_q, r.M)
+        ev[1].record()
+        L.append(r.v_new, r.kr_new, r.pos_new, i.block_table, i.v_pool, i.kr_pool)
+        ev[2].record()
+        L.attend(i.v_pool, i.kr_pool, i.block_table, i.seq_lens)
+        ev[3].record()
+
+
+def flusher():
+    buf = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device="cuda")
+
+    def flush():
+        buf.fill_(1.0)
+    return flush
+
+
+def run_ours(args, rank, ws):
+    torch.cuda.init()
+    w = synth.WORKLOADS[args.workload]
+    S = Setup(w, seed=rank, path=args.path, split_tokens=args.split_tokens)
+    need_flush = S.cache_bytes < 2 * L2_BYTES
+    flush = flusher() if need_flush else None
+    stream = torch.cuda.current_stream()
+
+    for _ in range(max(3, args.warmup)):
+        if flush:
+            flush()
+        S.step()
+    torch.cuda.synchronize()
+    if S.layer.device_error():
+        raise RuntimeError("device reported an index error during warm-up")
+
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    barrier(ws)
+    torch.cuda.synchronize()
+    with ClockSampler() as clocks:
+        for k in range(K):
+            if flush:
+                flush()
+            S.timed_step(evs[k])
+        torch.cuda.synchronize()
+    barrier(ws)
+    step_ms = [e[0].elapsed_time(e[3]) for e in evs]
+    dec_ms = [e[2].elapsed_time(e[3]) for e in evs]
+    absorb_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    append_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    total_s = max_over_ranks(sum(step_ms) / 1e3, ws)
+    dec_s = max_over_ranks(sum(dec_ms) / 1e3, ws)
+    ms_per_step = total_s * 1e3 / K
+    value = whole_job(S.cache_bytes * K, ws, total_s) / 1e9
+    tokens_per_s = whole_job(S.sum_T * K, ws, total_s)
+    pk, pk_kind = peaks()
+    dec_us = dec_s * 1e6 / K
+    achieved = S.decode_bytes / (dec_s / K) / 1e9
+    hbm_peak = pk["hbm_gbs"]
+
+    out = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws, "steps": K,
+        "warmup": max(3, args.warmup), "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+        "config": dict(w.describe(), step="absorb+append+decode", decode_path=args.path,
+                       split_plan=dict(zip(("split_tokens", "max_splits"), S.layer.plan())),
+                       l2="flushed between steps (256 MB write)" if need_flush else
+                       f"inputs larger than L2 ({S.cache_bytes / 1e6:.0f} MB cache)",
+                       parallelism=f"replicas x{ws}" if ws > 1 else "single GPU"),
+        "pct_of_hbm_peak": round(100 * value / ws / hbm_peak, 2),
+        "context_tokens_per_s": round(tokens_per_s, 1),
+        "decode_steps_per_s": round(K * ws / total_s, 2),
+        "breakdown_us": {"absorb": round(1e3 * sum(absorb_ms) / K, 3), "append": round(1e3 * sum(append_ms) / K, 3),
+                         "decode": round(1e3 * sum(dec_ms) / K, 3)},
+        "roofline": {"kernel": "gva_decode_attention (split-T partial + combine)", "bound": "hbm",
+                     "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
+                     "frac": round(achieved / hbm_peak, 4), "peak_kind": f"{pk_kind} copy bandwidth",
+                     "algorithmic_bytes_per_launch": S.decode_bytes, "decode_us": round(dec_us, 3),
+                     "traffic": None},
+        "gpu_launches": 4 * K,
+        "clocks": clocks.summary(),
+    }
+    if rank == 0 and ws == 1:
+        out["e2e"] = run_e2e(S, args.e2e_steps, flush)
+    if not args.no_gqa and rank == 0:
+        out["gqa_same_build"] = run_gqa(S, flush, min(K, 500))
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(S, args)
+    return out
+
+
+def run_e2e(S, steps, flush):
+    """Same step, with the step's inputs copied from pinned host memory and the output read back."""
+    r = S.raw
+    host_in = {k: getattr(r, k).cpu().pin_memory() for k in ("q_c", "q_r", "pos_q", "v_new", "kr_new", "pos_new")}
+    dev_in = {k: torch.empty_like(getattr(r, k)) for k in host_in}
+    host_out = torch.empty(S.layer.out.shape, dtype=torch.float32).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = host_out.numel() * 4
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for k in range(steps + 3):
+        if flush:
+            flush()
+        e = ev[k - 3] if k >= 3 else None
+        if e:
+            e[0].record()
+        for name, t in host_in.items():
+            dev_in[name].copy_(t, non_blocking=True)
+        S.layer.step(dev_in["q_c"], dev_in["q_r"], dev_in["pos_q"], r.M, dev_in["v_new"], dev_in["kr_new"],
+                     dev_in["pos_new"], S.inp.block_table, S.inp.seq_lens, S.inp.v_pool, S.inp.kr_pool)
+        host_out.copy_(S.layer.out, non_blocking=True)
+        if e:
+            e[1].record()
+    torch.cuda.synchronize()
+    t = sum(a.elapsed_time(b) for a, b in ev) / 1e3
+    return {"value": round(S.cache_bytes * steps / t / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": round(1e3 * t / steps, 5)}
+
+
+def run_gqa(S, flush, steps):
+    """The same-build GQA decode on a matching K+V cache (same B, T, G, head width), timed alike."""
+    w = S.w
+    wg = synth.custom(name=w.name + "-gqa", dtype=w.dtype, B=w.B, H=w.H, G=w.G, d_v=w.d_v, d_r=0,
+                      T=w.T, T_range=w.T_range, shuffled=w.shuffled)
+    inp = synth.decode_inputs(wg, seed=1, device="cuda", k_pool=True)
+    ctx = gva.gva_create(w.H, w.G, w.d_v, w.d_v, 0, w.dtype)
+    out = torch.empty((w.B, w.H, w.d_v), device="cuda")
+    wsb = torch.empty(gva.gva_decode_workspace_size(ctx, w.B, w.max_seq_len), dtype=torch.uint8, device="cuda")
+    gqa_bytes = int(inp.seq_lens.sum()) * 2 * w.G * w.d_v * w.elem_bytes
+
+    def call():
+        gva.gqa_decode_attention(ctx, inp.extra["q"], inp.extra["k_pool"], inp.v_pool, inp.block_table, inp.seq_lens,
+                                 w.max_seq_len, out, wsb)
+    for _ in range(5):
+        call()
+    need_flush = gqa_bytes < 2 * L2_BYTES
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for k in range(steps):
+        if need_flush and flush:
+            flush()
+        ev[k][0].record()
+        call()
+        ev[k][1].record()
+    torch.cuda.synchronize()
+    t = sum(a.elapsed_time(b) for a, b in ev) / 1e3 / steps
+    del inp
+    return {"decode_us": round(t * 1e6, 3), "cache_bytes": gqa_bytes, "GBps": round(gqa_bytes / t / 1e9, 1)}
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+
+def cpu_sample(S, nseq):
+    """Host copy of the first nseq sequences (their blocks, identity table) + the step's raw inputs."""
+    w, inp = S.w, S.inp
+    seqs = []
+    for b in range(nseq):
+        T = int(S.lens_cpu[b])
+        nblk = (T + 63) // 64
+        ids = inp.block_table[b, :nblk].long()
+        seqs.append((b, T, synth.pool_bits(inp.v_pool.index_select(0, ids)),
+                     synth.pool_bits(inp.kr_pool.index_select(0, ids))))
+    raw = {k: getattr(S.raw, k).cpu() for k in ("q_c", "q_r", "pos_q", "M", "v_new", "kr_new", "pos_new")}
+    return seqs, raw
+
+
+def oracle_step(w, seqs, raw):
+    """One oracle step on the sample: absorb + append + decode of every head of each sequence.
+    Returns (seconds, cache bytes read)."""
+    import numpy as np
+    import oracle
+    t0 = time.perf_counter()
+    nbytes = 0
+    for b, T, vp, kp in seqs:
+        vp = vp.copy()
+        kp = kp.copy()
+        table = np.arange(vp.shape[0], dtype=np.int32)[None]
+        qa, qr = oracle.absorb(raw["q_c"][b:b + 1].double().numpy(), raw["q_r"][b:b + 1].double().numpy(),
+                               raw["pos_q"][b:b + 1].numpy(), raw["M"].double().numpy())
+        oracle.append(synth.pool_bits(raw["v_new"][b:b + 1]), synth.pool_bits(raw["kr_new"][b:b + 1]),
+                      raw["pos_new"][b:b + 1].numpy(), table, vp, kp)
+        oracle.decode(qa, qr, vp, kp, table, np.array([T], np.int32), G=w.G, d_n=w.d_n)
+        nbytes += T * (w.G * w.d_v + w.d_r) * w.elem_bytes
+    return time.perf_counter() - t0, nbytes
+
+
+def auto_sample_seqs(S):
+    # about 1.5e9 multiply-adds of fp64 oracle work: seconds of CPU time on the host cores
+    w = S.w
+    per_token = w.H * (2 * w.d_v + w.d_r)
+    budget = 1.5e9
+    n, acc = 0, 0
+    for b in range(w.B):
+        acc += int(S.lens_cpu[b]) * per_token
+        n += 1
+        if acc >= budget:
+            break
+    return n
+
+
+def cpu_baseline(S, args):
+    import oracle
+    nseq = args.cpu_sample_seqs or auto_sample_seqs(S)
+    seqs, raw = cpu_sample(S, nseq)
+    threads = oracle.get_threads()
+    secs, nbytes = oracle_step(S.w, seqs, raw)
+    toks = sum(T for _, T, _, _ in seqs)
+    return {"value": round(nbytes / secs / 1e9, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": f"one step (absorb+append+decode, all {S.w.H} heads) of the first {nseq} sequence(s) "
+                      f"of the workload, {toks} context tokens, {secs:.2f} s wall",
+            "context_tokens_per_s": round(toks / secs, 1)}
+
+
+def run_reference(args, rank, ws):
+    """The oracle as the reference arm: K timed steps of a bounded sample on the host cores."""
+    import oracle
+    w = synth.WORKLOADS[args.workload]
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    S = Setup.__new__(Setup)
+    S.w = w
+    S.inp = synth.decode_inputs(w, seed=0, device=dev)
+    S.lens_cpu = S.inp.seq_lens.cpu()
+    S.raw = synth.raw_inputs(w, S.lens_cpu, n_new=1, seed=1000, device=dev)
+    nseq = 1
+    seqs, raw = cpu_sample(S, nseq)
+    for _ in range(args.warmup):
+        oracle_step(w, seqs, raw)
+    t, nbytes = 0.0, 0
+    for _ in range(args.steps):
+        dt, nb = oracle_step(w, seqs, raw)
+        t += dt
+        nbytes += nb
+    value = nbytes / t / 1e9
+    threads = oracle.get_threads()
+    sample = (f"per step: absorb+append+decode of all {w.H} heads of sequence 0 "
+              f"({int(S.lens_cpu[0])} context tokens) of the workload")
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * t / args.steps, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": w.describe(),
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse()
+    rank, ws = dist_setup(args.gpus)
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args, rank, ws)), flush=True)
+        return
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device (no CPU fallback)")
+    out = run_ours(args, rank, ws)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

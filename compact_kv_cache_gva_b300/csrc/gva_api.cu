@@ -1,0 +1,274 @@
+// gva_api.cu -- the C ABI (include/gva.h): argument checks, the split-T plan and launches.
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+
+#include "gva_internal.h"
+
+namespace {
+
+constexpr int kVersion = 100;  // 0.1.0
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool on_ctx_device(const gva_ctx* ctx) {
+  int dev = -1;
+  return cudaGetDevice(&dev) == cudaSuccess && dev == ctx->device;
+}
+
+int elem_bytes(gva_dtype t) { return t == GVA_F32 ? 4 : 2; }
+
+gva_status from_cuda(cudaError_t e) { return e == cudaSuccess ? GVA_OK : GVA_ERR_CUDA; }
+
+// Which decode kernel family runs for these dims.
+int choose_path(const gva_ctx* ctx, bool sep_k) {
+  const bool mma_ok = gva::mma_supported(ctx->dims, sep_k);
+  if (ctx->path == GVA_PATH_MMA) return mma_ok ? GVA_PATH_MMA : -1;
+  if (ctx->path == GVA_PATH_FMA) return gva::fma_supported(ctx->dims, sep_k) ? GVA_PATH_FMA : -1;
+  if (mma_ok) return GVA_PATH_MMA;
+  return gva::fma_supported(ctx->dims, sep_k) ? GVA_PATH_FMA : -1;
+}
+
+// Split-T plan: how many 64-token blocks each partial covers.  Automatic plans aim at about
+// two waves of CTAs over the device when every sequence is at max_seq_len; a chunk is at
+// least one tile per warp of a CTA, and never longer than the longest context.
+bool make_plan(const gva_ctx* ctx, int B, int max_seq_len, bool sep_k, gva::Plan* plan) {
+  const int path = choose_path(ctx, sep_k);
+  if (path < 0) return false;
+  const int nt_max = (max_seq_len + GVA_BLOCK_TOKENS - 1) / GVA_BLOCK_TOKENS;
+  int chunk;
+  if (ctx->split_tokens > 0) {
+    chunk = ctx->split_tokens / GVA_BLOCK_TOKENS;
+  } else {
+    const int quantum = path == GVA_PATH_MMA ? gva::mma_tiles_per_cta_unit(ctx->dims) : 4;
+    const int per_sm = path == GVA_PATH_MMA ? gva::mma_ctas_per_sm(ctx->dims, sep_k)
+                                            : gva::fma_ctas_per_sm(ctx->dims, sep_k);
+    // one CTA per (chunk, value group, sequence)
+    const long long units = static_cast<long long>(B) * ctx->dims.G * nt_max;
+    const long long target = 2LL * ctx->num_sms * per_sm;
+    long long c = (units + target - 1) / target;
+    c = ((c + quantum - 1) / quantum) * quantum;
+    if (c < quantum) c = quantum;
+    chunk = static_cast<int>(c);
+  }
+  if (chunk > nt_max) chunk = nt_max;
+  if (chunk < 1) chunk = 1;
+  plan->path = path;
+  plan->chunk_tiles = chunk;
+  plan->n_chunks = (nt_max + chunk - 1) / chunk;
+  plan->ws_bytes = sizeof(float) * static_cast<size_t>(B) * plan->n_chunks * ctx->dims.H *
+                   gva::partial_stride_floats(ctx->dims.d_v);
+  return true;
+}
+
+gva_status decode_common(gva_ctx* ctx, bool sep_k, int B, const float* q_abs, const float* q_rot,
+                         const void* k_pool, const void* v_pool, const void* kr_pool,
+                         const int32_t* block_table, int max_blocks, int num_blocks,
+                         const int32_t* seq_lens, int max_seq_len, float* out, void* workspace,
+                         size_t ws_bytes, cudaStream_t stream) {
+  if (!ctx || B < 0 || max_seq_len < 1 || max_blocks < 1 || num_blocks < 1)
+    return GVA_ERR_INVALID_ARG;
+  if (B == 0) return GVA_OK;
+  if (B > 65535) return GVA_ERR_UNSUPPORTED;  // sequences are a grid dimension
+  const gva_dims& d = ctx->dims;
+  if (!q_abs || !v_pool || !block_table || !seq_lens || !out) return GVA_ERR_INVALID_ARG;
+  if (sep_k && !k_pool) return GVA_ERR_INVALID_ARG;
+  if (!sep_k && d.d_r > 0 && (!q_rot || !kr_pool)) return GVA_ERR_INVALID_ARG;
+  if (static_cast<long long>(max_blocks) * GVA_BLOCK_TOKENS < max_seq_len) return GVA_ERR_INVALID_ARG;
+  if (!aligned16(q_abs) || !aligned16(v_pool) || !aligned16(out) || (k_pool && !aligned16(k_pool)) ||
+      (kr_pool && !aligned16(kr_pool)) || (q_rot && !aligned16(q_rot)))
+    return GVA_ERR_INVALID_ARG;
+  if (!on_ctx_device(ctx)) return GVA_ERR_INVALID_ARG;
+  gva::Plan plan;
+  if (!make_plan(ctx, B, max_seq_len, sep_k, &plan)) return GVA_ERR_UNSUPPORTED;
+  if (!workspace || ws_bytes < plan.ws_bytes || !aligned16(workspace)) return GVA_ERR_WORKSPACE;
+
+  gva::DecodeArgs a;
+  a.q_abs = q_abs;
+  a.q_rot = sep_k ? nullptr : q_rot;
+  a.v_pool = v_pool;
+  a.k_pool = k_pool;
+  a.kr_pool = sep_k ? nullptr : kr_pool;
+  a.block_table = block_table;
+  a.seq_lens = seq_lens;
+  a.out = out;
+  a.part = static_cast<float*>(workspace);
+  a.err = ctx->d_err;
+  a.B = B;
+  a.H = d.H;
+  a.G = d.G;
+  a.d_v = d.d_v;
+  a.d_r = sep_k ? 0 : d.d_r;
+  a.max_blocks = max_blocks;
+  a.num_blocks = num_blocks;
+  a.max_seq_len = max_seq_len;
+  a.chunk_tiles = plan.chunk_tiles;
+  a.n_chunks = plan.n_chunks;
+  a.scale_log2 = static_cast<float>(static_cast<double>(ctx->scale) * 1.4426950408889634);
+  cudaError_t e = plan.path == GVA_PATH_MMA ? gva::launch_decode_mma(a, sep_k, stream)
+                                            : gva::launch_decode_fma(a, d.cache_dtype, sep_k, stream);
+  if (e != cudaSuccess) return GVA_ERR_CUDA;
+  return from_cuda(gva::launch_combine(a, stream));
+}
+
+}  // namespace
+
+extern "C" {
+
+gva_status gva_create(const gva_dims* dims, gva_ctx** out) {
+  if (!dims || !out) return GVA_ERR_INVALID_ARG;
+  const gva_dims& d = *dims;
+  if (d.H <= 0 || d.G <= 0 || d.H % d.G != 0 || d.d_v <= 0 || d.d_n <= 0 || d.d_r < 0 ||
+      (d.d_r & 1) || d.d_v % 32 != 0 || d.d_n % 4 != 0 || d.block_size != GVA_BLOCK_TOKENS)
+    return GVA_ERR_INVALID_ARG;
+  if (d.cache_dtype != GVA_F32 && d.cache_dtype != GVA_BF16) return GVA_ERR_INVALID_ARG;
+  if (d.d_r > 32) return GVA_ERR_UNSUPPORTED;
+  if (!gva::fma_supported(d, false) && !gva::mma_supported(d, false) &&
+      !(d.d_r == 0 && (gva::fma_supported(d, true) || gva::mma_supported(d, true))))
+    return GVA_ERR_UNSUPPORTED;
+  gva_ctx* ctx = static_cast<gva_ctx*>(calloc(1, sizeof(gva_ctx)));
+  if (!ctx) return GVA_ERR_CUDA;
+  ctx->dims = d;
+  ctx->scale = d.scale > 0.f ? d.scale : static_cast<float>(1.0 / sqrt(static_cast<double>(d.d_n + d.d_r)));
+  ctx->rope_base = d.rope_base > 0.0 ? d.rope_base : 10000.0;
+  ctx->split_tokens = 0;
+  ctx->path = GVA_PATH_AUTO;
+  if (cudaGetDevice(&ctx->device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&ctx->num_sms, cudaDevAttrMultiProcessorCount, ctx->device) != cudaSuccess ||
+      cudaMalloc(reinterpret_cast<void**>(&ctx->d_err), sizeof(unsigned)) != cudaSuccess) {
+    free(ctx);
+    return GVA_ERR_CUDA;
+  }
+  if (cudaMemset(ctx->d_err, 0, sizeof(unsigned)) != cudaSuccess) {
+    cudaFree(ctx->d_err);
+    free(ctx);
+    return GVA_ERR_CUDA;
+  }
+  *out = ctx;
+  return GVA_OK;
+}
+
+void gva_destroy(gva_ctx* ctx) {
+  if (!ctx) return;
+  if (ctx->d_err) cudaFree(ctx->d_err);
+  free(ctx);
+}
+
+gva_status gva_absorb_query(gva_ctx* ctx, int B, const float* q_c, const float* q_r,
+                            const int32_t* pos_q, const float* M, float* q_abs, float* q_rot,
+                            gva_stream_t stream) {
+  if (!ctx || B < 0) return GVA_ERR_INVALID_ARG;
+  if (B == 0) return GVA_OK;
+  if (!q_c || !pos_q || !M || !q_abs) return GVA_ERR_INVALID_ARG;
+  if (ctx->dims.d_r > 0 && (!q_r || !q_rot)) return GVA_ERR_INVALID_ARG;
+  if (!aligned16(q_c) || !aligned16(M) || !aligned16(q_abs)) return GVA_ERR_INVALID_ARG;
+  if (!on_ctx_device(ctx)) return GVA_ERR_INVALID_ARG;
+  return from_cuda(gva::launch_absorb(ctx, B, q_c, q_r, pos_q, M, q_abs, q_rot,
+                                      reinterpret_cast<cudaStream_t>(stream)));
+}
+
+gva_status gva_cache_append(gva_ctx* ctx, int B, int n, const void* v_new, const void* kr_new,
+                            const int32_t* pos, const int32_t* block_table, int max_blocks,
+                            int num_blocks, void* v_pool, void* kr_pool, gva_stream_t stream) {
+  if (!ctx || B < 0 || n < 0) return GVA_ERR_INVALID_ARG;
+  if (B == 0 || n == 0) return GVA_OK;
+  if (!v_new || !pos || !block_table || !v_pool || max_blocks < 1 || num_blocks < 1)
+    return GVA_ERR_INVALID_ARG;
+  if (ctx->dims.d_r > 0 && (!kr_new || !kr_pool)) return GVA_ERR_INVALID_ARG;
+  if (!aligned16(v_new) || !aligned16(v_pool)) return GVA_ERR_INVALID_ARG;
+  if (static_cast<long long>(B) * n > (1LL << 40)) return GVA_ERR_INVALID_ARG;
+  if (!on_ctx_device(ctx)) return GVA_ERR_INVALID_ARG;
+  return from_cuda(gva::launch_append(ctx, B, n, v_new, kr_new, pos, block_table, max_blocks,
+                                      num_blocks, v_pool, kr_pool,
+                                      reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t gva_decode_workspace_size(const gva_ctx* ctx, int B, int max_seq_len) {
+  if (!ctx || B <= 0 || max_seq_len < 1) return 0;
+  gva::Plan plan;
+  const bool sep_k = false;
+  if (!make_plan(ctx, B, max_seq_len, sep_k, &plan)) {
+    if (!make_plan(ctx, B, max_seq_len, true, &plan)) return 0;
+  }
+  // The GQA form of a d_r == 0 context may plan differently; cover both.
+  gva::Plan other;
+  if (ctx->dims.d_r == 0 && make_plan(ctx, B, max_seq_len, true, &other) &&
+      other.ws_bytes > plan.ws_bytes)
+    plan = other;
+  return plan.ws_bytes;
+}
+
+gva_status gva_decode_attention(gva_ctx* ctx, int B, const float* q_abs, const float* q_rot,
+                                const void* v_pool, const void* kr_pool,
+                                const int32_t* block_table, int max_blocks, int num_blocks,
+                                const int32_t* seq_lens, int max_seq_len, float* out,
+                                void* workspace, size_t ws_bytes, gva_stream_t stream) {
+  return decode_common(ctx, false, B, q_abs, q_rot, nullptr, v_pool, kr_pool, block_table,
+                       max_blocks, num_blocks, seq_lens, max_seq_len, out, workspace, ws_bytes,
+                       reinterpret_cast<cudaStream_t>(stream));
+}
+
+gva_status gqa_decode_attention(gva_ctx* ctx, int B, const float* q, const void* k_pool,
+                                const void* v_pool, const int32_t* block_table, int max_blocks,
+                                int num_blocks, const int32_t* seq_lens, int max_seq_len,
+                                float* out, void* workspace, size_t ws_bytes,
+                                gva_stream_t stream) {
+  if (ctx && ctx->dims.d_r != 0) return GVA_ERR_INVALID_ARG;
+  return decode_common(ctx, true, B, q, nullptr, k_pool, v_pool, nullptr, block_table,
+                       max_blocks, num_blocks, seq_lens, max_seq_len, out, workspace, ws_bytes,
+                       reinterpret_cast<cudaStream_t>(stream));
+}
+
+gva_status gva_set_split_tokens(gva_ctx* ctx, int split_tokens) {
+  if (!ctx || split_tokens < 0 || split_tokens % GVA_BLOCK_TOKENS != 0) return GVA_ERR_INVALID_ARG;
+  ctx->split_tokens = split_tokens;
+  return GVA_OK;
+}
+
+gva_status gva_set_decode_path(gva_ctx* ctx, gva_decode_path path) {
+  if (!ctx || (path != GVA_PATH_AUTO && path != GVA_PATH_FMA && path != GVA_PATH_MMA))
+    return GVA_ERR_INVALID_ARG;
+  ctx->path = path;
+  return GVA_OK;
+}
+
+gva_status gva_decode_plan(const gva_ctx* ctx, int B, int max_seq_len, int* split_tokens,
+                           int* max_splits) {
+  if (!ctx || B <= 0 || max_seq_len < 1) return GVA_ERR_INVALID_ARG;
+  gva::Plan plan;
+  // the GVA form when it applies, else the GQA form (d_r == 0 contexts)
+  if (!make_plan(ctx, B, max_seq_len, false, &plan) && !make_plan(ctx, B, max_seq_len, true, &plan))
+    return GVA_ERR_UNSUPPORTED;
+  if (split_tokens) *split_tokens = plan.chunk_tiles * GVA_BLOCK_TOKENS;
+  if (max_splits) *max_splits = plan.n_chunks;
+  return GVA_OK;
+}
+
+gva_status gva_get_device_error(gva_ctx* ctx, unsigned* bits) {
+  if (!ctx || !bits) return GVA_ERR_INVALID_ARG;
+  if (!on_ctx_device(ctx)) return GVA_ERR_INVALID_ARG;
+  unsigned v = 0;
+  if (cudaDeviceSynchronize() != cudaSuccess ||
+      cudaMemcpy(&v, ctx->d_err, sizeof(unsigned), cudaMemcpyDeviceToHost) != cudaSuccess ||
+      cudaMemset(ctx->d_err, 0, sizeof(unsigned)) != cudaSuccess ||
+      cudaDeviceSynchronize() != cudaSuccess)
+    return GVA_ERR_CUDA;
+  *bits = v;
+  return v ? GVA_ERR_DEVICE_INDEX : GVA_OK;
+}
+
+const char* gva_status_string(gva_status s) {
+  switch (s) {
+    case GVA_OK: return "ok";
+    case GVA_ERR_INVALID_ARG: return "invalid argument";
+    case GVA_ERR_UNSUPPORTED: return "unsupported shape or dtype";
+    case GVA_ERR_WORKSPACE: return "workspace missing or too small";
+    case GVA_ERR_CUDA: return "CUDA runtime error";
+    case GVA_ERR_DEVICE_INDEX: return "device reported an index error";
+  }
+  return "unknown status";
+}
+
+int gva_version(void) { return kVersion; }
+
+}  // extern "C"

@@ -1,0 +1,114 @@
+// gva_append.cu -- writes new tokens into the compact GVA cache.
+//
+// Per token the cache gets the G grouped value rows (a bit copy) and ONE positional key,
+// rotated to the token's own position (the cache holds grouped values plus a small,
+// separately cached, rotated positional key: abstract "Grouped Value Attention: Efficient
+// KV Caching via On-Demand Key Reconstruction"; review "[논문리뷰] Grouped Value Attention",
+// section 3, Decoupled RoPE).  One warp per token: the value rows move as 16-byte vectors,
+// lanes rotate the positional pairs in fp64 and round once to the cache dtype.
+#include "gva_device.cuh"
+#include "gva_internal.h"
+
+namespace gva {
+namespace {
+
+struct AppendArgs {
+  const void* v_new;
+  const void* kr_new;
+  const int32_t* pos;
+  const int32_t* block_table;
+  void* v_pool;
+  void* kr_pool;
+  unsigned* err;
+  int B, n, G, d_v, d_r, max_blocks, num_blocks;
+  double base;
+};
+
+constexpr int kAppendThreads = 256;
+
+template <typename T>
+__global__ void __launch_bounds__(kAppendThreads) append_kernel(const AppendArgs a) {
+  const long long warp_id =
+      (static_cast<long long>(blockIdx.x) * kAppendThreads + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  const long long ntok = static_cast<long long>(a.B) * a.n;
+  if (warp_id >= ntok) return;
+  const int b = static_cast<int>(warp_id / a.n);
+  const int t = static_cast<int>(warp_id % a.n);
+  const long long p = static_cast<long long>(a.pos[b]) + t;
+
+  // Resolve the slot; an unresolvable one skips the token and is reported.
+  if (p < 0 || (p >> 6) >= a.max_blocks) {
+    if (lane == 0) flag_error(a.err, GVA_DEVERR_POSITION);
+    return;
+  }
+  const int blk = a.block_table[static_cast<long long>(b) * a.max_blocks + (p >> 6)];
+  if (blk < 0 || blk >= a.num_blocks) {
+    if (lane == 0) flag_error(a.err, GVA_DEVERR_BLOCK_ID);
+    return;
+  }
+  const int o = static_cast<int>(p & (kBlockTokens - 1));
+  const long long tok = static_cast<long long>(b) * a.n + t;
+
+  // Grouped value rows: G rows of d_v elements, 16-byte vectors.
+  const int vec_per_row = a.d_v * static_cast<int>(sizeof(T)) / 16;
+  const int nvec = a.G * vec_per_row;
+  const uint4* src = reinterpret_cast<const uint4*>(static_cast<const T*>(a.v_new) +
+                                                    tok * a.G * a.d_v);
+  for (int i = lane; i < nvec; i += 32) {
+    const int g = i / vec_per_row, w = i - g * vec_per_row;
+    uint4* dst = reinterpret_cast<uint4*>(
+                     static_cast<T*>(a.v_pool) +
+                     ((static_cast<long long>(blk) * a.G + g) * kBlockTokens + o) * a.d_v) +
+                 w;
+    *dst = src[i];
+  }
+
+  // Shared positional key, rotated to position p: pair (2i, 2i+1) turned by p*theta_i.
+  const T* x = static_cast<const T*>(a.kr_new) + tok * a.d_r;
+  T* y = static_cast<T*>(a.kr_pool) + (static_cast<long long>(blk) * kBlockTokens + o) * a.d_r;
+  for (int i = lane; i < a.d_r / 2; i += 32) {
+    const double x0 = CacheElem<T>::to_double(x[2 * i]);
+    const double x1 = CacheElem<T>::to_double(x[2 * i + 1]);
+    double s, c;
+    sincos(rope_angle(p, i, a.d_r, a.base), &s, &c);
+    // explicit roundings (no contraction) so each product is rounded on its own
+    const double y0 = __dsub_rn(__dmul_rn(x0, c), __dmul_rn(x1, s));
+    const double y1 = __dadd_rn(__dmul_rn(x0, s), __dmul_rn(x1, c));
+    y[2 * i] = CacheElem<T>::from_double(y0);
+    y[2 * i + 1] = CacheElem<T>::from_double(y1);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_append(const gva_ctx* ctx, int B, int n, const void* v_new,
+                          const void* kr_new, const int32_t* pos, const int32_t* block_table,
+                          int max_blocks, int num_blocks, void* v_pool, void* kr_pool,
+                          cudaStream_t stream) {
+  AppendArgs a;
+  a.v_new = v_new;
+  a.kr_new = kr_new;
+  a.pos = pos;
+  a.block_table = block_table;
+  a.v_pool = v_pool;
+  a.kr_pool = kr_pool;
+  a.err = ctx->d_err;
+  a.B = B;
+  a.n = n;
+  a.G = ctx->dims.G;
+  a.d_v = ctx->dims.d_v;
+  a.d_r = ctx->dims.d_r;
+  a.max_blocks = max_blocks;
+  a.num_blocks = num_blocks;
+  a.base = ctx->rope_base;
+  const long long threads = static_cast<long long>(B) * n * 32;
+  const unsigned grid = static_cast<unsigned>((threads + kAppendThreads - 1) / kAppendThreads);
+  if (ctx->dims.cache_dtype == GVA_F32)
+    append_kernel<float><<<grid, kAppendThreads, 0, stream>>>(a);
+  else
+    append_kernel<__nv_bfloat16><<<grid, kAppendThreads, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace gva

@@ -1,0 +1,156 @@
+// gva_device.cuh -- device-side helpers shared by the GVA kernels (sm_103a).
+//
+// Inline PTX for the Blackwell async-copy machinery (mbarrier transaction counts and the
+// bulk-copy engine), bounded waits that report instead of hanging, and the number-format
+// conversions the cache needs.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "gva.h"
+
+namespace gva {
+
+constexpr int kBlockTokens = GVA_BLOCK_TOKENS;
+constexpr unsigned kFullMask = 0xffffffffu;
+constexpr int kMaxDevices = 64;
+// A wait on an async copy gives up after this long (the copy engine finishes a tile in
+// microseconds; a second means something is wrong) and the kernel reports
+// GVA_DEVERR_TIMEOUT instead of spinning forever.
+constexpr uint64_t kWaitLimitNs = 1000ull * 1000ull * 1000ull;
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// ---- mbarrier ---------------------------------------------------------------------------
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
+               : "memory");
+}
+
+// Makes barrier initialisation visible to the async proxy (the copy engine) and to the
+// other threads of the CTA.
+__device__ __forceinline__ void mbar_init_fence() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Waits for the phase with the given parity to complete.  Returns false if it did not
+// complete within kWaitLimitNs.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 64; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (global_ns() - t0 > kWaitLimitNs) return false;
+  }
+}
+
+// ---- bulk copy engine -------------------------------------------------------------------
+
+// Contiguous global -> shared copy by the bulk-copy (TMA) engine; completion is counted on
+// `bar` as transaction bytes.  dst and src 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes,
+                                         uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(smem_addr(dst)),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar))
+      : "memory");
+}
+
+// Orders this thread's earlier generic-proxy accesses to shared memory before later
+// async-proxy (copy engine) accesses, so a buffer can be refilled after it was read.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// ---- number formats ---------------------------------------------------------------------
+
+__device__ __forceinline__ float bf16_bits_to_float(uint32_t bits16) {
+  return __uint_as_float(bits16 << 16);
+}
+
+// Two bf16 packed in a 32-bit word -> two floats (exact).
+__device__ __forceinline__ void bf16x2_to_float2(uint32_t w, float& lo, float& hi) {
+  lo = __uint_as_float(w << 16);
+  hi = __uint_as_float(w & 0xffff0000u);
+}
+
+// Double -> bf16 with a single round-to-nearest-even.  The double is first narrowed to
+// binary32 with round-to-odd (truncate, then force the last bit to 1 if anything was cut
+// off); because binary32 keeps at least two more bits than bf16, rounding that value to
+// nearest even gives the correctly rounded bf16 (Boldo & Melquiond, "Emulation of FMA and
+// correctly rounded sums: proved algorithms using rounding to odd", IEEE TC 2008).
+__device__ __forceinline__ __nv_bfloat16 double_to_bf16_rne(double x) {
+  float t = __double2float_rz(x);
+  if (static_cast<double>(t) != x && isfinite(t)) t = __uint_as_float(__float_as_uint(t) | 1u);
+  return __float2bfloat16_rn(t);
+}
+
+template <typename T>
+struct CacheElem;
+
+template <>
+struct CacheElem<float> {
+  static __device__ __forceinline__ double to_double(float v) { return static_cast<double>(v); }
+  static __device__ __forceinline__ float from_double(double v) { return __double2float_rn(v); }
+  static __device__ __forceinline__ float to_float(float v) { return v; }
+};
+
+template <>
+struct CacheElem<__nv_bfloat16> {
+  static __device__ __forceinline__ double to_double(__nv_bfloat16 v) {
+    return static_cast<double>(__bfloat162float(v));
+  }
+  static __device__ __forceinline__ __nv_bfloat16 from_double(double v) {
+    return double_to_bf16_rne(v);
+  }
+  static __device__ __forceinline__ float to_float(__nv_bfloat16 v) { return __bfloat162float(v); }
+};
+
+// RoPE angle for pair i of a d_r-wide slice at position p, in fp64:
+// p * base^(-2i/d_r).
+__device__ __forceinline__ double rope_angle(long long p, int i, int d_r, double base) {
+  return static_cast<double>(p) * pow(base, -2.0 * static_cast<double>(i) / static_cast<double>(d_r));
+}
+
+__device__ __forceinline__ void flag_error(unsigned* err, unsigned bit) {
+  if (err) atomicOr(err, bit);
+}
+
+}  // namespace gva

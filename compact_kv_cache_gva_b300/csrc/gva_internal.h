@@ -1,0 +1,72 @@
+// gva_internal.h -- host-side structures shared by the GVA translation units (not part of
+// the public ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "gva.h"
+
+struct gva_ctx {
+  gva_dims dims;
+  float scale;          // resolved softmax scale
+  double rope_base;     // resolved RoPE base
+  int device;           // device the context was created on
+  int num_sms;          // SM count of that device
+  unsigned* d_err;      // device error word
+  int split_tokens;     // 0 = automatic
+  gva_decode_path path;
+};
+
+namespace gva {
+
+// Arguments of the decode partial kernels (GVA and the matching GQA form).
+struct DecodeArgs {
+  const float* q_abs;        // [B,H,d_v] absorbed query (GQA: the plain query)
+  const float* q_rot;        // [B,H,d_r] rotated positional query (nullptr when d_r == 0)
+  const void* v_pool;        // [NB][G][64][d_v]
+  const void* k_pool;        // GQA only: [NB][G][64][d_v]
+  const void* kr_pool;       // [NB][64][d_r]
+  const int32_t* block_table;
+  const int32_t* seq_lens;
+  float* out;                // [B,H,d_v]
+  float* part;               // partial records [B][n_chunks][H][d_v + 4]
+  unsigned* err;
+  int B, H, G, d_v, d_r;
+  int max_blocks, num_blocks, max_seq_len;
+  int chunk_tiles;           // 64-token tiles per chunk
+  int n_chunks;              // chunks per sequence in the plan (grid extent)
+  float scale_log2;          // softmax scale * log2(e)
+};
+
+// Record layout of one partial: m (log2 domain), l, two pad words, then d_v weighted sums.
+__host__ __device__ inline size_t partial_stride_floats(int d_v) { return static_cast<size_t>(d_v) + 4; }
+
+struct Plan {
+  int path;          // GVA_PATH_FMA or GVA_PATH_MMA
+  int chunk_tiles;
+  int n_chunks;
+  size_t ws_bytes;
+};
+
+// Launchers (return cudaSuccess or the launch error).
+cudaError_t launch_absorb(const gva_ctx* ctx, int B, const float* q_c, const float* q_r,
+                          const int32_t* pos_q, const float* M, float* q_abs, float* q_rot,
+                          cudaStream_t stream);
+cudaError_t launch_append(const gva_ctx* ctx, int B, int n, const void* v_new,
+                          const void* kr_new, const int32_t* pos, const int32_t* block_table,
+                          int max_blocks, int num_blocks, void* v_pool, void* kr_pool,
+                          cudaStream_t stream);
+// Decode: partial kernel + combine.  sep_k selects the GQA form (k_pool used, d_r == 0).
+bool fma_supported(const gva_dims& d, bool sep_k);
+int fma_ctas_per_sm(const gva_dims& d, bool sep_k);
+cudaError_t launch_decode_fma(const DecodeArgs& a, int cache_dtype, bool sep_k,
+                              cudaStream_t stream);
+bool mma_supported(const gva_dims& d, bool sep_k);
+int mma_ctas_per_sm(const gva_dims& d, bool sep_k);
+int mma_tiles_per_cta_unit(const gva_dims& d);
+cudaError_t launch_decode_mma(const DecodeArgs& a, bool sep_k, cudaStream_t stream);
+cudaError_t launch_combine(const DecodeArgs& a, cudaStream_t stream);
+
+}  // namespace gva

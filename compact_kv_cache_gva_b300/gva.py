@@ -1,0 +1,274 @@
+"""Thin Python binding of libgva.so (the C ABI in include/gva.h), by ctypes.
+
+Argument marshalling only: every function takes torch tensors, checks that they are CUDA,
+contiguous and of the dtype the C ABI states, derives the sizes from their shapes, and
+calls the C function of the same name on the current torch stream (or the stream given).
+All computation happens in the library's kernels.  There is no CPU fallback: if the
+library is missing or cannot be loaded, the first call raises.
+"""
+import ctypes as C
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libgva.so")
+
+GVA_OK, GVA_ERR_INVALID_ARG, GVA_ERR_UNSUPPORTED, GVA_ERR_WORKSPACE, GVA_ERR_CUDA, GVA_ERR_DEVICE_INDEX = range(6)
+GVA_F32, GVA_BF16 = 0, 1
+GVA_PATH_AUTO, GVA_PATH_FMA, GVA_PATH_MMA = 0, 1, 2
+GVA_DEVERR_POSITION, GVA_DEVERR_BLOCK_ID, GVA_DEVERR_SEQ_LEN, GVA_DEVERR_TIMEOUT = 1, 2, 4, 8
+BLOCK_TOKENS = 64
+
+# Exported symbols the header declares (checked by the CPU tests).
+EXPORTS = ("gva_create", "gva_destroy", "gva_absorb_query", "gva_cache_append", "gva_decode_workspace_size",
+           "gva_decode_attention", "gqa_decode_attention", "gva_set_split_tokens", "gva_set_decode_path",
+           "gva_decode_plan", "gva_get_device_error", "gva_status_string", "gva_version")
+
+
+class GVAError(RuntimeError):
+    def __init__(self, status, what):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} (status {status})")
+
+
+class gva_dims(C.Structure):
+    _fields_ = [("H", C.c_int), ("G", C.c_int), ("d_v", C.c_int), ("d_n", C.c_int), ("d_r", C.c_int),
+                ("block_size", C.c_int), ("cache_dtype", C.c_int), ("rope_base", C.c_double), ("scale", C.c_float)]
+
+
+_lib = None
+
+
+def load():
+    """Loads libgva.so once; raises if it is not built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"libgva.so is not built ({LIB_PATH}); run `python -m compact_kv_cache_gva_b300.build`")
+    L = C.CDLL(LIB_PATH)
+    vp, ip, i, st = C.c_void_p, C.c_void_p, C.c_int, C.c_void_p
+    L.gva_create.argtypes = [C.POINTER(gva_dims), C.POINTER(C.c_void_p)]
+    L.gva_destroy.argtypes = [vp]
+    L.gva_destroy.restype = None
+    L.gva_absorb_query.argtypes = [vp, i, vp, vp, ip, vp, vp, vp, st]
+    L.gva_cache_append.argtypes = [vp, i, i, vp, vp, ip, ip, i, i, vp, vp, st]
+    L.gva_decode_workspace_size.argtypes = [vp, i, i]
+    L.gva_decode_workspace_size.restype = C.c_size_t
+    L.gva_decode_attention.argtypes = [vp, i, vp, vp, vp, vp, ip, i, i, ip, i, vp, vp, C.c_size_t, st]
+    L.gqa_decode_attention.argtypes = [vp, i, vp, vp, vp, ip, i, i, ip, i, vp, vp, C.c_size_t, st]
+    L.gva_set_split_tokens.argtypes = [vp, i]
+    L.gva_set_decode_path.argtypes = [vp, i]
+    L.gva_decode_plan.argtypes = [vp, i, i, C.POINTER(C.c_int), C.POINTER(C.c_int)]
+    L.gva_get_device_error.argtypes = [vp, C.POINTER(C.c_uint)]
+    L.gva_status_string.argtypes = [i]
+    L.gva_status_string.restype = C.c_char_p
+    L.gva_version.argtypes = []
+    for name in EXPORTS:
+        if name not in ("gva_destroy", "gva_decode_workspace_size", "gva_status_string", "gva_version"):
+            getattr(L, name).restype = C.c_int
+    _lib = L
+    return L
+
+
+def status_string(status):
+    try:
+        return load().gva_status_string(int(status)).decode()
+    except Exception:
+        return "unknown"
+
+
+def _check(status, what):
+    if status != GVA_OK:
+        raise GVAError(status, what)
+
+
+def _stream(stream):
+    if stream is None:
+        return C.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, torch.cuda.Stream):
+        return C.c_void_p(stream.cuda_stream)
+    return C.c_void_p(int(stream))
+
+
+def _ptr(t, dtype, name, allow_none=False):
+    if t is None:
+        if allow_none:
+            return C.c_void_p(0)
+        raise ValueError(f"{name} is required")
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if dtype is not None and t.dtype not in (dtype if isinstance(dtype, tuple) else (dtype,)):
+        raise TypeError(f"{name} has dtype {t.dtype}, expected {dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return C.c_void_p(t.data_ptr())
+
+
+class Context:
+    """Owns one gva_ctx (bound to the device current at creation)."""
+
+    def __init__(self, H, G, d_v, d_n, d_r, cache_dtype, rope_base=10000.0, scale=0.0):
+        self.dims = gva_dims(H, G, d_v, d_n, d_r, BLOCK_TOKENS,
+                             GVA_F32 if cache_dtype in ("f32", torch.float32) else GVA_BF16, rope_base, scale)
+        self.cache_torch_dtype = torch.float32 if self.dims.cache_dtype == GVA_F32 else torch.bfloat16
+        h = C.c_void_p()
+        _check(load().gva_create(C.byref(self.dims), C.byref(h)), "gva_create")
+        self.handle = h
+
+    def close(self):
+        if self.handle:
+            load().gva_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    @property
+    def H(self):
+        return self.dims.H
+
+
+def gva_create(H, G, d_v, d_n, d_r, cache_dtype="bf16", rope_base=10000.0, scale=0.0):
+    return Context(H, G, d_v, d_n, d_r, cache_dtype, rope_base, scale)
+
+
+def gva_destroy(ctx):
+    ctx.close()
+
+
+def _shape(t, shape, name):
+    if t is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+def _check_pools(ctx, v_pool, kr_pool, k_pool=None):
+    d = ctx.dims
+    NB = v_pool.shape[0]
+    _shape(v_pool, (NB, d.G, BLOCK_TOKENS, d.d_v), "v_pool")
+    if k_pool is not None:
+        _shape(k_pool, (NB, d.G, BLOCK_TOKENS, d.d_v), "k_pool")
+    if d.d_r > 0 and kr_pool is not None:
+        _shape(kr_pool, (NB, BLOCK_TOKENS, d.d_r), "kr_pool")
+    return NB
+
+
+def _check_table(block_table, B, seq_lens=None):
+    if block_table.dim() != 2 or block_table.shape[0] < B:
+        raise ValueError("block_table must be [>=B, max_blocks]")
+    if seq_lens is not None and (seq_lens.dim() != 1 or seq_lens.shape[0] < B):
+        raise ValueError("seq_lens must be [>=B]")
+
+
+def gva_absorb_query(ctx, q_c, q_r, pos_q, M, q_abs, q_rot, stream=None):
+    B = q_c.shape[0]
+    d = ctx.dims
+    _shape(q_c, (B, d.H, d.d_n), "q_c")
+    _shape(M, (d.H, d.d_v, d.d_n), "M")
+    _shape(q_abs, (B, d.H, d.d_v), "q_abs")
+    _shape(pos_q, (B,), "pos_q")
+    has_r = d.d_r > 0
+    if has_r:
+        _shape(q_r, (B, d.H, d.d_r), "q_r")
+        _shape(q_rot, (B, d.H, d.d_r), "q_rot")
+    _check(load().gva_absorb_query(ctx.handle, B, _ptr(q_c, torch.float32, "q_c"),
+                                   _ptr(q_r, torch.float32, "q_r", allow_none=not has_r),
+                                   _ptr(pos_q, torch.int32, "pos_q"), _ptr(M, torch.float32, "M"),
+                                   _ptr(q_abs, torch.float32, "q_abs"),
+                                   _ptr(q_rot, torch.float32, "q_rot", allow_none=not has_r), _stream(stream)),
+           "gva_absorb_query")
+
+
+def gva_cache_append(ctx, v_new, kr_new, pos, block_table, v_pool, kr_pool, stream=None):
+    d = ctx.dims
+    B, n = v_new.shape[0], v_new.shape[1]
+    _shape(v_new, (B, n, d.G, d.d_v), "v_new")
+    _shape(pos, (B,), "pos")
+    _check_table(block_table, B)
+    dt = ctx.cache_torch_dtype
+    has_r = d.d_r > 0
+    if has_r:
+        _shape(kr_new, (B, n, d.d_r), "kr_new")
+    _check_pools(ctx, v_pool, kr_pool if has_r else None)
+    _check(load().gva_cache_append(ctx.handle, B, n, _ptr(v_new, dt, "v_new"),
+                                   _ptr(kr_new, dt, "kr_new", allow_none=not has_r), _ptr(pos, torch.int32, "pos"),
+                                   _ptr(block_table, torch.int32, "block_table"), block_table.shape[1],
+                                   v_pool.shape[0], _ptr(v_pool, dt, "v_pool"),
+                                   _ptr(kr_pool, dt, "kr_pool", allow_none=not has_r), _stream(stream)),
+           "gva_cache_append")
+
+
+def gva_decode_workspace_size(ctx, B, max_seq_len):
+    return int(load().gva_decode_workspace_size(ctx.handle, int(B), int(max_seq_len)))
+
+
+def gva_decode_attention(ctx, q_abs, q_rot, v_pool, kr_pool, block_table, seq_lens, max_seq_len, out, workspace,
+                         stream=None):
+    d = ctx.dims
+    B = q_abs.shape[0]
+    dt = ctx.cache_torch_dtype
+    has_r = d.d_r > 0
+    _shape(q_abs, (B, d.H, d.d_v), "q_abs")
+    _shape(out, (B, d.H, d.d_v), "out")
+    if has_r:
+        _shape(q_rot, (B, d.H, d.d_r), "q_rot")
+    _check_table(block_table, B, seq_lens)
+    _check_pools(ctx, v_pool, kr_pool if has_r else None)
+    _check(load().gva_decode_attention(ctx.handle, B, _ptr(q_abs, torch.float32, "q_abs"),
+                                       _ptr(q_rot, torch.float32, "q_rot", allow_none=not has_r),
+                                       _ptr(v_pool, dt, "v_pool"), _ptr(kr_pool, dt, "kr_pool", allow_none=not has_r),
+                                       _ptr(block_table, torch.int32, "block_table"), block_table.shape[1],
+                                       v_pool.shape[0], _ptr(seq_lens, torch.int32, "seq_lens"), int(max_seq_len),
+                                       _ptr(out, torch.float32, "out"), _ptr(workspace, None, "workspace"),
+                                       workspace.numel() * workspace.element_size(), _stream(stream)),
+           "gva_decode_attention")
+
+
+def gqa_decode_attention(ctx, q, k_pool, v_pool, block_table, seq_lens, max_seq_len, out, workspace, stream=None):
+    d = ctx.dims
+    B = q.shape[0]
+    dt = ctx.cache_torch_dtype
+    _shape(q, (B, d.H, d.d_v), "q")
+    _shape(out, (B, d.H, d.d_v), "out")
+    _check_table(block_table, B, seq_lens)
+    _check_pools(ctx, v_pool, None, k_pool)
+    _check(load().gqa_decode_attention(ctx.handle, B, _ptr(q, torch.float32, "q"), _ptr(k_pool, dt, "k_pool"),
+                                       _ptr(v_pool, dt, "v_pool"), _ptr(block_table, torch.int32, "block_table"),
+                                       block_table.shape[1], v_pool.shape[0], _ptr(seq_lens, torch.int32, "seq_lens"),
+                                       int(max_seq_len), _ptr(out, torch.float32, "out"),
+                                       _ptr(workspace, None, "workspace"),
+                                       workspace.numel() * workspace.element_size(), _stream(stream)),
+           "gqa_decode_attention")
+
+
+def gva_set_split_tokens(ctx, split_tokens):
+    _check(load().gva_set_split_tokens(ctx.handle, int(split_tokens)), "gva_set_split_tokens")
+
+
+def gva_set_decode_path(ctx, path):
+    _check(load().gva_set_decode_path(ctx.handle, int(path)), "gva_set_decode_path")
+
+
+def gva_decode_plan(ctx, B, max_seq_len):
+    st, ms = C.c_int(), C.c_int()
+    _check(load().gva_decode_plan(ctx.handle, int(B), int(max_seq_len), C.byref(st), C.byref(ms)), "gva_decode_plan")
+    return st.value, ms.value
+
+
+def gva_get_device_error(ctx):
+    """Returns the device error bits (0 when clean) and clears them; synchronises the device."""
+    bits = C.c_uint()
+    st = load().gva_get_device_error(ctx.handle, C.byref(bits))
+    if st not in (GVA_OK, GVA_ERR_DEVICE_INDEX):
+        raise GVAError(st, "gva_get_device_error")
+    return bits.value
+
+
+def gva_version():
+    return int(load().gva_version())

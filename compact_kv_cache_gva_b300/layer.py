@@ -1,0 +1,50 @@
+"""One decode step of one GVA layer through the C ABI: absorb -> append -> decode.
+
+Holds the step's device buffers (absorbed/rotated queries, output, workspace) so a caller
+only passes the step's inputs and the cache.  Marshalling only; the work is in libgva.so.
+"""
+import torch
+
+from . import gva
+
+
+class GVADecodeLayer:
+    def __init__(self, H, G, d_v, d_n, d_r, cache_dtype, B, max_seq_len, device="cuda", split_tokens=0,
+                 path=gva.GVA_PATH_AUTO, rope_base=10000.0, scale=0.0):
+        self.ctx = gva.gva_create(H, G, d_v, d_n, d_r, cache_dtype, rope_base, scale)
+        if split_tokens:
+            gva.gva_set_split_tokens(self.ctx, split_tokens)
+        if path != gva.GVA_PATH_AUTO:
+            gva.gva_set_decode_path(self.ctx, path)
+        self.B, self.max_seq_len = B, max_seq_len
+        self.q_abs = torch.empty((B, H, d_v), dtype=torch.float32, device=device)
+        self.q_rot = torch.empty((B, H, d_r), dtype=torch.float32, device=device)
+        self.out = torch.empty((B, H, d_v), dtype=torch.float32, device=device)
+        ws = max(16, gva.gva_decode_workspace_size(self.ctx, B, max_seq_len))
+        self.workspace = torch.empty(ws, dtype=torch.uint8, device=device)
+
+    def plan(self):
+        return gva.gva_decode_plan(self.ctx, self.B, self.max_seq_len)
+
+    def absorb(self, q_c, q_r, pos_q, M, stream=None):
+        gva.gva_absorb_query(self.ctx, q_c, q_r if self.ctx.dims.d_r else None, pos_q, M, self.q_abs,
+                             self.q_rot if self.ctx.dims.d_r else None, stream)
+
+    def append(self, v_new, kr_new, pos, block_table, v_pool, kr_pool, stream=None):
+        gva.gva_cache_append(self.ctx, v_new, kr_new, pos, block_table, v_pool, kr_pool, stream)
+
+    def attend(self, v_pool, kr_pool, block_table, seq_lens, q_abs=None, q_rot=None, stream=None):
+        gva.gva_decode_attention(self.ctx, self.q_abs if q_abs is None else q_abs,
+                                 (self.q_rot if q_rot is None else q_rot) if self.ctx.dims.d_r else None,
+                                 v_pool, kr_pool if self.ctx.dims.d_r else None, block_table, seq_lens,
+                                 self.max_seq_len, self.out, self.workspace, stream)
+        return self.out
+
+    def step(self, q_c, q_r, pos_q, M, v_new, kr_new, pos_new, block_table, seq_lens, v_pool, kr_pool, stream=None):
+        """absorb the query, append the new token(s), attend through the current position."""
+        self.absorb(q_c, q_r, pos_q, M, stream)
+        self.append(v_new, kr_new, pos_new, block_table, v_pool, kr_pool, stream)
+        return self.attend(v_pool, kr_pool, block_table, seq_lens, stream=stream)
+
+    def device_error(self):
+        return gva.gva_get_device_error(self.ctx)

@@ -1,0 +1,198 @@
+/*
+ * gva.h -- C ABI of the Grouped Value Attention (GVA) decode hot path for NVIDIA B300
+ * (sm_103a).
+ *
+ * GVA keeps, per token and layer, only the G grouped value heads V_g and ONE small
+ * positional key k_r of width d_r, stored already RoPE-rotated and shared by every query
+ * head; there is no content-key cache.  Each query head h scores the cache through the
+ * absorbed query q'_h = M_h q_c,h (the content key K_h = V_g(h) M_h is never built), adds
+ * the decoupled positional score q~_r,h . k_r,j, and returns o_h = sum_j softmax(s)_j v_j.
+ *   - "Grouped Value Attention: Efficient KV Caching via On-Demand Key Reconstruction"
+ *     (abstract): grouped values, learned linear key map absorbed into the query, shared
+ *     decoupled RoPE channel with a separately cached positional key.
+ *   - ai-feeds.com summary "Grouped Value Attention:通过按需 key 重建实现高效 KV 缓存",
+ *     section 方法: K_h = V_g(h) M_h, Q' = Q M^T, output is the value-weighted sum.
+ *   - review "[논문리뷰] Grouped Value Attention ...", section 3, Decoupled RoPE: query and
+ *     key split into an unrotated content slice (d_n) and a rotated positional slice (d_r);
+ *     RoPE on the positional slice only; positional key shared across heads.
+ *
+ * Conventions shared by every call
+ *   - Pointers are DEVICE pointers unless a parameter says otherwise; they must be
+ *     16-byte aligned.  All tensors are dense, row-major, in the shapes given.
+ *   - The caller owns every buffer (inputs, outputs, cache pools, block table, workspace).
+ *     The library allocates device memory only in gva_create (its error word) and frees it
+ *     in gva_destroy; nothing is allocated on the decode path.
+ *   - Calls are asynchronous on `stream` (NULL = the legacy default stream).  GVA_OK means
+ *     the work was enqueued.  Host-side argument errors return a status and enqueue
+ *     nothing.  Index errors that only the device can see (a position past the block
+ *     table, a block id outside the pool, a bad context length) make the kernel skip that
+ *     access and set a bit in the context's device error word; gva_get_device_error
+ *     reads it.  No kernel traps.
+ *   - Cache layout, 64-token blocks (GVA_BLOCK_TOKENS), NB blocks in a pool:
+ *       V pool   [NB][G][64][d_v]   element (blk, g, o, i) at ((blk*G + g)*64 + o)*d_v + i
+ *       k_r pool [NB][64][d_r]      element (blk, o, c)    at (blk*64 + o)*d_r + c
+ *     Position p of sequence b lives in block block_table[b*max_blocks + p/64], slot p%64.
+ *   - Head h reads value group g(h) = h / (H/G) (contiguous head blocks, as in grouped-
+ *     query attention).  RoPE turns pair (2i, 2i+1) by p * base^(-2i/d_r).  The softmax
+ *     scale defaults to 1/sqrt(d_n + d_r).
+ */
+#ifndef GVA_H_
+#define GVA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define GVA_BLOCK_TOKENS 64
+
+/* Same type as cudaStream_t, so callers need no CUDA header. */
+typedef struct CUstream_st* gva_stream_t;
+
+typedef enum {
+  GVA_OK = 0,
+  GVA_ERR_INVALID_ARG = 1,  /* null pointer, negative size, inconsistent shape */
+  GVA_ERR_UNSUPPORTED = 2,  /* valid, but a shape or dtype no kernel here was built for */
+  GVA_ERR_WORKSPACE = 3,    /* workspace null or smaller than gva_decode_workspace_size() */
+  GVA_ERR_CUDA = 4,         /* a CUDA runtime call failed (launch, attribute, copy) */
+  GVA_ERR_DEVICE_INDEX = 5  /* gva_get_device_error found a device-side error bit set */
+} gva_status;
+
+typedef enum { GVA_F32 = 0, GVA_BF16 = 1 } gva_dtype;
+
+/* Bits of the device error word. */
+#define GVA_DEVERR_POSITION 1u /* position < 0, or position/64 >= max_blocks */
+#define GVA_DEVERR_BLOCK_ID 2u /* block-table entry outside [0, num_blocks) */
+#define GVA_DEVERR_SEQ_LEN 4u  /* seq_lens[b] <= 0 or > max_seq_len (that row's output is 0) */
+#define GVA_DEVERR_TIMEOUT 8u  /* a bounded wait for an async copy gave up (tile skipped) */
+
+/* Decode kernel family for gva_set_decode_path. */
+typedef enum {
+  GVA_PATH_AUTO = 0, /* tensor-core path where it applies, else the CUDA-core path */
+  GVA_PATH_FMA = 1,  /* CUDA-core fp32 FMA path (every dtype) */
+  GVA_PATH_MMA = 2   /* tensor-core path (bf16 cache only; GVA_ERR_UNSUPPORTED otherwise) */
+} gva_decode_path;
+
+typedef struct {
+  int H;                 /* query heads */
+  int G;                 /* value heads (groups); H % G == 0 */
+  int d_v;               /* value width; multiple of 32 */
+  int d_n;               /* content query width (absorbed query input); multiple of 4 */
+  int d_r;               /* positional width; even, 0 <= d_r <= 32 (0 = no positional slice) */
+  int block_size;        /* tokens per cache block; must be 64 */
+  gva_dtype cache_dtype; /* GVA_F32 or GVA_BF16 */
+  double rope_base;      /* <= 0 selects 10000 */
+  float scale;           /* softmax scale; <= 0 selects 1/sqrt(d_n + d_r) */
+} gva_dims;
+
+typedef struct gva_ctx gva_ctx;
+
+/* Validates dims and creates a context bound to the CURRENT device: it holds the dims, the
+ * decode options and a device error word (4 bytes of cudaMalloc).  Returns
+ * GVA_ERR_INVALID_ARG / GVA_ERR_UNSUPPORTED for bad dims, GVA_ERR_CUDA if the allocation
+ * fails.  *out is set only on success. */
+gva_status gva_create(const gva_dims* dims, gva_ctx** out);
+
+/* Frees the context (synchronises nothing; call after the context's work has finished). */
+void gva_destroy(gva_ctx* ctx);
+
+/* gva_absorb_query -- per-step query preparation.
+ * Folds the key map into the query, q'_{b,h} = M_h q_c,{b,h} (column form of Q' = Q M^T,
+ * ai-feeds.com summary section 方法; m.szthrk.cn explainer section "GVA 的正式方案"), and
+ * rotates the positional query q~_r,{b,h} = RoPE(q_r,{b,h}, pos_q[b]) (review section 3,
+ * Decoupled RoPE).
+ *   q_c   [B,H,d_n] f32      content query
+ *   q_r   [B,H,d_r] f32      positional query, unrotated (may be NULL when d_r == 0)
+ *   pos_q [B] int32          query position (normally seq_len - 1)
+ *   M     [H,d_v,d_n] f32    key maps, M[h][i][k]
+ *   q_abs [B,H,d_v] f32 out  absorbed query (no scale folded in)
+ *   q_rot [B,H,d_r] f32 out  rotated positional query (may be NULL when d_r == 0)
+ * fp32 accumulation; the rotation angle, sin and cos are fp64.  B == 0 is a no-op. */
+gva_status gva_absorb_query(gva_ctx* ctx, int B, const float* q_c, const float* q_r,
+                            const int32_t* pos_q, const float* M, float* q_abs, float* q_rot,
+                            gva_stream_t stream);
+
+/* gva_cache_append -- write n new tokens per sequence into the compact cache (the
+ * "append the new token's state, then read through the current position" step of the
+ * decode lifecycle, GQA explainer section "与位置编码和 KV Cache 的关系"; cache content per
+ * the abstract and the review's section 3: grouped values plus one rotated positional key).
+ *   v_new  [B,n,G,d_v] cache dtype   new values, copied bit for bit
+ *   kr_new [B,n,d_r]   cache dtype   new positional keys, UNROTATED; each is rotated to its
+ *                                    own position in fp64 and rounded to nearest even
+ *   pos    [B] int32                 position of the first new token of each sequence
+ *   block_table [B,max_blocks] int32, pools as in the layout above (NB = num_blocks)
+ * Token t of sequence b goes to position pos[b]+t.  A position beyond the table or a block
+ * id outside [0,num_blocks) skips that token and sets a device error bit.  seq_lens is not
+ * touched (the caller advances it), so a call can be repeated.  n == 0 or B == 0 is a
+ * no-op. */
+gva_status gva_cache_append(gva_ctx* ctx, int B, int n, const void* v_new, const void* kr_new,
+                            const int32_t* pos, const int32_t* block_table, int max_blocks,
+                            int num_blocks, void* v_pool, void* kr_pool, gva_stream_t stream);
+
+/* Bytes of workspace gva_decode_attention needs for this batch (partial softmax states of
+ * the split-T plan).  max_seq_len is the host's upper bound on seq_lens.  Depends on the
+ * context's split option, so query it after gva_set_split_tokens. */
+size_t gva_decode_workspace_size(const gva_ctx* ctx, int B, int max_seq_len);
+
+/* gva_decode_attention -- decode attention over the compact cache.
+ * For each b and head h with g = g(h) and T = seq_lens[b]:
+ *   s_j = scale * (q_abs[b,h,:] . V[g] at position j  +  q_rot[b,h,:] . k_r at position j)
+ *   out[b,h,:] = sum_{j<T} softmax(s)_j  V[g] at position j
+ * (summary section 方法: content score as one inner product with the stored value, output
+ * the value-weighted sum; review section 3: positional score from the shared rotated key.)
+ * Split-T flash decoding: the context of each sequence is cut into chunks of
+ * whole 64-token blocks, each chunk yields a partial (max, sum, weighted sum) in the
+ * workspace, and a combine pass merges them.
+ *   q_abs [B,H,d_v] f32, q_rot [B,H,d_r] f32 (NULL when d_r == 0)
+ *   seq_lens [B] int32 (device), each in [1, max_seq_len]
+ *   out [B,H,d_v] f32
+ *   workspace: device scratch of at least gva_decode_workspace_size(ctx, B, max_seq_len)
+ *   bytes, 16-byte aligned; its contents are not needed between calls.
+ * fp32 accumulation for every cache dtype. */
+gva_status gva_decode_attention(gva_ctx* ctx, int B, const float* q_abs, const float* q_rot,
+                                const void* v_pool, const void* kr_pool,
+                                const int32_t* block_table, int max_blocks, int num_blocks,
+                                const int32_t* seq_lens, int max_seq_len, float* out,
+                                void* workspace, size_t ws_bytes, gva_stream_t stream);
+
+/* gqa_decode_attention -- the matching grouped-query attention decode, built with the same
+ * tiling and pools so that the cost of a key cache can be timed beside GVA (GQA explainer,
+ * section "一次 GQA 计算如何展开": grouped keys and values, head h reads group g(h)).
+ * Uses the context's H, G, d_v (= head width d), cache dtype and scale; the context must
+ * have d_r == 0 (so the default scale is 1/sqrt(d_n)).
+ *   q [B,H,d] f32 (already rotated), k_pool and v_pool [NB][G][64][d] cache dtype.
+ * Workspace as for gva_decode_attention. */
+gva_status gqa_decode_attention(gva_ctx* ctx, int B, const float* q, const void* k_pool,
+                                const void* v_pool, const int32_t* block_table, int max_blocks,
+                                int num_blocks, const int32_t* seq_lens, int max_seq_len,
+                                float* out, void* workspace, size_t ws_bytes,
+                                gva_stream_t stream);
+
+/* Decode options.  split_tokens: context chunk length per partial, a multiple of 64
+ * (0 = automatic plan from B, max_seq_len and the SM count).  path: kernel family. */
+gva_status gva_set_split_tokens(gva_ctx* ctx, int split_tokens);
+gva_status gva_set_decode_path(gva_ctx* ctx, gva_decode_path path);
+
+/* Chunk length (tokens) and partial count per sequence the next decode call will use for
+ * this batch shape, so a caller can predict the workspace and the combine work. */
+gva_status gva_decode_plan(const gva_ctx* ctx, int B, int max_seq_len, int* split_tokens,
+                           int* max_splits);
+
+/* Synchronises the device, reads the device error word into *bits and clears it.
+ * Returns GVA_ERR_DEVICE_INDEX if any bit was set, GVA_OK if none, GVA_ERR_CUDA if the
+ * copy failed. */
+gva_status gva_get_device_error(gva_ctx* ctx, unsigned* bits);
+
+/* Static description of a status code. */
+const char* gva_status_string(gva_status status);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int gva_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GVA_H_ */
