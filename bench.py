@@ -101,8 +101,61 @@ def whole_job(per_rank_units, ws, seconds):
 
 # ----------------------------------------------------------------------------- clocks
 
+class SmiClockSampler:
+    """Fallback sampler: polls nvidia-smi (SM clock, max clock, active event-reason bits)."""
+
+    def __init__(self, period_ms=20):
+        import subprocess
+        self.subprocess = subprocess
+        self.period_ms = period_ms
+        self.samples = []
+        self.max_mhz = None
+        self.proc = None
+        try:
+            self.dev = "GPU-" + str(torch.cuda.get_device_properties(torch.cuda.current_device()).uuid).replace(
+                "GPU-", "")
+        except Exception:
+            self.dev = str(torch.cuda.current_device())
+        self.ok = True
+        self.err = ""
+
+    def __enter__(self):
+        try:
+            self.proc = self.subprocess.Popen(
+                ["nvidia-smi", "-i", self.dev, "--query-gpu=clocks.sm,clocks.max.sm,clocks_event_reasons.active",
+                 "--format=csv,noheader,nounits", "-lms", str(self.period_ms)],
+                stdout=self.subprocess.PIPE, stderr=self.subprocess.DEVNULL, text=True)
+        except Exception as e:
+            self.ok, self.err = False, repr(e)
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        for line in out.splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            try:
+                sm, mx = int(parts[0]), int(parts[1])
+                reasons = int(parts[2], 16) if parts[2].startswith("0x") else int(parts[2])
+            except Exception:
+                continue
+            self.max_mhz = mx
+            self.samples.append((sm, reasons))
+
+    summary = None  # set below
+
+
 class ClockSampler:
     """Samples SM clock and clock-event reasons through NVML while the timed region runs."""
+
+    def __new__(cls, period_s=0.01):
+        try:
+            import pynvml  # noqa: F401
+        except ImportError:
+            return SmiClockSampler()
+        return super().__new__(cls)
 
     def __init__(self, period_s=0.01):
         self.period = period_s
@@ -153,7 +206,7 @@ class ClockSampler:
 
     def summary(self):
         if not self.ok:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "note": "NVML unavailable"}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "note": "NVML unavailable: " + self.err}
         if not self.samples:
             return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": [], "samples": 0}
         mhz = sorted(s for s, _ in self.samples)
@@ -163,6 +216,9 @@ class ClockSampler:
         names = [n for b, n in NVML_REASONS.items() if bits & b and n != "gpu_idle"]
         return {"sm_mhz": mhz[len(mhz) // 2], "sm_max_mhz": self.max_mhz, "reasons": names,
                 "samples": len(self.samples)}
+
+
+SmiClockSampler.summary = ClockSampler.summary
 
 
 # ----------------------------------------------------------------------------- workload

@@ -25,8 +25,9 @@ struct AbsorbArgs {
   const float* M;
   float* q_abs;
   float* q_rot;
+  const double2* rope;
+  unsigned* err;
   int B, H, d_v, d_n, d_r;
-  double base;
 };
 
 __global__ void __launch_bounds__(kAbsorbThreads) absorb_kernel(const AbsorbArgs a) {
@@ -64,14 +65,18 @@ __global__ void __launch_bounds__(kAbsorbThreads) absorb_kernel(const AbsorbArgs
       if (bt < nb) a.q_abs[(static_cast<long long>(b0 + bt) * a.H + h) * a.d_v + i] = acc[bt];
   }
 
-  // Positional slice of the query, rotated at pos_q[b] (fp64 angle, sin, cos).
+  // Positional slice of the query, rotated at pos_q[b] in fp64 (digit-table rotation).
   const int pairs = a.d_r / 2;
   for (int idx = threadIdx.x; idx < nb * pairs; idx += kAbsorbThreads) {
     const int bt = idx / pairs, i = idx - bt * pairs;
     const long long row = (static_cast<long long>(b0 + bt) * a.H + h) * a.d_r;
     const double x0 = a.q_r[row + 2 * i], x1 = a.q_r[row + 2 * i + 1];
-    double s, c;
-    sincos(rope_angle(a.pos_q[b0 + bt], i, a.d_r, a.base), &s, &c);
+    const long long p = a.pos_q[b0 + bt];
+    double c = 1.0, s = 0.0;
+    if (p >= 0)
+      rope_cos_sin(a.rope, pairs, p, i, c, s);
+    else if (i == 0)
+      flag_error(a.err, GVA_DEVERR_POSITION);  // left unrotated
     a.q_rot[row + 2 * i] = __double2float_rn(__dsub_rn(__dmul_rn(x0, c), __dmul_rn(x1, s)));
     a.q_rot[row + 2 * i + 1] = __double2float_rn(__dadd_rn(__dmul_rn(x0, s), __dmul_rn(x1, c)));
   }
@@ -94,7 +99,8 @@ cudaError_t launch_absorb(const gva_ctx* ctx, int B, const float* q_c, const flo
   a.d_v = ctx->dims.d_v;
   a.d_n = ctx->dims.d_n;
   a.d_r = ctx->dims.d_r;
-  a.base = ctx->rope_base;
+  a.rope = ctx->d_rope;
+  a.err = ctx->d_err;
   const size_t smem = sizeof(float) * kAbsorbSeqs * a.d_n;
   if (smem > 48 * 1024) {
     cudaError_t e =

@@ -20,6 +20,27 @@ int elem_bytes(gva_dtype t) { return t == GVA_F32 ? 4 : 2; }
 
 gva_status from_cuda(cudaError_t e) { return e == cudaSuccess ? GVA_OK : GVA_ERR_CUDA; }
 
+// RoPE digit table: entry (k, dgt, i) holds cos and sin of dgt * 256^k * theta_i,
+// theta_i = base^(-2i/d_r), in fp64 (pairs (2i, 2i+1) turned by position * theta_i).
+bool build_rope_table(gva_ctx* ctx) {
+  const int pairs = ctx->dims.d_r / 2;
+  if (pairs == 0) return true;
+  const size_t n = static_cast<size_t>(4) * 256 * pairs;
+  double2* host = static_cast<double2*>(malloc(n * sizeof(double2)));
+  if (!host) return false;
+  for (int k = 0; k < 4; ++k)
+    for (int dgt = 0; dgt < 256; ++dgt)
+      for (int i = 0; i < pairs; ++i) {
+        const double theta = pow(ctx->rope_base, -2.0 * i / static_cast<double>(ctx->dims.d_r));
+        const double a = ldexp(static_cast<double>(dgt), 8 * k) * theta;
+        host[(static_cast<size_t>(k) * 256 + dgt) * pairs + i] = make_double2(cos(a), sin(a));
+      }
+  bool ok = cudaMalloc(reinterpret_cast<void**>(&ctx->d_rope), n * sizeof(double2)) == cudaSuccess &&
+            cudaMemcpy(ctx->d_rope, host, n * sizeof(double2), cudaMemcpyHostToDevice) == cudaSuccess;
+  free(host);
+  return ok;
+}
+
 // Which decode kernel family runs for these dims.
 int choose_path(const gva_ctx* ctx, bool sep_k) {
   const bool mma_ok = gva::mma_supported(ctx->dims, sep_k);
@@ -53,6 +74,7 @@ bool make_plan(const gva_ctx* ctx, int B, int max_seq_len, bool sep_k, gva::Plan
   }
   if (chunk > nt_max) chunk = nt_max;
   if (chunk < 1) chunk = 1;
+  if ((nt_max + chunk - 1) / chunk > 65535) chunk = (nt_max + 65534) / 65535;  // grid extent
   plan->path = path;
   plan->chunk_tiles = chunk;
   plan->n_chunks = (nt_max + chunk - 1) / chunk;
@@ -81,6 +103,9 @@ gva_status decode_common(gva_ctx* ctx, bool sep_k, int B, const float* q_abs, co
   if (!on_ctx_device(ctx)) return GVA_ERR_INVALID_ARG;
   gva::Plan plan;
   if (!make_plan(ctx, B, max_seq_len, sep_k, &plan)) return GVA_ERR_UNSUPPORTED;
+  if (plan.path == GVA_PATH_MMA &&
+      static_cast<long long>(num_blocks) * d.G * GVA_BLOCK_TOKENS >= (1LL << 31))
+    return GVA_ERR_UNSUPPORTED;  // token rows are int32 tensor-copy coordinates
   if (!workspace || ws_bytes < plan.ws_bytes || !aligned16(workspace)) return GVA_ERR_WORKSPACE;
 
   gva::DecodeArgs a;
@@ -136,12 +161,11 @@ gva_status gva_create(const gva_dims* dims, gva_ctx** out) {
   if (cudaGetDevice(&ctx->device) != cudaSuccess ||
       cudaDeviceGetAttribute(&ctx->num_sms, cudaDevAttrMultiProcessorCount, ctx->device) != cudaSuccess ||
       cudaMalloc(reinterpret_cast<void**>(&ctx->d_err), sizeof(unsigned)) != cudaSuccess) {
-    free(ctx);
+    gva_destroy(ctx);
     return GVA_ERR_CUDA;
   }
-  if (cudaMemset(ctx->d_err, 0, sizeof(unsigned)) != cudaSuccess) {
-    cudaFree(ctx->d_err);
-    free(ctx);
+  if (cudaMemset(ctx->d_err, 0, sizeof(unsigned)) != cudaSuccess || !build_rope_table(ctx)) {
+    gva_destroy(ctx);
     return GVA_ERR_CUDA;
   }
   *out = ctx;
@@ -151,6 +175,7 @@ gva_status gva_create(const gva_dims* dims, gva_ctx** out) {
 void gva_destroy(gva_ctx* ctx) {
   if (!ctx) return;
   if (ctx->d_err) cudaFree(ctx->d_err);
+  if (ctx->d_rope) cudaFree(ctx->d_rope);
   free(ctx);
 }
 

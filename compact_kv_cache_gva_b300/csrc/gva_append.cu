@@ -19,9 +19,9 @@ struct AppendArgs {
   const int32_t* block_table;
   void* v_pool;
   void* kr_pool;
+  const double2* rope;
   unsigned* err;
   int B, n, G, d_v, d_r, max_blocks, num_blocks;
-  double base;
 };
 
 constexpr int kAppendThreads = 256;
@@ -38,7 +38,7 @@ __global__ void __launch_bounds__(kAppendThreads) append_kernel(const AppendArgs
   const long long p = static_cast<long long>(a.pos[b]) + t;
 
   // Resolve the slot; an unresolvable one skips the token and is reported.
-  if (p < 0 || (p >> 6) >= a.max_blocks) {
+  if (p < 0 || (p >> 6) >= a.max_blocks || p >= (1LL << 32)) {
     if (lane == 0) flag_error(a.err, GVA_DEVERR_POSITION);
     return;
   }
@@ -70,8 +70,8 @@ __global__ void __launch_bounds__(kAppendThreads) append_kernel(const AppendArgs
   for (int i = lane; i < a.d_r / 2; i += 32) {
     const double x0 = CacheElem<T>::to_double(x[2 * i]);
     const double x1 = CacheElem<T>::to_double(x[2 * i + 1]);
-    double s, c;
-    sincos(rope_angle(p, i, a.d_r, a.base), &s, &c);
+    double c, s;
+    rope_cos_sin(a.rope, a.d_r / 2, p, i, c, s);
     // explicit roundings (no contraction) so each product is rounded on its own
     const double y0 = __dsub_rn(__dmul_rn(x0, c), __dmul_rn(x1, s));
     const double y1 = __dadd_rn(__dmul_rn(x0, s), __dmul_rn(x1, c));
@@ -101,7 +101,7 @@ cudaError_t launch_append(const gva_ctx* ctx, int B, int n, const void* v_new,
   a.d_r = ctx->dims.d_r;
   a.max_blocks = max_blocks;
   a.num_blocks = num_blocks;
-  a.base = ctx->rope_base;
+  a.rope = ctx->d_rope;
   const long long threads = static_cast<long long>(B) * n * 32;
   const unsigned grid = static_cast<unsigned>((threads + kAppendThreads - 1) / kAppendThreads);
   if (ctx->dims.cache_dtype == GVA_F32)

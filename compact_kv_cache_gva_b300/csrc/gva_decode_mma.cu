@@ -1,13 +1,519 @@
-// gva_decode_mma.cu -- tensor-core decode path (bf16 cache).  Not built yet: every shape
-// reports unsupported, so the CUDA-core path runs.
+// gva_decode_mma.cu -- split-T decode attention over a bf16 GVA cache on the tensor cores.
+//
+// Same contract and partial records as the CUDA-core kernel (gva_decode_fma.cu): for head h
+// of value group g, s_j = scale * (q'_h . v_j + q~_r,h . k_r,j), online softmax, o_h =
+// sum_j p_j v_j (ai-feeds.com summary "Grouped Value Attention:通过按需 key 重建实现高效 KV
+// 缓存", section 方法; review "[논문리뷰] Grouped Value Attention", section 3).
+//
+// Per 64-token tile of group g, with the r = H/G heads of the group packed into the N=8
+// columns of a warp-level bf16 MMA (m16n8k16 / m16n8k8, fp32 accumulate):
+//   scores  S^T[64 tok x 8] = [V | k_r][64 x (d_v+d_r)] . [q'_hi | q'_lo]^T
+//   output  O^T[d_v x 8]   += V^T[d_v x 64] . [p_hi | p_lo][64 x 8]
+// Each head occupies two columns: its query (and later its probabilities) split into a
+// bf16 high part and a bf16 remainder, so both products keep about 16 significant bits
+// while using columns that the 4-head group would leave empty anyway.  The V tile arrives
+// by TMA (tensor copy, 128-byte swizzle) so that ldmatrix reads it without bank conflicts,
+// both as V (scores) and transposed as V^T (output); k_r arrives by a plain bulk copy.
+// Probabilities never leave registers: movmatrix turns the score fragment (tokens on rows)
+// into the B fragment of the output product (tokens on k).  Each of the 4 warps owns every
+// 4th tile of the CTA's chunk through a private ring; warps merge at the end.
+#include <cuda.h>
+#include <math.h>
+
 #include "gva_device.cuh"
 #include "gva_internal.h"
 
 namespace gva {
+namespace {
 
-bool mma_supported(const gva_dims&, bool) { return false; }
-int mma_ctas_per_sm(const gva_dims&, bool) { return 1; }
-int mma_tiles_per_cta_unit(const gva_dims&) { return 4; }
-cudaError_t launch_decode_mma(const DecodeArgs&, bool, cudaStream_t) { return cudaErrorNotSupported; }
+constexpr int kMmaWarps = 4;
+constexpr int kMmaThreads = 32 * kMmaWarps;
+constexpr int kSubTileBytes = kBlockTokens * 128;  // one [64 tokens][64 columns] bf16 swizzled box
+
+// ---- PTX wrappers ------------------------------------------------------------------------
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x2(uint32_t addr, uint32_t& r0, uint32_t& r1) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0, %1}, [%2];"
+               : "=r"(r0), "=r"(r1)
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void mma_16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
+                                          uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+      "{%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void mma_1688(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t b0) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k8.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5}, {%6}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(b0));
+}
+
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+
+// Packs two floats as bf16 (first in the low half).
+__device__ __forceinline__ uint32_t pack_bf16(float lo_half, float hi_half) {
+  const uint32_t a = __bfloat16_as_ushort(__float2bfloat16_rn(lo_half));
+  const uint32_t b = __bfloat16_as_ushort(__float2bfloat16_rn(hi_half));
+  return a | (b << 16);
+}
+
+// x = hi + lo with hi = bf16(x) and lo = bf16(x - hi); returns (hi, lo) packed.
+__device__ __forceinline__ uint32_t split_pack(float x) {
+  const __nv_bfloat16 hi = __float2bfloat16_rn(x);
+  const __nv_bfloat16 lo = __float2bfloat16_rn(x - __bfloat162float(hi));
+  return static_cast<uint32_t>(__bfloat16_as_ushort(hi)) |
+         (static_cast<uint32_t>(__bfloat16_as_ushort(lo)) << 16);
+}
+
+__device__ __forceinline__ float split_part(float x, int part) {
+  const __nv_bfloat16 hi = __float2bfloat16_rn(x);
+  return part == 0 ? __bfloat162float(hi) : x - __bfloat162float(hi);
+}
+
+// Zeroes the bf16 halves of a fragment register whose token index is >= nv.
+__device__ __forceinline__ uint32_t mask_pair(uint32_t v, int tok, int nv) {
+  const uint32_t lo = tok < nv ? 0x0000ffffu : 0u;
+  const uint32_t hi = tok + 1 < nv ? 0xffff0000u : 0u;
+  return v & (lo | hi);
+}
+
+template <int DV, int DR>
+struct MmaLayout {
+  static constexpr int kSub = DV / 64;                          // 64-column swizzled boxes
+  static constexpr int kVBytes = kSub * kSubTileBytes;
+  static constexpr int kKrBytes = kBlockTokens * DR * 2;
+  static constexpr int kStage = kVBytes + ((kKrBytes + 1023) / 1024) * 1024;
+};
+
+template <int DV, int DR, int R, int NST>
+__global__ void __launch_bounds__(kMmaThreads) decode_mma_kernel(const DecodeArgs a,
+                                                                 const __grid_constant__ CUtensorMap tmv) {
+  using L = MmaLayout<DV, DR>;
+  constexpr int NT = (2 * R + 7) / 8;  // n-tiles of 8 columns (4 heads each)
+  constexpr int KSV = DV / 16;         // k16 steps over the value columns
+  constexpr int KSR = DR / 16;         // k16 steps over the positional columns
+  constexpr bool KR8 = (DR % 16) != 0;  // one trailing k8 step
+  constexpr int MD = DV / 16;          // m16 tiles over d_v in the output product
+  static_assert(DR % 8 == 0, "positional width must be a multiple of 8 on this path");
+
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  // 1 KB header (mbarriers), then the 1 KB-aligned rings (swizzled boxes need that alignment)
+  unsigned char* smem = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int gid = lane >> 2, tq = lane & 3;
+  const int g = blockIdx.x, c = blockIdx.y, b = blockIdx.z;
+
+  const int T_b = a.seq_lens[b];
+  if (T_b <= 0 || T_b > a.max_seq_len) {
+    if (c == 0 && g == 0 && threadIdx.x == 0) flag_error(a.err, GVA_DEVERR_SEQ_LEN);
+    return;
+  }
+  const int nt_b = (T_b + kBlockTokens - 1) / kBlockTokens;
+  const int t0 = c * a.chunk_tiles;
+  if (t0 >= nt_b) return;
+  const int t1 = min(nt_b, t0 + a.chunk_tiles);
+
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem) + warp * NST;
+  unsigned char* ring = smem + 1024 + warp * NST * L::kStage;
+
+  // ---- query fragments (B operand of the score product), pre-scaled by scale*log2(e) ----
+  // column n = 2*head + part; part 0 = bf16(q), part 1 = bf16 remainder.
+  const int h0 = g * R;
+  uint32_t qb[NT][KSV + KSR][2];
+  uint32_t qt[NT];
+  {
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const int head = nt * 4 + (gid >> 1), part = gid & 1;
+      const bool valid = head < R;
+      const long long row = static_cast<long long>(b) * a.H + h0 + (valid ? head : 0);
+      const float* qa = a.q_abs + row * DV;
+      const float* qr = a.q_rot + row * DR;
+      auto qv = [&](int k) -> float {
+        if (!valid) return 0.f;
+        const float x = (k < DV ? qa[k] : qr[k - DV]) * a.scale_log2;
+        return split_part(x, part);
+      };
+#pragma unroll
+      for (int ks = 0; ks < KSV + KSR; ++ks) {
+        const int k0 = 16 * ks + 2 * tq;
+        qb[nt][ks][0] = pack_bf16(qv(k0), qv(k0 + 1));
+        qb[nt][ks][1] = pack_bf16(qv(k0 + 8), qv(k0 + 9));
+      }
+      if (KR8) {
+        const int k0 = 16 * (KSV + KSR) + 2 * tq;
+        qt[nt] = pack_bf16(qv(k0), qv(k0 + 1));
+      }
+    }
+  }
+
+  const int n_my = (t0 + warp < t1) ? (t1 - t0 - warp + kMmaWarps - 1) / kMmaWarps : 0;
+  if (lane == 0) {
+    for (int s = 0; s < NST; ++s) mbar_init(&bars[s], 1);
+    mbar_init_fence();
+  }
+  __syncwarp();
+
+  auto block_id = [&](int t) -> int {
+    if (t >= a.max_blocks) return -1;
+    const int blk = a.block_table[static_cast<long long>(b) * a.max_blocks + t];
+    return (blk >= 0 && blk < a.num_blocks) ? blk : -1;
+  };
+  auto issue = [&](int k) {  // lane 0 only
+    const int s = k % NST;
+    const int t = t0 + warp + k * kMmaWarps;
+    const int blk = block_id(t);
+    if (blk < 0) {
+      flag_error(a.err, t >= a.max_blocks ? GVA_DEVERR_POSITION : GVA_DEVERR_BLOCK_ID);
+      mbar_arrive(&bars[s]);
+      return;
+    }
+    unsigned char* st = ring + s * L::kStage;
+    mbar_arrive_expect_tx(&bars[s], L::kVBytes + L::kKrBytes);
+    const int y = (blk * a.G + g) * kBlockTokens;
+#pragma unroll
+    for (int sub = 0; sub < L::kSub; ++sub) tma_load_2d(st + sub * kSubTileBytes, &tmv, 64 * sub, y, &bars[s]);
+    if (DR > 0)
+      bulk_g2s(st + L::kVBytes,
+               static_cast<const __nv_bfloat16*>(a.kr_pool) + static_cast<size_t>(blk) * kBlockTokens * DR,
+               L::kKrBytes, &bars[s]);
+  };
+  if (lane == 0)
+    for (int k = 0; k < min(NST, n_my); ++k) issue(k);
+
+  float m[NT], l[NT], o[NT][MD][4];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    m[nt] = -INFINITY;
+    l[nt] = 0.f;
+#pragma unroll
+    for (int md = 0; md < MD; ++md)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) o[nt][md][e] = 0.f;
+  }
+
+  // lane-dependent parts of the ldmatrix addresses
+  const int ld_row = (lane & 7) + ((lane >> 3) & 1) * 8;  // non-transposed: row within m16
+  const int ld_kc = lane >> 4;                             // non-transposed: 8-column chunk
+  const int tr_tok = (lane & 7) + ((lane >> 4) & 1) * 8;   // transposed: token within k16
+  const int tr_dc = (lane >> 3) & 1;                       // transposed: 8-column chunk
+
+  int k = 0;
+  bool ok = true;
+  for (; k < n_my; ++k) {
+    const int s = k % NST;
+    const bool got = mbar_wait_bounded(&bars[s], (k / NST) & 1);
+    if (!__all_sync(kFullMask, got)) {
+      ok = false;
+      break;
+    }
+    const int t = t0 + warp + k * kMmaWarps;
+    if (block_id(t) >= 0) {
+      const uint32_t vbase = smem_addr(ring + s * L::kStage);
+      const uint32_t krbase = vbase + L::kVBytes;
+      const int nv = min(kBlockTokens, T_b - t * kBlockTokens);
+
+      // scores
+      float sc[NT][4][4];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int mt = 0; mt < 4; ++mt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) sc[nt][mt][e] = 0.f;
+#pragma unroll
+      for (int mt = 0; mt < 4; ++mt) {
+        const int row = 16 * mt + ld_row;
+#pragma unroll
+        for (int ks = 0; ks < KSV; ++ks) {
+          const int kc = 2 * ks + ld_kc;
+          const uint32_t addr = vbase + (kc >> 3) * kSubTileBytes + row * 128 + (((kc & 7) ^ (row & 7)) << 4);
+          uint32_t af[4];
+          ldsm_x4(addr, af);
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) mma_16816(sc[nt][mt], af, qb[nt][ks][0], qb[nt][ks][1]);
+        }
+#pragma unroll
+        for (int ks = 0; ks < KSR; ++ks) {
+          uint32_t af[4];
+          ldsm_x4(krbase + row * (2 * DR) + (2 * ks + ld_kc) * 16, af);
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) mma_16816(sc[nt][mt], af, qb[nt][KSV + ks][0], qb[nt][KSV + ks][1]);
+        }
+        if (KR8) {
+          uint32_t a0, a1;
+          ldsm_x2(krbase + row * (2 * DR) + (2 * KSR) * 16, a0, a1);
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) mma_1688(sc[nt][mt], a0, a1, qt[nt]);
+        }
+      }
+
+      // online softmax (log2 domain); thread holds head (nt*4 + tq) for tokens
+      // 16*mt + gid and 16*mt + gid + 8
+      uint32_t pb[NT][4][2];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        float sv[4][2];
+        float mx = -INFINITY;
+#pragma unroll
+        for (int mt = 0; mt < 4; ++mt) {
+          const int j0 = 16 * mt + gid;
+          sv[mt][0] = j0 < nv ? sc[nt][mt][0] + sc[nt][mt][1] : -INFINITY;
+          sv[mt][1] = j0 + 8 < nv ? sc[nt][mt][2] + sc[nt][mt][3] : -INFINITY;
+          mx = fmaxf(mx, fmaxf(sv[mt][0], sv[mt][1]));
+        }
+        mx = fmaxf(mx, __shfl_xor_sync(kFullMask, mx, 4));
+        mx = fmaxf(mx, __shfl_xor_sync(kFullMask, mx, 8));
+        mx = fmaxf(mx, __shfl_xor_sync(kFullMask, mx, 16));
+        const float mn = fmaxf(m[nt], mx);
+        const float alpha = exp2f(m[nt] - mn);
+        m[nt] = mn;
+        float ps = 0.f;
+#pragma unroll
+        for (int mt = 0; mt < 4; ++mt) {
+          const float p0 = exp2f(sv[mt][0] - mn);
+          const float p1 = exp2f(sv[mt][1] - mn);
+          ps += p0 + p1;
+          pb[nt][mt][0] = movmatrix_trans(split_pack(p0));
+          pb[nt][mt][1] = movmatrix_trans(split_pack(p1));
+        }
+        l[nt] = fmaf(l[nt], alpha, ps);
+#pragma unroll
+        for (int md = 0; md < MD; ++md)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) o[nt][md][e] *= alpha;
+      }
+
+      // output: O^T[d x n] += V^T[d x tok] P[tok x n]
+#pragma unroll
+      for (int kt = 0; kt < 4; ++kt) {
+        const int tok = 16 * kt + tr_tok;
+        const int jt = 16 * kt + 2 * tq;  // tokens of this thread's A-fragment halves
+#pragma unroll
+        for (int md = 0; md < MD; ++md) {
+          const int dc = 2 * md + tr_dc;
+          const uint32_t addr = vbase + (dc >> 3) * kSubTileBytes + tok * 128 + (((dc & 7) ^ (tok & 7)) << 4);
+          uint32_t af[4];
+          ldsm_x4_trans(addr, af);
+          if (nv < kBlockTokens) {  // slots past the context may hold anything: zero them
+            af[0] = mask_pair(af[0], jt, nv);
+            af[1] = mask_pair(af[1], jt, nv);
+            af[2] = mask_pair(af[2], jt + 8, nv);
+            af[3] = mask_pair(af[3], jt + 8, nv);
+          }
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) mma_16816(o[nt][md], af, pb[nt][kt][0], pb[nt][kt][1]);
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0 && k + NST < n_my) {
+      fence_proxy_async_smem();
+      issue(k + NST);
+    }
+  }
+  if (!ok) {
+    if (lane == 0) flag_error(a.err, GVA_DEVERR_TIMEOUT);
+    for (int kk = k; kk < min(n_my, k + NST); ++kk) mbar_wait_bounded(&bars[kk % NST], (kk / NST) & 1);
+    __syncwarp();
+  }
+
+  // finish this warp's state: sum over the 8 lanes sharing a head, fold hi/lo columns
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    l[nt] += __shfl_xor_sync(kFullMask, l[nt], 4);
+    l[nt] += __shfl_xor_sync(kFullMask, l[nt], 8);
+    l[nt] += __shfl_xor_sync(kFullMask, l[nt], 16);
+  }
+  constexpr int kRec = DV + 4;
+  float* mine = reinterpret_cast<float*>(ring);
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    const int head = nt * 4 + tq;
+    if (head < R) {
+      if (gid == 0) {
+        mine[head * kRec] = m[nt];
+        mine[head * kRec + 1] = l[nt];
+      }
+#pragma unroll
+      for (int md = 0; md < MD; ++md) {
+        mine[head * kRec + 4 + 16 * md + gid] = o[nt][md][0] + o[nt][md][1];
+        mine[head * kRec + 4 + 16 * md + gid + 8] = o[nt][md][2] + o[nt][md][3];
+      }
+    }
+  }
+  __syncthreads();
+  const size_t rec_stride = partial_stride_floats(DV);
+  for (int idx = threadIdx.x; idx < R * DV; idx += kMmaThreads) {
+    const int h = idx / DV, d = idx - h * DV;
+    float Mx = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kMmaWarps; ++w)
+      Mx = fmaxf(Mx, reinterpret_cast<const float*>(smem + 1024 + w * NST * L::kStage)[h * kRec]);
+    float Ls = 0.f, Os = 0.f;
+    if (Mx != -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < kMmaWarps; ++w) {
+        const float* ws = reinterpret_cast<const float*>(smem + 1024 + w * NST * L::kStage) + h * kRec;
+        if (ws[0] == -INFINITY) continue;  // a warp without tiles
+        const float sc = exp2f(ws[0] - Mx);
+        Ls = fmaf(sc, ws[1], Ls);
+        Os = fmaf(sc, ws[4 + d], Os);
+      }
+    }
+    float* rec = a.part + ((static_cast<size_t>(b) * a.n_chunks + c) * a.H + h0 + h) * rec_stride;
+    if (d == 0) {
+      rec[0] = Mx;
+      rec[1] = Ls;
+    }
+    rec[4 + d] = Os;
+  }
+}
+
+constexpr int kMmaStages = 2;
+
+template <int DV, int DR>
+constexpr int mma_smem_bytes() {
+  return 2048 + kMmaWarps * kMmaStages * MmaLayout<DV, DR>::kStage;  // header + alignment slack
+}
+
+template <int DV, int DR, int R>
+cudaError_t launch_mma_t(const DecodeArgs& a, const CUtensorMap& map, cudaStream_t stream) {
+  constexpr int smem = mma_smem_bytes<DV, DR>();
+  static int configured[kMaxDevices] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= kMaxDevices || !configured[dev]) {
+    e = cudaFuncSetAttribute(decode_mma_kernel<DV, DR, R, kMmaStages>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    if (dev < kMaxDevices) configured[dev] = 1;
+  }
+  dim3 grid(a.G, a.n_chunks, a.B);
+  decode_mma_kernel<DV, DR, R, kMmaStages><<<grid, kMmaThreads, smem, stream>>>(a, map);
+  return cudaGetLastError();
+}
+
+template <int DV, int DR>
+cudaError_t dispatch_r(const DecodeArgs& a, const CUtensorMap& map, cudaStream_t stream) {
+  switch (a.H / a.G) {
+    case 1: return launch_mma_t<DV, DR, 1>(a, map, stream);
+    case 2: return launch_mma_t<DV, DR, 2>(a, map, stream);
+    case 4: return launch_mma_t<DV, DR, 4>(a, map, stream);
+    case 8: return launch_mma_t<DV, DR, 8>(a, map, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+template <int DV>
+cudaError_t dispatch_dr(const DecodeArgs& a, const CUtensorMap& map, cudaStream_t stream) {
+  switch (a.d_r) {
+    case 0: return dispatch_r<DV, 0>(a, map, stream);
+    case 8: return dispatch_r<DV, 8>(a, map, stream);
+    case 16: return dispatch_r<DV, 16>(a, map, stream);
+    case 24: return dispatch_r<DV, 24>(a, map, stream);
+    case 32: return dispatch_r<DV, 32>(a, map, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no libcuda link).
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+// The value pool seen as a 2-D bf16 tensor: rows = NB*G*64 token rows of d_v columns; one
+// box = 64 columns x 64 rows, swizzled in 128-byte rows.
+bool make_value_map(CUtensorMap* map, const void* v_pool, int num_blocks, int G, int d_v) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(d_v),
+                              static_cast<cuuint64_t>(num_blocks) * G * kBlockTokens};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(d_v) * 2};
+  const cuuint32_t box[2] = {64, kBlockTokens};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(v_pool), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+bool mma_supported(const gva_dims& d, bool sep_k) {
+  if (sep_k) return false;  // the matching GQA form runs on the CUDA-core kernel
+  if (d.cache_dtype != GVA_BF16) return false;
+  if (!(d.d_v == 64 || d.d_v == 128)) return false;
+  if (!(d.d_r == 0 || d.d_r == 8 || d.d_r == 16 || d.d_r == 24 || d.d_r == 32)) return false;
+  const int r = d.H / d.G;
+  return r == 1 || r == 2 || r == 4 || r == 8;
+}
+
+int mma_ctas_per_sm(const gva_dims& d, bool) {
+  const int stage = (d.d_v / 64) * kSubTileBytes + ((kBlockTokens * d.d_r * 2 + 1023) / 1024) * 1024;
+  const int smem = 2048 + kMmaWarps * kMmaStages * stage;
+  int per_sm = (228 * 1024) / (smem + 1024);
+  return per_sm < 1 ? 1 : per_sm;
+}
+
+int mma_tiles_per_cta_unit(const gva_dims&) { return kMmaWarps; }
+
+cudaError_t launch_decode_mma(const DecodeArgs& a, bool sep_k, cudaStream_t stream) {
+  if (sep_k) return cudaErrorNotSupported;
+  CUtensorMap map;
+  if (!make_value_map(&map, a.v_pool, a.num_blocks, a.G, a.d_v)) return cudaErrorInvalidValue;
+  switch (a.d_v) {
+    case 64: return dispatch_dr<64>(a, map, stream);
+    case 128: return dispatch_dr<128>(a, map, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
 
 }  // namespace gva

@@ -143,10 +143,30 @@ struct CacheElem<__nv_bfloat16> {
   static __device__ __forceinline__ float to_float(__nv_bfloat16 v) { return __bfloat162float(v); }
 };
 
-// RoPE angle for pair i of a d_r-wide slice at position p, in fp64:
-// p * base^(-2i/d_r).
-__device__ __forceinline__ double rope_angle(long long p, int i, int d_r, double base) {
-  return static_cast<double>(p) * pow(base, -2.0 * static_cast<double>(i) / static_cast<double>(d_r));
+// RoPE rotation of pair i at position p >= 0: (cos, sin) of p * theta_i, theta_i =
+// base^(-2i/d_r).  The context holds, per 8-bit digit of the position, the fp64 cos/sin of
+// digit * 256^k * theta_i (computed on the host); the angle of p is the sum of its digits'
+// angles, so the rotation is the product of at most four table rotations (fp64 complex
+// products).  No transcendental function runs on the device and every int32 position is
+// covered.  Table layout: [4 levels][256 digits][pairs] of double2 (cos, sin).
+constexpr int kRopeLevels = 4;
+constexpr int kRopeDigits = 256;
+
+__device__ __forceinline__ void rope_cos_sin(const double2* __restrict__ tab, int pairs,
+                                             long long p, int i, double& c, double& s) {
+  c = 1.0;
+  s = 0.0;
+#pragma unroll
+  for (int k = 0; k < kRopeLevels; ++k) {
+    const int dgt = static_cast<int>((p >> (8 * k)) & (kRopeDigits - 1));
+    if (dgt) {
+      const double2 r = tab[(k * kRopeDigits + dgt) * pairs + i];
+      const double c2 = c * r.x - s * r.y;
+      const double s2 = s * r.x + c * r.y;
+      c = c2;
+      s = s2;
+    }
+  }
 }
 
 __device__ __forceinline__ void flag_error(unsigned* err, unsigned bit) {

@@ -15,6 +15,7 @@ struct gva_ctx {
   int device;           // device the context was created on
   int num_sms;          // SM count of that device
   unsigned* d_err;      // device error word
+  double2* d_rope;      // RoPE digit table [4][256][d_r/2] (nullptr when d_r == 0)
   int split_tokens;     // 0 = automatic
   gva_decode_path path;
 };
