@@ -22,6 +22,8 @@ struct gva_ctx {
 
 namespace gva {
 
+constexpr int kMaxDevicesHost = 64;  // per-device host caches (function attributes, addresses)
+
 // Arguments of the decode partial kernels (GVA and the matching GQA form).
 struct DecodeArgs {
   const float* q_abs;        // [B,H,d_v] absorbed query (GQA: the plain query)

@@ -20,8 +20,8 @@
  *   - Pointers are DEVICE pointers unless a parameter says otherwise; they must be
  *     16-byte aligned.  All tensors are dense, row-major, in the shapes given.
  *   - The caller owns every buffer (inputs, outputs, cache pools, block table, workspace).
- *     The library allocates device memory only in gva_create (its error word) and frees it
- *     in gva_destroy; nothing is allocated on the decode path.
+ *     The library allocates device memory only in gva_create (its error word and RoPE
+ *     table) and frees it in gva_destroy; nothing is allocated on the decode path.
  *   - Calls are asynchronous on `stream` (NULL = the legacy default stream).  GVA_OK means
  *     the work was enqueued.  Host-side argument errors return a status and enqueue
  *     nothing.  Index errors that only the device can see (a position past the block
@@ -179,6 +179,33 @@ gva_status gva_set_decode_path(gva_ctx* ctx, gva_decode_path path);
  * this batch shape, so a caller can predict the workspace and the combine work. */
 gva_status gva_decode_plan(const gva_ctx* ctx, int B, int max_seq_len, int* split_tokens,
                            int* max_splits);
+
+/* Bytes of device scratch that gva_decode_attention_noalloc holds on every GPU that loads
+ * this library (4 MiB). */
+#define GVA_NOALLOC_SCRATCH_BYTES (4u << 20)
+
+/* gva_decode_attention_noalloc -- gva_decode_attention for callers that cannot allocate
+ * device memory: an operator inside a host framework that hands it only its inputs and
+ * outputs, an engine that has already given all device memory to its own pools, or a
+ * latency-critical loop that must not call the CUDA allocator (it may synchronise the device
+ * and takes an unbounded time).  The paper has no counterpart to this call: it is a
+ * convenience of this library.
+ * Same arguments, computation and results as gva_decode_attention, without the workspace:
+ * the scratch is a fixed GVA_NOALLOC_SCRATCH_BYTES array that is part of the library's
+ * device image, so it exists on every GPU that loads the library until the process exits.
+ * Nothing is allocated.
+ *   - Batches whose gva_decode_workspace_size() exceeds GVA_NOALLOC_SCRATCH_BYTES are
+ *     rejected with GVA_ERR_WORKSPACE before anything is enqueued.
+ *   - The first call on each device looks up the array's device address (with that device
+ *     current); make that first call before any stream capture.
+ *   - Every call on a device shares the one array, and it keeps the previous call's
+ *     contents.  Calls whose work can overlap on the GPU (different streams without
+ *     ordering between them) race on it and give wrong results; order them on one stream. */
+gva_status gva_decode_attention_noalloc(gva_ctx* ctx, int B, const float* q_abs,
+                                        const float* q_rot, const void* v_pool,
+                                        const void* kr_pool, const int32_t* block_table,
+                                        int max_blocks, int num_blocks, const int32_t* seq_lens,
+                                        int max_seq_len, float* out, gva_stream_t stream);
 
 /* Synchronises the device, reads the device error word into *bits and clears it.
  * Returns GVA_ERR_DEVICE_INDEX if any bit was set, GVA_OK if none, GVA_ERR_CUDA if the
