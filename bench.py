@@ -49,6 +49,7 @@ def parse():
     p.add_argument("--no-gqa", action="store_true")
     p.add_argument("--e2e-steps", type=int, default=200)
     p.add_argument("--cpu-sample-seqs", type=int, default=0, help="sequences in the CPU sample (0 = auto)")
+    p.add_argument("--graph", type=int, default=1, help="replay the step as a captured CUDA graph (1) or launch it (0)")
     return p.parse_args()
 
 
@@ -271,13 +272,47 @@ def flusher():
     return flush
 
 
+def time_steps(run_step, K, flush):
+    """Device seconds for K steps.  Inputs larger than L2: one event pair around the K
+    back-to-back steps.  Otherwise L2 is flushed before every step, outside per-step events."""
+    if flush is None:
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(K):
+            run_step()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / 1e3
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    for a, b in evs:
+        flush()
+        a.record()
+        run_step()
+        b.record()
+    torch.cuda.synchronize()
+    return sum(a.elapsed_time(b) for a, b in evs) / 1e3
+
+
+def capture(fn):
+    """fn's launches captured once into a CUDA graph (after a warm call on the capture stream)."""
+    cap = torch.cuda.Stream()
+    cap.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(cap):
+        fn()
+        cap.synchronize()
+        with torch.cuda.graph(graph, stream=cap):
+            fn()
+    torch.cuda.current_stream().wait_stream(cap)
+    return graph
+
+
 def run_ours(args, rank, ws):
     torch.cuda.init()
     w = synth.WORKLOADS[args.workload]
     S = Setup(w, seed=rank, path=args.path, split_tokens=args.split_tokens)
     need_flush = S.cache_bytes < 2 * L2_BYTES
     flush = flusher() if need_flush else None
-    stream = torch.cuda.current_stream()
 
     for _ in range(max(3, args.warmup)):
         if flush:
@@ -286,24 +321,35 @@ def run_ours(args, rank, ws):
     torch.cuda.synchronize()
     if S.layer.device_error():
         raise RuntimeError("device reported an index error during warm-up")
+    run_step = S.step
+    if args.graph:  # the three C-ABI calls of a step, replayed as one graph
+        run_step = capture(S.step).replay
+        for _ in range(3):
+            run_step()
+        torch.cuda.synchronize()
 
     K = args.steps
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
     barrier(ws)
     torch.cuda.synchronize()
     with ClockSampler() as clocks:
-        for k in range(K):
-            if flush:
-                flush()
-            S.timed_step(evs[k])
-        torch.cuda.synchronize()
+        step_s = time_steps(run_step, K, flush)
     barrier(ws)
-    step_ms = [e[0].elapsed_time(e[3]) for e in evs]
-    dec_ms = [e[2].elapsed_time(e[3]) for e in evs]
-    absorb_ms = [e[0].elapsed_time(e[1]) for e in evs]
-    append_ms = [e[1].elapsed_time(e[2]) for e in evs]
-    total_s = max_over_ranks(sum(step_ms) / 1e3, ws)
-    dec_s = max_over_ranks(sum(dec_ms) / 1e3, ws)
+    total_s = max_over_ranks(step_s, ws)
+
+    # the decode call alone (split-T partial + combine), timed the same way
+    dec_s = max_over_ranks(time_steps(lambda: S.layer.attend(S.inp.v_pool, S.inp.kr_pool, S.inp.block_table,
+                                                             S.inp.seq_lens), K, flush), ws)
+    # per-call breakdown (events between calls; informative only, they stop launch overlap)
+    nb = min(K, 100)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(nb)]
+    for k in range(nb):
+        if flush:
+            flush()
+        S.timed_step(evs[k])
+    torch.cuda.synchronize()
+    br = {name: round(1e3 * sum(e[i].elapsed_time(e[i + 1]) for e in evs) / nb, 3)
+          for i, name in enumerate(("absorb", "append", "decode"))}
+
     ms_per_step = total_s * 1e3 / K
     value = whole_job(S.cache_bytes * K, ws, total_s) / 1e9
     tokens_per_s = whole_job(S.sum_T * K, ws, total_s)
@@ -317,15 +363,15 @@ def run_ours(args, rank, ws):
         "warmup": max(3, args.warmup), "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
         "config": dict(w.describe(), step="absorb+append+decode", decode_path=args.path,
-                       split_plan=dict(zip(("split_tokens", "max_splits"), S.layer.plan())),
-                       l2="flushed between steps (256 MB write)" if need_flush else
+                       cuda_graph=bool(args.graph),
+                       split_plan=dict(zip(("split_tokens", "partial_warps"), S.layer.plan())),
+                       l2="flushed before every step (256 MB write)" if need_flush else
                        f"inputs larger than L2 ({S.cache_bytes / 1e6:.0f} MB cache)",
                        parallelism=f"replicas x{ws}" if ws > 1 else "single GPU"),
         "pct_of_hbm_peak": round(100 * value / ws / hbm_peak, 2),
         "context_tokens_per_s": round(tokens_per_s, 1),
         "decode_steps_per_s": round(K * ws / total_s, 2),
-        "breakdown_us": {"absorb": round(1e3 * sum(absorb_ms) / K, 3), "append": round(1e3 * sum(append_ms) / K, 3),
-                         "decode": round(1e3 * sum(dec_ms) / K, 3)},
+        "breakdown_us": br,
         "roofline": {"kernel": "gva_decode_attention (split-T partial + combine)", "bound": "hbm",
                      "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
                      "frac": round(achieved / hbm_peak, 4), "peak_kind": f"{pk_kind} copy bandwidth",
@@ -388,15 +434,7 @@ def run_gqa(S, flush, steps):
     for _ in range(5):
         call()
     need_flush = gqa_bytes < 2 * L2_BYTES
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
-    for k in range(steps):
-        if need_flush and flush:
-            flush()
-        ev[k][0].record()
-        call()
-        ev[k][1].record()
-    torch.cuda.synchronize()
-    t = sum(a.elapsed_time(b) for a, b in ev) / 1e3 / steps
+    t = time_steps(call, steps, flush if need_flush else None) / steps
     del inp
     return {"decode_us": round(t * 1e6, 3), "cache_bytes": gqa_bytes, "GBps": round(gqa_bytes / t / 1e9, 1)}
 

@@ -7,15 +7,19 @@
 // Decoupled RoPE: only the positional slice of the query is rotated, at the query's
 // position (review "[논문리뷰] Grouped Value Attention", section 3).
 //
-// One CTA per (head, 16 sequences): M_h rows are read through L1 as 16-byte vectors and the
-// 16 content queries sit in shared memory (broadcast reads); fp32 FMA in k order.
+// The work is tiny and latency-bound, so the kernel is laid out for few dependent memory
+// round trips: one CTA per (head, 16 sequences); warps 0-3 stage M_h and the content
+// queries in shared memory with bulk copies (one round trip), then compute the GEMV (fp32
+// FMA in k order); warps 4-7 meanwhile rotate the positional queries (fp64, digit table).
 #include "gva_device.cuh"
 #include "gva_internal.h"
+#include "gva_sched.cuh"
 
 namespace gva {
 namespace {
 
-constexpr int kAbsorbThreads = 128;
+constexpr int kGemvThreads = 128;
+constexpr int kAbsorbThreads = 256;
 constexpr int kAbsorbSeqs = 16;
 
 struct AbsorbArgs {
@@ -31,54 +35,90 @@ struct AbsorbArgs {
 };
 
 __global__ void __launch_bounds__(kAbsorbThreads) absorb_kernel(const AbsorbArgs a) {
-  extern __shared__ __align__(16) float qs[];  // [kAbsorbSeqs][d_n]
+  extern __shared__ __align__(16) float sm[];
+  __shared__ __align__(8) uint64_t bar;
+  const int ldm = a.d_n + 4;     // padded row: conflict-free 16-byte reads by row
+  float* Ms = sm;                // [d_v][d_n + 4]
+  float* qs = sm + a.d_v * ldm;  // [kAbsorbSeqs][d_n]
   const int h = blockIdx.x;
   const int b0 = blockIdx.y * kAbsorbSeqs;
   const int nb = min(kAbsorbSeqs, a.B - b0);
+  griddep_wait();
+  griddep_launch_dependents();
 
-  for (int idx = threadIdx.x; idx < nb * a.d_n; idx += kAbsorbThreads) {
-    const int bt = idx / a.d_n, k = idx - bt * a.d_n;
-    qs[bt * a.d_n + k] = a.q_c[(static_cast<long long>(b0 + bt) * a.H + h) * a.d_n + k];
+  if (threadIdx.x >= kGemvThreads) {
+    // positional slice of the query, rotated at pos_q[b] in fp64
+    const int pairs = a.d_r / 2;
+    for (int idx = threadIdx.x - kGemvThreads; idx < nb * pairs; idx += kAbsorbThreads - kGemvThreads) {
+      const int bt = idx / pairs, i = idx - bt * pairs;
+      const long long row = (static_cast<long long>(b0 + bt) * a.H + h) * a.d_r;
+      const float2 x = *reinterpret_cast<const float2*>(a.q_r + row + 2 * i);
+      const long long p = a.pos_q[b0 + bt];
+      double c = 1.0, s = 0.0;
+      if (p >= 0)
+        rope_cos_sin(a.rope, pairs, p, i, c, s);
+      else if (i == 0)
+        flag_error(a.err, GVA_DEVERR_POSITION);  // left unrotated
+      const double x0 = x.x, x1 = x.y;
+      float2 y;
+      y.x = __double2float_rn(__dsub_rn(__dmul_rn(x0, c), __dmul_rn(x1, s)));
+      y.y = __double2float_rn(__dadd_rn(__dmul_rn(x0, s), __dmul_rn(x1, c)));
+      *reinterpret_cast<float2*>(a.q_rot + row + 2 * i) = y;
+    }
+    return;
   }
-  __syncthreads();
 
-  for (int i = threadIdx.x; i < a.d_v; i += kAbsorbThreads) {
+  // stage M_h (padded rows) and the content queries with bulk copies: one DRAM round trip
+  const int t = threadIdx.x;
+  if (t == 0) {
+    mbar_init(&bar, 1);
+    mbar_init_fence();
+  }
+  asm volatile("bar.sync 1, %0;" ::"n"(kGemvThreads) : "memory");
+  const uint32_t row_bytes = static_cast<uint32_t>(a.d_n) * 4;
+  if (t == 0) mbar_arrive_expect_tx(&bar, row_bytes * static_cast<uint32_t>(a.d_v + nb));
+  asm volatile("bar.sync 1, %0;" ::"n"(kGemvThreads) : "memory");
+  if (t < 32) {
+    const float* Mh = a.M + static_cast<long long>(h) * a.d_v * a.d_n;
+    for (int i = t; i < a.d_v; i += 32)
+      bulk_g2s(Ms + i * ldm, Mh + static_cast<long long>(i) * a.d_n, row_bytes, &bar);
+    for (int bt = t; bt < nb; bt += 32)
+      bulk_g2s(qs + bt * a.d_n, a.q_c + (static_cast<long long>(b0 + bt) * a.H + h) * a.d_n, row_bytes, &bar);
+  }
+  if (!mbar_wait_bounded(&bar, 0)) {
+    if (t == 0) flag_error(a.err, GVA_DEVERR_TIMEOUT);
+    return;
+  }
+
+  // thread -> output row i (rows split over threads) and a set of sequences (when d_v is
+  // smaller than the thread count, the sequences are split over `sets` threads per row)
+  const int sets = a.d_v < kGemvThreads ? kGemvThreads / a.d_v : 1;
+  const int rows_per_pass = kGemvThreads / sets;
+  const int set = t / rows_per_pass;
+  for (int i = t % rows_per_pass; i < a.d_v; i += rows_per_pass) {
     float acc[kAbsorbSeqs];
 #pragma unroll
-    for (int bt = 0; bt < kAbsorbSeqs; ++bt) acc[bt] = 0.f;
-    const float* row = a.M + (static_cast<long long>(h) * a.d_v + i) * a.d_n;
+    for (int j = 0; j < kAbsorbSeqs; ++j) acc[j] = 0.f;
+    const float* mrow = Ms + i * ldm;
     for (int k = 0; k < a.d_n; k += 4) {
-      const float4 m4 = *reinterpret_cast<const float4*>(row + k);
+      const float4 m4 = *reinterpret_cast<const float4*>(mrow + k);
 #pragma unroll
-      for (int bt = 0; bt < kAbsorbSeqs; ++bt) {
+      for (int j = 0; j < kAbsorbSeqs; ++j) {
+        const int bt = set + j * sets;
         if (bt < nb) {
           const float4 q4 = *reinterpret_cast<const float4*>(qs + bt * a.d_n + k);
-          acc[bt] = fmaf(m4.x, q4.x, acc[bt]);
-          acc[bt] = fmaf(m4.y, q4.y, acc[bt]);
-          acc[bt] = fmaf(m4.z, q4.z, acc[bt]);
-          acc[bt] = fmaf(m4.w, q4.w, acc[bt]);
+          acc[j] = fmaf(m4.x, q4.x, acc[j]);
+          acc[j] = fmaf(m4.y, q4.y, acc[j]);
+          acc[j] = fmaf(m4.z, q4.z, acc[j]);
+          acc[j] = fmaf(m4.w, q4.w, acc[j]);
         }
       }
     }
 #pragma unroll
-    for (int bt = 0; bt < kAbsorbSeqs; ++bt)
-      if (bt < nb) a.q_abs[(static_cast<long long>(b0 + bt) * a.H + h) * a.d_v + i] = acc[bt];
-  }
-
-  // Positional slice of the query, rotated at pos_q[b] in fp64 (digit-table rotation).
-  const int pairs = a.d_r / 2;
-  for (int idx = threadIdx.x; idx < nb * pairs; idx += kAbsorbThreads) {
-    const int bt = idx / pairs, i = idx - bt * pairs;
-    const long long row = (static_cast<long long>(b0 + bt) * a.H + h) * a.d_r;
-    const double x0 = a.q_r[row + 2 * i], x1 = a.q_r[row + 2 * i + 1];
-    const long long p = a.pos_q[b0 + bt];
-    double c = 1.0, s = 0.0;
-    if (p >= 0)
-      rope_cos_sin(a.rope, pairs, p, i, c, s);
-    else if (i == 0)
-      flag_error(a.err, GVA_DEVERR_POSITION);  // left unrotated
-    a.q_rot[row + 2 * i] = __double2float_rn(__dsub_rn(__dmul_rn(x0, c), __dmul_rn(x1, s)));
-    a.q_rot[row + 2 * i + 1] = __double2float_rn(__dadd_rn(__dmul_rn(x0, s), __dmul_rn(x1, c)));
+    for (int j = 0; j < kAbsorbSeqs; ++j) {
+      const int bt = set + j * sets;
+      if (bt < nb) a.q_abs[(static_cast<long long>(b0 + bt) * a.H + h) * a.d_v + i] = acc[j];
+    }
   }
 }
 
@@ -101,16 +141,29 @@ cudaError_t launch_absorb(const gva_ctx* ctx, int B, const float* q_c, const flo
   a.d_r = ctx->dims.d_r;
   a.rope = ctx->d_rope;
   a.err = ctx->d_err;
-  const size_t smem = sizeof(float) * kAbsorbSeqs * a.d_n;
-  if (smem > 48 * 1024) {
-    cudaError_t e =
-        cudaFuncSetAttribute(absorb_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  const size_t smem = sizeof(float) * (static_cast<size_t>(a.d_v) * (a.d_n + 4) + kAbsorbSeqs * a.d_n);
+  if (smem > 200 * 1024) return cudaErrorInvalidValue;
+  static int configured[kMaxDevicesHost] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= kMaxDevicesHost || configured[dev] < static_cast<int>(smem)) {
+    e = cudaFuncSetAttribute(absorb_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem));
     if (e != cudaSuccess) return e;
+    if (dev < kMaxDevicesHost) configured[dev] = static_cast<int>(smem);
   }
-  dim3 grid(a.H, (B + kAbsorbSeqs - 1) / kAbsorbSeqs);
-  absorb_kernel<<<grid, kAbsorbThreads, smem, stream>>>(a);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.H, (B + kAbsorbSeqs - 1) / kAbsorbSeqs);
+  cfg.blockDim = dim3(kAbsorbThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, absorb_kernel, a);
 }
 
 }  // namespace gva

@@ -4,6 +4,7 @@
 #include <stdlib.h>
 
 #include "gva_internal.h"
+#include "gva_sched.cuh"
 
 namespace {
 
@@ -15,8 +16,6 @@ bool on_ctx_device(const gva_ctx* ctx) {
   int dev = -1;
   return cudaGetDevice(&dev) == cudaSuccess && dev == ctx->device;
 }
-
-int elem_bytes(gva_dtype t) { return t == GVA_F32 ? 4 : 2; }
 
 gva_status from_cuda(cudaError_t e) { return e == cudaSuccess ? GVA_OK : GVA_ERR_CUDA; }
 
@@ -50,36 +49,36 @@ int choose_path(const gva_ctx* ctx, bool sep_k) {
   return gva::fma_supported(ctx->dims, sep_k) ? GVA_PATH_FMA : -1;
 }
 
-// Split-T plan: how many 64-token blocks each partial covers.  Automatic plans aim at about
-// two waves of CTAs over the device when every sequence is at max_seq_len; a chunk is at
-// least one tile per warp of a CTA, and never longer than the longest context.
+// Split-T plan.  The partial kernel runs W = 4 * grid warps, each over an equal share of the
+// batch's (sequence, group, 64-token tile) units.  Automatic plans launch exactly one wave of
+// CTAs (SMs x resident CTAs per SM), fewer when the batch has fewer units than that; a
+// caller-set split length asks for about split_tokens tokens per warp at max_seq_len.
 bool make_plan(const gva_ctx* ctx, int B, int max_seq_len, bool sep_k, gva::Plan* plan) {
   const int path = choose_path(ctx, sep_k);
-  if (path < 0) return false;
-  const int nt_max = (max_seq_len + GVA_BLOCK_TOKENS - 1) / GVA_BLOCK_TOKENS;
-  int chunk;
+  if (path < 0 || B > gva::kMaxBatch) return false;
+  const long long nt_max = (max_seq_len + GVA_BLOCK_TOKENS - 1) / GVA_BLOCK_TOKENS;
+  const long long units_max = static_cast<long long>(B) * ctx->dims.G * nt_max;
+  long long grid;
   if (ctx->split_tokens > 0) {
-    chunk = ctx->split_tokens / GVA_BLOCK_TOKENS;
+    const long long per_warp = ctx->split_tokens / GVA_BLOCK_TOKENS;
+    const long long W = (units_max + per_warp - 1) / per_warp;
+    grid = (W + 3) / 4;
   } else {
-    const int quantum = path == GVA_PATH_MMA ? gva::mma_tiles_per_cta_unit(ctx->dims) : 4;
-    const int per_sm = path == GVA_PATH_MMA ? gva::mma_ctas_per_sm(ctx->dims, sep_k)
-                                            : gva::fma_ctas_per_sm(ctx->dims, sep_k);
-    // one CTA per (chunk, value group, sequence)
-    const long long units = static_cast<long long>(B) * ctx->dims.G * nt_max;
-    const long long target = 2LL * ctx->num_sms * per_sm;
-    long long c = (units + target - 1) / target;
-    c = ((c + quantum - 1) / quantum) * quantum;
-    if (c < quantum) c = quantum;
-    chunk = static_cast<int>(c);
+    const int per_sm = path == GVA_PATH_MMA ? gva::mma_ctas_per_sm(ctx->dims, sep_k, B)
+                                            : gva::fma_ctas_per_sm(ctx->dims, sep_k, B);
+    grid = static_cast<long long>(ctx->num_sms) * per_sm;
+    const long long useful = (units_max + 3) / 4;
+    if (grid > useful) grid = useful;
   }
-  if (chunk > nt_max) chunk = nt_max;
-  if (chunk < 1) chunk = 1;
-  if ((nt_max + chunk - 1) / chunk > 65535) chunk = (nt_max + 65534) / 65535;  // grid extent
+  if (grid < 1) grid = 1;
+  if (grid > (1LL << 20)) return false;
   plan->path = path;
-  plan->chunk_tiles = chunk;
-  plan->n_chunks = (nt_max + chunk - 1) / chunk;
-  plan->ws_bytes = sizeof(float) * static_cast<size_t>(B) * plan->n_chunks * ctx->dims.H *
-                   gva::partial_stride_floats(ctx->dims.d_v);
+  plan->grid = static_cast<int>(grid);
+  plan->n_warps = static_cast<int>(4 * grid);
+  const int R = ctx->dims.H / ctx->dims.G;
+  plan->ws_bytes = gva::header_bytes(B) +
+                   sizeof(float) * (static_cast<size_t>(plan->n_warps) + static_cast<size_t>(B) * ctx->dims.G) *
+                       R * gva::partial_stride_floats(ctx->dims.d_v);
   return true;
 }
 
@@ -91,7 +90,7 @@ gva_status decode_common(gva_ctx* ctx, bool sep_k, int B, const float* q_abs, co
   if (!ctx || B < 0 || max_seq_len < 1 || max_blocks < 1 || num_blocks < 1)
     return GVA_ERR_INVALID_ARG;
   if (B == 0) return GVA_OK;
-  if (B > 65535) return GVA_ERR_UNSUPPORTED;  // sequences are a grid dimension
+  if (B > gva::kMaxBatch) return GVA_ERR_UNSUPPORTED;  // prefix sums live in shared memory
   const gva_dims& d = ctx->dims;
   if (!q_abs || !v_pool || !block_table || !seq_lens || !out) return GVA_ERR_INVALID_ARG;
   if (sep_k && !k_pool) return GVA_ERR_INVALID_ARG;
@@ -127,11 +126,11 @@ gva_status decode_common(gva_ctx* ctx, bool sep_k, int B, const float* q_abs, co
   a.max_blocks = max_blocks;
   a.num_blocks = num_blocks;
   a.max_seq_len = max_seq_len;
-  a.chunk_tiles = plan.chunk_tiles;
-  a.n_chunks = plan.n_chunks;
+  a.n_warps = plan.n_warps;
   a.scale_log2 = static_cast<float>(static_cast<double>(ctx->scale) * 1.4426950408889634);
-  cudaError_t e = plan.path == GVA_PATH_MMA ? gva::launch_decode_mma(a, sep_k, stream)
-                                            : gva::launch_decode_fma(a, d.cache_dtype, sep_k, stream);
+  cudaError_t e = plan.path == GVA_PATH_MMA
+                      ? gva::launch_decode_mma(a, sep_k, plan.grid, stream)
+                      : gva::launch_decode_fma(a, d.cache_dtype, sep_k, plan.grid, stream);
   if (e != cudaSuccess) return GVA_ERR_CUDA;
   return from_cuda(gva::launch_combine(a, stream));
 }
@@ -186,7 +185,9 @@ gva_status gva_absorb_query(gva_ctx* ctx, int B, const float* q_c, const float* 
   if (B == 0) return GVA_OK;
   if (!q_c || !pos_q || !M || !q_abs) return GVA_ERR_INVALID_ARG;
   if (ctx->dims.d_r > 0 && (!q_r || !q_rot)) return GVA_ERR_INVALID_ARG;
-  if (!aligned16(q_c) || !aligned16(M) || !aligned16(q_abs)) return GVA_ERR_INVALID_ARG;
+  if (!aligned16(q_c) || !aligned16(M) || !aligned16(q_abs) || (q_r && !aligned16(q_r)) ||
+      (q_rot && !aligned16(q_rot)))
+    return GVA_ERR_INVALID_ARG;
   if (!on_ctx_device(ctx)) return GVA_ERR_INVALID_ARG;
   return from_cuda(gva::launch_absorb(ctx, B, q_c, q_r, pos_q, M, q_abs, q_rot,
                                       reinterpret_cast<cudaStream_t>(stream)));
@@ -264,8 +265,11 @@ gva_status gva_decode_plan(const gva_ctx* ctx, int B, int max_seq_len, int* spli
   // the GVA form when it applies, else the GQA form (d_r == 0 contexts)
   if (!make_plan(ctx, B, max_seq_len, false, &plan) && !make_plan(ctx, B, max_seq_len, true, &plan))
     return GVA_ERR_UNSUPPORTED;
-  if (split_tokens) *split_tokens = plan.chunk_tiles * GVA_BLOCK_TOKENS;
-  if (max_splits) *max_splits = plan.n_chunks;
+  const long long units_max = static_cast<long long>(B) * ctx->dims.G *
+                              ((max_seq_len + GVA_BLOCK_TOKENS - 1) / GVA_BLOCK_TOKENS);
+  if (split_tokens)
+    *split_tokens = static_cast<int>((units_max + plan.n_warps - 1) / plan.n_warps) * GVA_BLOCK_TOKENS;
+  if (max_splits) *max_splits = plan.n_warps;
   return GVA_OK;
 }
 

@@ -4,10 +4,12 @@
 // rotated to the token's own position (the cache holds grouped values plus a small,
 // separately cached, rotated positional key: abstract "Grouped Value Attention: Efficient
 // KV Caching via On-Demand Key Reconstruction"; review "[논문리뷰] Grouped Value Attention",
-// section 3, Decoupled RoPE).  One warp per token: the value rows move as 16-byte vectors,
-// lanes rotate the positional pairs in fp64 and round once to the cache dtype.
+// section 3, Decoupled RoPE).  One warp per token: the value rows move as 16-byte vectors
+// (loaded before the slot is known), lanes rotate the positional pairs in fp64 and round
+// once to the cache dtype.
 #include "gva_device.cuh"
 #include "gva_internal.h"
+#include "gva_sched.cuh"
 
 namespace gva {
 namespace {
@@ -26,15 +28,39 @@ struct AppendArgs {
 
 constexpr int kAppendThreads = 256;
 
+constexpr int kAppendVecPerLane = 8;  // value-row 16-byte vectors held per lane
+
 template <typename T>
 __global__ void __launch_bounds__(kAppendThreads) append_kernel(const AppendArgs a) {
   const long long warp_id =
       (static_cast<long long>(blockIdx.x) * kAppendThreads + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
+  griddep_wait();
+  griddep_launch_dependents();
   const long long ntok = static_cast<long long>(a.B) * a.n;
   if (warp_id >= ntok) return;
   const int b = static_cast<int>(warp_id / a.n);
   const int t = static_cast<int>(warp_id % a.n);
+  const long long tok = static_cast<long long>(b) * a.n + t;
+
+  // Loads that do not depend on the slot go out first.
+  const int vec_per_row = a.d_v * static_cast<int>(sizeof(T)) / 16;
+  const int nvec = a.G * vec_per_row;
+  const uint4* src = reinterpret_cast<const uint4*>(static_cast<const T*>(a.v_new) +
+                                                    tok * a.G * a.d_v);
+  uint4 vreg[kAppendVecPerLane];
+#pragma unroll
+  for (int c = 0; c < kAppendVecPerLane; ++c) {
+    const int i = lane + 32 * c;
+    if (i < nvec) vreg[c] = src[i];
+  }
+  const int pairs = a.d_r / 2;
+  const T* x = static_cast<const T*>(a.kr_new) + tok * a.d_r;
+  double x0 = 0.0, x1 = 0.0;
+  if (lane < pairs) {
+    x0 = CacheElem<T>::to_double(x[2 * lane]);
+    x1 = CacheElem<T>::to_double(x[2 * lane + 1]);
+  }
   const long long p = static_cast<long long>(a.pos[b]) + t;
 
   // Resolve the slot; an unresolvable one skips the token and is reported.
@@ -43,40 +69,36 @@ __global__ void __launch_bounds__(kAppendThreads) append_kernel(const AppendArgs
     return;
   }
   const int blk = a.block_table[static_cast<long long>(b) * a.max_blocks + (p >> 6)];
+  double c = 1.0, s = 0.0;
+  if (lane < pairs) rope_cos_sin(a.rope, pairs, p, lane, c, s);
   if (blk < 0 || blk >= a.num_blocks) {
     if (lane == 0) flag_error(a.err, GVA_DEVERR_BLOCK_ID);
     return;
   }
   const int o = static_cast<int>(p & (kBlockTokens - 1));
-  const long long tok = static_cast<long long>(b) * a.n + t;
 
-  // Grouped value rows: G rows of d_v elements, 16-byte vectors.
-  const int vec_per_row = a.d_v * static_cast<int>(sizeof(T)) / 16;
-  const int nvec = a.G * vec_per_row;
-  const uint4* src = reinterpret_cast<const uint4*>(static_cast<const T*>(a.v_new) +
-                                                    tok * a.G * a.d_v);
-  for (int i = lane; i < nvec; i += 32) {
+  // Grouped value rows: G rows of d_v elements, copied bit for bit.
+  auto dst_of = [&](int i) {
     const int g = i / vec_per_row, w = i - g * vec_per_row;
-    uint4* dst = reinterpret_cast<uint4*>(
-                     static_cast<T*>(a.v_pool) +
-                     ((static_cast<long long>(blk) * a.G + g) * kBlockTokens + o) * a.d_v) +
-                 w;
-    *dst = src[i];
+    return reinterpret_cast<uint4*>(static_cast<T*>(a.v_pool) +
+                                    ((static_cast<long long>(blk) * a.G + g) * kBlockTokens + o) * a.d_v) +
+           w;
+  };
+#pragma unroll
+  for (int cc = 0; cc < kAppendVecPerLane; ++cc) {
+    const int i = lane + 32 * cc;
+    if (i < nvec) *dst_of(i) = vreg[cc];
   }
+  for (int i = lane + 32 * kAppendVecPerLane; i < nvec; i += 32) *dst_of(i) = src[i];
 
   // Shared positional key, rotated to position p: pair (2i, 2i+1) turned by p*theta_i.
-  const T* x = static_cast<const T*>(a.kr_new) + tok * a.d_r;
   T* y = static_cast<T*>(a.kr_pool) + (static_cast<long long>(blk) * kBlockTokens + o) * a.d_r;
-  for (int i = lane; i < a.d_r / 2; i += 32) {
-    const double x0 = CacheElem<T>::to_double(x[2 * i]);
-    const double x1 = CacheElem<T>::to_double(x[2 * i + 1]);
-    double c, s;
-    rope_cos_sin(a.rope, a.d_r / 2, p, i, c, s);
+  if (lane < pairs) {
     // explicit roundings (no contraction) so each product is rounded on its own
     const double y0 = __dsub_rn(__dmul_rn(x0, c), __dmul_rn(x1, s));
     const double y1 = __dadd_rn(__dmul_rn(x0, s), __dmul_rn(x1, c));
-    y[2 * i] = CacheElem<T>::from_double(y0);
-    y[2 * i + 1] = CacheElem<T>::from_double(y1);
+    y[2 * lane] = CacheElem<T>::from_double(y0);
+    y[2 * lane + 1] = CacheElem<T>::from_double(y1);
   }
 }
 
@@ -103,12 +125,17 @@ cudaError_t launch_append(const gva_ctx* ctx, int B, int n, const void* v_new,
   a.num_blocks = num_blocks;
   a.rope = ctx->d_rope;
   const long long threads = static_cast<long long>(B) * n * 32;
-  const unsigned grid = static_cast<unsigned>((threads + kAppendThreads - 1) / kAppendThreads);
-  if (ctx->dims.cache_dtype == GVA_F32)
-    append_kernel<float><<<grid, kAppendThreads, 0, stream>>>(a);
-  else
-    append_kernel<__nv_bfloat16><<<grid, kAppendThreads, 0, stream>>>(a);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>((threads + kAppendThreads - 1) / kAppendThreads));
+  cfg.blockDim = dim3(kAppendThreads);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (ctx->dims.cache_dtype == GVA_F32) return cudaLaunchKernelEx(&cfg, append_kernel<float>, a);
+  return cudaLaunchKernelEx(&cfg, append_kernel<__nv_bfloat16>, a);
 }
 
 }  // namespace gva

@@ -1,0 +1,192 @@
+// gva_decode_combine.cu -- merges the split-T partial records of each (sequence, group).
+//
+// For one head, partials (m_w, l_w, u_w) over disjoint token ranges (m in the log2 domain)
+// combine exactly: M = max m_w, out = sum 2^(m_w - M) u_w / sum 2^(m_w - M) l_w.  The records
+// of segment f = b*G + g were written by the warps whose unit ranges meet the segment's
+// units [G*cum[b] + g*nt_b, ... + nt_b), found with warp_of (gva_sched.cuh); record index =
+// warp + f, so a segment's records are one contiguous block.  One CTA per (g, b) stages that
+// block into shared memory with bulk copies (one round trip per 64 KB round, usually one),
+// then merges it with online rescaling between rounds.  Launched as a programmatic dependent
+// of the partial kernel, so its launch overlaps that kernel's run; it waits for the partial
+// results before reading them.
+#include <math.h>
+
+#include "gva_device.cuh"
+#include "gva_internal.h"
+#include "gva_sched.cuh"
+
+namespace gva {
+namespace {
+
+constexpr int kCombineWarps = 8;
+constexpr int kCombineThreads = 32 * kCombineWarps;
+constexpr int kStageBytes = 64 * 1024;  // records staged per round
+
+template <int DV, int R>
+struct CombineShape {
+  static constexpr int kRs = DV + 4;  // floats per head record
+  static constexpr int kRch = kStageBytes / (R * kRs * 4) < 64 ? kStageBytes / (R * kRs * 4) : 64;
+  static constexpr int kOut = (R * DV + kCombineThreads - 1) / kCombineThreads;  // outputs per thread
+};
+
+template <int DV, int R>
+__global__ void __launch_bounds__(kCombineThreads) combine_kernel(const DecodeArgs a) {
+  using S = CombineShape<DV, R>;
+  constexpr int rs = S::kRs;
+  extern __shared__ __align__(16) float stage[];  // [kRch][R][rs] records of this round
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ float wgt[S::kRch][R];               // 2^(m_j - M) of the round, 0 for unused
+  __shared__ float Mrun[R], Lrun[R], scale_old[R];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g = blockIdx.x, b = blockIdx.y;
+  if (tid == 0) {
+    mbar_init(&bar, 1);
+    mbar_init_fence();
+  }
+  griddep_wait();
+  griddep_launch_dependents();
+  const int* cum = reinterpret_cast<const int*>(a.part);
+  const float* recs = a.part + header_bytes(a.B) / 4;
+  const int nt = cum[b + 1] - cum[b];
+  float* outg = a.out + (static_cast<size_t>(b) * a.H + static_cast<size_t>(g) * R) * DV;
+  if (nt == 0) {  // length outside [1, max_seq_len]: reported by the partial kernel
+    for (int i = tid; i < R * DV; i += kCombineThreads) outg[i] = 0.f;
+    return;
+  }
+  const long long U = static_cast<long long>(a.G) * cum[a.B];
+  const long long W = a.n_warps;
+  const long long s = static_cast<long long>(a.G) * cum[b] + static_cast<long long>(g) * nt;
+  const long long w0 = warp_of(s, U, W);
+  const int nrec = static_cast<int>(warp_of(s + nt - 1, U, W) - w0) + 1;
+  const long long f = static_cast<long long>(b) * a.G + g;
+  const float* base = recs + (w0 + f) * R * rs;  // record j of this segment: base + j*R*rs
+  // With at least as many units as warps every warp owns a non-empty range; otherwise a
+  // warp in [w0, w1] may own nothing and have written nothing.
+  const bool may_be_empty = U < W;
+  if (tid < R) {
+    Mrun[tid] = -INFINITY;
+    Lrun[tid] = 0.f;
+  }
+  float acc[S::kOut];
+#pragma unroll
+  for (int k = 0; k < S::kOut; ++k) acc[k] = 0.f;
+  __syncthreads();
+
+  uint32_t phase = 0;
+  for (int j0 = 0; j0 < nrec; j0 += S::kRch) {
+    const int n = min(S::kRch, nrec - j0);
+    if (tid == 0) {
+      fence_proxy_async_smem();  // earlier reads of the stage come before the copy's writes
+      const uint32_t bytes = static_cast<uint32_t>(n) * R * rs * 4;
+      mbar_arrive_expect_tx(&bar, bytes);
+      bulk_g2s(stage, base + static_cast<size_t>(j0) * R * rs, bytes, &bar);
+    }
+    const bool got = mbar_wait_bounded(&bar, phase);
+    phase ^= 1;
+    if (!__syncthreads_and(got)) {
+      if (tid == 0) flag_error(a.err, GVA_DEVERR_TIMEOUT);
+      return;
+    }
+    // round maximum per head (warp hh), then weights and the rescale of the running sums
+    for (int hh = warp; hh < R; hh += kCombineWarps) {
+      float mx = -INFINITY;
+      for (int j = lane; j < n; j += 32) {
+        const long long w = w0 + j0 + j;
+        if (may_be_empty && (w * U) / W == ((w + 1) * U) / W) continue;
+        mx = fmaxf(mx, stage[(j * R + hh) * rs]);
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFullMask, mx, o));
+      const float mnew = fmaxf(Mrun[hh], mx);
+      float ls = 0.f;
+      for (int j = lane; j < n; j += 32) {
+        const long long w = w0 + j0 + j;
+        const float mj = stage[(j * R + hh) * rs];
+        const bool use = mnew != -INFINITY && mj != -INFINITY &&
+                         !(may_be_empty && (w * U) / W == ((w + 1) * U) / W);
+        const float wj = use ? exp2f(mj - mnew) : 0.f;
+        wgt[j][hh] = wj;
+        ls = fmaf(wj, use ? stage[(j * R + hh) * rs + 1] : 0.f, ls);
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) ls += __shfl_xor_sync(kFullMask, ls, o);
+      if (lane == 0) {
+        const float sc = (mnew == -INFINITY) ? 1.f : exp2f(Mrun[hh] - mnew);
+        scale_old[hh] = sc;
+        Lrun[hh] = Lrun[hh] * sc + ls;
+        Mrun[hh] = mnew;
+      }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int k = 0; k < S::kOut; ++k) {
+      const int i = tid + k * kCombineThreads;
+      if (i < R * DV) {
+        const int hh = i / DV, d = i - hh * DV;
+        float v = acc[k] * scale_old[hh];
+        for (int j = 0; j < n; ++j) v = fmaf(wgt[j][hh], stage[(j * R + hh) * rs + 4 + d], v);
+        acc[k] = v;
+      }
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int k = 0; k < S::kOut; ++k) {
+    const int i = tid + k * kCombineThreads;
+    if (i < R * DV) {
+      const int hh = i / DV;
+      outg[i] = Lrun[hh] > 0.f ? acc[k] / Lrun[hh] : 0.f;
+    }
+  }
+}
+
+template <int DV, int R>
+cudaError_t launch_t(const DecodeArgs& a, cudaLaunchConfig_t& cfg) {
+  using S = CombineShape<DV, R>;
+  const int smem = S::kRch * R * S::kRs * 4;
+  static int configured[kMaxDevicesHost] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= kMaxDevicesHost || !configured[dev]) {
+    e = cudaFuncSetAttribute(combine_kernel<DV, R>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    if (dev < kMaxDevicesHost) configured[dev] = 1;
+  }
+  cfg.dynamicSmemBytes = smem;
+  return cudaLaunchKernelEx(&cfg, combine_kernel<DV, R>, a);
+}
+
+template <int DV>
+cudaError_t launch_dv(const DecodeArgs& a, cudaLaunchConfig_t& cfg) {
+  switch (a.H / a.G) {
+    case 1: return launch_t<DV, 1>(a, cfg);
+    case 2: return launch_t<DV, 2>(a, cfg);
+    case 4: return launch_t<DV, 4>(a, cfg);
+    case 8: return launch_t<DV, 8>(a, cfg);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_combine(const DecodeArgs& a, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.G, a.B);
+  cfg.blockDim = dim3(kCombineThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  switch (a.d_v) {
+    case 32: return launch_dv<32>(a, cfg);
+    case 64: return launch_dv<64>(a, cfg);
+    case 128: return launch_dv<128>(a, cfg);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace gva

@@ -15,13 +15,18 @@
 // by TMA (tensor copy, 128-byte swizzle) so that ldmatrix reads it without bank conflicts,
 // both as V (scores) and transposed as V^T (output); k_r arrives by a plain bulk copy.
 // Probabilities never leave registers: movmatrix turns the score fragment (tokens on rows)
-// into the B fragment of the output product (tokens on k).  Each of the 4 warps owns every
-// 4th tile of the CTA's chunk through a private ring; warps merge at the end.
+// into the B fragment of the output product (tokens on k).
+//
+// Work split (gva_sched.cuh): every warp streams a balanced range of (sequence, group,
+// tile) units through a private ring filled by TMA, and writes one partial record per
+// (sequence, group) it touches.  The matching GQA form (a separate key cache, no positional
+// slice) reuses the kernel with the key tile scored instead of the value tile.
 #include <cuda.h>
 #include <math.h>
 
 #include "gva_device.cuh"
 #include "gva_internal.h"
+#include "gva_sched.cuh"
 
 namespace gva {
 namespace {
@@ -109,57 +114,114 @@ __device__ __forceinline__ uint32_t mask_pair(uint32_t v, int tok, int nv) {
   return v & (lo | hi);
 }
 
-template <int DV, int DR>
+template <int DV, int DR, bool SEPK>
 struct MmaLayout {
   static constexpr int kSub = DV / 64;                          // 64-column swizzled boxes
-  static constexpr int kVBytes = kSub * kSubTileBytes;
-  static constexpr int kKrBytes = kBlockTokens * DR * 2;
-  static constexpr int kStage = kVBytes + ((kKrBytes + 1023) / 1024) * 1024;
+  static constexpr int kVBytes = kSub * kSubTileBytes;          // one operand tile
+  static constexpr int kKrBytes = SEPK ? 0 : kBlockTokens * DR * 2;
+  static constexpr int kTx = kVBytes * (SEPK ? 2 : 1) + kKrBytes;  // bytes landing per stage
+  static constexpr int kStage = kVBytes * (SEPK ? 2 : 1) + ((kKrBytes + 1023) / 1024) * 1024;
 };
 
-template <int DV, int DR, int R, int NST>
+// Ring depth per warp: two stages when four warps' rings, the header and the largest prefix
+// array fit in shared memory, else one.
+__host__ __device__ constexpr int mma_stages(int stage) {
+  return 2048 + kMmaWarps * 2 * stage + (kMaxBatch + 1) * 4 + 16 <= 227 * 1024 ? 2 : 1;
+}
+__host__ __device__ constexpr int mma_ring_bytes(int stage) { return kMmaWarps * mma_stages(stage) * stage; }
+
+// One warp's work: the units [u0, u1) of the balanced split, streamed through a private
+// ring of NST stages.  SEPK selects the matching GQA form: a separate key tile (second
+// tensor map) is scored instead of the value tile, and there is no positional slice.
+template <int DV, int DR, int R, int NST, bool SEPK>
 __global__ void __launch_bounds__(kMmaThreads) decode_mma_kernel(const DecodeArgs a,
-                                                                 const __grid_constant__ CUtensorMap tmv) {
-  using L = MmaLayout<DV, DR>;
+                                                                 const __grid_constant__ CUtensorMap tmv,
+                                                                 const __grid_constant__ CUtensorMap tmk) {
+  using L = MmaLayout<DV, DR, SEPK>;
   constexpr int NT = (2 * R + 7) / 8;  // n-tiles of 8 columns (4 heads each)
-  constexpr int KSV = DV / 16;         // k16 steps over the value columns
+  constexpr int KSV = DV / 16;         // k16 steps over the value (key) columns
   constexpr int KSR = DR / 16;         // k16 steps over the positional columns
   constexpr bool KR8 = (DR % 16) != 0;  // one trailing k8 step
   constexpr int MD = DV / 16;          // m16 tiles over d_v in the output product
   static_assert(DR % 8 == 0, "positional width must be a multiple of 8 on this path");
+  static_assert(!SEPK || DR == 0, "the key-cache form has no positional slice");
 
   extern __shared__ __align__(1024) unsigned char smem_raw[];
-  // 1 KB header (mbarriers), then the 1 KB-aligned rings (swizzled boxes need that alignment)
+  // [1 KB mbarriers][rings, 1 KB aligned for the swizzled boxes][cum: B+1 ints]
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gid = lane >> 2, tq = lane & 3;
-  const int g = blockIdx.x, c = blockIdx.y, b = blockIdx.z;
-
-  const int T_b = a.seq_lens[b];
-  if (T_b <= 0 || T_b > a.max_seq_len) {
-    if (c == 0 && g == 0 && threadIdx.x == 0) flag_error(a.err, GVA_DEVERR_SEQ_LEN);
-    return;
-  }
-  const int nt_b = (T_b + kBlockTokens - 1) / kBlockTokens;
-  const int t0 = c * a.chunk_tiles;
-  if (t0 >= nt_b) return;
-  const int t1 = min(nt_b, t0 + a.chunk_tiles);
-
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem) + warp * NST;
   unsigned char* ring = smem + 1024 + warp * NST * L::kStage;
+  int* cum = reinterpret_cast<int*>(smem + 1024 + mma_ring_bytes(L::kStage));
 
-  // ---- query fragments (B operand of the score product), pre-scaled by scale*log2(e) ----
-  // column n = 2*head + part; part 0 = bf16(q), part 1 = bf16 remainder.
-  const int h0 = g * R;
+  if (lane == 0) {
+    for (int s = 0; s < NST; ++s) mbar_init(&bars[s], 1);
+    mbar_init_fence();
+  }
+  if (threadIdx.x == 0) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmv)) : "memory");
+    if (SEPK) asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmk)) : "memory");
+  }
+  // Everything below may read what earlier work in the stream wrote.
+  griddep_wait();
+  build_prefix<kMmaThreads>(a, cum);
+  griddep_launch_dependents();
+
+  const long long U = static_cast<long long>(a.G) * cum[a.B];
+  const long long W = a.n_warps;
+  const long long gw = static_cast<long long>(blockIdx.x) * kMmaWarps + warp;
+  const long long u0 = gw * U / W, u1 = (gw + 1) * U / W;
+  const int n = static_cast<int>(u1 - u0);
+  if (n <= 0) return;  // warp-uniform; no CTA-wide barrier follows
+
+  constexpr int rec_floats = DV + 4;
+  float* recs = a.part + header_bytes(a.B) / 4;
+
+  UnitCursor ic = cursor_at(u0, cum, a.B, a.G);  // issue cursor (lane 0 advances it)
+  UnitCursor cc = ic;                             // consume cursor
+
+  auto block_id = [&](int b, int t) -> int {
+    if (t >= a.max_blocks) return -1;
+    const int blk = a.block_table[static_cast<long long>(b) * a.max_blocks + t];
+    return (blk >= 0 && blk < a.num_blocks) ? blk : -1;
+  };
+  auto issue = [&](int k) {  // lane 0: the k-th unit of this warp, at the issue cursor
+    const int s = k % NST;
+    const int blk = block_id(ic.b, ic.t);
+    if (blk < 0) {
+      flag_error(a.err, ic.t >= a.max_blocks ? GVA_DEVERR_POSITION : GVA_DEVERR_BLOCK_ID);
+      mbar_arrive(&bars[s]);
+    } else {
+      unsigned char* st = ring + s * L::kStage;
+      mbar_arrive_expect_tx(&bars[s], L::kTx);
+      const int y = (blk * a.G + ic.g) * kBlockTokens;
+#pragma unroll
+      for (int sub = 0; sub < L::kSub; ++sub) {
+        tma_load_2d(st + sub * kSubTileBytes, &tmv, 64 * sub, y, &bars[s]);
+        if (SEPK) tma_load_2d(st + L::kVBytes + sub * kSubTileBytes, &tmk, 64 * sub, y, &bars[s]);
+      }
+      if (!SEPK && DR > 0)
+        bulk_g2s(st + L::kVBytes,
+                 static_cast<const __nv_bfloat16*>(a.kr_pool) + static_cast<size_t>(blk) * kBlockTokens * DR,
+                 L::kKrBytes, &bars[s]);
+    }
+    cursor_next(ic, cum, a.B, a.G);
+  };
+  if (lane == 0)
+    for (int k = 0; k < min(NST, n); ++k) issue(k);
+
+  // query fragments (B operand of the score product) of the current (b, g), pre-scaled by
+  // scale*log2(e); column n = 2*head + part, part 0 = bf16(q), part 1 = bf16 remainder.
   uint32_t qb[NT][KSV + KSR][2];
   uint32_t qt[NT];
-  {
+  auto load_q = [&](int b, int g) {
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       const int head = nt * 4 + (gid >> 1), part = gid & 1;
       const bool valid = head < R;
-      const long long row = static_cast<long long>(b) * a.H + h0 + (valid ? head : 0);
+      const long long row = static_cast<long long>(b) * a.H + g * R + (valid ? head : 0);
       const float* qa = a.q_abs + row * DV;
       const float* qr = a.q_rot + row * DR;
       auto qv = [&](int k) -> float {
@@ -178,52 +240,44 @@ __global__ void __launch_bounds__(kMmaThreads) decode_mma_kernel(const DecodeArg
         qt[nt] = pack_bf16(qv(k0), qv(k0 + 1));
       }
     }
-  }
-
-  const int n_my = (t0 + warp < t1) ? (t1 - t0 - warp + kMmaWarps - 1) / kMmaWarps : 0;
-  if (lane == 0) {
-    for (int s = 0; s < NST; ++s) mbar_init(&bars[s], 1);
-    mbar_init_fence();
-  }
-  __syncwarp();
-
-  auto block_id = [&](int t) -> int {
-    if (t >= a.max_blocks) return -1;
-    const int blk = a.block_table[static_cast<long long>(b) * a.max_blocks + t];
-    return (blk >= 0 && blk < a.num_blocks) ? blk : -1;
   };
-  auto issue = [&](int k) {  // lane 0 only
-    const int s = k % NST;
-    const int t = t0 + warp + k * kMmaWarps;
-    const int blk = block_id(t);
-    if (blk < 0) {
-      flag_error(a.err, t >= a.max_blocks ? GVA_DEVERR_POSITION : GVA_DEVERR_BLOCK_ID);
-      mbar_arrive(&bars[s]);
-      return;
-    }
-    unsigned char* st = ring + s * L::kStage;
-    mbar_arrive_expect_tx(&bars[s], L::kVBytes + L::kKrBytes);
-    const int y = (blk * a.G + g) * kBlockTokens;
-#pragma unroll
-    for (int sub = 0; sub < L::kSub; ++sub) tma_load_2d(st + sub * kSubTileBytes, &tmv, 64 * sub, y, &bars[s]);
-    if (DR > 0)
-      bulk_g2s(st + L::kVBytes,
-               static_cast<const __nv_bfloat16*>(a.kr_pool) + static_cast<size_t>(blk) * kBlockTokens * DR,
-               L::kKrBytes, &bars[s]);
-  };
-  if (lane == 0)
-    for (int k = 0; k < min(NST, n_my); ++k) issue(k);
 
   float m[NT], l[NT], o[NT][MD][4];
+  auto reset_state = [&]() {
 #pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
-    m[nt] = -INFINITY;
-    l[nt] = 0.f;
+    for (int nt = 0; nt < NT; ++nt) {
+      m[nt] = -INFINITY;
+      l[nt] = 0.f;
 #pragma unroll
-    for (int md = 0; md < MD; ++md)
+      for (int md = 0; md < MD; ++md)
 #pragma unroll
-      for (int e = 0; e < 4; ++e) o[nt][md][e] = 0.f;
-  }
+        for (int e = 0; e < 4; ++e) o[nt][md][e] = 0.f;
+    }
+  };
+  // Partial record of segment f for this warp: per head (m, l, 0, 0, o[0..DV)).
+  auto flush = [&](long long f) {
+    float* rec = recs + (gw + f) * R * rec_floats;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      float lt = l[nt];
+      lt += __shfl_xor_sync(kFullMask, lt, 4);
+      lt += __shfl_xor_sync(kFullMask, lt, 8);
+      lt += __shfl_xor_sync(kFullMask, lt, 16);
+      const int head = nt * 4 + tq;
+      if (head < R) {
+        float* r = rec + head * rec_floats;
+        if (gid == 0) {
+          r[0] = m[nt];
+          r[1] = lt;
+        }
+#pragma unroll
+        for (int md = 0; md < MD; ++md) {
+          r[4 + 16 * md + gid] = o[nt][md][0] + o[nt][md][1];
+          r[4 + 16 * md + gid + 8] = o[nt][md][2] + o[nt][md][3];
+        }
+      }
+    }
+  };
 
   // lane-dependent parts of the ldmatrix addresses
   const int ld_row = (lane & 7) + ((lane >> 3) & 1) * 8;  // non-transposed: row within m16
@@ -231,20 +285,22 @@ __global__ void __launch_bounds__(kMmaThreads) decode_mma_kernel(const DecodeArg
   const int tr_tok = (lane & 7) + ((lane >> 4) & 1) * 8;   // transposed: token within k16
   const int tr_dc = (lane >> 3) & 1;                       // transposed: 8-column chunk
 
+  reset_state();
+  load_q(cc.b, cc.g);
   int k = 0;
   bool ok = true;
-  for (; k < n_my; ++k) {
+  for (; k < n; ++k) {
     const int s = k % NST;
     const bool got = mbar_wait_bounded(&bars[s], (k / NST) & 1);
     if (!__all_sync(kFullMask, got)) {
       ok = false;
       break;
     }
-    const int t = t0 + warp + k * kMmaWarps;
-    if (block_id(t) >= 0) {
+    if (block_id(cc.b, cc.t) >= 0) {
       const uint32_t vbase = smem_addr(ring + s * L::kStage);
+      const uint32_t kbase = SEPK ? vbase + L::kVBytes : vbase;  // tile that is scored
       const uint32_t krbase = vbase + L::kVBytes;
-      const int nv = min(kBlockTokens, T_b - t * kBlockTokens);
+      const int nv = min(kBlockTokens, a.seq_lens[cc.b] - cc.t * kBlockTokens);
 
       // scores
       float sc[NT][4][4];
@@ -260,7 +316,7 @@ __global__ void __launch_bounds__(kMmaThreads) decode_mma_kernel(const DecodeArg
 #pragma unroll
         for (int ks = 0; ks < KSV; ++ks) {
           const int kc = 2 * ks + ld_kc;
-          const uint32_t addr = vbase + (kc >> 3) * kSubTileBytes + row * 128 + (((kc & 7) ^ (row & 7)) << 4);
+          const uint32_t addr = kbase + (kc >> 3) * kSubTileBytes + row * 128 + (((kc & 7) ^ (row & 7)) << 4);
           uint32_t af[4];
           ldsm_x4(addr, af);
 #pragma unroll
@@ -340,113 +396,94 @@ __global__ void __launch_bounds__(kMmaThreads) decode_mma_kernel(const DecodeArg
       }
     }
     __syncwarp();
-    if (lane == 0 && k + NST < n_my) {
+    if (lane == 0 && k + NST < n) {
       fence_proxy_async_smem();
       issue(k + NST);
     }
-  }
-  if (!ok) {
-    if (lane == 0) flag_error(a.err, GVA_DEVERR_TIMEOUT);
-    for (int kk = k; kk < min(n_my, k + NST); ++kk) mbar_wait_bounded(&bars[kk % NST], (kk / NST) & 1);
-    __syncwarp();
-  }
-
-  // finish this warp's state: sum over the 8 lanes sharing a head, fold hi/lo columns
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
-    l[nt] += __shfl_xor_sync(kFullMask, l[nt], 4);
-    l[nt] += __shfl_xor_sync(kFullMask, l[nt], 8);
-    l[nt] += __shfl_xor_sync(kFullMask, l[nt], 16);
-  }
-  constexpr int kRec = DV + 4;
-  float* mine = reinterpret_cast<float*>(ring);
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
-    const int head = nt * 4 + tq;
-    if (head < R) {
-      if (gid == 0) {
-        mine[head * kRec] = m[nt];
-        mine[head * kRec + 1] = l[nt];
-      }
-#pragma unroll
-      for (int md = 0; md < MD; ++md) {
-        mine[head * kRec + 4 + 16 * md + gid] = o[nt][md][0] + o[nt][md][1];
-        mine[head * kRec + 4 + 16 * md + gid + 8] = o[nt][md][2] + o[nt][md][3];
+    if (k + 1 < n) {
+      const int pb_ = cc.b, pg = cc.g;
+      cursor_next(cc, cum, a.B, a.G);
+      if (cc.b != pb_ || cc.g != pg) {  // segment boundary: emit, start the next (b, g)
+        flush(static_cast<long long>(pb_) * a.G + pg);
+        reset_state();
+        load_q(cc.b, cc.g);
       }
     }
   }
-  __syncthreads();
-  const size_t rec_stride = partial_stride_floats(DV);
-  for (int idx = threadIdx.x; idx < R * DV; idx += kMmaThreads) {
-    const int h = idx / DV, d = idx - h * DV;
-    float Mx = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < kMmaWarps; ++w)
-      Mx = fmaxf(Mx, reinterpret_cast<const float*>(smem + 1024 + w * NST * L::kStage)[h * kRec]);
-    float Ls = 0.f, Os = 0.f;
-    if (Mx != -INFINITY) {
-#pragma unroll
-      for (int w = 0; w < kMmaWarps; ++w) {
-        const float* ws = reinterpret_cast<const float*>(smem + 1024 + w * NST * L::kStage) + h * kRec;
-        if (ws[0] == -INFINITY) continue;  // a warp without tiles
-        const float sc = exp2f(ws[0] - Mx);
-        Ls = fmaf(sc, ws[1], Ls);
-        Os = fmaf(sc, ws[4 + d], Os);
-      }
-    }
-    float* rec = a.part + ((static_cast<size_t>(b) * a.n_chunks + c) * a.H + h0 + h) * rec_stride;
-    if (d == 0) {
-      rec[0] = Mx;
-      rec[1] = Ls;
-    }
-    rec[4 + d] = Os;
+  if (ok) {
+    flush(static_cast<long long>(cc.b) * a.G + cc.g);
+    return;
+  }
+  // A copy never arrived: report, wait (bounded) for this warp's copies still in flight, and
+  // leave empty records for every segment still owed so the combine reads defined values.
+  if (lane == 0) flag_error(a.err, GVA_DEVERR_TIMEOUT);
+  for (int kk = k; kk < min(n, k + NST); ++kk) mbar_wait_bounded(&bars[kk % NST], (kk / NST) & 1);
+  __syncwarp();
+  reset_state();
+  flush(static_cast<long long>(cc.b) * a.G + cc.g);
+  for (int kk = k + 1; kk < n; ++kk) {
+    const int pb_ = cc.b, pg = cc.g;
+    cursor_next(cc, cum, a.B, a.G);
+    if (cc.b != pb_ || cc.g != pg) flush(static_cast<long long>(cc.b) * a.G + cc.g);
   }
 }
 
-constexpr int kMmaStages = 2;
-
-template <int DV, int DR>
-constexpr int mma_smem_bytes() {
-  return 2048 + kMmaWarps * kMmaStages * MmaLayout<DV, DR>::kStage;  // header + alignment slack
+template <int DV, int DR, bool SEPK>
+constexpr int mma_smem_bytes_fixed() {
+  return 2048 + mma_ring_bytes(MmaLayout<DV, DR, SEPK>::kStage);  // header + alignment slack + rings
 }
 
-template <int DV, int DR, int R>
-cudaError_t launch_mma_t(const DecodeArgs& a, const CUtensorMap& map, cudaStream_t stream) {
-  constexpr int smem = mma_smem_bytes<DV, DR>();
+inline int cum_bytes(int B) { return ((B + 1) * 4 + 15) / 16 * 16; }
+
+template <int DV, int DR, int R, bool SEPK>
+cudaError_t launch_mma_t(const DecodeArgs& a, const CUtensorMap& mv, const CUtensorMap& mk, int grid,
+                         cudaStream_t stream) {
+  const int smem = mma_smem_bytes_fixed<DV, DR, SEPK>() + cum_bytes(a.B);
+  auto kern = decode_mma_kernel<DV, DR, R, mma_stages(MmaLayout<DV, DR, SEPK>::kStage), SEPK>;
   static int configured[kMaxDevices] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev >= kMaxDevices || !configured[dev]) {
-    e = cudaFuncSetAttribute(decode_mma_kernel<DV, DR, R, kMmaStages>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (dev >= kMaxDevices || configured[dev] < smem) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    if (dev < kMaxDevices) configured[dev] = 1;
+    if (dev < kMaxDevices) configured[dev] = smem;
   }
-  dim3 grid(a.G, a.n_chunks, a.B);
-  decode_mma_kernel<DV, DR, R, kMmaStages><<<grid, kMmaThreads, smem, stream>>>(a, map);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kMmaThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, a, mv, mk);
 }
 
-template <int DV, int DR>
-cudaError_t dispatch_r(const DecodeArgs& a, const CUtensorMap& map, cudaStream_t stream) {
+template <int DV, int DR, bool SEPK>
+cudaError_t dispatch_r(const DecodeArgs& a, const CUtensorMap& mv, const CUtensorMap& mk, int grid,
+                       cudaStream_t stream) {
   switch (a.H / a.G) {
-    case 1: return launch_mma_t<DV, DR, 1>(a, map, stream);
-    case 2: return launch_mma_t<DV, DR, 2>(a, map, stream);
-    case 4: return launch_mma_t<DV, DR, 4>(a, map, stream);
-    case 8: return launch_mma_t<DV, DR, 8>(a, map, stream);
+    case 1: return launch_mma_t<DV, DR, 1, SEPK>(a, mv, mk, grid, stream);
+    case 2: return launch_mma_t<DV, DR, 2, SEPK>(a, mv, mk, grid, stream);
+    case 4: return launch_mma_t<DV, DR, 4, SEPK>(a, mv, mk, grid, stream);
+    case 8: return launch_mma_t<DV, DR, 8, SEPK>(a, mv, mk, grid, stream);
     default: return cudaErrorInvalidValue;
   }
 }
 
 template <int DV>
-cudaError_t dispatch_dr(const DecodeArgs& a, const CUtensorMap& map, cudaStream_t stream) {
+cudaError_t dispatch_dr(const DecodeArgs& a, const CUtensorMap& mv, const CUtensorMap& mk, bool sep_k,
+                        int grid, cudaStream_t stream) {
+  if (sep_k) return dispatch_r<DV, 0, true>(a, mv, mk, grid, stream);
   switch (a.d_r) {
-    case 0: return dispatch_r<DV, 0>(a, map, stream);
-    case 8: return dispatch_r<DV, 8>(a, map, stream);
-    case 16: return dispatch_r<DV, 16>(a, map, stream);
-    case 24: return dispatch_r<DV, 24>(a, map, stream);
-    case 32: return dispatch_r<DV, 32>(a, map, stream);
+    case 0: return dispatch_r<DV, 0, false>(a, mv, mk, grid, stream);
+    case 8: return dispatch_r<DV, 8, false>(a, mv, mk, grid, stream);
+    case 16: return dispatch_r<DV, 16, false>(a, mv, mk, grid, stream);
+    case 24: return dispatch_r<DV, 24, false>(a, mv, mk, grid, stream);
+    case 32: return dispatch_r<DV, 32, false>(a, mv, mk, grid, stream);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -470,9 +507,9 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// The value pool seen as a 2-D bf16 tensor: rows = NB*G*64 token rows of d_v columns; one
-// box = 64 columns x 64 rows, swizzled in 128-byte rows.
-bool make_value_map(CUtensorMap* map, const void* v_pool, int num_blocks, int G, int d_v) {
+// A pool seen as a 2-D bf16 tensor: rows = NB*G*64 token rows of d_v columns; one box = 64
+// columns x 64 rows, swizzled in 128-byte rows.
+bool make_pool_map(CUtensorMap* map, const void* pool, int num_blocks, int G, int d_v) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(d_v),
@@ -480,7 +517,7 @@ bool make_value_map(CUtensorMap* map, const void* v_pool, int num_blocks, int G,
   const cuuint64_t strides[1] = {static_cast<cuuint64_t>(d_v) * 2};
   const cuuint32_t box[2] = {64, kBlockTokens};
   const cuuint32_t estr[2] = {1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(v_pool), dims, strides, box,
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(pool), dims, strides, box,
             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -488,30 +525,38 @@ bool make_value_map(CUtensorMap* map, const void* v_pool, int num_blocks, int G,
 }  // namespace
 
 bool mma_supported(const gva_dims& d, bool sep_k) {
-  if (sep_k) return false;  // the matching GQA form runs on the CUDA-core kernel
   if (d.cache_dtype != GVA_BF16) return false;
   if (!(d.d_v == 64 || d.d_v == 128)) return false;
-  if (!(d.d_r == 0 || d.d_r == 8 || d.d_r == 16 || d.d_r == 24 || d.d_r == 32)) return false;
+  if (sep_k) {
+    if (d.d_r != 0) return false;
+  } else if (!(d.d_r == 0 || d.d_r == 8 || d.d_r == 16 || d.d_r == 24 || d.d_r == 32)) {
+    return false;
+  }
   const int r = d.H / d.G;
   return r == 1 || r == 2 || r == 4 || r == 8;
 }
 
-int mma_ctas_per_sm(const gva_dims& d, bool) {
-  const int stage = (d.d_v / 64) * kSubTileBytes + ((kBlockTokens * d.d_r * 2 + 1023) / 1024) * 1024;
-  const int smem = 2048 + kMmaWarps * kMmaStages * stage;
+int mma_ctas_per_sm(const gva_dims& d, bool sep_k, int B) {
+  const int tile = (d.d_v / 64) * kSubTileBytes;
+  const int kr = sep_k ? 0 : ((kBlockTokens * d.d_r * 2 + 1023) / 1024) * 1024;
+  const int stage = tile * (sep_k ? 2 : 1) + kr;
+  const int smem = 2048 + mma_ring_bytes(stage) + cum_bytes(B);
   int per_sm = (228 * 1024) / (smem + 1024);
+  if (per_sm > 4) per_sm = 4;
   return per_sm < 1 ? 1 : per_sm;
 }
 
-int mma_tiles_per_cta_unit(const gva_dims&) { return kMmaWarps; }
-
-cudaError_t launch_decode_mma(const DecodeArgs& a, bool sep_k, cudaStream_t stream) {
-  if (sep_k) return cudaErrorNotSupported;
-  CUtensorMap map;
-  if (!make_value_map(&map, a.v_pool, a.num_blocks, a.G, a.d_v)) return cudaErrorInvalidValue;
+cudaError_t launch_decode_mma(const DecodeArgs& a, bool sep_k, int grid, cudaStream_t stream) {
+  CUtensorMap mv, mk;
+  if (!make_pool_map(&mv, a.v_pool, a.num_blocks, a.G, a.d_v)) return cudaErrorInvalidValue;
+  if (sep_k) {
+    if (!make_pool_map(&mk, a.k_pool, a.num_blocks, a.G, a.d_v)) return cudaErrorInvalidValue;
+  } else {
+    mk = mv;
+  }
   switch (a.d_v) {
-    case 64: return dispatch_dr<64>(a, map, stream);
-    case 128: return dispatch_dr<128>(a, map, stream);
+    case 64: return dispatch_dr<64>(a, mv, mk, sep_k, grid, stream);
+    case 128: return dispatch_dr<128>(a, mv, mk, sep_k, grid, stream);
     default: return cudaErrorInvalidValue;
   }
 }

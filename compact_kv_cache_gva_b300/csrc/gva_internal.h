@@ -34,22 +34,23 @@ struct DecodeArgs {
   const int32_t* block_table;
   const int32_t* seq_lens;
   float* out;                // [B,H,d_v]
-  float* part;               // partial records [B][n_chunks][H][d_v + 4]
+  float* part;               // workspace: header (prefix sums) + partial records
   unsigned* err;
   int B, H, G, d_v, d_r;
   int max_blocks, num_blocks, max_seq_len;
-  int chunk_tiles;           // 64-token tiles per chunk
-  int n_chunks;              // chunks per sequence in the plan (grid extent)
+  int n_warps;               // W: warps of the partial grid (grid = W / 4 CTAs)
   float scale_log2;          // softmax scale * log2(e)
 };
 
 // Record layout of one partial: m (log2 domain), l, two pad words, then d_v weighted sums.
 __host__ __device__ inline size_t partial_stride_floats(int d_v) { return static_cast<size_t>(d_v) + 4; }
 
+constexpr int kMaxBatch = 8192;  // sequences per decode call (prefix sums live in shared memory)
+
 struct Plan {
-  int path;          // GVA_PATH_FMA or GVA_PATH_MMA
-  int chunk_tiles;
-  int n_chunks;
+  int path;      // GVA_PATH_FMA or GVA_PATH_MMA
+  int grid;      // CTAs of the partial kernel (4 warps each)
+  int n_warps;   // 4 * grid
   size_t ws_bytes;
 };
 
@@ -62,14 +63,16 @@ cudaError_t launch_append(const gva_ctx* ctx, int B, int n, const void* v_new,
                           int max_blocks, int num_blocks, void* v_pool, void* kr_pool,
                           cudaStream_t stream);
 // Decode: partial kernel + combine.  sep_k selects the GQA form (k_pool used, d_r == 0).
+// Partial kernels: one CTA = 4 warps, each warp a balanced range of (b, g, tile) units.
 bool fma_supported(const gva_dims& d, bool sep_k);
-int fma_ctas_per_sm(const gva_dims& d, bool sep_k);
-cudaError_t launch_decode_fma(const DecodeArgs& a, int cache_dtype, bool sep_k,
+int fma_ctas_per_sm(const gva_dims& d, bool sep_k, int B);
+cudaError_t launch_decode_fma(const DecodeArgs& a, int cache_dtype, bool sep_k, int grid,
                               cudaStream_t stream);
 bool mma_supported(const gva_dims& d, bool sep_k);
-int mma_ctas_per_sm(const gva_dims& d, bool sep_k);
-int mma_tiles_per_cta_unit(const gva_dims& d);
-cudaError_t launch_decode_mma(const DecodeArgs& a, bool sep_k, cudaStream_t stream);
+int mma_ctas_per_sm(const gva_dims& d, bool sep_k, int B);
+cudaError_t launch_decode_mma(const DecodeArgs& a, bool sep_k, int grid, cudaStream_t stream);
+// Merges the partial records of each (b, g) into out; launched as a programmatic dependent
+// of the partial kernel.
 cudaError_t launch_combine(const DecodeArgs& a, cudaStream_t stream);
 
 }  // namespace gva

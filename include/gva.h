@@ -142,9 +142,10 @@ size_t gva_decode_workspace_size(const gva_ctx* ctx, int B, int max_seq_len);
  *   out[b,h,:] = sum_{j<T} softmax(s)_j  V[g] at position j
  * (summary section 方法: content score as one inner product with the stored value, output
  * the value-weighted sum; review section 3: positional score from the shared rotated key.)
- * Split-T flash decoding: the context of each sequence is cut into chunks of
- * whole 64-token blocks, each chunk yields a partial (max, sum, weighted sum) in the
- * workspace, and a combine pass merges them.
+ * Split-T flash decoding: the batch's (sequence, value group, 64-token block) units are
+ * shared out evenly over the warps of one wave of CTAs; each warp yields a partial (max,
+ * sum, weighted sum) per (sequence, group) it covers, in the workspace, and a combine pass
+ * merges them.  B <= 8192.
  *   q_abs [B,H,d_v] f32, q_rot [B,H,d_r] f32 (NULL when d_r == 0)
  *   seq_lens [B] int32 (device), each in [1, max_seq_len]
  *   out [B,H,d_v] f32
@@ -170,13 +171,16 @@ gva_status gqa_decode_attention(gva_ctx* ctx, int B, const float* q, const void*
                                 float* out, void* workspace, size_t ws_bytes,
                                 gva_stream_t stream);
 
-/* Decode options.  split_tokens: context chunk length per partial, a multiple of 64
- * (0 = automatic plan from B, max_seq_len and the SM count).  path: kernel family. */
+/* Decode options.  split_tokens: about how many context tokens each warp of the split-T
+ * partial kernel covers when every sequence is at max_seq_len, a multiple of 64 (0 =
+ * automatic: one wave of CTAs over the GPU, every warp an equal share of the batch's tiles).
+ * path: kernel family. */
 gva_status gva_set_split_tokens(gva_ctx* ctx, int split_tokens);
 gva_status gva_set_decode_path(gva_ctx* ctx, gva_decode_path path);
 
-/* Chunk length (tokens) and partial count per sequence the next decode call will use for
- * this batch shape, so a caller can predict the workspace and the combine work. */
+/* The split the next decode call uses for this batch shape: *split_tokens = context tokens
+ * per warp when every sequence is at max_seq_len, *max_splits = warps of the partial kernel
+ * (each writes one partial record per (sequence, group) its range touches). */
 gva_status gva_decode_plan(const gva_ctx* ctx, int B, int max_seq_len, int* split_tokens,
                            int* max_splits);
 

@@ -378,3 +378,30 @@ def test_long_context_full_step_sampled_rows():
         want.append(oracle.decode_one(qa[b:b + 1], qr[b:b + 1], vp, kp, tb, sl, G=w.G, b=0, h=h, d_n=w.d_n))
         have.append(got[b, h])
     assert_parity(np.array(have), np.array(want), "bf16", "long-context step")
+
+
+def test_step_replays_in_a_cuda_graph():
+    """The three C-ABI calls of a step, captured once and replayed, give the direct result."""
+    w = synth.custom(dtype="bf16", B=4, H=16, G=4, d_v=64, d_r=16, T_range=(100, 900), shuffled=True)
+    inp = synth.decode_inputs(w, seed=60, device="cuda")
+    raw = synth.raw_inputs(w, inp.seq_lens.cpu(), n_new=1, seed=61, device="cuda")
+    layer = make_layer(w)
+
+    def step():
+        return layer.step(raw.q_c, raw.q_r, raw.pos_q, raw.M, raw.v_new, raw.kr_new, raw.pos_new, inp.block_table,
+                          inp.seq_lens, inp.v_pool, inp.kr_pool)
+    want = step().clone()
+    cap = torch.cuda.Stream()
+    cap.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(cap):
+        step()
+        cap.synchronize()
+        with torch.cuda.graph(graph, stream=cap):
+            step()
+    torch.cuda.current_stream().wait_stream(cap)
+    layer.out.fill_(float("nan"))
+    graph.replay()
+    torch.cuda.synchronize()
+    assert layer.device_error() == 0
+    assert torch.equal(layer.out, want)
