@@ -49,36 +49,47 @@ int choose_path(const gva_ctx* ctx, bool sep_k) {
   return gva::fma_supported(ctx->dims, sep_k) ? GVA_PATH_FMA : -1;
 }
 
-// Split-T plan.  The partial kernel runs W = 4 * grid warps, each over an equal share of the
-// batch's (sequence, group, 64-token tile) units.  Automatic plans launch exactly one wave of
-// CTAs (SMs x resident CTAs per SM), fewer when the batch has fewer units than that; a
+// Split-T plan.  The batch's (sequence, group, 64-token tile) units are cut into equal
+// contiguous ranges (gva_sched.cuh).  Tensor-core path: one range per CTA, one CTA per SM;
+// its P consumer warps share the range, each fed by its own copy warp (mma_shape picks P).
+// CUDA-core path: one range per warp, 4 warps per CTA, as many CTAs as fit on the SMs.
+// Automatic plans launch one wave, fewer CTAs when the batch has fewer units than that; a
 // caller-set split length asks for about split_tokens tokens per warp at max_seq_len.
 bool make_plan(const gva_ctx* ctx, int B, int max_seq_len, bool sep_k, gva::Plan* plan) {
   const int path = choose_path(ctx, sep_k);
   if (path < 0 || B > gva::kMaxBatch) return false;
   const long long nt_max = (max_seq_len + GVA_BLOCK_TOKENS - 1) / GVA_BLOCK_TOKENS;
   const long long units_max = static_cast<long long>(B) * ctx->dims.G * nt_max;
+  const bool mma = path == GVA_PATH_MMA;
+  int pairs = 0, stages = 0;
+  if (mma && !gva::mma_shape(ctx->dims, sep_k, B, &pairs, &stages)) return false;
+  const int warps_per_cta = mma ? pairs : 4;  // warps that stream units
   long long grid;
   if (ctx->split_tokens > 0) {
     const long long per_warp = ctx->split_tokens / GVA_BLOCK_TOKENS;
     const long long W = (units_max + per_warp - 1) / per_warp;
-    grid = (W + 3) / 4;
+    grid = (W + warps_per_cta - 1) / warps_per_cta;
   } else {
-    const int per_sm = path == GVA_PATH_MMA ? gva::mma_ctas_per_sm(ctx->dims, sep_k, B)
-                                            : gva::fma_ctas_per_sm(ctx->dims, sep_k, B);
+    const int per_sm = mma ? 1 : gva::fma_ctas_per_sm(ctx->dims, sep_k, B);
     grid = static_cast<long long>(ctx->num_sms) * per_sm;
-    const long long useful = (units_max + 3) / 4;
+    // G*Q ranges: the G ranges of slice q read the same blocks together (gva_sched.cuh),
+    // so each block's positional-key tile is read from HBM once
+    if (mma && grid >= ctx->dims.G) grid -= grid % ctx->dims.G;
+    const long long useful = (units_max + warps_per_cta - 1) / warps_per_cta;
     if (grid > useful) grid = useful;
   }
   if (grid < 1) grid = 1;
   if (grid > (1LL << 20)) return false;
   plan->path = path;
   plan->grid = static_cast<int>(grid);
-  plan->n_warps = static_cast<int>(4 * grid);
+  plan->n_warps = static_cast<int>(warps_per_cta * grid);
+  plan->n_groups = mma ? plan->grid : plan->n_warps;
+  plan->group_warps = mma ? pairs : 1;
+  plan->n_stages = mma ? stages : 0;
   const int R = ctx->dims.H / ctx->dims.G;
   plan->ws_bytes = gva::header_bytes(B) +
-                   sizeof(float) * (static_cast<size_t>(plan->n_warps) + static_cast<size_t>(B) * ctx->dims.G) *
-                       R * gva::partial_stride_floats(ctx->dims.d_v);
+                   sizeof(float) * (static_cast<size_t>(plan->n_groups) + static_cast<size_t>(B) * ctx->dims.G) *
+                       plan->group_warps * R * gva::partial_stride_floats(ctx->dims.d_v);
   return true;
 }
 
@@ -127,6 +138,9 @@ gva_status decode_common(gva_ctx* ctx, bool sep_k, int B, const float* q_abs, co
   a.num_blocks = num_blocks;
   a.max_seq_len = max_seq_len;
   a.n_warps = plan.n_warps;
+  a.n_groups = plan.n_groups;
+  a.group_warps = plan.group_warps;
+  a.n_stages = plan.n_stages;
   a.scale_log2 = static_cast<float>(static_cast<double>(ctx->scale) * 1.4426950408889634);
   cudaError_t e = plan.path == GVA_PATH_MMA
                       ? gva::launch_decode_mma(a, sep_k, plan.grid, stream)

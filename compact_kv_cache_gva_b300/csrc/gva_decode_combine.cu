@@ -2,11 +2,12 @@
 //
 // For one head, partials (m_w, l_w, u_w) over disjoint token ranges (m in the log2 domain)
 // combine exactly: M = max m_w, out = sum 2^(m_w - M) u_w / sum 2^(m_w - M) l_w.  The records
-// of segment f = b*G + g were written by the warps whose unit ranges meet the segment's
-// units [G*cum[b] + g*nt_b, ... + nt_b), found with warp_of (gva_sched.cuh); record index =
-// warp + f, so a segment's records are one contiguous block.  One CTA per (g, b) stages that
-// block into shared memory with bulk copies (one round trip per 64 KB round, usually one),
-// then merges it with online rescaling between rounds.  Launched as a programmatic dependent
+// of segment f = g*B + b were written by the warps of the unit ranges that meet the
+// segment's units [g*cum[B] + cum[b], ... + nt_b) (range_of, gva_sched.cuh); record index =
+// (range + f)*C + warp, so a segment's records are one contiguous block, and warp_touched
+// says which records of the block hold data.  One CTA per (g, b) stages that block into
+// shared memory with bulk copies (one round trip per 64 KB round, usually one), then merges
+// it with online rescaling between rounds.  Launched as a programmatic dependent
 // of the partial kernel, so its launch overlaps that kernel's run; it waits for the partial
 // results before reading them.
 #include <math.h>
@@ -54,15 +55,21 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const DecodeAr
     return;
   }
   const long long U = static_cast<long long>(a.G) * cum[a.B];
-  const long long W = a.n_warps;
-  const long long s = static_cast<long long>(a.G) * cum[b] + static_cast<long long>(g) * nt;
-  const long long w0 = warp_of(s, U, W);
-  const int nrec = static_cast<int>(warp_of(s + nt - 1, U, W) - w0) + 1;
-  const long long f = static_cast<long long>(b) * a.G + g;
-  const float* base = recs + (w0 + f) * R * rs;  // record j of this segment: base + j*R*rs
-  // With at least as many units as warps every warp owns a non-empty range; otherwise a
-  // warp in [w0, w1] may own nothing and have written nothing.
-  const bool may_be_empty = U < W;
+  const long long NG = a.n_groups;
+  const int C = a.group_warps;
+  const long long s = static_cast<long long>(g) * cum[a.B] + cum[b];  // first unit of (g, b)
+  const long long c0 = range_of(s, U, NG);
+  const int nrec = static_cast<int>(range_of(s + nt - 1, U, NG) - c0 + 1) * C;
+  const long long f = segment_of(g, b, a.B);
+  const float* base = recs + (c0 + f) * C * R * rs;  // record j of this segment: base + j*R*rs
+  // Record j belongs to warp j % C of range c0 + j / C; it holds data only if that warp
+  // streamed a unit of this segment.
+  auto has_data = [&](long long j) {
+    const long long c = c0 + j / C;
+    const long long rb = range_begin(c, U, NG), re = range_begin(c + 1, U, NG);
+    const long long lo = (s > rb ? s : rb) - rb, hi = (s + nt < re ? s + nt : re) - rb;
+    return warp_touched(lo, hi, static_cast<int>(j % C), C);
+  };
   if (tid < R) {
     Mrun[tid] = -INFINITY;
     Lrun[tid] = 0.f;
@@ -91,8 +98,7 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const DecodeAr
     for (int hh = warp; hh < R; hh += kCombineWarps) {
       float mx = -INFINITY;
       for (int j = lane; j < n; j += 32) {
-        const long long w = w0 + j0 + j;
-        if (may_be_empty && (w * U) / W == ((w + 1) * U) / W) continue;
+        if (!has_data(j0 + j)) continue;
         mx = fmaxf(mx, stage[(j * R + hh) * rs]);
       }
 #pragma unroll
@@ -100,10 +106,8 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const DecodeAr
       const float mnew = fmaxf(Mrun[hh], mx);
       float ls = 0.f;
       for (int j = lane; j < n; j += 32) {
-        const long long w = w0 + j0 + j;
         const float mj = stage[(j * R + hh) * rs];
-        const bool use = mnew != -INFINITY && mj != -INFINITY &&
-                         !(may_be_empty && (w * U) / W == ((w + 1) * U) / W);
+        const bool use = mnew != -INFINITY && has_data(j0 + j) && mj != -INFINITY;
         const float wj = use ? exp2f(mj - mnew) : 0.f;
         wgt[j][hh] = wj;
         ls = fmaf(wj, use ? stage[(j * R + hh) * rs + 1] : 0.f, ls);
@@ -124,7 +128,11 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const DecodeAr
       if (i < R * DV) {
         const int hh = i / DV, d = i - hh * DV;
         float v = acc[k] * scale_old[hh];
-        for (int j = 0; j < n; ++j) v = fmaf(wgt[j][hh], stage[(j * R + hh) * rs + 4 + d], v);
+        for (int j = 0; j < n; ++j) {
+          const float wj = wgt[j][hh];
+          // records without data hold stale bytes (possibly NaN): skip rather than scale by 0
+          if (wj != 0.f) v = fmaf(wj, stage[(j * R + hh) * rs + 4 + d], v);
+        }
         acc[k] = v;
       }
     }

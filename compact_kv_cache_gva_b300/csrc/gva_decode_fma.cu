@@ -128,10 +128,10 @@ __global__ void __launch_bounds__(kFmaThreads) decode_fma_kernel(const DecodeArg
   build_prefix<kFmaThreads>(a, cum);
   griddep_launch_dependents();
 
+  // one range per warp (n_groups = warps, group_warps = 1): record index gw + f
   const long long U = static_cast<long long>(a.G) * cum[a.B];
-  const long long W = a.n_warps;
   const long long gw = static_cast<long long>(blockIdx.x) * kFmaWarps + warp;
-  const long long u0 = gw * U / W, u1 = (gw + 1) * U / W;
+  const long long u0 = range_begin(gw, U, a.n_groups), u1 = range_begin(gw + 1, U, a.n_groups);
   const int n = static_cast<int>(u1 - u0);
   if (n <= 0) return;  // warp-uniform; no CTA-wide barrier follows
   float* recs = a.part + header_bytes(a.B) / 4;
@@ -293,14 +293,14 @@ __global__ void __launch_bounds__(kFmaThreads) decode_fma_kernel(const DecodeArg
       const int pb = cc.b, pg = cc.g;
       cursor_next(cc, cum, a.B, a.G);
       if (cc.b != pb || cc.g != pg) {
-        flush(static_cast<long long>(pb) * a.G + pg);
+        flush(segment_of(pg, pb, a.B));
         reset_state();
         load_q(cc.b, cc.g);
       }
     }
   }
   if (ok) {
-    flush(static_cast<long long>(cc.b) * a.G + cc.g);
+    flush(segment_of(cc.g, cc.b, a.B));
     return;
   }
   // Report, wait (bounded) for this warp's copies still in flight, and leave empty records
@@ -310,11 +310,11 @@ __global__ void __launch_bounds__(kFmaThreads) decode_fma_kernel(const DecodeArg
     mbar_wait_bounded(&bars[kk % kFmaStages], (kk / kFmaStages) & 1);
   __syncwarp();
   reset_state();
-  flush(static_cast<long long>(cc.b) * a.G + cc.g);
+  flush(segment_of(cc.g, cc.b, a.B));
   for (int kk = k + 1; kk < n; ++kk) {
     const int pb = cc.b, pg = cc.g;
     cursor_next(cc, cum, a.B, a.G);
-    if (cc.b != pb || cc.g != pg) flush(static_cast<long long>(cc.b) * a.G + cc.g);
+    if (cc.b != pb || cc.g != pg) flush(segment_of(cc.g, cc.b, a.B));
   }
 }
 

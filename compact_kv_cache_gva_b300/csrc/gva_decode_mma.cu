@@ -17,9 +17,10 @@
 // Probabilities never leave registers: movmatrix turns the score fragment (tokens on rows)
 // into the B fragment of the output product (tokens on k).
 //
-// Work split (gva_sched.cuh): every warp streams a balanced range of (sequence, group,
-// tile) units through a private ring filled by TMA, and writes one partial record per
-// (sequence, group) it touches.  The matching GQA form (a separate key cache, no positional
+// Work split (gva_sched.cuh): one CTA per SM streams a balanced range of (sequence, group,
+// tile) units with a few warp pairs: a copy warp keeps its consumer's private ring of tiles
+// full (TMA), and the consumer warps take the range's tiles round-robin, each writing one
+// partial record per (sequence, group) it touched.  The matching GQA form (a separate key cache, no positional
 // slice) reuses the kernel with the key tile scored instead of the value tile.
 #include <cuda.h>
 #include <math.h>
@@ -31,8 +32,7 @@
 namespace gva {
 namespace {
 
-constexpr int kMmaWarps = 4;
-constexpr int kMmaThreads = 32 * kMmaWarps;
+constexpr int kMmaMaxThreads = 64 * kMmaMaxPairs;  // consumer warps + as many copy warps
 constexpr int kSubTileBytes = kBlockTokens * 128;  // one [64 tokens][64 columns] bf16 swizzled box
 
 // ---- PTX wrappers ------------------------------------------------------------------------
@@ -116,101 +116,175 @@ __device__ __forceinline__ uint32_t mask_pair(uint32_t v, int tok, int nv) {
 
 template <int DV, int DR, bool SEPK>
 struct MmaLayout {
-  static constexpr int kSub = DV / 64;                          // 64-column swizzled boxes
-  static constexpr int kVBytes = kSub * kSubTileBytes;          // one operand tile
+  static constexpr int kSub = DV / 64;                        // 64-column swizzled boxes
+  static constexpr int kVBytes = kSub * kSubTileBytes;        // one operand tile
+  static constexpr int kOpBytes = kVBytes * (SEPK ? 2 : 1);   // operand tiles of a stage (1 KB multiple)
   static constexpr int kKrBytes = SEPK ? 0 : kBlockTokens * DR * 2;
-  static constexpr int kTx = kVBytes * (SEPK ? 2 : 1) + kKrBytes;  // bytes landing per stage
-  static constexpr int kStage = kVBytes * (SEPK ? 2 : 1) + ((kKrBytes + 1023) / 1024) * 1024;
+  static constexpr int kTx = kOpBytes + kKrBytes;             // bytes landing per stage
+  static constexpr int kStageBytes = kOpBytes + kKrBytes;
 };
 
-// Ring depth per warp: two stages when four warps' rings, the header and the largest prefix
-// array fit in shared memory, else one.
-__host__ __device__ constexpr int mma_stages(int stage) {
-  return 2048 + kMmaWarps * 2 * stage + (kMaxBatch + 1) * 4 + 16 <= 227 * 1024 ? 2 : 1;
-}
-__host__ __device__ constexpr int mma_ring_bytes(int stage) { return kMmaWarps * mma_stages(stage) * stage; }
+// Shared memory: [alignment slack 1 KB][control 1 KB: full and empty mbarrier and valid
+// length of every stage][P*D operand tiles, 1 KB aligned for the swizzled boxes][P*D k_r
+// tiles][cum: B+1 ints].  Stage (c, slot) is index c*D + slot.
+constexpr int kMaxStages = 40;
+constexpr int kCtrlBytes = 1024;
+static_assert(kMaxStages * (2 * 8 + 4) <= kCtrlBytes, "control block");
+// dynamic shared memory per CTA: the 227 KB opt-in limit less 1 KB for the kernel's static
+// shared memory (the prefix scan's scratch, placed ahead of the 1 KB aligned dynamic block)
+constexpr int kSmemLimit = 226 * 1024;
+inline int cum_bytes(int B) { return ((B + 1) * 4 + 15) / 16 * 16; }
+inline int ring_fixed_bytes(int B) { return 1024 + kCtrlBytes + cum_bytes(B); }
 
-// One warp's work: the units [u0, u1) of the balanced split, streamed through a private
-// ring of NST stages.  SEPK selects the matching GQA form: a separate key tile (second
-// tensor map) is scored instead of the value tile, and there is no positional slice.
-template <int DV, int DR, int R, int NST, bool SEPK>
-__global__ void __launch_bounds__(kMmaThreads) decode_mma_kernel(const DecodeArgs a,
-                                                                 const __grid_constant__ CUtensorMap tmv,
-                                                                 const __grid_constant__ CUtensorMap tmk) {
+// One CTA streams one contiguous range of units (gva_sched.cuh) with P warp pairs.  Consumer
+// warp c (warps 0..P-1) takes units k = c, c + P, c + 2P, ... of the range; its d-th unit
+// lands in its private ring slot d % D.  Copy warp c (warp P + c) serves consumer c alone:
+// its lanes look up the block ids of the consumer's next 32 units at once, one batch ahead,
+// and lane 0 issues each unit's copies (TMA for the value (and key) tile, a bulk copy for
+// the positional-key tile) as soon as the consumer has released the slot.  Every barrier
+// has one waiter that waits in order (the consumer on "full", the copy warp on "empty"),
+// so phase parities are unambiguous, and about P*(D-1) tiles are in flight per SM while P
+// are being computed.  The copy warps take the issue work (a few hundred cycles per tile)
+// and the dependent block-table reads off the consumers' path.
+template <int DV, int DR, int R, bool SEPK>
+__global__ void __launch_bounds__(kMmaMaxThreads, 1) decode_mma_kernel(const DecodeArgs a,
+                                                                       const __grid_constant__ CUtensorMap tmv,
+                                                                       const __grid_constant__ CUtensorMap tmk) {
   using L = MmaLayout<DV, DR, SEPK>;
-  constexpr int NT = (2 * R + 7) / 8;  // n-tiles of 8 columns (4 heads each)
-  constexpr int KSV = DV / 16;         // k16 steps over the value (key) columns
-  constexpr int KSR = DR / 16;         // k16 steps over the positional columns
+  constexpr int NT = (2 * R + 7) / 8;   // n-tiles of 8 columns (4 heads each)
+  constexpr int KSV = DV / 16;          // k16 steps over the value (key) columns
+  constexpr int KSR = DR / 16;          // k16 steps over the positional columns
   constexpr bool KR8 = (DR % 16) != 0;  // one trailing k8 step
-  constexpr int MD = DV / 16;          // m16 tiles over d_v in the output product
+  constexpr int MD = DV / 16;           // m16 tiles over d_v in the output product
   static_assert(DR % 8 == 0, "positional width must be a multiple of 8 on this path");
   static_assert(!SEPK || DR == 0, "the key-cache form has no positional slice");
 
   extern __shared__ __align__(1024) unsigned char smem_raw[];
-  // [1 KB mbarriers][rings, 1 KB aligned for the swizzled boxes][cum: B+1 ints]
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const int P = a.group_warps;  // warp pairs; blockDim.x == 64 * P
+  const int D = a.n_stages;     // ring slots per pair
+  const int N = P * D;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem);
+  uint64_t* empty = full + kMaxStages;
+  int* nvs = reinterpret_cast<int*>(empty + kMaxStages);  // valid tokens of each stage's tile (0 = skip)
+  unsigned char* tiles = smem + kCtrlBytes;
+  unsigned char* krs = tiles + N * L::kOpBytes;
+  int* cum = reinterpret_cast<int*>(krs + N * L::kKrBytes);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int gid = lane >> 2, tq = lane & 3;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem) + warp * NST;
-  unsigned char* ring = smem + 1024 + warp * NST * L::kStage;
-  int* cum = reinterpret_cast<int*>(smem + 1024 + mma_ring_bytes(L::kStage));
 
-  if (lane == 0) {
-    for (int s = 0; s < NST; ++s) mbar_init(&bars[s], 1);
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < N; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
     mbar_init_fence();
   }
-  if (threadIdx.x == 0) {
+  if (warp == P && lane == 0) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmv)) : "memory");
     if (SEPK) asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmk)) : "memory");
   }
   // Everything below may read what earlier work in the stream wrote.
   griddep_wait();
-  build_prefix<kMmaThreads>(a, cum);
+  build_prefix<kMmaMaxThreads>(a, cum);  // ends with __syncthreads: the barriers are set up
   griddep_launch_dependents();
 
   const long long U = static_cast<long long>(a.G) * cum[a.B];
-  const long long W = a.n_warps;
-  const long long gw = static_cast<long long>(blockIdx.x) * kMmaWarps + warp;
-  const long long u0 = gw * U / W, u1 = (gw + 1) * U / W;
-  const int n = static_cast<int>(u1 - u0);
-  if (n <= 0) return;  // warp-uniform; no CTA-wide barrier follows
+  const long long u0 = range_begin(blockIdx.x, U, a.n_groups);
+  const int n = static_cast<int>(range_begin(blockIdx.x + 1, U, a.n_groups) - u0);
+  if (n <= 0) return;  // CTA-uniform; no CTA-wide barrier follows
 
-  constexpr int rec_floats = DV + 4;
-  float* recs = a.part + header_bytes(a.B) / 4;
-
-  UnitCursor ic = cursor_at(u0, cum, a.B, a.G);  // issue cursor (lane 0 advances it)
-  UnitCursor cc = ic;                             // consume cursor
-
-  auto block_id = [&](int b, int t) -> int {
-    if (t >= a.max_blocks) return -1;
-    const int blk = a.block_table[static_cast<long long>(b) * a.max_blocks + t];
-    return (blk >= 0 && blk < a.num_blocks) ? blk : -1;
-  };
-  auto issue = [&](int k) {  // lane 0: the k-th unit of this warp, at the issue cursor
-    const int s = k % NST;
-    const int blk = block_id(ic.b, ic.t);
-    if (blk < 0) {
-      flag_error(a.err, ic.t >= a.max_blocks ? GVA_DEVERR_POSITION : GVA_DEVERR_BLOCK_ID);
-      mbar_arrive(&bars[s]);
-    } else {
-      unsigned char* st = ring + s * L::kStage;
-      mbar_arrive_expect_tx(&bars[s], L::kTx);
-      const int y = (blk * a.G + ic.g) * kBlockTokens;
-#pragma unroll
-      for (int sub = 0; sub < L::kSub; ++sub) {
-        tma_load_2d(st + sub * kSubTileBytes, &tmv, 64 * sub, y, &bars[s]);
-        if (SEPK) tma_load_2d(st + L::kVBytes + sub * kSubTileBytes, &tmk, 64 * sub, y, &bars[s]);
+  // ------------------------------------------------------------------ copy warps
+  if (warp >= P) {
+    const int c = warp - P;                        // the consumer this warp serves
+    const int n_mine = n > c ? (n - c + P - 1) / P : 0;  // its units: k = c + P*d, d < n_mine
+    // lane i: block id (or -1), group and valid tokens of the consumer's unit d0 + i
+    auto lookup = [&](int d0, int& blk, int& grp, int& nv) {
+      blk = -1;
+      grp = 0;
+      nv = 0;
+      const int d = d0 + lane;
+      if (d < n_mine) {
+        const UnitCursor cu = cursor_at(u0 + c + static_cast<long long>(P) * d, cum, a.B, a.G);
+        grp = cu.g;
+        if (cu.t >= a.max_blocks) {
+          flag_error(a.err, GVA_DEVERR_POSITION);
+        } else {
+          const int id = a.block_table[static_cast<long long>(cu.b) * a.max_blocks + cu.t];
+          if (id >= 0 && id < a.num_blocks) {
+            blk = id;
+            nv = min(kBlockTokens, a.seq_lens[cu.b] - cu.t * kBlockTokens);
+          } else {
+            flag_error(a.err, GVA_DEVERR_BLOCK_ID);
+          }
+        }
       }
-      if (!SEPK && DR > 0)
-        bulk_g2s(st + L::kVBytes,
-                 static_cast<const __nv_bfloat16*>(a.kr_pool) + static_cast<size_t>(blk) * kBlockTokens * DR,
-                 L::kKrBytes, &bars[s]);
+    };
+    int blk, grp, nv;
+    lookup(0, blk, grp, nv);
+    int slot = 0, ph = 0, issued = 0;
+    bool ok = true;
+    for (int d0 = 0; d0 < n_mine && ok; d0 += 32) {
+      int nblk, ngrp, nnv;
+      lookup(d0 + 32, nblk, ngrp, nnv);  // next batch: loads in flight while this one issues
+      const int cnt = min(32, n_mine - d0);
+      for (int j = 0; j < cnt; ++j) {
+        const int bj = __shfl_sync(kFullMask, blk, j);
+        const int gj = __shfl_sync(kFullMask, grp, j);
+        const int vj = __shfl_sync(kFullMask, nv, j);
+        if (lane == 0) {
+          const int s = c * D + slot;
+          // the slot's previous unit must have been released by the consumer
+          if (d0 + j >= D && !mbar_wait_bounded(&empty[s], ph ^ 1)) ok = false;
+          if (ok) {
+            nvs[s] = bj >= 0 ? vj : 0;  // published by the arrive below (release)
+            if (bj >= 0) {
+              mbar_arrive_expect_tx(&full[s], L::kTx);
+              unsigned char* st = tiles + s * L::kOpBytes;
+              const int y = (bj * a.G + gj) * kBlockTokens;
+#pragma unroll
+              for (int sub = 0; sub < L::kSub; ++sub) {
+                tma_load_2d(st + sub * kSubTileBytes, &tmv, 64 * sub, y, &full[s]);
+                if (SEPK) tma_load_2d(st + L::kVBytes + sub * kSubTileBytes, &tmk, 64 * sub, y, &full[s]);
+              }
+              if (!SEPK && DR > 0)
+                bulk_g2s(krs + s * L::kKrBytes,
+                         static_cast<const __nv_bfloat16*>(a.kr_pool) + static_cast<size_t>(bj) * kBlockTokens * DR,
+                         L::kKrBytes, &full[s]);
+            } else {
+              mbar_arrive(&full[s]);  // completes the phase with no data; the tile is skipped
+            }
+            ++issued;
+          }
+        }
+        ok = __shfl_sync(kFullMask, ok, 0);
+        if (!ok) break;
+        if (++slot == D) {
+          slot = 0;
+          ph ^= 1;
+        }
+      }
+      blk = nblk;
+      grp = ngrp;
+      nv = nnv;
     }
-    cursor_next(ic, cum, a.B, a.G);
-  };
-  if (lane == 0)
-    for (int k = 0; k < min(NST, n); ++k) issue(k);
+    if (lane == 0) {
+      if (!ok) flag_error(a.err, GVA_DEVERR_TIMEOUT);
+      // no copy may still be landing in shared memory when the CTA exits
+      for (int d = max(0, issued - D); d < issued; ++d)
+        if (!mbar_wait_bounded(&full[c * D + d % D], (d / D) & 1)) flag_error(a.err, GVA_DEVERR_TIMEOUT);
+    }
+    return;
+  }
+
+  // ------------------------------------------------------------------ consumer warps
+  const int NC = P;  // consumer warps sharing the range
+  int k = warp;
+  if (k >= n) return;
+  float* recs = a.part + header_bytes(a.B) / 4;
+  constexpr int rec_floats = DV + 4;
+  UnitCursor cc = cursor_at(u0 + k, cum, a.B, a.G);
+  int slot = 0, ph = 0;  // ring slot and phase parity of this warp's next unit
 
   // query fragments (B operand of the score product) of the current (b, g), pre-scaled by
   // scale*log2(e); column n = 2*head + part, part 0 = bf16(q), part 1 = bf16 remainder.
@@ -219,14 +293,15 @@ __global__ void __launch_bounds__(kMmaThreads) decode_mma_kernel(const DecodeArg
   auto load_q = [&](int b, int g) {
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-      const int head = nt * 4 + (gid >> 1), part = gid & 1;
+      const int head = nt * 4 + ((lane >> 2) >> 1), part = (lane >> 2) & 1;
+      const int tq = lane & 3;
       const bool valid = head < R;
       const long long row = static_cast<long long>(b) * a.H + g * R + (valid ? head : 0);
       const float* qa = a.q_abs + row * DV;
       const float* qr = a.q_rot + row * DR;
-      auto qv = [&](int k) -> float {
+      auto qv = [&](int kk) -> float {
         if (!valid) return 0.f;
-        const float x = (k < DV ? qa[k] : qr[k - DV]) * a.scale_log2;
+        const float x = (kk < DV ? qa[kk] : qr[kk - DV]) * a.scale_log2;
         return split_part(x, part);
       };
 #pragma unroll
@@ -254,9 +329,10 @@ __global__ void __launch_bounds__(kMmaThreads) decode_mma_kernel(const DecodeArg
         for (int e = 0; e < 4; ++e) o[nt][md][e] = 0.f;
     }
   };
+  const int gid = lane >> 2, tq = lane & 3;
   // Partial record of segment f for this warp: per head (m, l, 0, 0, o[0..DV)).
   auto flush = [&](long long f) {
-    float* rec = recs + (gw + f) * R * rec_floats;
+    float* rec = recs + ((static_cast<long long>(blockIdx.x) + f) * NC + warp) * R * rec_floats;
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       float lt = l[nt];
@@ -287,20 +363,19 @@ __global__ void __launch_bounds__(kMmaThreads) decode_mma_kernel(const DecodeArg
 
   reset_state();
   load_q(cc.b, cc.g);
-  int k = 0;
   bool ok = true;
-  for (; k < n; ++k) {
-    const int s = k % NST;
-    const bool got = mbar_wait_bounded(&bars[s], (k / NST) & 1);
+  while (true) {
+    const int s = warp * D + slot;
+    const bool got = mbar_wait_bounded(&full[s], ph);
     if (!__all_sync(kFullMask, got)) {
       ok = false;
       break;
     }
-    if (block_id(cc.b, cc.t) >= 0) {
-      const uint32_t vbase = smem_addr(ring + s * L::kStage);
+    const int nv = nvs[s];
+    if (nv > 0) {
+      const uint32_t vbase = smem_addr(tiles + s * L::kOpBytes);
       const uint32_t kbase = SEPK ? vbase + L::kVBytes : vbase;  // tile that is scored
-      const uint32_t krbase = vbase + L::kVBytes;
-      const int nv = min(kBlockTokens, a.seq_lens[cc.b] - cc.t * kBlockTokens);
+      const uint32_t krbase = smem_addr(krs + s * L::kKrBytes);
 
       // scores
       float sc[NT][4][4];
@@ -396,62 +471,58 @@ __global__ void __launch_bounds__(kMmaThreads) decode_mma_kernel(const DecodeArg
       }
     }
     __syncwarp();
-    if (lane == 0 && k + NST < n) {
-      fence_proxy_async_smem();
-      issue(k + NST);
+    if (lane == 0) mbar_arrive(&empty[s]);  // the stage may be refilled
+    k += NC;
+    if (k >= n) break;
+    const int pb_ = cc.b, pg = cc.g;
+    cursor_advance(cc, NC, cum, a.B, a.G);
+    if (cc.b != pb_ || cc.g != pg) {  // segment boundary: emit, start the next (b, g)
+      flush(segment_of(pg, pb_, a.B));
+      reset_state();
+      load_q(cc.b, cc.g);
     }
-    if (k + 1 < n) {
-      const int pb_ = cc.b, pg = cc.g;
-      cursor_next(cc, cum, a.B, a.G);
-      if (cc.b != pb_ || cc.g != pg) {  // segment boundary: emit, start the next (b, g)
-        flush(static_cast<long long>(pb_) * a.G + pg);
-        reset_state();
-        load_q(cc.b, cc.g);
-      }
+    if (++slot == D) {
+      slot = 0;
+      ph ^= 1;
     }
   }
   if (ok) {
-    flush(static_cast<long long>(cc.b) * a.G + cc.g);
+    flush(segment_of(cc.g, cc.b, a.B));
     return;
   }
-  // A copy never arrived: report, wait (bounded) for this warp's copies still in flight, and
-  // leave empty records for every segment still owed so the combine reads defined values.
+  // A copy never arrived: report, and leave empty records for every segment still owed so
+  // the combine reads defined values.  (The copy warp waits for its copies in flight.)
   if (lane == 0) flag_error(a.err, GVA_DEVERR_TIMEOUT);
-  for (int kk = k; kk < min(n, k + NST); ++kk) mbar_wait_bounded(&bars[kk % NST], (kk / NST) & 1);
-  __syncwarp();
   reset_state();
-  flush(static_cast<long long>(cc.b) * a.G + cc.g);
-  for (int kk = k + 1; kk < n; ++kk) {
+  flush(segment_of(cc.g, cc.b, a.B));
+  for (k += NC; k < n; k += NC) {
     const int pb_ = cc.b, pg = cc.g;
-    cursor_next(cc, cum, a.B, a.G);
-    if (cc.b != pb_ || cc.g != pg) flush(static_cast<long long>(cc.b) * a.G + cc.g);
+    cursor_advance(cc, NC, cum, a.B, a.G);
+    if (cc.b != pb_ || cc.g != pg) flush(segment_of(cc.g, cc.b, a.B));
   }
 }
-
-template <int DV, int DR, bool SEPK>
-constexpr int mma_smem_bytes_fixed() {
-  return 2048 + mma_ring_bytes(MmaLayout<DV, DR, SEPK>::kStage);  // header + alignment slack + rings
-}
-
-inline int cum_bytes(int B) { return ((B + 1) * 4 + 15) / 16 * 16; }
 
 template <int DV, int DR, int R, bool SEPK>
 cudaError_t launch_mma_t(const DecodeArgs& a, const CUtensorMap& mv, const CUtensorMap& mk, int grid,
                          cudaStream_t stream) {
-  const int smem = mma_smem_bytes_fixed<DV, DR, SEPK>() + cum_bytes(a.B);
-  auto kern = decode_mma_kernel<DV, DR, R, mma_stages(MmaLayout<DV, DR, SEPK>::kStage), SEPK>;
+  using L = MmaLayout<DV, DR, SEPK>;
+  const int P = a.group_warps, D = a.n_stages;
+  if (P < 1 || P > kMmaMaxPairs || D < 1 || P * D > kMaxStages) return cudaErrorInvalidValue;
+  const int smem = ring_fixed_bytes(a.B) + P * D * L::kStageBytes;
+  if (smem > kSmemLimit) return cudaErrorInvalidValue;
+  auto kern = decode_mma_kernel<DV, DR, R, SEPK>;
   static int configured[kMaxDevices] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev >= kMaxDevices || configured[dev] < smem) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (dev >= kMaxDevices || !configured[dev]) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
     if (e != cudaSuccess) return e;
-    if (dev < kMaxDevices) configured[dev] = smem;
+    if (dev < kMaxDevices) configured[dev] = 1;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kMmaThreads);
+  cfg.blockDim = dim3(64 * P);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -536,14 +607,20 @@ bool mma_supported(const gva_dims& d, bool sep_k) {
   return r == 1 || r == 2 || r == 4 || r == 8;
 }
 
-int mma_ctas_per_sm(const gva_dims& d, bool sep_k, int B) {
-  const int tile = (d.d_v / 64) * kSubTileBytes;
-  const int kr = sep_k ? 0 : ((kBlockTokens * d.d_r * 2 + 1023) / 1024) * 1024;
-  const int stage = tile * (sep_k ? 2 : 1) + kr;
-  const int smem = 2048 + mma_ring_bytes(stage) + cum_bytes(B);
-  int per_sm = (228 * 1024) / (smem + 1024);
-  if (per_sm > 4) per_sm = 4;
-  return per_sm < 1 ? 1 : per_sm;
+// Warp pairs and ring depth.  Four pairs keep the tensor pipes ahead of HBM with a margin
+// when a stage is small (d_v = 64: 10 KB with its positional key); with d_v = 128 a stage
+// holds 19 KB and three pairs leave a deeper ring for the same compute margin.  D takes the
+// rest of shared memory.
+bool mma_shape(const gva_dims& d, bool sep_k, int B, int* pairs, int* stages) {
+  const int op = (d.d_v / 64) * kSubTileBytes * (sep_k ? 2 : 1);
+  const int stage = op + (sep_k ? 0 : kBlockTokens * d.d_r * 2);
+  const int P = stage <= 12 * 1024 ? 4 : 3;
+  int D = (kSmemLimit - ring_fixed_bytes(B)) / (P * stage);
+  if (D > kMaxStages / P) D = kMaxStages / P;
+  if (D < 1) return false;
+  *pairs = P;
+  *stages = D;
+  return true;
 }
 
 cudaError_t launch_decode_mma(const DecodeArgs& a, bool sep_k, int grid, cudaStream_t stream) {

@@ -38,7 +38,12 @@ struct DecodeArgs {
   unsigned* err;
   int B, H, G, d_v, d_r;
   int max_blocks, num_blocks, max_seq_len;
-  int n_warps;               // W: warps of the partial grid (grid = W / 4 CTAs)
+  int n_warps;               // warps of the partial grid that stream units
+  // The batch's units are cut into n_groups equal contiguous ranges; the group_warps warps
+  // of a range share it round-robin (unit k of the range goes to warp k % group_warps).
+  // Warp w of range c writes its partial record of segment f at index (c + f)*group_warps + w.
+  int n_groups, group_warps;
+  int n_stages;              // tensor-core kernel: ring depth of each warp pair (tiles)
   float scale_log2;          // softmax scale * log2(e)
 };
 
@@ -48,9 +53,12 @@ __host__ __device__ inline size_t partial_stride_floats(int d_v) { return static
 constexpr int kMaxBatch = 8192;  // sequences per decode call (prefix sums live in shared memory)
 
 struct Plan {
-  int path;      // GVA_PATH_FMA or GVA_PATH_MMA
-  int grid;      // CTAs of the partial kernel (4 warps each)
-  int n_warps;   // 4 * grid
+  int path;         // GVA_PATH_FMA or GVA_PATH_MMA
+  int grid;         // CTAs of the partial kernel
+  int n_warps;      // warps that stream units (grid * unit warps per CTA)
+  int n_groups;     // unit ranges (FMA: one per warp; MMA: one per CTA)
+  int group_warps;  // warps sharing one range
+  int n_stages;     // MMA ring depth per warp pair
   size_t ws_bytes;
 };
 
@@ -69,7 +77,11 @@ int fma_ctas_per_sm(const gva_dims& d, bool sep_k, int B);
 cudaError_t launch_decode_fma(const DecodeArgs& a, int cache_dtype, bool sep_k, int grid,
                               cudaStream_t stream);
 bool mma_supported(const gva_dims& d, bool sep_k);
-int mma_ctas_per_sm(const gva_dims& d, bool sep_k, int B);
+// Tensor-core kernel: one CTA per range, made of P warp pairs (a copy warp filling a private
+// ring of D tiles, and the consumer warp that computes on it); P consumer warps share the
+// range.  mma_shape picks P and D for the dims (0 if no ring fits).
+constexpr int kMmaMaxPairs = 4;
+bool mma_shape(const gva_dims& d, bool sep_k, int B, int* pairs, int* stages);
 cudaError_t launch_decode_mma(const DecodeArgs& a, bool sep_k, int grid, cudaStream_t stream);
 // Merges the partial records of each (b, g) into out; launched as a programmatic dependent
 // of the partial kernel.

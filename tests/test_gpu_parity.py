@@ -205,6 +205,66 @@ def test_small_bf16_decode_matches_oracle(shape, split_tokens, path):
     assert_parity(got, oracle_decode_all(w, inp), "bf16", f"shape {shape}")
 
 
+# Shapes and split lengths that stress the tensor-core kernel's shared ring: few CTAs with
+# long ranges (the ring wraps many times), many short sequences (segments shorter than the
+# number of consumer warps, so warps skip whole segments), and ranges with fewer units than
+# consumer warps.
+RING_CASES = [
+    (dict(B=16, H=16, G=4, d_v=64, d_r=16, T_range=(1, 3000)), 64 * 64),
+    (dict(B=40, H=16, G=4, d_v=64, d_r=16, T_range=(1, 130)), 64 * 5),
+    (dict(B=6, H=32, G=8, d_v=128, d_r=24, T_range=(1, 2500)), 64 * 48),
+    (dict(B=3, H=8, G=1, d_v=128, d_r=32, T_range=(700, 1500)), 64 * 100),
+    (dict(B=2, H=4, G=2, d_v=64, d_r=16, T_range=(1, 100)), 0),
+    (dict(B=64, H=16, G=4, d_v=64, d_r=24, T_range=(1, 64)), 0),
+]
+
+
+@pytest.mark.parametrize("case", range(len(RING_CASES)))
+def test_tensor_core_ring_schedules_match_oracle(case):
+    shape, split = RING_CASES[case]
+    w = synth.custom(dtype="bf16", shuffled=True, **shape)
+    inp = synth.decode_inputs(w, seed=70 + case, device="cuda", spare_blocks=1)
+    got, layer = run_decode(w, inp, split_tokens=split, path=gva.GVA_PATH_MMA)
+    assert_parity(got, oracle_decode_all(w, inp), "bf16", f"ring case {case} plan {layer.plan()}")
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_gqa_comparison_kernel_ring_depths(d):
+    # at d = 128 the key and value tiles of a stage take 32 KB: the ring is shallower than the
+    # number of consumer warps
+    w = synth.custom(dtype="bf16", B=5, H=16, G=4, d_v=d, d_r=0, T_range=(1, 2000), shuffled=True)
+    inp = synth.decode_inputs(w, seed=80 + d, device="cuda", k_pool=True)
+    ctx = gva.gva_create(w.H, w.G, w.d_v, w.d_v, 0, "bf16")
+    gva.gva_set_split_tokens(ctx, 64 * 16)
+    out = torch.empty((w.B, w.H, w.d_v), device="cuda")
+    ws = torch.empty(gva.gva_decode_workspace_size(ctx, w.B, w.max_seq_len), dtype=torch.uint8, device="cuda")
+    gva.gqa_decode_attention(ctx, inp.extra["q"], inp.extra["k_pool"], inp.v_pool, inp.block_table, inp.seq_lens,
+                             w.max_seq_len, out, ws)
+    torch.cuda.synchronize()
+    assert gva.gva_get_device_error(ctx) == 0
+    kp, vp = to_np_bits(inp.extra["k_pool"]), to_np_bits(inp.v_pool)
+    q = inp.extra["q"].double().cpu().numpy()
+    want = np.stack([np.stack([oracle.gqa_decode_one(q, kp, vp, inp.block_table.cpu().numpy(),
+                                                     inp.seq_lens.cpu().numpy(), G=w.G, b=b, h=h)
+                               for h in range(w.H)]) for b in range(w.B)])
+    assert_parity(out.cpu().numpy(), want, "bf16", f"gqa d={d}")
+
+
+def test_workspace_with_stale_nan_bytes():
+    # the combine must never scale a record that holds no data (stale bytes may be NaN)
+    w = synth.custom(dtype="bf16", B=9, H=16, G=4, d_v=64, d_r=16, T_range=(1, 300), shuffled=True)
+    inp = synth.decode_inputs(w, seed=90, device="cuda")
+    want = oracle_decode_all(w, inp)
+    for path in (gva.GVA_PATH_FMA, gva.GVA_PATH_MMA):
+        layer = make_layer(w, path=path)
+        layer.workspace.fill_(0xFF)  # every float in the workspace is a NaN
+        out = layer.attend(inp.v_pool, inp.kr_pool, inp.block_table, inp.seq_lens, q_abs=inp.q_abs,
+                           q_rot=inp.q_rot)
+        torch.cuda.synchronize()
+        assert layer.device_error() == 0
+        assert_parity(out.cpu().numpy(), want, "bf16", f"stale workspace, path {path}")
+
+
 def test_ragged_tail_slots_are_never_read():
     # fill every slot past each sequence's end with NaN bits: the output must stay finite
     w = synth.custom(dtype="bf16", B=4, H=16, G=4, d_v=64, d_r=16, T_range=(1, 200), shuffled=True)
