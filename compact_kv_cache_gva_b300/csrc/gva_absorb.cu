@@ -8,9 +8,11 @@
 // position (review "[논문리뷰] Grouped Value Attention", section 3).
 //
 // The work is tiny and latency-bound, so the kernel is laid out for few dependent memory
-// round trips: one CTA per (head, 16 sequences); warps 0-3 stage M_h and the content
-// queries in shared memory with bulk copies (one round trip), then compute the GEMV (fp32
-// FMA in k order); warps 4-7 meanwhile rotate the positional queries (fp64, digit table).
+// round trips: one CTA per (head, 16 sequences).  Every thread first issues its loads (the
+// positional query and its position; a share of M_h and of the content queries as 16-byte
+// vectors), then the threads that own a positional pair load the four RoPE table rows of
+// its position at once and rotate it (fp32); M_h and the queries go to shared memory and
+// the GEMV runs in fp32 in k order.  Two memory round trips in all.
 #include "gva_device.cuh"
 #include "gva_internal.h"
 #include "gva_sched.cuh"
@@ -18,9 +20,9 @@
 namespace gva {
 namespace {
 
-constexpr int kGemvThreads = 128;
 constexpr int kAbsorbThreads = 256;
 constexpr int kAbsorbSeqs = 16;
+constexpr int kAbsorbVecs = 8;  // 16-byte vectors of M_h and q_c held per thread per pass
 
 struct AbsorbArgs {
   const float* q_c;
@@ -29,71 +31,83 @@ struct AbsorbArgs {
   const float* M;
   float* q_abs;
   float* q_rot;
-  const double2* rope;
+  const float2* rope;  // fp32 RoPE digit table
   unsigned* err;
   int B, H, d_v, d_n, d_r;
 };
 
 __global__ void __launch_bounds__(kAbsorbThreads) absorb_kernel(const AbsorbArgs a) {
   extern __shared__ __align__(16) float sm[];
-  __shared__ __align__(8) uint64_t bar;
-  const int ldm = a.d_n + 4;     // padded row: conflict-free 16-byte reads by row
+  const int ldm = a.d_n + 4;     // padded rows: conflict-free 16-byte reads by row
   float* Ms = sm;                // [d_v][d_n + 4]
-  float* qs = sm + a.d_v * ldm;  // [kAbsorbSeqs][d_n]
+  float* qs = sm + a.d_v * ldm;  // [kAbsorbSeqs][d_n + 4]
   const int h = blockIdx.x;
   const int b0 = blockIdx.y * kAbsorbSeqs;
   const int nb = min(kAbsorbSeqs, a.B - b0);
+  const int t = threadIdx.x;
   griddep_wait();
   griddep_launch_dependents();
 
-  if (threadIdx.x >= kGemvThreads) {
-    // positional slice of the query, rotated at pos_q[b] in fp64
-    const int pairs = a.d_r / 2;
-    for (int idx = threadIdx.x - kGemvThreads; idx < nb * pairs; idx += kAbsorbThreads - kGemvThreads) {
-      const int bt = idx / pairs, i = idx - bt * pairs;
-      const long long row = (static_cast<long long>(b0 + bt) * a.H + h) * a.d_r;
-      const float2 x = *reinterpret_cast<const float2*>(a.q_r + row + 2 * i);
-      const long long p = a.pos_q[b0 + bt];
-      double c = 1.0, s = 0.0;
-      if (p >= 0)
-        rope_cos_sin(a.rope, pairs, p, i, c, s);
-      else if (i == 0)
-        flag_error(a.err, GVA_DEVERR_POSITION);  // left unrotated
-      const double x0 = x.x, x1 = x.y;
-      float2 y;
-      y.x = __double2float_rn(__dsub_rn(__dmul_rn(x0, c), __dmul_rn(x1, s)));
-      y.y = __double2float_rn(__dadd_rn(__dmul_rn(x0, s), __dmul_rn(x1, c)));
-      *reinterpret_cast<float2*>(a.q_rot + row + 2 * i) = y;
-    }
-    return;
+  // positional slice: thread t < nb * pairs owns pair (t % pairs) of sequence b0 + t / pairs
+  const int pairs = a.d_r / 2;
+  const bool rot = t < nb * pairs;
+  long long p = 0;
+  float2 x = make_float2(0.f, 0.f);
+  long long qrow = 0;
+  int pi = 0;
+  if (rot) {
+    const int bt = t / pairs;
+    pi = t - bt * pairs;
+    qrow = (static_cast<long long>(b0 + bt) * a.H + h) * a.d_r;
+    p = a.pos_q[b0 + bt];
+    x = *reinterpret_cast<const float2*>(a.q_r + qrow + 2 * pi);
   }
 
-  // stage M_h (padded rows) and the content queries with bulk copies: one DRAM round trip
-  const int t = threadIdx.x;
-  if (t == 0) {
-    mbar_init(&bar, 1);
-    mbar_init_fence();
+  // M_h rows and the content queries into shared memory, 16-byte vectors
+  const int v4 = a.d_n / 4;
+  const int nm = a.d_v * v4, nq = nb * v4, ntot = nm + nq;
+  const float4* Mg = reinterpret_cast<const float4*>(a.M + static_cast<long long>(h) * a.d_v * a.d_n);
+  for (int base = 0; base < ntot; base += kAbsorbThreads * kAbsorbVecs) {
+    float4 r[kAbsorbVecs];
+#pragma unroll
+    for (int j = 0; j < kAbsorbVecs; ++j) {
+      const int i = base + t + j * kAbsorbThreads;
+      if (i < nm) {
+        r[j] = Mg[i];
+      } else if (i < ntot) {
+        const int bt = (i - nm) / v4, c = (i - nm) - bt * v4;
+        r[j] = reinterpret_cast<const float4*>(a.q_c + (static_cast<long long>(b0 + bt) * a.H + h) * a.d_n)[c];
+      }
+    }
+    if (base == 0 && rot) {  // the rotation overlaps the first pass's loads
+      float c = 1.f, s = 0.f;
+      if (p >= 0)
+        rope_cos_sin_f32(a.rope, pairs, p, pi, c, s);
+      else if (pi == 0)
+        flag_error(a.err, GVA_DEVERR_POSITION);  // left unrotated
+      float2 y;
+      y.x = fmaf(x.x, c, -x.y * s);
+      y.y = fmaf(x.x, s, x.y * c);
+      *reinterpret_cast<float2*>(a.q_rot + qrow + 2 * pi) = y;
+    }
+#pragma unroll
+    for (int j = 0; j < kAbsorbVecs; ++j) {
+      const int i = base + t + j * kAbsorbThreads;
+      if (i < nm) {
+        const int row = i / v4, c = i - row * v4;
+        *reinterpret_cast<float4*>(Ms + row * ldm + 4 * c) = r[j];
+      } else if (i < ntot) {
+        const int bt = (i - nm) / v4, c = (i - nm) - bt * v4;
+        *reinterpret_cast<float4*>(qs + bt * ldm + 4 * c) = r[j];
+      }
+    }
   }
-  asm volatile("bar.sync 1, %0;" ::"n"(kGemvThreads) : "memory");
-  const uint32_t row_bytes = static_cast<uint32_t>(a.d_n) * 4;
-  if (t == 0) mbar_arrive_expect_tx(&bar, row_bytes * static_cast<uint32_t>(a.d_v + nb));
-  asm volatile("bar.sync 1, %0;" ::"n"(kGemvThreads) : "memory");
-  if (t < 32) {
-    const float* Mh = a.M + static_cast<long long>(h) * a.d_v * a.d_n;
-    for (int i = t; i < a.d_v; i += 32)
-      bulk_g2s(Ms + i * ldm, Mh + static_cast<long long>(i) * a.d_n, row_bytes, &bar);
-    for (int bt = t; bt < nb; bt += 32)
-      bulk_g2s(qs + bt * a.d_n, a.q_c + (static_cast<long long>(b0 + bt) * a.H + h) * a.d_n, row_bytes, &bar);
-  }
-  if (!mbar_wait_bounded(&bar, 0)) {
-    if (t == 0) flag_error(a.err, GVA_DEVERR_TIMEOUT);
-    return;
-  }
+  __syncthreads();
 
   // thread -> output row i (rows split over threads) and a set of sequences (when d_v is
   // smaller than the thread count, the sequences are split over `sets` threads per row)
-  const int sets = a.d_v < kGemvThreads ? kGemvThreads / a.d_v : 1;
-  const int rows_per_pass = kGemvThreads / sets;
+  const int sets = a.d_v < kAbsorbThreads ? kAbsorbThreads / a.d_v : 1;
+  const int rows_per_pass = kAbsorbThreads / sets;
   const int set = t / rows_per_pass;
   for (int i = t % rows_per_pass; i < a.d_v; i += rows_per_pass) {
     float acc[kAbsorbSeqs];
@@ -106,7 +120,7 @@ __global__ void __launch_bounds__(kAbsorbThreads) absorb_kernel(const AbsorbArgs
       for (int j = 0; j < kAbsorbSeqs; ++j) {
         const int bt = set + j * sets;
         if (bt < nb) {
-          const float4 q4 = *reinterpret_cast<const float4*>(qs + bt * a.d_n + k);
+          const float4 q4 = *reinterpret_cast<const float4*>(qs + bt * ldm + k);
           acc[j] = fmaf(m4.x, q4.x, acc[j]);
           acc[j] = fmaf(m4.y, q4.y, acc[j]);
           acc[j] = fmaf(m4.z, q4.z, acc[j]);
@@ -139,9 +153,9 @@ cudaError_t launch_absorb(const gva_ctx* ctx, int B, const float* q_c, const flo
   a.d_v = ctx->dims.d_v;
   a.d_n = ctx->dims.d_n;
   a.d_r = ctx->dims.d_r;
-  a.rope = ctx->d_rope;
+  a.rope = ctx->d_rope32;
   a.err = ctx->d_err;
-  const size_t smem = sizeof(float) * (static_cast<size_t>(a.d_v) * (a.d_n + 4) + kAbsorbSeqs * a.d_n);
+  const size_t smem = sizeof(float) * static_cast<size_t>(a.d_v + kAbsorbSeqs) * (a.d_n + 4);
   if (smem > 200 * 1024) return cudaErrorInvalidValue;
   static int configured[kMaxDevicesHost] = {};
   int dev = 0;

@@ -19,24 +19,33 @@ bool on_ctx_device(const gva_ctx* ctx) {
 
 gva_status from_cuda(cudaError_t e) { return e == cudaSuccess ? GVA_OK : GVA_ERR_CUDA; }
 
-// RoPE digit table: entry (k, dgt, i) holds cos and sin of dgt * 256^k * theta_i,
-// theta_i = base^(-2i/d_r), in fp64 (pairs (2i, 2i+1) turned by position * theta_i).
+// RoPE digit tables: entry (k, dgt, i) holds cos and sin of dgt * 256^k * theta_i,
+// theta_i = base^(-2i/d_r), in fp64 (pairs (2i, 2i+1) turned by position * theta_i), and
+// the same values rounded to fp32.
 bool build_rope_table(gva_ctx* ctx) {
   const int pairs = ctx->dims.d_r / 2;
   if (pairs == 0) return true;
   const size_t n = static_cast<size_t>(4) * 256 * pairs;
   double2* host = static_cast<double2*>(malloc(n * sizeof(double2)));
-  if (!host) return false;
-  for (int k = 0; k < 4; ++k)
-    for (int dgt = 0; dgt < 256; ++dgt)
-      for (int i = 0; i < pairs; ++i) {
-        const double theta = pow(ctx->rope_base, -2.0 * i / static_cast<double>(ctx->dims.d_r));
-        const double a = ldexp(static_cast<double>(dgt), 8 * k) * theta;
-        host[(static_cast<size_t>(k) * 256 + dgt) * pairs + i] = make_double2(cos(a), sin(a));
-      }
-  bool ok = cudaMalloc(reinterpret_cast<void**>(&ctx->d_rope), n * sizeof(double2)) == cudaSuccess &&
-            cudaMemcpy(ctx->d_rope, host, n * sizeof(double2), cudaMemcpyHostToDevice) == cudaSuccess;
+  float2* host32 = static_cast<float2*>(malloc(n * sizeof(float2)));
+  bool ok = host && host32;
+  if (ok) {
+    for (int k = 0; k < 4; ++k)
+      for (int dgt = 0; dgt < 256; ++dgt)
+        for (int i = 0; i < pairs; ++i) {
+          const double theta = pow(ctx->rope_base, -2.0 * i / static_cast<double>(ctx->dims.d_r));
+          const double a = ldexp(static_cast<double>(dgt), 8 * k) * theta;
+          const size_t e = (static_cast<size_t>(k) * 256 + dgt) * pairs + i;
+          host[e] = make_double2(cos(a), sin(a));
+          host32[e] = make_float2(static_cast<float>(host[e].x), static_cast<float>(host[e].y));
+        }
+    ok = cudaMalloc(reinterpret_cast<void**>(&ctx->d_rope), n * sizeof(double2)) == cudaSuccess &&
+         cudaMemcpy(ctx->d_rope, host, n * sizeof(double2), cudaMemcpyHostToDevice) == cudaSuccess &&
+         cudaMalloc(reinterpret_cast<void**>(&ctx->d_rope32), n * sizeof(float2)) == cudaSuccess &&
+         cudaMemcpy(ctx->d_rope32, host32, n * sizeof(float2), cudaMemcpyHostToDevice) == cudaSuccess;
+  }
   free(host);
+  free(host32);
   return ok;
 }
 
@@ -189,6 +198,7 @@ void gva_destroy(gva_ctx* ctx) {
   if (!ctx) return;
   if (ctx->d_err) cudaFree(ctx->d_err);
   if (ctx->d_rope) cudaFree(ctx->d_rope);
+  if (ctx->d_rope32) cudaFree(ctx->d_rope32);
   free(ctx);
 }
 

@@ -5,8 +5,10 @@
 // separately cached, rotated positional key: abstract "Grouped Value Attention: Efficient
 // KV Caching via On-Demand Key Reconstruction"; review "[논문리뷰] Grouped Value Attention",
 // section 3, Decoupled RoPE).  One warp per token: the value rows move as 16-byte vectors
-// (loaded before the slot is known), lanes rotate the positional pairs in fp64 and round
-// once to the cache dtype.
+// (loaded before the slot is known), lanes rotate the positional pairs (fp32 for bf16
+// caches, fp64 for fp32 caches) and round once to the cache dtype.
+#include <type_traits>
+
 #include "gva_device.cuh"
 #include "gva_internal.h"
 #include "gva_sched.cuh"
@@ -21,7 +23,8 @@ struct AppendArgs {
   const int32_t* block_table;
   void* v_pool;
   void* kr_pool;
-  const double2* rope;
+  const double2* rope;   // fp64 RoPE digit table (fp32 caches)
+  const float2* rope32;  // fp32 RoPE digit table (bf16 caches)
   unsigned* err;
   int B, n, G, d_v, d_r, max_blocks, num_blocks;
 };
@@ -55,11 +58,16 @@ __global__ void __launch_bounds__(kAppendThreads) append_kernel(const AppendArgs
     if (i < nvec) vreg[c] = src[i];
   }
   const int pairs = a.d_r / 2;
+  // bf16 keys are rotated in fp32: its error (a few units of 2^-24, relative) moves the bf16
+  // result only for values that close to a rounding boundary, and then by one ulp.  fp32
+  // keys are rotated in fp64 and rounded once.
+  constexpr bool kF64 = sizeof(T) == 4;
+  using R = typename std::conditional<kF64, double, float>::type;
   const T* x = static_cast<const T*>(a.kr_new) + tok * a.d_r;
-  double x0 = 0.0, x1 = 0.0;
+  R x0 = 0, x1 = 0;
   if (lane < pairs) {
-    x0 = CacheElem<T>::to_double(x[2 * lane]);
-    x1 = CacheElem<T>::to_double(x[2 * lane + 1]);
+    x0 = static_cast<R>(CacheElem<T>::to_float(x[2 * lane]));
+    x1 = static_cast<R>(CacheElem<T>::to_float(x[2 * lane + 1]));
   }
   const long long p = static_cast<long long>(a.pos[b]) + t;
 
@@ -69,8 +77,13 @@ __global__ void __launch_bounds__(kAppendThreads) append_kernel(const AppendArgs
     return;
   }
   const int blk = a.block_table[static_cast<long long>(b) * a.max_blocks + (p >> 6)];
-  double c = 1.0, s = 0.0;
-  if (lane < pairs) rope_cos_sin(a.rope, pairs, p, lane, c, s);
+  R c = 1, s = 0;
+  if (lane < pairs) {
+    if constexpr (kF64)
+      rope_cos_sin(a.rope, pairs, p, lane, c, s);
+    else
+      rope_cos_sin_f32(a.rope32, pairs, p, lane, c, s);
+  }
   if (blk < 0 || blk >= a.num_blocks) {
     if (lane == 0) flag_error(a.err, GVA_DEVERR_BLOCK_ID);
     return;
@@ -94,11 +107,16 @@ __global__ void __launch_bounds__(kAppendThreads) append_kernel(const AppendArgs
   // Shared positional key, rotated to position p: pair (2i, 2i+1) turned by p*theta_i.
   T* y = static_cast<T*>(a.kr_pool) + (static_cast<long long>(blk) * kBlockTokens + o) * a.d_r;
   if (lane < pairs) {
-    // explicit roundings (no contraction) so each product is rounded on its own
-    const double y0 = __dsub_rn(__dmul_rn(x0, c), __dmul_rn(x1, s));
-    const double y1 = __dadd_rn(__dmul_rn(x0, s), __dmul_rn(x1, c));
-    y[2 * lane] = CacheElem<T>::from_double(y0);
-    y[2 * lane + 1] = CacheElem<T>::from_double(y1);
+    if constexpr (kF64) {
+      // explicit roundings (no contraction) so each product is rounded on its own
+      const double y0 = __dsub_rn(__dmul_rn(x0, c), __dmul_rn(x1, s));
+      const double y1 = __dadd_rn(__dmul_rn(x0, s), __dmul_rn(x1, c));
+      y[2 * lane] = CacheElem<T>::from_double(y0);
+      y[2 * lane + 1] = CacheElem<T>::from_double(y1);
+    } else {
+      y[2 * lane] = __float2bfloat16_rn(fmaf(x0, c, -x1 * s));
+      y[2 * lane + 1] = __float2bfloat16_rn(fmaf(x0, s, x1 * c));
+    }
   }
 }
 
@@ -124,6 +142,7 @@ cudaError_t launch_append(const gva_ctx* ctx, int B, int n, const void* v_new,
   a.max_blocks = max_blocks;
   a.num_blocks = num_blocks;
   a.rope = ctx->d_rope;
+  a.rope32 = ctx->d_rope32;
   const long long threads = static_cast<long long>(B) * n * 32;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>((threads + kAppendThreads - 1) / kAppendThreads));

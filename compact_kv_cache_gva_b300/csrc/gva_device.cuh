@@ -146,26 +146,53 @@ struct CacheElem<__nv_bfloat16> {
 // RoPE rotation of pair i at position p >= 0: (cos, sin) of p * theta_i, theta_i =
 // base^(-2i/d_r).  The context holds, per 8-bit digit of the position, the fp64 cos/sin of
 // digit * 256^k * theta_i (computed on the host); the angle of p is the sum of its digits'
-// angles, so the rotation is the product of at most four table rotations (fp64 complex
-// products).  No transcendental function runs on the device and every int32 position is
-// covered.  Table layout: [4 levels][256 digits][pairs] of double2 (cos, sin).
+// angles, so the rotation is the product of four table rotations (fp64 complex products).
+// No transcendental function runs on the device and every int32 position is covered.  The
+// four table rows are loaded together (one memory round trip); the digit-0 row is exactly
+// (1, 0), so multiplying by it changes nothing.  Table layout: [4 levels][256 digits][pairs]
+// of double2 (cos, sin).
 constexpr int kRopeLevels = 4;
 constexpr int kRopeDigits = 256;
 
 __device__ __forceinline__ void rope_cos_sin(const double2* __restrict__ tab, int pairs,
                                              long long p, int i, double& c, double& s) {
-  c = 1.0;
-  s = 0.0;
+  double2 r[kRopeLevels];
 #pragma unroll
   for (int k = 0; k < kRopeLevels; ++k) {
     const int dgt = static_cast<int>((p >> (8 * k)) & (kRopeDigits - 1));
-    if (dgt) {
-      const double2 r = tab[(k * kRopeDigits + dgt) * pairs + i];
-      const double c2 = c * r.x - s * r.y;
-      const double s2 = s * r.x + c * r.y;
-      c = c2;
-      s = s2;
-    }
+    r[k] = __ldg(&tab[(k * kRopeDigits + dgt) * pairs + i]);
+  }
+  c = r[0].x;
+  s = r[0].y;
+#pragma unroll
+  for (int k = 1; k < kRopeLevels; ++k) {
+    const double c2 = __dsub_rn(__dmul_rn(c, r[k].x), __dmul_rn(s, r[k].y));
+    const double s2 = __dadd_rn(__dmul_rn(s, r[k].x), __dmul_rn(c, r[k].y));
+    c = c2;
+    s = s2;
+  }
+}
+
+// The same rotation composed in fp32 from the fp32 table (B300's fp64 rate is a small
+// fraction of its fp32 rate).  Each table entry is the fp64 value rounded once, so the
+// result carries a relative error of a few units of 2^-24: ample for fp32 queries and for
+// keys rounded to bf16 afterwards.
+__device__ __forceinline__ void rope_cos_sin_f32(const float2* __restrict__ tab, int pairs,
+                                                 long long p, int i, float& c, float& s) {
+  float2 r[kRopeLevels];
+#pragma unroll
+  for (int k = 0; k < kRopeLevels; ++k) {
+    const int dgt = static_cast<int>((p >> (8 * k)) & (kRopeDigits - 1));
+    r[k] = __ldg(&tab[(k * kRopeDigits + dgt) * pairs + i]);
+  }
+  c = r[0].x;
+  s = r[0].y;
+#pragma unroll
+  for (int k = 1; k < kRopeLevels; ++k) {
+    const float c2 = fmaf(c, r[k].x, -s * r[k].y);
+    const float s2 = fmaf(s, r[k].x, c * r[k].y);
+    c = c2;
+    s = s2;
   }
 }
 

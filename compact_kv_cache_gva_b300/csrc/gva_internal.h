@@ -15,7 +15,8 @@ struct gva_ctx {
   int device;           // device the context was created on
   int num_sms;          // SM count of that device
   unsigned* d_err;      // device error word
-  double2* d_rope;      // RoPE digit table [4][256][d_r/2] (nullptr when d_r == 0)
+  double2* d_rope;      // RoPE digit table [4][256][d_r/2] in fp64 (nullptr when d_r == 0)
+  float2* d_rope32;     // the same table rounded to fp32
   int split_tokens;     // 0 = automatic
   gva_decode_path path;
 };

@@ -90,7 +90,9 @@ typedef struct {
 typedef struct gva_ctx gva_ctx;
 
 /* Validates dims and creates a context bound to the CURRENT device: it holds the dims, the
- * decode options and a device error word (4 bytes of cudaMalloc).  Returns
+ * decode options, a device error word and the RoPE digit tables (cos and sin of every 8-bit
+ * digit of a position times each pair's frequency, computed in fp64 on the host, kept in fp64 and fp32; 12*d_r KB
+ * of cudaMalloc in all).  Returns
  * GVA_ERR_INVALID_ARG / GVA_ERR_UNSUPPORTED for bad dims, GVA_ERR_CUDA if the allocation
  * fails.  *out is set only on success. */
 gva_status gva_create(const gva_dims* dims, gva_ctx** out);
@@ -109,7 +111,9 @@ void gva_destroy(gva_ctx* ctx);
  *   M     [H,d_v,d_n] f32    key maps, M[h][i][k]
  *   q_abs [B,H,d_v] f32 out  absorbed query (no scale folded in)
  *   q_rot [B,H,d_r] f32 out  rotated positional query (may be NULL when d_r == 0)
- * fp32 accumulation; the rotation angle, sin and cos are fp64.  B == 0 is a no-op. */
+ * fp32 accumulation.  The rotation for position p is the product of the table rotations of
+ * p's four bytes, composed in fp32 (relative error a few units of 2^-24).  B == 0 is a
+ * no-op. */
 gva_status gva_absorb_query(gva_ctx* ctx, int B, const float* q_c, const float* q_r,
                             const int32_t* pos_q, const float* M, float* q_abs, float* q_rot,
                             gva_stream_t stream);
@@ -120,7 +124,8 @@ gva_status gva_absorb_query(gva_ctx* ctx, int B, const float* q_c, const float* 
  * the abstract and the review's section 3: grouped values plus one rotated positional key).
  *   v_new  [B,n,G,d_v] cache dtype   new values, copied bit for bit
  *   kr_new [B,n,d_r]   cache dtype   new positional keys, UNROTATED; each is rotated to its
- *                                    own position in fp64 and rounded to nearest even
+ *                                    own position (fp64 for fp32 caches, fp32 for bf16
+ *                                    caches) and rounded once to nearest even
  *   pos    [B] int32                 position of the first new token of each sequence
  *   block_table [B,max_blocks] int32, pools as in the layout above (NB = num_blocks)
  * Token t of sequence b goes to position pos[b]+t.  A position beyond the table or a block
