@@ -104,35 +104,22 @@ __global__ void __launch_bounds__(kAbsorbThreads) absorb_kernel(const AbsorbArgs
   }
   __syncthreads();
 
-  // thread -> output row i (rows split over threads) and a set of sequences (when d_v is
-  // smaller than the thread count, the sequences are split over `sets` threads per row)
-  const int sets = a.d_v < kAbsorbThreads ? kAbsorbThreads / a.d_v : 1;
-  const int rows_per_pass = kAbsorbThreads / sets;
-  const int set = t / rows_per_pass;
-  for (int i = t % rows_per_pass; i < a.d_v; i += rows_per_pass) {
-    float acc[kAbsorbSeqs];
-#pragma unroll
-    for (int j = 0; j < kAbsorbSeqs; ++j) acc[j] = 0.f;
+  // one dot product per output (sequence bt, row i), over d_n in k order; consecutive
+  // threads take consecutive rows, so the query vector read is a shared-memory broadcast
+  for (int o = t; o < nb * a.d_v; o += kAbsorbThreads) {
+    const int bt = o / a.d_v, i = o - bt * a.d_v;
     const float* mrow = Ms + i * ldm;
+    const float* qrow = qs + bt * ldm;
+    float acc = 0.f;
     for (int k = 0; k < a.d_n; k += 4) {
       const float4 m4 = *reinterpret_cast<const float4*>(mrow + k);
-#pragma unroll
-      for (int j = 0; j < kAbsorbSeqs; ++j) {
-        const int bt = set + j * sets;
-        if (bt < nb) {
-          const float4 q4 = *reinterpret_cast<const float4*>(qs + bt * ldm + k);
-          acc[j] = fmaf(m4.x, q4.x, acc[j]);
-          acc[j] = fmaf(m4.y, q4.y, acc[j]);
-          acc[j] = fmaf(m4.z, q4.z, acc[j]);
-          acc[j] = fmaf(m4.w, q4.w, acc[j]);
-        }
-      }
+      const float4 q4 = *reinterpret_cast<const float4*>(qrow + k);
+      acc = fmaf(m4.x, q4.x, acc);
+      acc = fmaf(m4.y, q4.y, acc);
+      acc = fmaf(m4.z, q4.z, acc);
+      acc = fmaf(m4.w, q4.w, acc);
     }
-#pragma unroll
-    for (int j = 0; j < kAbsorbSeqs; ++j) {
-      const int bt = set + j * sets;
-      if (bt < nb) a.q_abs[(static_cast<long long>(b0 + bt) * a.H + h) * a.d_v + i] = acc[j];
-    }
+    a.q_abs[(static_cast<long long>(b0 + bt) * a.H + h) * a.d_v + i] = acc;
   }
 }
 
