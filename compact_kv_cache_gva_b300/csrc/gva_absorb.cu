@@ -104,22 +104,47 @@ __global__ void __launch_bounds__(kAbsorbThreads) absorb_kernel(const AbsorbArgs
   }
   __syncthreads();
 
-  // one dot product per output (sequence bt, row i), over d_n in k order; consecutive
-  // threads take consecutive rows, so the query vector read is a shared-memory broadcast
-  for (int o = t; o < nb * a.d_v; o += kAbsorbThreads) {
-    const int bt = o / a.d_v, i = o - bt * a.d_v;
-    const float* mrow = Ms + i * ldm;
-    const float* qrow = qs + bt * ldm;
-    float acc = 0.f;
+  // Register tiles of 2 rows x 4 sequences per thread: rows i and i + d_v/2 (the two rows'
+  // 16-byte reads stay conflict-free across a warp), sequences 4s..4s+3 (the warp shares s,
+  // so the query reads are broadcasts).  6 shared-memory reads feed 32 FMAs; each output
+  // is one dot product in k order.
+  const int half = a.d_v / 2;
+  const int nsb = (nb + 3) / 4;
+  for (int o = t; o < half * nsb; o += kAbsorbThreads) {
+    const int i = o % half, sb = o / half;
+    const float* m0 = Ms + i * ldm;
+    const float* m1 = Ms + (i + half) * ldm;
+    float acc[2][4];
+#pragma unroll
+    for (int r = 0; r < 2; ++r)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) acc[r][j] = 0.f;
     for (int k = 0; k < a.d_n; k += 4) {
-      const float4 m4 = *reinterpret_cast<const float4*>(mrow + k);
-      const float4 q4 = *reinterpret_cast<const float4*>(qrow + k);
-      acc = fmaf(m4.x, q4.x, acc);
-      acc = fmaf(m4.y, q4.y, acc);
-      acc = fmaf(m4.z, q4.z, acc);
-      acc = fmaf(m4.w, q4.w, acc);
+      const float4 ma = *reinterpret_cast<const float4*>(m0 + k);
+      const float4 mb = *reinterpret_cast<const float4*>(m1 + k);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int bt = min(4 * sb + j, nb - 1);  // rows past nb repeat a valid one, unused
+        const float4 q4 = *reinterpret_cast<const float4*>(qs + bt * ldm + k);
+        acc[0][j] = fmaf(ma.x, q4.x, acc[0][j]);
+        acc[0][j] = fmaf(ma.y, q4.y, acc[0][j]);
+        acc[0][j] = fmaf(ma.z, q4.z, acc[0][j]);
+        acc[0][j] = fmaf(ma.w, q4.w, acc[0][j]);
+        acc[1][j] = fmaf(mb.x, q4.x, acc[1][j]);
+        acc[1][j] = fmaf(mb.y, q4.y, acc[1][j]);
+        acc[1][j] = fmaf(mb.z, q4.z, acc[1][j]);
+        acc[1][j] = fmaf(mb.w, q4.w, acc[1][j]);
+      }
     }
-    a.q_abs[(static_cast<long long>(b0 + bt) * a.H + h) * a.d_v + i] = acc;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int bt = 4 * sb + j;
+      if (bt < nb) {
+        float* dst = a.q_abs + (static_cast<long long>(b0 + bt) * a.H + h) * a.d_v;
+        dst[i] = acc[0][j];
+        dst[i + half] = acc[1][j];
+      }
+    }
   }
 }
 

@@ -6,7 +6,7 @@
 // segment's units [g*cum[B] + cum[b], ... + nt_b) (range_of, gva_sched.cuh); record index =
 // (range + f)*C + warp, so a segment's records are one contiguous block, and warp_touched
 // says which records of the block hold data.  One CTA per (g, b) stages that block into
-// shared memory with bulk copies (one round trip per 64 KB round, usually one), then merges
+// shared memory with bulk copies (one round trip per 32 KB round, usually one), then merges
 // it with online rescaling between rounds.  Launched as a programmatic dependent
 // of the partial kernel, so its launch overlaps that kernel's run; it waits for the partial
 // results before reading them.
@@ -21,7 +21,7 @@ namespace {
 
 constexpr int kCombineWarps = 8;
 constexpr int kCombineThreads = 32 * kCombineWarps;
-constexpr int kStageBytes = 64 * 1024;  // records staged per round
+constexpr int kStageBytes = 32 * 1024;  // records staged per round (7 CTAs fit on an SM)
 
 template <int DV, int R>
 struct CombineShape {

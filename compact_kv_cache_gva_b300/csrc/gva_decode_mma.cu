@@ -207,13 +207,14 @@ __global__ void __launch_bounds__(kMmaMaxThreads, 1) decode_mma_kernel(const Dec
       if (d < n_mine) {
         const UnitCursor cu = cursor_at(u0 + c + static_cast<long long>(P) * d, cum, a.B, a.G);
         grp = cu.g;
+        const int T = a.seq_lens[cu.b];  // issued beside the table read: one round trip
         if (cu.t >= a.max_blocks) {
           flag_error(a.err, GVA_DEVERR_POSITION);
         } else {
           const int id = a.block_table[static_cast<long long>(cu.b) * a.max_blocks + cu.t];
           if (id >= 0 && id < a.num_blocks) {
             blk = id;
-            nv = min(kBlockTokens, a.seq_lens[cu.b] - cu.t * kBlockTokens);
+            nv = min(kBlockTokens, T - cu.t * kBlockTokens);
           } else {
             flag_error(a.err, GVA_DEVERR_BLOCK_ID);
           }

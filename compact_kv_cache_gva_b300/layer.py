@@ -22,6 +22,7 @@ class GVADecodeLayer:
         self.out = torch.empty((B, H, d_v), dtype=torch.float32, device=device)
         ws = max(16, gva.gva_decode_workspace_size(self.ctx, B, max_seq_len))
         self.workspace = torch.empty(ws, dtype=torch.uint8, device=device)
+        self._side = None  # side stream of step(overlap=True), created on first use
 
     def plan(self):
         return gva.gva_decode_plan(self.ctx, self.B, self.max_seq_len)
@@ -40,11 +41,25 @@ class GVADecodeLayer:
                                  self.max_seq_len, self.out, self.workspace, stream)
         return self.out
 
-    def step(self, q_c, q_r, pos_q, M, v_new, kr_new, pos_new, block_table, seq_lens, v_pool, kr_pool, stream=None):
-        """absorb the query, append the new token(s), attend through the current position."""
-        self.absorb(q_c, q_r, pos_q, M, stream)
-        self.append(v_new, kr_new, pos_new, block_table, v_pool, kr_pool, stream)
-        return self.attend(v_pool, kr_pool, block_table, seq_lens, stream=stream)
+    def step(self, q_c, q_r, pos_q, M, v_new, kr_new, pos_new, block_table, seq_lens, v_pool, kr_pool, stream=None,
+             overlap=True):
+        """absorb the query, append the new token(s), attend through the current position.
+
+        The append does not depend on the absorbed query, so with overlap=True it is issued on a
+        side stream that forks from and joins back into the step's stream (also inside CUDA-graph
+        capture), and the two small kernels run side by side."""
+        main = torch.cuda.current_stream() if stream is None else stream
+        if not overlap:
+            self.absorb(q_c, q_r, pos_q, M, main)
+            self.append(v_new, kr_new, pos_new, block_table, v_pool, kr_pool, main)
+            return self.attend(v_pool, kr_pool, block_table, seq_lens, stream=main)
+        if self._side is None:
+            self._side = torch.cuda.Stream(device=main.device)
+        self._side.wait_stream(main)
+        self.append(v_new, kr_new, pos_new, block_table, v_pool, kr_pool, self._side)
+        self.absorb(q_c, q_r, pos_q, M, main)
+        main.wait_stream(self._side)
+        return self.attend(v_pool, kr_pool, block_table, seq_lens, stream=main)
 
     def device_error(self):
         return gva.gva_get_device_error(self.ctx)
