@@ -102,27 +102,35 @@ bool make_plan(const gva_ctx* ctx, int B, int max_seq_len, bool sep_k, gva::Plan
   return true;
 }
 
-gva_status decode_common(gva_ctx* ctx, bool sep_k, int B, const float* q_abs, const float* q_rot,
-                         const void* k_pool, const void* v_pool, const void* kr_pool,
-                         const int32_t* block_table, int max_blocks, int num_blocks,
-                         const int32_t* seq_lens, int max_seq_len, float* out, void* workspace,
-                         size_t ws_bytes, cudaStream_t stream) {
-  if (!ctx || B < 0 || max_seq_len < 1 || max_blocks < 1 || num_blocks < 1)
-    return GVA_ERR_INVALID_ARG;
+// Phases of a decode call: the split-T partial pass and the combine pass.
+constexpr int kPhasePartial = 1;
+constexpr int kPhaseCombine = 2;
+
+gva_status decode_common(gva_ctx* ctx, bool sep_k, int phases, int B, const float* q_abs,
+                         const float* q_rot, const void* k_pool, const void* v_pool,
+                         const void* kr_pool, const int32_t* block_table, int max_blocks,
+                         int num_blocks, const int32_t* seq_lens, int max_seq_len, float* out,
+                         void* workspace, size_t ws_bytes, cudaStream_t stream) {
+  const bool partial = phases & kPhasePartial, combine = phases & kPhaseCombine;
+  if (!ctx || B < 0 || max_seq_len < 1) return GVA_ERR_INVALID_ARG;
+  if (partial && (max_blocks < 1 || num_blocks < 1)) return GVA_ERR_INVALID_ARG;
   if (B == 0) return GVA_OK;
   if (B > gva::kMaxBatch) return GVA_ERR_UNSUPPORTED;  // prefix sums live in shared memory
   const gva_dims& d = ctx->dims;
-  if (!q_abs || !v_pool || !block_table || !seq_lens || !out) return GVA_ERR_INVALID_ARG;
-  if (sep_k && !k_pool) return GVA_ERR_INVALID_ARG;
-  if (!sep_k && d.d_r > 0 && (!q_rot || !kr_pool)) return GVA_ERR_INVALID_ARG;
-  if (static_cast<long long>(max_blocks) * GVA_BLOCK_TOKENS < max_seq_len) return GVA_ERR_INVALID_ARG;
-  if (!aligned16(q_abs) || !aligned16(v_pool) || !aligned16(out) || (k_pool && !aligned16(k_pool)) ||
-      (kr_pool && !aligned16(kr_pool)) || (q_rot && !aligned16(q_rot)))
-    return GVA_ERR_INVALID_ARG;
+  if (partial) {
+    if (!q_abs || !v_pool || !block_table || !seq_lens) return GVA_ERR_INVALID_ARG;
+    if (sep_k && !k_pool) return GVA_ERR_INVALID_ARG;
+    if (!sep_k && d.d_r > 0 && (!q_rot || !kr_pool)) return GVA_ERR_INVALID_ARG;
+    if (static_cast<long long>(max_blocks) * GVA_BLOCK_TOKENS < max_seq_len) return GVA_ERR_INVALID_ARG;
+    if (!aligned16(q_abs) || !aligned16(v_pool) || (k_pool && !aligned16(k_pool)) ||
+        (kr_pool && !aligned16(kr_pool)) || (q_rot && !aligned16(q_rot)))
+      return GVA_ERR_INVALID_ARG;
+  }
+  if (combine && (!out || !aligned16(out))) return GVA_ERR_INVALID_ARG;
   if (!on_ctx_device(ctx)) return GVA_ERR_INVALID_ARG;
   gva::Plan plan;
   if (!make_plan(ctx, B, max_seq_len, sep_k, &plan)) return GVA_ERR_UNSUPPORTED;
-  if (plan.path == GVA_PATH_MMA &&
+  if (partial && plan.path == GVA_PATH_MMA &&
       static_cast<long long>(num_blocks) * d.G * GVA_BLOCK_TOKENS >= (1LL << 31))
     return GVA_ERR_UNSUPPORTED;  // token rows are int32 tensor-copy coordinates
   if (!workspace || ws_bytes < plan.ws_bytes || !aligned16(workspace)) return GVA_ERR_WORKSPACE;
@@ -151,11 +159,13 @@ gva_status decode_common(gva_ctx* ctx, bool sep_k, int B, const float* q_abs, co
   a.group_warps = plan.group_warps;
   a.n_stages = plan.n_stages;
   a.scale_log2 = static_cast<float>(static_cast<double>(ctx->scale) * 1.4426950408889634);
-  cudaError_t e = plan.path == GVA_PATH_MMA
-                      ? gva::launch_decode_mma(a, sep_k, plan.grid, stream)
-                      : gva::launch_decode_fma(a, d.cache_dtype, sep_k, plan.grid, stream);
-  if (e != cudaSuccess) return GVA_ERR_CUDA;
-  return from_cuda(gva::launch_combine(a, stream));
+  if (partial) {
+    const cudaError_t e = plan.path == GVA_PATH_MMA
+                              ? gva::launch_decode_mma(a, sep_k, plan.grid, stream)
+                              : gva::launch_decode_fma(a, d.cache_dtype, sep_k, plan.grid, stream);
+    if (e != cudaSuccess) return GVA_ERR_CUDA;
+  }
+  return combine ? from_cuda(gva::launch_combine(a, stream)) : GVA_OK;
 }
 
 }  // namespace
@@ -253,8 +263,25 @@ gva_status gva_decode_attention(gva_ctx* ctx, int B, const float* q_abs, const f
                                 const int32_t* block_table, int max_blocks, int num_blocks,
                                 const int32_t* seq_lens, int max_seq_len, float* out,
                                 void* workspace, size_t ws_bytes, gva_stream_t stream) {
-  return decode_common(ctx, false, B, q_abs, q_rot, nullptr, v_pool, kr_pool, block_table,
-                       max_blocks, num_blocks, seq_lens, max_seq_len, out, workspace, ws_bytes,
+  return decode_common(ctx, false, kPhasePartial | kPhaseCombine, B, q_abs, q_rot, nullptr, v_pool,
+                       kr_pool, block_table, max_blocks, num_blocks, seq_lens, max_seq_len, out,
+                       workspace, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+gva_status gva_decode_partial(gva_ctx* ctx, int B, const float* q_abs, const float* q_rot,
+                              const void* v_pool, const void* kr_pool, const int32_t* block_table,
+                              int max_blocks, int num_blocks, const int32_t* seq_lens,
+                              int max_seq_len, void* workspace, size_t ws_bytes,
+                              gva_stream_t stream) {
+  return decode_common(ctx, false, kPhasePartial, B, q_abs, q_rot, nullptr, v_pool, kr_pool,
+                       block_table, max_blocks, num_blocks, seq_lens, max_seq_len, nullptr,
+                       workspace, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+gva_status gva_decode_combine(gva_ctx* ctx, int B, int max_seq_len, float* out, void* workspace,
+                              size_t ws_bytes, gva_stream_t stream) {
+  return decode_common(ctx, false, kPhaseCombine, B, nullptr, nullptr, nullptr, nullptr, nullptr,
+                       nullptr, 0, 0, nullptr, max_seq_len, out, workspace, ws_bytes,
                        reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -264,9 +291,9 @@ gva_status gqa_decode_attention(gva_ctx* ctx, int B, const float* q, const void*
                                 float* out, void* workspace, size_t ws_bytes,
                                 gva_stream_t stream) {
   if (ctx && ctx->dims.d_r != 0) return GVA_ERR_INVALID_ARG;
-  return decode_common(ctx, true, B, q, nullptr, k_pool, v_pool, nullptr, block_table,
-                       max_blocks, num_blocks, seq_lens, max_seq_len, out, workspace, ws_bytes,
-                       reinterpret_cast<cudaStream_t>(stream));
+  return decode_common(ctx, true, kPhasePartial | kPhaseCombine, B, q, nullptr, k_pool, v_pool,
+                       nullptr, block_table, max_blocks, num_blocks, seq_lens, max_seq_len, out,
+                       workspace, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
 }
 
 gva_status gva_set_split_tokens(gva_ctx* ctx, int split_tokens) {

@@ -24,7 +24,7 @@ BLOCK_TOKENS = 64
 EXPORTS = ("gva_create", "gva_destroy", "gva_absorb_query", "gva_cache_append", "gva_decode_workspace_size",
            "gva_decode_attention", "gqa_decode_attention", "gva_set_split_tokens", "gva_set_decode_path",
            "gva_decode_plan", "gva_get_device_error", "gva_status_string", "gva_version",
-           "gva_decode_attention_noalloc")
+           "gva_decode_attention_noalloc", "gva_decode_partial", "gva_decode_combine")
 NOALLOC_SCRATCH_BYTES = 4 << 20
 
 
@@ -61,6 +61,8 @@ def load():
     L.gva_decode_attention.argtypes = [vp, i, vp, vp, vp, vp, ip, i, i, ip, i, vp, vp, C.c_size_t, st]
     L.gqa_decode_attention.argtypes = [vp, i, vp, vp, vp, ip, i, i, ip, i, vp, vp, C.c_size_t, st]
     L.gva_decode_attention_noalloc.argtypes = [vp, i, vp, vp, vp, vp, ip, i, i, ip, i, vp, st]
+    L.gva_decode_partial.argtypes = [vp, i, vp, vp, vp, vp, ip, i, i, ip, i, vp, C.c_size_t, st]
+    L.gva_decode_combine.argtypes = [vp, i, i, vp, vp, C.c_size_t, st]
     L.gva_set_split_tokens.argtypes = [vp, i]
     L.gva_set_decode_path.argtypes = [vp, i]
     L.gva_decode_plan.argtypes = [vp, i, i, C.POINTER(C.c_int), C.POINTER(C.c_int)]
@@ -231,6 +233,38 @@ def gva_decode_attention(ctx, q_abs, q_rot, v_pool, kr_pool, block_table, seq_le
                                        _ptr(out, torch.float32, "out"), _ptr(workspace, None, "workspace"),
                                        workspace.numel() * workspace.element_size(), _stream(stream)),
            "gva_decode_attention")
+
+
+def gva_decode_partial(ctx, q_abs, q_rot, v_pool, kr_pool, block_table, seq_lens, max_seq_len, workspace,
+                       stream=None):
+    """The split-T pass of gva_decode_attention alone; its results stay in the workspace."""
+    d = ctx.dims
+    B = q_abs.shape[0]
+    dt = ctx.cache_torch_dtype
+    has_r = d.d_r > 0
+    _shape(q_abs, (B, d.H, d.d_v), "q_abs")
+    if has_r:
+        _shape(q_rot, (B, d.H, d.d_r), "q_rot")
+    _check_table(block_table, B, seq_lens)
+    _check_pools(ctx, v_pool, kr_pool if has_r else None)
+    _check(load().gva_decode_partial(ctx.handle, B, _ptr(q_abs, torch.float32, "q_abs"),
+                                     _ptr(q_rot, torch.float32, "q_rot", allow_none=not has_r),
+                                     _ptr(v_pool, dt, "v_pool"), _ptr(kr_pool, dt, "kr_pool", allow_none=not has_r),
+                                     _ptr(block_table, torch.int32, "block_table"), block_table.shape[1],
+                                     v_pool.shape[0], _ptr(seq_lens, torch.int32, "seq_lens"), int(max_seq_len),
+                                     _ptr(workspace, None, "workspace"), workspace.numel() * workspace.element_size(),
+                                     _stream(stream)),
+           "gva_decode_partial")
+
+
+def gva_decode_combine(ctx, B, max_seq_len, out, workspace, stream=None):
+    """The combine pass: merges the partial results of the preceding gva_decode_partial into out."""
+    d = ctx.dims
+    _shape(out, (B, d.H, d.d_v), "out")
+    _check(load().gva_decode_combine(ctx.handle, int(B), int(max_seq_len), _ptr(out, torch.float32, "out"),
+                                     _ptr(workspace, None, "workspace"),
+                                     workspace.numel() * workspace.element_size(), _stream(stream)),
+           "gva_decode_combine")
 
 
 def gva_decode_attention_noalloc(ctx, q_abs, q_rot, v_pool, kr_pool, block_table, seq_lens, max_seq_len, out,

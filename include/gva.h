@@ -163,6 +163,24 @@ gva_status gva_decode_attention(gva_ctx* ctx, int B, const float* q_abs, const f
                                 const int32_t* seq_lens, int max_seq_len, float* out,
                                 void* workspace, size_t ws_bytes, gva_stream_t stream);
 
+/* The two passes of gva_decode_attention as separate calls, for callers that schedule them
+ * apart (or time them apart).  gva_decode_attention(...) is exactly gva_decode_partial
+ * followed by gva_decode_combine on the same stream.
+ *   gva_decode_partial: the split-T pass (the north-star's "split-T flash-decoding kernel");
+ *     arguments as gva_decode_attention without `out`.  Its results (partial maxima, sums
+ *     and weighted value sums, plus the batch's tile prefix sums) stay in the workspace.
+ *   gva_decode_combine: merges them into out [B,H,d_v] f32.  It must follow the partial pass
+ *     of the same context, B, max_seq_len and workspace on the same stream, with no change
+ *     to the context's decode options in between (both passes derive the same split plan
+ *     from them); the workspace is read, not written. */
+gva_status gva_decode_partial(gva_ctx* ctx, int B, const float* q_abs, const float* q_rot,
+                              const void* v_pool, const void* kr_pool,
+                              const int32_t* block_table, int max_blocks, int num_blocks,
+                              const int32_t* seq_lens, int max_seq_len, void* workspace,
+                              size_t ws_bytes, gva_stream_t stream);
+gva_status gva_decode_combine(gva_ctx* ctx, int B, int max_seq_len, float* out, void* workspace,
+                              size_t ws_bytes, gva_stream_t stream);
+
 /* gqa_decode_attention -- the matching grouped-query attention decode, built with the same
  * tiling and pools so that the cost of a key cache can be timed beside GVA (GQA explainer,
  * section "一次 GQA 计算如何展开": grouped keys and values, head h reads group g(h)).

@@ -265,6 +265,24 @@ def test_workspace_with_stale_nan_bytes():
         assert_parity(out.cpu().numpy(), want, "bf16", f"stale workspace, path {path}")
 
 
+@pytest.mark.parametrize("path", [gva.GVA_PATH_FMA, gva.GVA_PATH_AUTO])
+def test_partial_then_combine_equals_one_call(path):
+    """gva_decode_partial followed by gva_decode_combine gives gva_decode_attention's bits."""
+    w = synth.custom(dtype="bf16", B=7, H=16, G=4, d_v=64, d_r=16, T_range=(1, 1500), shuffled=True)
+    inp = synth.decode_inputs(w, seed=95, device="cuda")
+    layer = make_layer(w, path=path)
+    want = layer.attend(inp.v_pool, inp.kr_pool, inp.block_table, inp.seq_lens, q_abs=inp.q_abs,
+                        q_rot=inp.q_rot).clone()
+    out = torch.full_like(want, float("nan"))
+    gva.gva_decode_partial(layer.ctx, inp.q_abs, inp.q_rot, inp.v_pool, inp.kr_pool, inp.block_table, inp.seq_lens,
+                           w.max_seq_len, layer.workspace)
+    gva.gva_decode_combine(layer.ctx, w.B, w.max_seq_len, out, layer.workspace)
+    torch.cuda.synchronize()
+    assert layer.device_error() == 0
+    assert torch.equal(out, want)
+    assert_parity(out.cpu().numpy(), oracle_decode_all(w, inp), "bf16", "two calls")
+
+
 def test_ragged_tail_slots_are_never_read():
     # fill every slot past each sequence's end with NaN bits: the output must stay finite
     w = synth.custom(dtype="bf16", B=4, H=16, G=4, d_v=64, d_r=16, T_range=(1, 200), shuffled=True)
