@@ -12,6 +12,7 @@ Under torchrun every rank runs its own replica of the workload (sequences are in
 no collective on the data path) and the line reports the total over ranks (weak scaling).
 """
 import argparse
+import dataclasses
 import json
 import math
 import os
@@ -53,6 +54,9 @@ def parse():
     p.add_argument("--e2e-steps", type=int, default=200)
     p.add_argument("--cpu-sample-seqs", type=int, default=0, help="sequences in the CPU sample (0 = auto)")
     p.add_argument("--graph", type=int, default=1, help="replay the step as a captured CUDA graph (1) or launch it (0)")
+    p.add_argument("--dr", type=int, default=-1,
+                   help="override the workload's positional width d_r (0 = no positional slice, the Shared-KV "
+                        "cache layout); the workload is then named <name>-dr<d_r>")
     return p.parse_args()
 
 
@@ -316,9 +320,16 @@ def capture(fn):
     return graph
 
 
+def workload(args):
+    w = synth.WORKLOADS[args.workload]
+    if args.dr >= 0 and args.dr != w.d_r:
+        w = dataclasses.replace(w, d_r=args.dr, name=f"{w.name}-dr{args.dr}")
+    return w
+
+
 def run_ours(args, rank, ws):
     torch.cuda.init()
-    w = synth.WORKLOADS[args.workload]
+    w = workload(args)
     S = Setup(w, seed=rank, path=args.path, split_tokens=args.split_tokens)
     need_flush = S.cache_bytes < 2 * L2_BYTES
     flush = flusher() if need_flush else None
@@ -546,7 +557,7 @@ def cpu_baseline(S, args):
 def run_reference(args, rank, ws):
     """The oracle as the reference arm: K timed steps of a bounded sample on the host cores."""
     import oracle
-    w = synth.WORKLOADS[args.workload]
+    w = workload(args)
     dev = "cuda" if torch.cuda.is_available() else "cpu"
     S = Setup.__new__(Setup)
     S.w = w

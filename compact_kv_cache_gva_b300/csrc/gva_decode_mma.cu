@@ -23,6 +23,8 @@
 // partial record per (sequence, group) it touched.  The matching GQA form (a separate key cache, no positional
 // slice) reuses the kernel with the key tile scored instead of the value tile.
 #include <cuda.h>
+
+#include <algorithm>
 #include <math.h>
 
 #include "gva_device.cuh"
@@ -608,16 +610,19 @@ bool mma_supported(const gva_dims& d, bool sep_k) {
   return r == 1 || r == 2 || r == 4 || r == 8;
 }
 
-// Warp pairs and ring depth.  Four pairs keep the tensor pipes ahead of HBM with a margin
-// when a stage is small (d_v = 64: 10 KB with its positional key); with d_v = 128 a stage
-// holds 19 KB and three pairs leave a deeper ring for the same compute margin.  D takes the
-// rest of shared memory.
+// Warp pairs and ring depth, from measurements on B300 (the d_r sweep of the long-context
+// workload, 0 <= d_r <= 32, and the ragged batch): fewer than four pairs lose throughput
+// even with deeper rings; with d_v = 64, four pairs are best up to d_r = 24 (stages up to
+// 11 KB; five or six were 2-8 % slower) and six at d_r = 32 (12 KB stages, 12 % faster than
+// four); the 19 KB stages of d_v = 128 use three pairs (four give the same time with half
+// the depth).  D takes the rest of shared memory.
 bool mma_shape(const gva_dims& d, bool sep_k, int B, int* pairs, int* stages) {
   const int op = (d.d_v / 64) * kSubTileBytes * (sep_k ? 2 : 1);
   const int stage = op + (sep_k ? 0 : kBlockTokens * d.d_r * 2);
-  const int P = stage <= 12 * 1024 ? 4 : 3;
-  int D = (kSmemLimit - ring_fixed_bytes(B)) / (P * stage);
-  if (D > kMaxStages / P) D = kMaxStages / P;
+  const int avail = kSmemLimit - ring_fixed_bytes(B);
+  auto depth = [&](int p) { return std::min(avail / (p * stage), kMaxStages / p); };
+  const int P = stage <= 11 * 1024 ? 4 : stage <= 12 * 1024 ? 6 : 3;
+  const int D = depth(P);
   if (D < 1) return false;
   *pairs = P;
   *stages = D;

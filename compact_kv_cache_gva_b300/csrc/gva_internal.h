@@ -81,7 +81,7 @@ bool mma_supported(const gva_dims& d, bool sep_k);
 // Tensor-core kernel: one CTA per range, made of P warp pairs (a copy warp filling a private
 // ring of D tiles, and the consumer warp that computes on it); P consumer warps share the
 // range.  mma_shape picks P and D for the dims (0 if no ring fits).
-constexpr int kMmaMaxPairs = 4;
+constexpr int kMmaMaxPairs = 6;
 bool mma_shape(const gva_dims& d, bool sep_k, int B, int* pairs, int* stages);
 cudaError_t launch_decode_mma(const DecodeArgs& a, bool sep_k, int grid, cudaStream_t stream);
 // Merges the partial records of each (b, g) into out; launched as a programmatic dependent

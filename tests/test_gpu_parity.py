@@ -216,6 +216,9 @@ RING_CASES = [
     (dict(B=3, H=8, G=1, d_v=128, d_r=32, T_range=(700, 1500)), 64 * 100),
     (dict(B=2, H=4, G=2, d_v=64, d_r=16, T_range=(1, 100)), 0),
     (dict(B=64, H=16, G=4, d_v=64, d_r=24, T_range=(1, 64)), 0),
+    (dict(B=5, H=16, G=4, d_v=64, d_r=8, T_range=(1, 2000)), 0),      # trailing k8 step only
+    (dict(B=4, H=16, G=4, d_v=128, d_r=0, T_range=(100, 1000)), 0),   # no positional slice
+    (dict(B=6, H=16, G=4, d_v=64, d_r=32, T_range=(1, 3000)), 64 * 40),  # six warp pairs
 ]
 
 
