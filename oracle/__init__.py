@@ -41,6 +41,7 @@ def lib():
         L.oracle_decode_one.argtypes = ([C.c_int] * 6 + [C.c_double, vp, vp, ip, C.c_int, C.c_int, ip,
                                         C.c_int, C.c_int, dp, dp, dp])
         L.oracle_decode.argtypes = ([C.c_int] * 7 + [C.c_double, vp, vp, ip, C.c_int, C.c_int, ip, dp, dp, dp])
+        L.oracle_decode_multi.argtypes = ([C.c_int] * 8 + [C.c_double, vp, vp, ip, C.c_int, C.c_int, ip, dp, dp, dp])
         L.oracle_decode_split.argtypes = ([C.c_int] * 6 + [C.c_double, vp, vp, ip, C.c_int, C.c_int, ip,
                                           C.c_int, C.c_int, dp, dp, C.c_int, dp])
         L.oracle_decode_unabsorbed.argtypes = ([C.c_int] * 7 + [C.c_double, C.c_double, vp, vp, ip, C.c_int,
@@ -176,6 +177,21 @@ def decode(q_abs, q_rot, v_pool, kr_pool, block_table, seq_lens, G, d_n=None, sc
     out = np.empty((B, H, d_v))
     _check(lib().oracle_decode(code, B, H, G, d_v, d_n, d_r, float(scale), pv, pk, pbt, bt.shape[1], nb, psl,
                                pqa, pqr, out.ctypes.data_as(C.POINTER(C.c_double))), "decode")
+    return out
+
+
+def decode_multi(q_abs, q_rot, v_pool, kr_pool, block_table, seq_lens, G, d_n=None, scale=0.0):
+    """n_q queries per sequence, q_abs [B,n_q,H,d_v], q_rot [B,n_q,H,d_r]: query i of sequence b
+    reads positions 0..seq_lens[b]-n_q+i.  Output [B,n_q,H,d_v] (fp64)."""
+    q_abs, pqa = _d(q_abs)
+    q_rot, pqr = _d(q_rot)
+    B, n_q, H, d_v = q_abs.shape
+    d_r = q_rot.shape[3]
+    d_n = d_v if d_n is None else d_n
+    code, pv, pk, bt, pbt, sl, psl, nb = _decode_common(v_pool, kr_pool, block_table, seq_lens, G, d_v)
+    out = np.empty((B, n_q, H, d_v))
+    _check(lib().oracle_decode_multi(code, B, n_q, H, G, d_v, d_n, d_r, float(scale), pv, pk, pbt, bt.shape[1], nb,
+                                     psl, pqa, pqr, out.ctypes.data_as(C.POINTER(C.c_double))), "decode_multi")
     return out
 
 

@@ -318,6 +318,45 @@ int oracle_decode(int dtype, int B, int H, int G, int d_v, int d_n, int d_r, dou
   return status;
 }
 
+/* Several query tokens per sequence: the last n_q positions of the context (the tokens
+ * just appended).  Query i of sequence b sits at position p = seq_lens[b] - n_q + i and reads
+ * the cache up to and including its own position [GQA §与位置编码和 KV Cache 的关系], so
+ * its output is the single-query definition over positions 0..p.
+ * q_abs [B][n_q][H][d_v], q_rot [B][n_q][H][d_r], out [B][n_q][H][d_v].  Every seq_lens[b]
+ * must be at least n_q. */
+int oracle_decode_multi(int dtype, int B, int n_q, int H, int G, int d_v, int d_n, int d_r,
+                        double scale, const void* v_pool, const void* kr_pool,
+                        const int32_t* block_table, int max_blocks, int num_blocks,
+                        const int32_t* seq_lens, const double* q_abs, const double* q_rot,
+                        double* out) {
+  if (B < 0 || n_q < 1 || H <= 0 || G <= 0 || H % G != 0 || d_v <= 0 || d_r < 0) return OR_ERR_ARG;
+  for (int b = 0; b < B; ++b)
+    if (seq_lens[b] < n_q) return OR_ERR_ARG;
+  double sc = g_scale(d_n, d_r, scale);
+  int status = OR_OK;
+  int64_t rows = (int64_t)B * n_q * H;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t row = 0; row < rows; ++row) {
+    int h = (int)(row % H);
+    int64_t bi = row / H;
+    int b = (int)(bi / n_q), i = (int)(bi % n_q);
+    int64_t p = (int64_t)seq_lens[b] - n_q + i; /* the query's own position */
+    const double* qa = q_abs + row * d_v;
+    const double* qr = q_rot + row * (d_r > 0 ? d_r : 0);
+    double m, l;
+    double* o = out + row * d_v;
+    int st = partial_bh(dtype, H, G, d_v, d_r, sc, v_pool, kr_pool, block_table, max_blocks,
+                        num_blocks, b, h, 0, p + 1, qa, qr, &m, &l, o);
+    if (st != OR_OK) {
+#pragma omp critical
+      status = st;
+    } else {
+      for (int k = 0; k < d_v; ++k) o[k] /= l;
+    }
+  }
+  return status;
+}
+
 /* Split-T form: positions 0..T-1 cut into S contiguous ranges of near-equal length, one
  * partial (m, l, u) per range, then merged:  M = max m_s,  o = sum e^(m_s-M) u_s /
  * sum e^(m_s-M) l_s.  Must equal the unsplit result up to rounding. */

@@ -136,6 +136,63 @@ def test_hand_case_B_positional_term(oracle_mod):
     assert abs(out[0, 0, 0] - 1.492296285352) < 1e-7
 
 
+def test_hand_case_two_queries_causal(oracle_mod):
+    # the cache of case B (keys rotated at positions 0,1,2) read by two query tokens, the last
+    # two positions: query 0 at position 1 sees keys 0..1 only, with positional terms
+    # cos(1 - j):  s = 0.5 * ((0, 1) + (cos 1, 1)) = (0.270151152934, 1.0), so
+    # p_1 = e^1 / (e^0.270151 + e^1) = 0.674772102235 and o = (p_1 * 1, 0);
+    # query 1 at position 2 is case B itself
+    d_v, d_r = 2, 2
+    vals = np.array([[[0, 0]], [[1, 0]], [[2, 0]]], dtype=np.float32)[None]
+    kr_raw = np.tile(np.array([1.0, 0.0], dtype=np.float32), (1, 3, 1))
+    vp = np.zeros((1, 1, 64, d_v), dtype=np.float32)
+    kp = np.zeros((1, 64, d_r), dtype=np.float32)
+    oracle_mod.append(vals, kr_raw, [0], np.array([[0]]), vp, kp)
+    q_abs, q_rot = oracle_mod.absorb(np.array([[[1.0, 0.0]], [[1.0, 0.0]]]), np.array([[[1.0, 0.0]], [[1.0, 0.0]]]),
+                                     [1, 2], np.eye(2)[None])
+    out = oracle_mod.decode_multi(q_abs.reshape(1, 2, 1, 2), q_rot.reshape(1, 2, 1, 2), vp, kp, np.array([[0]]),
+                                  [3], G=1, d_n=2)
+    assert abs(out[0, 0, 0, 0] - 0.674772102235) < 1e-7 and out[0, 0, 0, 1] == 0.0
+    assert abs(out[0, 1, 0, 0] - 1.492296285352) < 1e-7
+
+
+def test_multi_query_decode_is_causally_masked_attention(oracle_mod):
+    # n_q queries on the last n_q positions == torch SDPA over the materialised keys
+    # [v_j ; k_r,j] with the mask j <= T - n_q + i, one row per (query, head)
+    n_q = 3
+    w = synth.custom(dtype="bf16", B=2, H=4, G=2, d_v=32, d_r=16, T_range=(3, 150), shuffled=True)
+    lens = torch.tensor([150, 70], dtype=torch.int32)
+    inp, vp, kp = _rand_cache(w, seed=5, lens=lens)
+    table = inp.block_table.numpy()
+    g = torch.Generator().manual_seed(6)
+    qa = torch.randn((2, n_q, 4, 32), generator=g, dtype=torch.float64).numpy()
+    qr = torch.randn((2, n_q, 4, 16), generator=g, dtype=torch.float64).numpy()
+    out = oracle_mod.decode_multi(qa, qr, vp, kp, table, lens.numpy(), G=2)
+    for b in range(2):
+        T = int(lens[b])
+        for h in range(4):
+            V = _gather_rows(vp, table, b, T, g=h // 2)
+            KR = _gather_rows(kp, table, b, T)
+            K = torch.tensor(np.concatenate([V, KR], axis=1))
+            q = torch.tensor(np.concatenate([qa[b, :, h], qr[b, :, h]], axis=1))
+            mask = torch.arange(T)[None, :] <= (T - n_q + torch.arange(n_q))[:, None]
+            ref = F.scaled_dot_product_attention(q[None, None], K[None, None], torch.tensor(V)[None, None],
+                                                 attn_mask=mask[None, None], scale=1 / math.sqrt(48))[0, 0]
+            assert np.abs(out[b, :, h] - ref.numpy()).max() < 1e-12
+
+
+def test_single_query_multi_decode_is_decode(oracle_mod):
+    w = synth.custom(dtype="bf16", B=3, H=4, G=2, d_v=32, d_r=16, T_range=(1, 200), shuffled=True)
+    inp, vp, kp = _rand_cache(w, seed=7)
+    table, lens = inp.block_table.numpy(), inp.seq_lens.numpy()
+    qa, qr = inp.q_abs.double().numpy(), inp.q_rot.double().numpy()
+    one = oracle_mod.decode(qa, qr, vp, kp, table, lens, G=2)
+    multi = oracle_mod.decode_multi(qa[:, None], qr[:, None], vp, kp, table, lens, G=2)
+    assert np.array_equal(one, multi[:, 0])
+    with pytest.raises(oracle_mod.OracleError):  # fewer context tokens than queries
+        oracle_mod.decode_multi(np.zeros((3, 300, 4, 32)), np.zeros((3, 300, 4, 16)), vp, kp, table, lens, G=2)
+
+
 # ---------------------------------------------------------------- special cases vs library
 
 def _sdpa(q, k, v, scale):
