@@ -64,14 +64,18 @@ int choose_path(const gva_ctx* ctx, bool sep_k) {
 // CUDA-core path: one range per warp, 4 warps per CTA, as many CTAs as fit on the SMs.
 // Automatic plans launch one wave, fewer CTAs when the batch has fewer units than that; a
 // caller-set split length asks for about split_tokens tokens per warp at max_seq_len.
-bool make_plan(const gva_ctx* ctx, int B, int max_seq_len, bool sep_k, gva::Plan* plan) {
+bool make_plan(const gva_ctx* ctx, int B, int max_seq_len, bool sep_k, gva::Plan* plan, int nq = 1) {
   const int path = choose_path(ctx, sep_k);
-  if (path < 0 || B > gva::kMaxBatch) return false;
+  if (path < 0 || B > gva::kMaxBatch || nq < 1) return false;
+  if (nq > 1 && (path != GVA_PATH_MMA || sep_k)) return false;  // several queries: tensor-core path
+  const int R = ctx->dims.H / ctx->dims.G;
+  int nqp = 1;  // queries per pass: powers of two up to the kernel's limit
+  while (2 * nqp <= nq && 2 * nqp <= gva::mma_max_queries_per_pass(R)) nqp *= 2;
   const long long nt_max = (max_seq_len + GVA_BLOCK_TOKENS - 1) / GVA_BLOCK_TOKENS;
   const long long units_max = static_cast<long long>(B) * ctx->dims.G * nt_max;
   const bool mma = path == GVA_PATH_MMA;
   int pairs = 0, stages = 0;
-  if (mma && !gva::mma_shape(ctx->dims, sep_k, B, &pairs, &stages)) return false;
+  if (mma && !gva::mma_shape(ctx->dims, sep_k, B, nqp, &pairs, &stages)) return false;
   const int warps_per_cta = mma ? pairs : 4;  // warps that stream units
   long long grid;
   if (ctx->split_tokens > 0) {
@@ -90,15 +94,15 @@ bool make_plan(const gva_ctx* ctx, int B, int max_seq_len, bool sep_k, gva::Plan
   if (grid < 1) grid = 1;
   if (grid > (1LL << 20)) return false;
   plan->path = path;
+  plan->nqp = nqp;
   plan->grid = static_cast<int>(grid);
   plan->n_warps = static_cast<int>(warps_per_cta * grid);
   plan->n_groups = mma ? plan->grid : plan->n_warps;
   plan->group_warps = mma ? pairs : 1;
   plan->n_stages = mma ? stages : 0;
-  const int R = ctx->dims.H / ctx->dims.G;
   plan->ws_bytes = gva::header_bytes(B) +
                    sizeof(float) * (static_cast<size_t>(plan->n_groups) + static_cast<size_t>(B) * ctx->dims.G) *
-                       plan->group_warps * R * gva::partial_stride_floats(ctx->dims.d_v);
+                       plan->group_warps * R * nqp * gva::partial_stride_floats(ctx->dims.d_v);
   return true;
 }
 
@@ -110,7 +114,7 @@ gva_status decode_common(gva_ctx* ctx, bool sep_k, int phases, int B, const floa
                          const float* q_rot, const void* k_pool, const void* v_pool,
                          const void* kr_pool, const int32_t* block_table, int max_blocks,
                          int num_blocks, const int32_t* seq_lens, int max_seq_len, float* out,
-                         void* workspace, size_t ws_bytes, cudaStream_t stream) {
+                         void* workspace, size_t ws_bytes, cudaStream_t stream, int nq = 1) {
   const bool partial = phases & kPhasePartial, combine = phases & kPhaseCombine;
   if (!ctx || B < 0 || max_seq_len < 1) return GVA_ERR_INVALID_ARG;
   if (partial && (max_blocks < 1 || num_blocks < 1)) return GVA_ERR_INVALID_ARG;
@@ -128,8 +132,9 @@ gva_status decode_common(gva_ctx* ctx, bool sep_k, int phases, int B, const floa
   }
   if (combine && (!out || !aligned16(out))) return GVA_ERR_INVALID_ARG;
   if (!on_ctx_device(ctx)) return GVA_ERR_INVALID_ARG;
+  if (nq < 1) return GVA_ERR_INVALID_ARG;
   gva::Plan plan;
-  if (!make_plan(ctx, B, max_seq_len, sep_k, &plan)) return GVA_ERR_UNSUPPORTED;
+  if (!make_plan(ctx, B, max_seq_len, sep_k, &plan, nq)) return GVA_ERR_UNSUPPORTED;
   if (partial && plan.path == GVA_PATH_MMA &&
       static_cast<long long>(num_blocks) * d.G * GVA_BLOCK_TOKENS >= (1LL << 31))
     return GVA_ERR_UNSUPPORTED;  // token rows are int32 tensor-copy coordinates
@@ -159,13 +164,24 @@ gva_status decode_common(gva_ctx* ctx, bool sep_k, int phases, int B, const floa
   a.group_warps = plan.group_warps;
   a.n_stages = plan.n_stages;
   a.scale_log2 = static_cast<float>(static_cast<double>(ctx->scale) * 1.4426950408889634);
-  if (partial) {
-    const cudaError_t e = plan.path == GVA_PATH_MMA
-                              ? gva::launch_decode_mma(a, sep_k, plan.grid, stream)
-                              : gva::launch_decode_fma(a, d.cache_dtype, sep_k, plan.grid, stream);
-    if (e != cudaSuccess) return GVA_ERR_CUDA;
+  a.nq = nq;
+  // passes over the queries, each a partial pass and a combine: the largest power of two
+  // that fits, then smaller ones for the rest (each pass reads the cache once more)
+  for (a.q0 = 0; a.q0 < nq; a.q0 += a.nqp) {
+    a.nqp = plan.nqp;
+    while (a.nqp > nq - a.q0) a.nqp /= 2;
+    if (partial) {
+      const cudaError_t e = plan.path == GVA_PATH_MMA
+                                ? gva::launch_decode_mma(a, sep_k, plan.grid, stream)
+                                : gva::launch_decode_fma(a, d.cache_dtype, sep_k, plan.grid, stream);
+      if (e != cudaSuccess) return GVA_ERR_CUDA;
+    }
+    if (combine) {
+      const cudaError_t e = gva::launch_combine(a, stream);
+      if (e != cudaSuccess) return GVA_ERR_CUDA;
+    }
   }
-  return combine ? from_cuda(gva::launch_combine(a, stream)) : GVA_OK;
+  return GVA_OK;
 }
 
 }  // namespace
@@ -283,6 +299,25 @@ gva_status gva_decode_combine(gva_ctx* ctx, int B, int max_seq_len, float* out, 
   return decode_common(ctx, false, kPhaseCombine, B, nullptr, nullptr, nullptr, nullptr, nullptr,
                        nullptr, 0, 0, nullptr, max_seq_len, out, workspace, ws_bytes,
                        reinterpret_cast<cudaStream_t>(stream));
+}
+
+gva_status gva_decode_attention_multi(gva_ctx* ctx, int B, int n_q, const float* q_abs,
+                                      const float* q_rot, const void* v_pool, const void* kr_pool,
+                                      const int32_t* block_table, int max_blocks, int num_blocks,
+                                      const int32_t* seq_lens, int max_seq_len, float* out,
+                                      void* workspace, size_t ws_bytes, gva_stream_t stream) {
+  if (n_q < 1) return GVA_ERR_INVALID_ARG;
+  if (n_q > max_seq_len) return GVA_ERR_INVALID_ARG;
+  return decode_common(ctx, false, kPhasePartial | kPhaseCombine, B, q_abs, q_rot, nullptr, v_pool,
+                       kr_pool, block_table, max_blocks, num_blocks, seq_lens, max_seq_len, out,
+                       workspace, ws_bytes, reinterpret_cast<cudaStream_t>(stream), n_q);
+}
+
+size_t gva_decode_workspace_size_multi(const gva_ctx* ctx, int B, int n_q, int max_seq_len) {
+  if (!ctx || B <= 0 || n_q < 1 || max_seq_len < 1) return 0;
+  gva::Plan plan;
+  if (!make_plan(ctx, B, max_seq_len, false, &plan, n_q)) return 0;
+  return plan.ws_bytes;
 }
 
 gva_status gqa_decode_attention(gva_ctx* ctx, int B, const float* q, const void* k_pool,

@@ -49,9 +49,14 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const DecodeAr
   const int* cum = reinterpret_cast<const int*>(a.part);
   const float* recs = a.part + header_bytes(a.B) / 4;
   const int nt = cum[b + 1] - cum[b];
-  float* outg = a.out + (static_cast<size_t>(b) * a.H + static_cast<size_t>(g) * R) * DV;
-  if (nt == 0) {  // length outside [1, max_seq_len]: reported by the partial kernel
-    for (int i = tid; i < R * DV; i += kCombineThreads) outg[i] = 0.f;
+  // sub-record hh of a record: query q0 + hh / Rh of the pass, head hh % Rh of group g
+  const int Rh = a.H / a.G;
+  auto out_row = [&](int hh) {
+    const int qi = hh / Rh, h = hh - qi * Rh;
+    return a.out + ((static_cast<long long>(b) * a.nq + a.q0 + qi) * a.H + static_cast<long long>(g) * Rh + h) * DV;
+  };
+  if (nt == 0) {  // length outside [max(1, nq), max_seq_len]: reported by the partial kernel
+    for (int i = tid; i < R * DV; i += kCombineThreads) out_row(i / DV)[i % DV] = 0.f;
     return;
   }
   const long long U = static_cast<long long>(a.G) * cum[a.B];
@@ -143,7 +148,7 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const DecodeAr
     const int i = tid + k * kCombineThreads;
     if (i < R * DV) {
       const int hh = i / DV;
-      outg[i] = Lrun[hh] > 0.f ? acc[k] / Lrun[hh] : 0.f;
+      out_row(hh)[i - hh * DV] = Lrun[hh] > 0.f ? acc[k] / Lrun[hh] : 0.f;
     }
   }
 }
@@ -165,9 +170,10 @@ cudaError_t launch_t(const DecodeArgs& a, cudaLaunchConfig_t& cfg) {
   return cudaLaunchKernelEx(&cfg, combine_kernel<DV, R>, a);
 }
 
+// R here counts the sub-records of a record: (heads per group) x (queries per pass).
 template <int DV>
 cudaError_t launch_dv(const DecodeArgs& a, cudaLaunchConfig_t& cfg) {
-  switch (a.H / a.G) {
+  switch (a.H / a.G * a.nqp) {
     case 1: return launch_t<DV, 1>(a, cfg);
     case 2: return launch_t<DV, 2>(a, cfg);
     case 4: return launch_t<DV, 4>(a, cfg);

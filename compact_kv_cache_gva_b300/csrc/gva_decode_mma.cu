@@ -25,6 +25,7 @@
 #include <cuda.h>
 
 #include <algorithm>
+#include <type_traits>
 #include <math.h>
 
 #include "gva_device.cuh"
@@ -35,6 +36,11 @@ namespace gva {
 namespace {
 
 constexpr int kMmaMaxThreads = 64 * kMmaMaxPairs;  // consumer warps + as many copy warps
+
+// Threads a kernel instance is compiled for: six warp pairs on the single-query d_v = 64
+// path, four elsewhere (d_v = 128 and several queries per pass hold twice the accumulators,
+// so they keep more registers per thread).
+__host__ __device__ constexpr int mma_max_threads(int dv, int nq) { return dv == 64 && nq == 1 ? 384 : 256; }
 constexpr int kSubTileBytes = kBlockTokens * 128;  // one [64 tokens][64 columns] bf16 swizzled box
 
 // ---- PTX wrappers ------------------------------------------------------------------------
@@ -148,12 +154,13 @@ inline int ring_fixed_bytes(int B) { return 1024 + kCtrlBytes + cum_bytes(B); }
 // so phase parities are unambiguous, and about P*(D-1) tiles are in flight per SM while P
 // are being computed.  The copy warps take the issue work (a few hundred cycles per tile)
 // and the dependent block-table reads off the consumers' path.
-template <int DV, int DR, int R, bool SEPK>
-__global__ void __launch_bounds__(kMmaMaxThreads, 1) decode_mma_kernel(const DecodeArgs a,
+template <int DV, int DR, int R, int NQ, bool CAUSAL, bool SEPK>
+__global__ void __launch_bounds__(mma_max_threads(DV, NQ), 1) decode_mma_kernel(const DecodeArgs a,
                                                                        const __grid_constant__ CUtensorMap tmv,
                                                                        const __grid_constant__ CUtensorMap tmk) {
   using L = MmaLayout<DV, DR, SEPK>;
-  constexpr int NT = (2 * R + 7) / 8;   // n-tiles of 8 columns (4 heads each)
+  constexpr int RQ = R * NQ;            // (query, head) column pairs of a group: c = i*R + h
+  constexpr int NT = (2 * RQ + 7) / 8;  // n-tiles of 8 columns (4 column pairs each)
   constexpr int KSV = DV / 16;          // k16 steps over the value (key) columns
   constexpr int KSR = DR / 16;          // k16 steps over the positional columns
   constexpr bool KR8 = (DR % 16) != 0;  // one trailing k8 step
@@ -169,7 +176,7 @@ __global__ void __launch_bounds__(kMmaMaxThreads, 1) decode_mma_kernel(const Dec
   const int N = P * D;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem);
   uint64_t* empty = full + kMaxStages;
-  int* nvs = reinterpret_cast<int*>(empty + kMaxStages);  // valid tokens of each stage's tile (0 = skip)
+  int* nvs = reinterpret_cast<int*>(empty + kMaxStages);  // tokens from each stage's tile to the end (0 = skip)
   unsigned char* tiles = smem + kCtrlBytes;
   unsigned char* krs = tiles + N * L::kOpBytes;
   int* cum = reinterpret_cast<int*>(krs + N * L::kKrBytes);
@@ -216,7 +223,7 @@ __global__ void __launch_bounds__(kMmaMaxThreads, 1) decode_mma_kernel(const Dec
           const int id = a.block_table[static_cast<long long>(cu.b) * a.max_blocks + cu.t];
           if (id >= 0 && id < a.num_blocks) {
             blk = id;
-            nv = min(kBlockTokens, T - cu.t * kBlockTokens);
+            nv = T - cu.t * kBlockTokens;  // tokens from the tile's start to the end (>= 1)
           } else {
             flag_error(a.err, GVA_DEVERR_BLOCK_ID);
           }
@@ -290,16 +297,18 @@ __global__ void __launch_bounds__(kMmaMaxThreads, 1) decode_mma_kernel(const Dec
   int slot = 0, ph = 0;  // ring slot and phase parity of this warp's next unit
 
   // query fragments (B operand of the score product) of the current (b, g), pre-scaled by
-  // scale*log2(e); column n = 2*head + part, part 0 = bf16(q), part 1 = bf16 remainder.
+  // scale*log2(e); column n = 2*c + part for column pair c = i*R + h (query q0 + i of this
+  // pass, head h of the group), part 0 = bf16(q), part 1 = bf16 remainder.
   uint32_t qb[NT][KSV + KSR][2];
   uint32_t qt[NT];
   auto load_q = [&](int b, int g) {
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-      const int head = nt * 4 + ((lane >> 2) >> 1), part = (lane >> 2) & 1;
+      const int cp = nt * 4 + ((lane >> 2) >> 1), part = (lane >> 2) & 1;
       const int tq = lane & 3;
-      const bool valid = head < R;
-      const long long row = static_cast<long long>(b) * a.H + g * R + (valid ? head : 0);
+      const bool valid = cp < RQ;
+      const int qi = valid ? cp / R : 0, head = valid ? cp % R : 0;
+      const long long row = (static_cast<long long>(b) * a.nq + a.q0 + qi) * a.H + g * R + head;
       const float* qa = a.q_abs + row * DV;
       const float* qr = a.q_rot + row * DR;
       auto qv = [&](int kk) -> float {
@@ -333,18 +342,18 @@ __global__ void __launch_bounds__(kMmaMaxThreads, 1) decode_mma_kernel(const Dec
     }
   };
   const int gid = lane >> 2, tq = lane & 3;
-  // Partial record of segment f for this warp: per head (m, l, 0, 0, o[0..DV)).
+  // Partial record of segment f for this warp: per column pair (m, l, 0, 0, o[0..DV)).
   auto flush = [&](long long f) {
-    float* rec = recs + ((static_cast<long long>(blockIdx.x) + f) * NC + warp) * R * rec_floats;
+    float* rec = recs + ((static_cast<long long>(blockIdx.x) + f) * NC + warp) * RQ * rec_floats;
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       float lt = l[nt];
       lt += __shfl_xor_sync(kFullMask, lt, 4);
       lt += __shfl_xor_sync(kFullMask, lt, 8);
       lt += __shfl_xor_sync(kFullMask, lt, 16);
-      const int head = nt * 4 + tq;
-      if (head < R) {
-        float* r = rec + head * rec_floats;
+      const int cp = nt * 4 + tq;
+      if (cp < RQ) {
+        float* r = rec + cp * rec_floats;
         if (gid == 0) {
           r[0] = m[nt];
           r[1] = lt;
@@ -374,8 +383,9 @@ __global__ void __launch_bounds__(kMmaMaxThreads, 1) decode_mma_kernel(const Dec
       ok = false;
       break;
     }
-    const int nv = nvs[s];
-    if (nv > 0) {
+    const int nrem = nvs[s];
+    if (nrem > 0) {
+      const int nv = min(nrem, kBlockTokens);  // valid tokens of the tile
       const uint32_t vbase = smem_addr(tiles + s * L::kOpBytes);
       const uint32_t kbase = SEPK ? vbase + L::kVBytes : vbase;  // tile that is scored
       const uint32_t krbase = smem_addr(krs + s * L::kKrBytes);
@@ -415,40 +425,99 @@ __global__ void __launch_bounds__(kMmaMaxThreads, 1) decode_mma_kernel(const Dec
         }
       }
 
-      // online softmax (log2 domain); thread holds head (nt*4 + tq) for tokens
-      // 16*mt + gid and 16*mt + gid + 8
+      // online softmax (log2 domain); thread holds column pair c = nt*4 + tq (query q0 + c/R,
+      // head c%R) for tokens 16*mt + gid and 16*mt + gid + 8.  Query q of nq reads positions
+      // up to T - nq + q: in this tile, tokens j < nrem - (nq - 1 - q).  Most tiles are seen
+      // whole by every query of the pass (the earliest one is q0) and take the unmasked form;
+      // the masked form also keeps the state of a query that sees no token of the tile (its
+      // position precedes the tile) unchanged.
       uint32_t pb[NT][4][2];
+      auto softmax = [&](auto masked) {
+        constexpr bool kMasked = decltype(masked)::value;
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        float sv[4][2];
-        float mx = -INFINITY;
+        for (int nt = 0; nt < NT; ++nt) {
+          float sv[4][2];
+          float mx = -INFINITY;
+          if constexpr (kMasked) {
+            const int cp = nt * 4 + tq;
+            const int lim = min(nv, nrem - (a.nq - 1 - (a.q0 + (cp < RQ ? cp / R : 0))));
 #pragma unroll
-        for (int mt = 0; mt < 4; ++mt) {
-          const int j0 = 16 * mt + gid;
-          sv[mt][0] = j0 < nv ? sc[nt][mt][0] + sc[nt][mt][1] : -INFINITY;
-          sv[mt][1] = j0 + 8 < nv ? sc[nt][mt][2] + sc[nt][mt][3] : -INFINITY;
-          mx = fmaxf(mx, fmaxf(sv[mt][0], sv[mt][1]));
+            for (int mt = 0; mt < 4; ++mt) {
+              const int j0 = 16 * mt + gid;
+              sv[mt][0] = j0 < lim ? sc[nt][mt][0] + sc[nt][mt][1] : -INFINITY;
+              sv[mt][1] = j0 + 8 < lim ? sc[nt][mt][2] + sc[nt][mt][3] : -INFINITY;
+              mx = fmaxf(mx, fmaxf(sv[mt][0], sv[mt][1]));
+            }
+          } else {
+#pragma unroll
+            for (int mt = 0; mt < 4; ++mt) {
+              sv[mt][0] = sc[nt][mt][0] + sc[nt][mt][1];
+              sv[mt][1] = sc[nt][mt][2] + sc[nt][mt][3];
+              mx = fmaxf(mx, fmaxf(sv[mt][0], sv[mt][1]));
+            }
+          }
+          mx = fmaxf(mx, __shfl_xor_sync(kFullMask, mx, 4));
+          mx = fmaxf(mx, __shfl_xor_sync(kFullMask, mx, 8));
+          mx = fmaxf(mx, __shfl_xor_sync(kFullMask, mx, 16));
+          const float mn = fmaxf(m[nt], mx);
+          const bool none = kMasked && mn == -INFINITY;
+          const float alpha = none ? 1.f : exp2f(m[nt] - mn);
+          m[nt] = mn;
+          float ps = 0.f;
+#pragma unroll
+          for (int mt = 0; mt < 4; ++mt) {
+            const float p0 = none ? 0.f : exp2f(sv[mt][0] - mn);
+            const float p1 = none ? 0.f : exp2f(sv[mt][1] - mn);
+            ps += p0 + p1;
+            pb[nt][mt][0] = movmatrix_trans(split_pack(p0));
+            pb[nt][mt][1] = movmatrix_trans(split_pack(p1));
+          }
+          l[nt] = fmaf(l[nt], alpha, ps);
+#pragma unroll
+          for (int md = 0; md < MD; ++md)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) o[nt][md][e] *= alpha;
         }
-        mx = fmaxf(mx, __shfl_xor_sync(kFullMask, mx, 4));
-        mx = fmaxf(mx, __shfl_xor_sync(kFullMask, mx, 8));
-        mx = fmaxf(mx, __shfl_xor_sync(kFullMask, mx, 16));
-        const float mn = fmaxf(m[nt], mx);
-        const float alpha = exp2f(m[nt] - mn);
-        m[nt] = mn;
-        float ps = 0.f;
+      };
+      if constexpr (!CAUSAL) {
+        // one query per sequence at its last position: only the tokens past the end of the
+        // context are masked
 #pragma unroll
-        for (int mt = 0; mt < 4; ++mt) {
-          const float p0 = exp2f(sv[mt][0] - mn);
-          const float p1 = exp2f(sv[mt][1] - mn);
-          ps += p0 + p1;
-          pb[nt][mt][0] = movmatrix_trans(split_pack(p0));
-          pb[nt][mt][1] = movmatrix_trans(split_pack(p1));
+        for (int nt = 0; nt < NT; ++nt) {
+          float sv[4][2];
+          float mx = -INFINITY;
+#pragma unroll
+          for (int mt = 0; mt < 4; ++mt) {
+            const int j0 = 16 * mt + gid;
+            sv[mt][0] = j0 < nv ? sc[nt][mt][0] + sc[nt][mt][1] : -INFINITY;
+            sv[mt][1] = j0 + 8 < nv ? sc[nt][mt][2] + sc[nt][mt][3] : -INFINITY;
+            mx = fmaxf(mx, fmaxf(sv[mt][0], sv[mt][1]));
+          }
+          mx = fmaxf(mx, __shfl_xor_sync(kFullMask, mx, 4));
+          mx = fmaxf(mx, __shfl_xor_sync(kFullMask, mx, 8));
+          mx = fmaxf(mx, __shfl_xor_sync(kFullMask, mx, 16));
+          const float mn = fmaxf(m[nt], mx);
+          const float alpha = exp2f(m[nt] - mn);
+          m[nt] = mn;
+          float ps = 0.f;
+#pragma unroll
+          for (int mt = 0; mt < 4; ++mt) {
+            const float p0 = exp2f(sv[mt][0] - mn);
+            const float p1 = exp2f(sv[mt][1] - mn);
+            ps += p0 + p1;
+            pb[nt][mt][0] = movmatrix_trans(split_pack(p0));
+            pb[nt][mt][1] = movmatrix_trans(split_pack(p1));
+          }
+          l[nt] = fmaf(l[nt], alpha, ps);
+#pragma unroll
+          for (int md = 0; md < MD; ++md)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) o[nt][md][e] *= alpha;
         }
-        l[nt] = fmaf(l[nt], alpha, ps);
-#pragma unroll
-        for (int md = 0; md < MD; ++md)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) o[nt][md][e] *= alpha;
+      } else if (nrem - (a.nq - 1 - a.q0) >= kBlockTokens) {
+        softmax(std::false_type{});
+      } else {
+        softmax(std::true_type{});
       }
 
       // output: O^T[d x n] += V^T[d x tok] P[tok x n]
@@ -505,15 +574,16 @@ __global__ void __launch_bounds__(kMmaMaxThreads, 1) decode_mma_kernel(const Dec
   }
 }
 
-template <int DV, int DR, int R, bool SEPK>
+template <int DV, int DR, int R, int NQ, bool CAUSAL, bool SEPK>
 cudaError_t launch_mma_t(const DecodeArgs& a, const CUtensorMap& mv, const CUtensorMap& mk, int grid,
                          cudaStream_t stream) {
   using L = MmaLayout<DV, DR, SEPK>;
   const int P = a.group_warps, D = a.n_stages;
-  if (P < 1 || P > kMmaMaxPairs || D < 1 || P * D > kMaxStages) return cudaErrorInvalidValue;
+  if (P < 1 || 64 * P > mma_max_threads(DV, NQ) || D < 1 || P * D > kMaxStages) return cudaErrorInvalidValue;
+  if (a.nqp != NQ || (a.nq > 1) != CAUSAL) return cudaErrorInvalidValue;
   const int smem = ring_fixed_bytes(a.B) + P * D * L::kStageBytes;
   if (smem > kSmemLimit) return cudaErrorInvalidValue;
-  auto kern = decode_mma_kernel<DV, DR, R, SEPK>;
+  auto kern = decode_mma_kernel<DV, DR, R, NQ, CAUSAL, SEPK>;
   static int configured[kMaxDevices] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -536,14 +606,29 @@ cudaError_t launch_mma_t(const DecodeArgs& a, const CUtensorMap& mv, const CUten
   return cudaLaunchKernelEx(&cfg, kern, a, mv, mk);
 }
 
+// Queries per pass: the instances built are NQ in {1, 2, 4} with R*NQ <= 8.
+template <int DV, int DR, int R, bool SEPK>
+cudaError_t dispatch_nq(const DecodeArgs& a, const CUtensorMap& mv, const CUtensorMap& mk, int grid,
+                        cudaStream_t stream) {
+  if constexpr (!SEPK) {
+    if constexpr (R * 4 <= 8)
+      if (a.nqp == 4) return launch_mma_t<DV, DR, R, 4, true, SEPK>(a, mv, mk, grid, stream);
+    if constexpr (R * 2 <= 8)
+      if (a.nqp == 2) return launch_mma_t<DV, DR, R, 2, true, SEPK>(a, mv, mk, grid, stream);
+    if (a.nqp == 1 && a.nq > 1) return launch_mma_t<DV, DR, R, 1, true, SEPK>(a, mv, mk, grid, stream);
+  }
+  if (a.nqp == 1 && a.nq == 1) return launch_mma_t<DV, DR, R, 1, false, SEPK>(a, mv, mk, grid, stream);
+  return cudaErrorInvalidValue;
+}
+
 template <int DV, int DR, bool SEPK>
 cudaError_t dispatch_r(const DecodeArgs& a, const CUtensorMap& mv, const CUtensorMap& mk, int grid,
                        cudaStream_t stream) {
   switch (a.H / a.G) {
-    case 1: return launch_mma_t<DV, DR, 1, SEPK>(a, mv, mk, grid, stream);
-    case 2: return launch_mma_t<DV, DR, 2, SEPK>(a, mv, mk, grid, stream);
-    case 4: return launch_mma_t<DV, DR, 4, SEPK>(a, mv, mk, grid, stream);
-    case 8: return launch_mma_t<DV, DR, 8, SEPK>(a, mv, mk, grid, stream);
+    case 1: return dispatch_nq<DV, DR, 1, SEPK>(a, mv, mk, grid, stream);
+    case 2: return dispatch_nq<DV, DR, 2, SEPK>(a, mv, mk, grid, stream);
+    case 4: return dispatch_nq<DV, DR, 4, SEPK>(a, mv, mk, grid, stream);
+    case 8: return dispatch_nq<DV, DR, 8, SEPK>(a, mv, mk, grid, stream);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -616,12 +701,15 @@ bool mma_supported(const gva_dims& d, bool sep_k) {
 // 11 KB; five or six were 2-8 % slower) and six at d_r = 32 (12 KB stages, 12 % faster than
 // four); the 19 KB stages of d_v = 128 use three pairs (four give the same time with half
 // the depth).  D takes the rest of shared memory.
-bool mma_shape(const gva_dims& d, bool sep_k, int B, int* pairs, int* stages) {
+int mma_max_queries_per_pass(int R) { return R <= 2 ? 4 : R == 4 ? 2 : 1; }
+
+bool mma_shape(const gva_dims& d, bool sep_k, int B, int nqp, int* pairs, int* stages) {
   const int op = (d.d_v / 64) * kSubTileBytes * (sep_k ? 2 : 1);
   const int stage = op + (sep_k ? 0 : kBlockTokens * d.d_r * 2);
   const int avail = kSmemLimit - ring_fixed_bytes(B);
   auto depth = [&](int p) { return std::min(avail / (p * stage), kMaxStages / p); };
-  const int P = stage <= 11 * 1024 ? 4 : stage <= 12 * 1024 ? 6 : 3;
+  const int P = std::min(stage <= 11 * 1024 ? 4 : stage <= 12 * 1024 ? 6 : 3,
+                         mma_max_threads(d.d_v, nqp) / 64);
   const int D = depth(P);
   if (D < 1) return false;
   *pairs = P;

@@ -38,6 +38,10 @@ struct DecodeArgs {
   float* part;               // workspace: header (prefix sums) + partial records
   unsigned* err;
   int B, H, G, d_v, d_r;
+  // Query tokens per sequence (the last nq positions; 1 for plain decode).  A pass of the
+  // tensor-core kernel handles queries [q0, q0 + nqp): queries are rows (b*nq + q)*H + h of
+  // q_abs / q_rot / out, and a partial record holds R*nqp (query, head) sub-records.
+  int nq, q0, nqp;
   int max_blocks, num_blocks, max_seq_len;
   int n_warps;               // warps of the partial grid that stream units
   // The batch's units are cut into n_groups equal contiguous ranges; the group_warps warps
@@ -55,6 +59,7 @@ constexpr int kMaxBatch = 8192;  // sequences per decode call (prefix sums live 
 
 struct Plan {
   int path;         // GVA_PATH_FMA or GVA_PATH_MMA
+  int nqp;          // queries per pass (records hold R*nqp sub-records)
   int grid;         // CTAs of the partial kernel
   int n_warps;      // warps that stream units (grid * unit warps per CTA)
   int n_groups;     // unit ranges (FMA: one per warp; MMA: one per CTA)
@@ -82,7 +87,9 @@ bool mma_supported(const gva_dims& d, bool sep_k);
 // ring of D tiles, and the consumer warp that computes on it); P consumer warps share the
 // range.  mma_shape picks P and D for the dims (0 if no ring fits).
 constexpr int kMmaMaxPairs = 6;
-bool mma_shape(const gva_dims& d, bool sep_k, int B, int* pairs, int* stages);
+bool mma_shape(const gva_dims& d, bool sep_k, int B, int nqp, int* pairs, int* stages);
+// Queries per pass of the tensor-core kernel (its (query, head) column pairs: R*nqp <= 8).
+int mma_max_queries_per_pass(int R);
 cudaError_t launch_decode_mma(const DecodeArgs& a, bool sep_k, int grid, cudaStream_t stream);
 // Merges the partial records of each (b, g) into out; launched as a programmatic dependent
 // of the partial kernel.

@@ -56,7 +56,7 @@ __host__ __device__ inline bool warp_touched(long long a, long long e, int w, in
 }
 
 // Per-CTA prologue: cum[0..B] in shared memory from seq_lens; lengths outside
-// [1, max_seq_len] count as zero tiles (and are reported once by CTA 0).  Uses all
+// [max(1, nq), max_seq_len] count as zero tiles (and are reported once by CTA 0).  Uses all
 // blockDim.x threads of the CTA (a multiple of 32, at most MAXT); ends with __syncthreads().
 // CTA 0 also publishes cum to the workspace header.
 template <int MAXT>
@@ -72,7 +72,7 @@ __device__ void build_prefix(const DecodeArgs& a, int* cum) {
     int nt = 0;
     if (b < a.B) {
       const int T = a.seq_lens[b];
-      if (T >= 1 && T <= a.max_seq_len)
+      if (T >= a.nq && T >= 1 && T <= a.max_seq_len)
         nt = (T + kBlockTokens - 1) / kBlockTokens;
       else if (blockIdx.x == 0)
         flag_error(a.err, GVA_DEVERR_SEQ_LEN);

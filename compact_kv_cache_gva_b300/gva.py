@@ -24,7 +24,8 @@ BLOCK_TOKENS = 64
 EXPORTS = ("gva_create", "gva_destroy", "gva_absorb_query", "gva_cache_append", "gva_decode_workspace_size",
            "gva_decode_attention", "gqa_decode_attention", "gva_set_split_tokens", "gva_set_decode_path",
            "gva_decode_plan", "gva_get_device_error", "gva_status_string", "gva_version",
-           "gva_decode_attention_noalloc", "gva_decode_partial", "gva_decode_combine")
+           "gva_decode_attention_noalloc", "gva_decode_partial", "gva_decode_combine",
+           "gva_decode_attention_multi", "gva_decode_workspace_size_multi")
 NOALLOC_SCRATCH_BYTES = 4 << 20
 
 
@@ -63,6 +64,9 @@ def load():
     L.gva_decode_attention_noalloc.argtypes = [vp, i, vp, vp, vp, vp, ip, i, i, ip, i, vp, st]
     L.gva_decode_partial.argtypes = [vp, i, vp, vp, vp, vp, ip, i, i, ip, i, vp, C.c_size_t, st]
     L.gva_decode_combine.argtypes = [vp, i, i, vp, vp, C.c_size_t, st]
+    L.gva_decode_attention_multi.argtypes = [vp, i, i, vp, vp, vp, vp, ip, i, i, ip, i, vp, vp, C.c_size_t, st]
+    L.gva_decode_workspace_size_multi.argtypes = [vp, i, i, i]
+    L.gva_decode_workspace_size_multi.restype = C.c_size_t
     L.gva_set_split_tokens.argtypes = [vp, i]
     L.gva_set_decode_path.argtypes = [vp, i]
     L.gva_decode_plan.argtypes = [vp, i, i, C.POINTER(C.c_int), C.POINTER(C.c_int)]
@@ -71,7 +75,8 @@ def load():
     L.gva_status_string.restype = C.c_char_p
     L.gva_version.argtypes = []
     for name in EXPORTS:
-        if name not in ("gva_destroy", "gva_decode_workspace_size", "gva_status_string", "gva_version"):
+        if name not in ("gva_destroy", "gva_decode_workspace_size", "gva_decode_workspace_size_multi",
+                        "gva_status_string", "gva_version"):
             getattr(L, name).restype = C.c_int
     _lib = L
     return L
@@ -265,6 +270,36 @@ def gva_decode_combine(ctx, B, max_seq_len, out, workspace, stream=None):
                                      _ptr(workspace, None, "workspace"),
                                      workspace.numel() * workspace.element_size(), _stream(stream)),
            "gva_decode_combine")
+
+
+def gva_decode_workspace_size_multi(ctx, B, n_q, max_seq_len):
+    return int(load().gva_decode_workspace_size_multi(ctx.handle, int(B), int(n_q), int(max_seq_len)))
+
+
+def gva_decode_attention_multi(ctx, q_abs, q_rot, v_pool, kr_pool, block_table, seq_lens, max_seq_len, out, workspace,
+                               stream=None):
+    """n_q query tokens per sequence (the last n_q positions), q_abs [B,n_q,H,d_v]; query i reads
+    positions 0..seq_lens[b]-n_q+i.  out [B,n_q,H,d_v]."""
+    d = ctx.dims
+    B, n_q = q_abs.shape[0], q_abs.shape[1]
+    dt = ctx.cache_torch_dtype
+    has_r = d.d_r > 0
+    _shape(q_abs, (B, n_q, d.H, d.d_v), "q_abs")
+    _shape(out, (B, n_q, d.H, d.d_v), "out")
+    if has_r:
+        _shape(q_rot, (B, n_q, d.H, d.d_r), "q_rot")
+    _check_table(block_table, B, seq_lens)
+    _check_pools(ctx, v_pool, kr_pool if has_r else None)
+    _check(load().gva_decode_attention_multi(ctx.handle, B, n_q, _ptr(q_abs, torch.float32, "q_abs"),
+                                             _ptr(q_rot, torch.float32, "q_rot", allow_none=not has_r),
+                                             _ptr(v_pool, dt, "v_pool"),
+                                             _ptr(kr_pool, dt, "kr_pool", allow_none=not has_r),
+                                             _ptr(block_table, torch.int32, "block_table"), block_table.shape[1],
+                                             v_pool.shape[0], _ptr(seq_lens, torch.int32, "seq_lens"),
+                                             int(max_seq_len), _ptr(out, torch.float32, "out"),
+                                             _ptr(workspace, None, "workspace"),
+                                             workspace.numel() * workspace.element_size(), _stream(stream)),
+           "gva_decode_attention_multi")
 
 
 def gva_decode_attention_noalloc(ctx, q_abs, q_rot, v_pool, kr_pool, block_table, seq_lens, max_seq_len, out,

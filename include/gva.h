@@ -181,6 +181,26 @@ gva_status gva_decode_partial(gva_ctx* ctx, int B, const float* q_abs, const flo
 gva_status gva_decode_combine(gva_ctx* ctx, int B, int max_seq_len, float* out, void* workspace,
                               size_t ws_bytes, gva_stream_t stream);
 
+/* gva_decode_attention_multi -- decode attention for n_q query tokens per sequence, the last
+ * n_q positions of its context (tokens just appended, e.g. drafts to verify in speculative
+ * decoding).  Query i of sequence b sits at position p = seq_lens[b] - n_q + i and reads the
+ * cache up to and including its own position (the decode lifecycle of the GQA explainer,
+ * section "与位置编码和 KV Cache 的关系": a query reads the cache through the current position),
+ * with the same scores and softmax as gva_decode_attention:
+ *   q_abs [B,n_q,H,d_v] f32 and q_rot [B,n_q,H,d_r] f32 (gva_absorb_query over B*n_q rows,
+ *   pos_q = p), out [B,n_q,H,d_v] f32; seq_lens[b] in [n_q, max_seq_len] (a shorter length
+ *   sets GVA_DEVERR_SEQ_LEN and zeroes that sequence's rows).
+ * Tensor-core path only (bf16 caches; GVA_ERR_UNSUPPORTED otherwise when n_q > 1).  The
+ * kernel packs R*nqp (query, head) pairs into its MMA columns, nqp = up to 4, 2, 1 queries
+ * per pass for R = H/G <= 2, 4, 8; more queries take more passes, each reading the cache.
+ * n_q == 1 is gva_decode_attention.  Workspace: gva_decode_workspace_size_multi bytes. */
+gva_status gva_decode_attention_multi(gva_ctx* ctx, int B, int n_q, const float* q_abs,
+                                      const float* q_rot, const void* v_pool, const void* kr_pool,
+                                      const int32_t* block_table, int max_blocks, int num_blocks,
+                                      const int32_t* seq_lens, int max_seq_len, float* out,
+                                      void* workspace, size_t ws_bytes, gva_stream_t stream);
+size_t gva_decode_workspace_size_multi(const gva_ctx* ctx, int B, int n_q, int max_seq_len);
+
 /* gqa_decode_attention -- the matching grouped-query attention decode, built with the same
  * tiling and pools so that the cost of a key cache can be timed beside GVA (GQA explainer,
  * section "一次 GQA 计算如何展开": grouped keys and values, head h reads group g(h)).
