@@ -54,6 +54,9 @@ def parse():
     p.add_argument("--e2e-steps", type=int, default=200)
     p.add_argument("--cpu-sample-seqs", type=int, default=0, help="sequences in the CPU sample (0 = auto)")
     p.add_argument("--graph", type=int, default=1, help="replay the step as a captured CUDA graph (1) or launch it (0)")
+    p.add_argument("--nq", type=int, default=1,
+                   help="query tokens per sequence per step (the last n_q positions: append n_q tokens, "
+                        "absorb B*n_q query rows, gva_decode_attention_multi)")
     p.add_argument("--dr", type=int, default=-1,
                    help="override the workload's positional width d_r (0 = no positional slice, the Shared-KV "
                         "cache layout); the workload is then named <name>-dr<d_r>")
@@ -234,23 +237,23 @@ SmiClockSampler.summary = ClockSampler.summary
 class Setup:
     """A resident workload: cache, block table, lengths, step inputs, layer buffers."""
 
-    def __init__(self, w, seed, path, split_tokens, device="cuda"):
-        self.w = w
+    def __init__(self, w, seed, path, split_tokens, device="cuda", n_q=1):
+        self.w, self.n_q = w, n_q
         self.inp = synth.decode_inputs(w, seed=seed, device=device)
         self.lens_cpu = self.inp.seq_lens.cpu()
-        # the step appends the current token at T_b - 1 and attends 0..T_b-1 (the token itself
-        # included), so every step has the same work
-        self.raw = synth.raw_inputs(w, self.lens_cpu, n_new=1, seed=seed + 1000, device=device)
+        # the step appends the current token(s) at T_b - n_q .. T_b - 1 and attends through them
+        # (each query through its own position), so every step has the same work
+        self.raw = synth.raw_inputs(w, self.lens_cpu, n_new=n_q, seed=seed + 1000, device=device, n_q=n_q)
         self.layer = GVADecodeLayer(w.H, w.G, w.d_v, w.d_n, w.d_r, w.dtype, w.B, w.max_seq_len, device=device,
                                     split_tokens=split_tokens,
                                     path={"auto": gva.GVA_PATH_AUTO, "fma": gva.GVA_PATH_FMA,
-                                          "mma": gva.GVA_PATH_MMA}[path])
+                                          "mma": gva.GVA_PATH_MMA}[path], n_q=n_q)
         self.sum_T = int(self.lens_cpu.sum())
         self.bytes_per_token = (w.G * w.d_v + w.d_r) * w.elem_bytes
         self.cache_bytes = self.sum_T * self.bytes_per_token
         # algorithmic bytes of the decode call: cache + queries + output + lengths + table rows used
         used_blocks = int(((self.lens_cpu + 63) // 64).sum())
-        self.decode_bytes = (self.cache_bytes + w.B * w.H * (w.d_v + w.d_r) * 4 + w.B * w.H * w.d_v * 4 +
+        self.decode_bytes = (self.cache_bytes + n_q * (w.B * w.H * (w.d_v + w.d_r) * 4 + w.B * w.H * w.d_v * 4) +
                              w.B * 4 + used_blocks * 4)
         self.decode_flops = self.sum_T * w.H * (2 * (w.d_v + w.d_r) + 2 * w.d_v)
 
@@ -324,13 +327,15 @@ def workload(args):
     w = synth.WORKLOADS[args.workload]
     if args.dr >= 0 and args.dr != w.d_r:
         w = dataclasses.replace(w, d_r=args.dr, name=f"{w.name}-dr{args.dr}")
+    if args.nq > 1:
+        w = dataclasses.replace(w, name=f"{w.name}-nq{args.nq}")
     return w
 
 
 def run_ours(args, rank, ws):
     torch.cuda.init()
     w = workload(args)
-    S = Setup(w, seed=rank, path=args.path, split_tokens=args.split_tokens)
+    S = Setup(w, seed=rank, path=args.path, split_tokens=args.split_tokens, n_q=args.nq)
     need_flush = S.cache_bytes < 2 * L2_BYTES
     flush = flusher() if need_flush else None
 
@@ -361,7 +366,8 @@ def run_ours(args, rank, ws):
                                                              S.inp.seq_lens), K, flush), ws)
     # the dominant kernel, the split-T partial pass, alone: events around each gva_decode_partial
     # call (the combine runs after each, outside them)
-    part_s = max_over_ranks(time_partial(S, min(K, 500), flush), ws)
+    # (several queries per sequence: the multi-query call, all its passes, is the unit timed)
+    part_s = (max_over_ranks(time_partial(S, min(K, 500), flush), ws) if S.n_q == 1 else dec_s / K)
     # per-call breakdown (events between calls; informative only, they stop launch overlap)
     nb = min(K, 100)
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(nb)]
@@ -386,7 +392,7 @@ def run_ours(args, rank, ws):
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws, "steps": K,
         "warmup": max(3, args.warmup), "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
-        "config": dict(w.describe(), step="absorb+append+decode", decode_path=args.path,
+        "config": dict(w.describe(), step="absorb+append+decode", decode_path=args.path, n_q=S.n_q,
                        cuda_graph=bool(args.graph),
                        split_plan=dict(zip(("split_tokens", "partial_warps"), S.layer.plan())),
                        l2="flushed before every step (252 MB write, then 252 MB read)" if need_flush else
@@ -396,7 +402,8 @@ def run_ours(args, rank, ws):
         "context_tokens_per_s": round(tokens_per_s, 1),
         "decode_steps_per_s": round(K * ws / total_s, 2),
         "breakdown_us": br,
-        "roofline": {"kernel": "split-T partial pass of gva_decode_attention (gva_decode_partial)",
+        "roofline": {"kernel": "split-T partial pass of gva_decode_attention (gva_decode_partial)" if S.n_q == 1
+                     else f"gva_decode_attention_multi, {S.n_q} queries per sequence (partial and combine passes)",
                      "bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
                      "frac": round(achieved / hbm_peak, 4), "peak_kind": f"{pk_kind} copy bandwidth (burst)",
                      "algorithmic_bytes_per_launch": S.decode_bytes, "partial_us": round(part_us, 3),
@@ -410,7 +417,7 @@ def run_ours(args, rank, ws):
         out["e2e"] = run_e2e(S, args.e2e_steps, flush)
     if not args.no_gqa and rank == 0:
         out["gqa_same_build"] = run_gqa(S, flush, min(K, 500))
-    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline and S.n_q == 1:
         out["cpu_baseline"] = cpu_baseline(S, args)
     return out
 

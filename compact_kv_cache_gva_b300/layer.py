@@ -9,18 +9,22 @@ from . import gva
 
 
 class GVADecodeLayer:
+    """With n_q > 1 a step decodes n_q query tokens per sequence (the last n_q positions, each
+    reading the cache through its own position): query rows are b*n_q + i, out is [B,n_q,H,d_v]."""
+
     def __init__(self, H, G, d_v, d_n, d_r, cache_dtype, B, max_seq_len, device="cuda", split_tokens=0,
-                 path=gva.GVA_PATH_AUTO, rope_base=10000.0, scale=0.0):
+                 path=gva.GVA_PATH_AUTO, rope_base=10000.0, scale=0.0, n_q=1):
         self.ctx = gva.gva_create(H, G, d_v, d_n, d_r, cache_dtype, rope_base, scale)
         if split_tokens:
             gva.gva_set_split_tokens(self.ctx, split_tokens)
         if path != gva.GVA_PATH_AUTO:
             gva.gva_set_decode_path(self.ctx, path)
-        self.B, self.max_seq_len = B, max_seq_len
-        self.q_abs = torch.empty((B, H, d_v), dtype=torch.float32, device=device)
-        self.q_rot = torch.empty((B, H, d_r), dtype=torch.float32, device=device)
-        self.out = torch.empty((B, H, d_v), dtype=torch.float32, device=device)
-        ws = max(16, gva.gva_decode_workspace_size(self.ctx, B, max_seq_len))
+        self.B, self.max_seq_len, self.n_q = B, max_seq_len, n_q
+        self.q_abs = torch.empty((B * n_q, H, d_v), dtype=torch.float32, device=device)
+        self.q_rot = torch.empty((B * n_q, H, d_r), dtype=torch.float32, device=device)
+        self.out = torch.empty((B, H, d_v) if n_q == 1 else (B, n_q, H, d_v), dtype=torch.float32, device=device)
+        ws = max(16, gva.gva_decode_workspace_size(self.ctx, B, max_seq_len) if n_q == 1 else
+                 gva.gva_decode_workspace_size_multi(self.ctx, B, n_q, max_seq_len))
         self.workspace = torch.empty(ws, dtype=torch.uint8, device=device)
         self._side = None  # side stream of step(overlap=True), created on first use
 
@@ -35,10 +39,18 @@ class GVADecodeLayer:
         gva.gva_cache_append(self.ctx, v_new, kr_new, pos, block_table, v_pool, kr_pool, stream)
 
     def attend(self, v_pool, kr_pool, block_table, seq_lens, q_abs=None, q_rot=None, stream=None):
-        gva.gva_decode_attention(self.ctx, self.q_abs if q_abs is None else q_abs,
-                                 (self.q_rot if q_rot is None else q_rot) if self.ctx.dims.d_r else None,
-                                 v_pool, kr_pool if self.ctx.dims.d_r else None, block_table, seq_lens,
-                                 self.max_seq_len, self.out, self.workspace, stream)
+        q_abs = self.q_abs if q_abs is None else q_abs
+        q_rot = (self.q_rot if q_rot is None else q_rot) if self.ctx.dims.d_r else None
+        kr_pool = kr_pool if self.ctx.dims.d_r else None
+        if self.n_q == 1:
+            gva.gva_decode_attention(self.ctx, q_abs, q_rot, v_pool, kr_pool, block_table, seq_lens,
+                                     self.max_seq_len, self.out, self.workspace, stream)
+        else:
+            B, H = self.B, self.ctx.dims.H
+            gva.gva_decode_attention_multi(self.ctx, q_abs.view(B, self.n_q, H, -1),
+                                           None if q_rot is None else q_rot.view(B, self.n_q, H, -1), v_pool,
+                                           kr_pool, block_table, seq_lens, self.max_seq_len, self.out,
+                                           self.workspace, stream)
         return self.out
 
     def step(self, q_c, q_r, pos_q, M, v_new, kr_new, pos_new, block_table, seq_lens, v_pool, kr_pool, stream=None,

@@ -125,26 +125,29 @@ def block_table(w: Workload, lens, seed_lens: int = 1, spare_blocks: int = 0):
 @dataclass
 class RawStep:
     """Raw inputs of one decode step (cache-dtype values where they enter the cache)."""
-    q_c: torch.Tensor     # [B,H,d_n] f32
-    q_r: torch.Tensor     # [B,H,d_r] f32 (unrotated)
+    q_c: torch.Tensor     # [B*n_q,H,d_n] f32
+    q_r: torch.Tensor     # [B*n_q,H,d_r] f32 (unrotated)
     M: torch.Tensor       # [H,d_v,d_n] f32
-    pos_q: torch.Tensor   # [B] int32
+    pos_q: torch.Tensor   # [B*n_q] int32
     v_new: torch.Tensor   # [B,n,G,d_v] cache dtype
     kr_new: torch.Tensor  # [B,n,d_r] cache dtype (unrotated)
     pos_new: torch.Tensor  # [B] int32, position of the first new token
 
 
-def raw_inputs(w: Workload, lens, n_new, seed=0, device="cpu", pos_new=None):
-    """Draws V (n_new tokens per sequence), the raw positional key, q_c, q_r and M, in that order."""
+def raw_inputs(w: Workload, lens, n_new, seed=0, device="cpu", pos_new=None, n_q=1):
+    """Draws V (n_new tokens per sequence), the raw positional key, q_c, q_r and M, in that order.
+
+    With n_q > 1 there are n_q query rows per sequence (row b*n_q + i at position T_b - n_q + i,
+    the last n_q positions); n_q = 1 gives one row per sequence at T_b - 1."""
     g = torch.Generator(device=device).manual_seed(seed)
     B, H, G, dv, dn, dr = w.B, w.H, w.G, w.d_v, w.d_n, w.d_r
     v = torch.randn((B, n_new, G, dv), generator=g, device=device).to(w.torch_dtype)
     kr = torch.randn((B, n_new, dr), generator=g, device=device).to(w.torch_dtype)
-    q_c = torch.randn((B, H, dn), generator=g, device=device)
-    q_r = torch.randn((B, H, dr), generator=g, device=device)
+    q_c = torch.randn((B * n_q, H, dn), generator=g, device=device)
+    q_r = torch.randn((B * n_q, H, dr), generator=g, device=device)
     M = torch.randn((H, dv, dn), generator=g, device=device) * (1.0 / math.sqrt(dv))
     lens = torch.as_tensor(lens, dtype=torch.int32)
-    pos_q = (lens - 1).to(torch.int32).to(device)
+    pos_q = (lens[:, None] - n_q + torch.arange(n_q, dtype=torch.int32)[None]).reshape(-1).to(torch.int32).to(device)
     if pos_new is None:
         pos_new = (lens - n_new).clamp(min=0).to(torch.int32)
     return RawStep(q_c, q_r, M, pos_q, v, kr, torch.as_tensor(pos_new, dtype=torch.int32).to(device))
