@@ -434,6 +434,31 @@ def test_full_size_workload_sampled_rows(wid):
     assert np.abs(got).max() <= vmax + 1e-3
 
 
+@pytest.mark.parametrize("path", [gva.GVA_PATH_MMA, gva.GVA_PATH_FMA])
+def test_largest_batch(path):
+    """B = 8192 sequences, the library's batch limit: the prefix array takes 32 KB of shared
+    memory beside the ring, and the combine merges 32768 segments.  Rows sampled for the oracle."""
+    w = synth.custom(dtype="bf16", B=8192, H=16, G=4, d_v=64, d_r=16, T_range=(1, 200), shuffled=True)
+    inp = synth.decode_inputs(w, seed=97, device="cuda")
+    got, layer = run_decode(w, inp, path=path)
+    rng = np.random.default_rng(97)
+    lens = inp.seq_lens.cpu().numpy()
+    bs = [0, w.B - 1, int(np.argmax(lens)), int(np.argmin(lens))] + list(rng.integers(0, w.B, 12))
+    rows = [(int(b), int(h)) for b in bs for h in (0, int(rng.integers(0, w.H)), w.H - 1)]
+    have, want = sample_rows(w, inp, got, rows)
+    assert_parity(have, want, "bf16", f"B=8192 path {path}")
+    assert np.isfinite(got).all()
+    # one more sequence is rejected on the host, before anything is enqueued
+    w2 = synth.custom(dtype="bf16", B=8193, H=16, G=4, d_v=64, d_r=16, T=64)
+    inp2 = synth.decode_inputs(w2, seed=98, device="cuda")
+    layer2 = make_layer(w2, path=path)
+    assert gva.gva_decode_workspace_size(layer2.ctx, w2.B, w2.T) == 0
+    with pytest.raises(gva.GVAError) as e:
+        layer2.attend(inp2.v_pool, inp2.kr_pool, inp2.block_table, inp2.seq_lens, q_abs=inp2.q_abs,
+                      q_rot=inp2.q_rot)
+    assert e.value.status == gva.GVA_ERR_UNSUPPORTED
+
+
 @pytest.mark.slow
 def test_long_context_full_step_sampled_rows():
     """The benchmark's step on the long-context workload: absorb + append at T-1 + decode."""
