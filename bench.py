@@ -32,7 +32,7 @@ from compact_kv_cache_gva_b300.layer import GVADecodeLayer  # noqa: E402
 METRIC = "GVA decode-attention cache-read GB/s (% of B300 HBM peak) and context tokens/s"
 # DRAM bytes (read + write) of one launch of the split-T partial kernel, from the ncu capture
 # summarised in profiles/ (None where no capture of the current kernel exists)
-TRAFFIC = {"long-context-bf16": 574_719_744}
+TRAFFIC = {"long-context-bf16": 574_461_568}
 L2_BYTES = 126 * 1024 * 1024
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 NVML_REASONS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap", 0x8: "hw_slowdown",
