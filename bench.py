@@ -414,7 +414,7 @@ def run_ours(args, rank, ws):
         "clocks": clocks.summary(),
     }
     if rank == 0 and ws == 1:
-        out["e2e"] = run_e2e(S, args.e2e_steps, flush)
+        out["e2e"] = run_e2e(S, args.e2e_steps, flush, graph=bool(args.graph))
     if not args.no_gqa and rank == 0:
         out["gqa_same_build"] = run_gqa(S, flush, min(K, 500))
     if rank == 0 and ws == 1 and not args.no_cpu_baseline and S.n_q == 1:
@@ -448,14 +448,40 @@ def time_partial(S, K, flush):
     return sum(a.elapsed_time(b) for a, b in evs) / 1e3 / K
 
 
-def run_e2e(S, steps, flush):
-    """Same step, with the step's inputs copied from pinned host memory and the output read back."""
+def run_e2e(S, steps, flush, graph=True):
+    """Same step, with the step's inputs copied from pinned host memory and the output read back.
+
+    The step's inputs (queries, the new tokens and their positions) sit in one pinned host
+    buffer, 256-byte aligned, and move with one copy; the output comes back with one copy.  With
+    graph=True the copy in, the step's kernels and the copy out are one captured CUDA graph,
+    replayed once per step, as a serving loop would run them."""
     r = S.raw
-    host_in = {k: getattr(r, k).cpu().pin_memory() for k in ("q_c", "q_r", "pos_q", "v_new", "kr_new", "pos_new")}
-    dev_in = {k: torch.empty_like(getattr(r, k)) for k in host_in}
+    names = ("q_c", "q_r", "pos_q", "v_new", "kr_new", "pos_new")
+    offs, total = {}, 0
+    for k in names:
+        t = getattr(r, k)
+        offs[k] = total
+        total += (t.numel() * t.element_size() + 255) // 256 * 256
+    host_buf = torch.empty(total, dtype=torch.uint8).pin_memory()
+    dev_buf = torch.empty(total, dtype=torch.uint8, device="cuda")
+
+    def view(buf, k):
+        t = getattr(r, k)
+        n = t.numel() * t.element_size()
+        return buf[offs[k]:offs[k] + n].view(t.dtype).view(t.shape)
+    for k in names:
+        view(host_buf, k).copy_(getattr(r, k).cpu())
+    dev_in = {k: view(dev_buf, k) for k in names}
     host_out = torch.empty(S.layer.out.shape, dtype=torch.float32).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    h2d = sum(getattr(r, k).numel() * getattr(r, k).element_size() for k in names)
     d2h = host_out.numel() * 4
+
+    def e2e_step():
+        dev_buf.copy_(host_buf, non_blocking=True)
+        S.layer.step(dev_in["q_c"], dev_in["q_r"], dev_in["pos_q"], r.M, dev_in["v_new"], dev_in["kr_new"],
+                     dev_in["pos_new"], S.inp.block_table, S.inp.seq_lens, S.inp.v_pool, S.inp.kr_pool)
+        host_out.copy_(S.layer.out, non_blocking=True)
+    run = capture(e2e_step).replay if graph else e2e_step
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     for k in range(steps + 3):
         if flush:
@@ -463,17 +489,13 @@ def run_e2e(S, steps, flush):
         e = ev[k - 3] if k >= 3 else None
         if e:
             e[0].record()
-        for name, t in host_in.items():
-            dev_in[name].copy_(t, non_blocking=True)
-        S.layer.step(dev_in["q_c"], dev_in["q_r"], dev_in["pos_q"], r.M, dev_in["v_new"], dev_in["kr_new"],
-                     dev_in["pos_new"], S.inp.block_table, S.inp.seq_lens, S.inp.v_pool, S.inp.kr_pool)
-        host_out.copy_(S.layer.out, non_blocking=True)
+        run()
         if e:
             e[1].record()
     torch.cuda.synchronize()
     t = sum(a.elapsed_time(b) for a, b in ev) / 1e3
     return {"value": round(S.cache_bytes * steps / t / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "ms_per_step": round(1e3 * t / steps, 5)}
+            "d2h_bytes_per_step": d2h, "ms_per_step": round(1e3 * t / steps, 5), "cuda_graph": bool(graph)}
 
 
 def run_gqa(S, flush, steps):
