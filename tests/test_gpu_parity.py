@@ -511,3 +511,56 @@ def test_step_replays_in_a_cuda_graph():
     torch.cuda.synchronize()
     assert layer.device_error() == 0
     assert torch.equal(layer.out, want)
+
+
+def test_two_streams_with_separate_workspaces():
+    """Decodes of two contexts issued on two streams at once (each with its own workspace) give
+    the results of running them one after the other."""
+    wa = synth.custom(dtype="bf16", B=6, H=16, G=4, d_v=64, d_r=16, T_range=(1, 3000), shuffled=True)
+    wb = synth.custom(dtype="bf16", B=4, H=32, G=8, d_v=128, d_r=24, T_range=(1, 2000), shuffled=True)
+    ia, ib = synth.decode_inputs(wa, seed=101, device="cuda"), synth.decode_inputs(wb, seed=102, device="cuda")
+    la, lb = make_layer(wa), make_layer(wb)
+
+    def run(layer, inp, stream=None):
+        return layer.attend(inp.v_pool, inp.kr_pool, inp.block_table, inp.seq_lens, q_abs=inp.q_abs,
+                            q_rot=inp.q_rot, stream=stream)
+    want_a, want_b = run(la, ia).clone(), run(lb, ib).clone()
+    torch.cuda.synchronize()
+    sa, sb = torch.cuda.Stream(), torch.cuda.Stream()
+    for _ in range(3):
+        la.out.fill_(float("nan"))
+        lb.out.fill_(float("nan"))
+        torch.cuda.synchronize()
+        run(la, ia, sa)
+        run(lb, ib, sb)
+        torch.cuda.synchronize()
+        assert torch.equal(la.out, want_a) and torch.equal(lb.out, want_b)
+    assert la.device_error() == 0 and lb.device_error() == 0
+
+
+def test_multi_query_step_replays_in_a_cuda_graph():
+    """A step with 2 query tokens per sequence (append 2 + absorb 2B rows + multi-query decode),
+    captured once and replayed, gives the direct result."""
+    w = synth.custom(dtype="bf16", B=4, H=16, G=4, d_v=64, d_r=16, T_range=(100, 900), shuffled=True)
+    inp = synth.decode_inputs(w, seed=103, device="cuda")
+    raw = synth.raw_inputs(w, inp.seq_lens.cpu(), n_new=2, seed=104, device="cuda", n_q=2)
+    layer = make_layer(w, n_q=2)
+
+    def step():
+        return layer.step(raw.q_c, raw.q_r, raw.pos_q, raw.M, raw.v_new, raw.kr_new, raw.pos_new, inp.block_table,
+                          inp.seq_lens, inp.v_pool, inp.kr_pool)
+    want = step().clone()
+    cap = torch.cuda.Stream()
+    cap.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(cap):
+        step()
+        cap.synchronize()
+        with torch.cuda.graph(graph, stream=cap):
+            step()
+    torch.cuda.current_stream().wait_stream(cap)
+    layer.out.fill_(float("nan"))
+    graph.replay()
+    torch.cuda.synchronize()
+    assert layer.device_error() == 0
+    assert torch.equal(layer.out, want)
