@@ -12,7 +12,12 @@
 // positional query and its position; a share of M_h and of the content queries as 16-byte
 // vectors), then the threads that own a positional pair load the four RoPE table rows of
 // its position at once and rotate it (fp32); M_h and the queries go to shared memory and
-// the GEMV runs in fp32 in k order.  Two memory round trips in all.
+// the GEMV runs in fp32.  Two memory round trips in all.
+//
+// Summation order of q'_i = sum_k M_h[i][k] q_c[k] (shared with the fused decode step, which
+// forms the same values in the decode kernel's prologue): k is cut into 4-element chunks; chunk
+// c goes to partial sum c mod 4, each partial accumulating its chunks in increasing k with one
+// fused multiply-add per element; q'_i = (p0 + p1) + (p2 + p3).
 #include "gva_device.cuh"
 #include "gva_internal.h"
 #include "gva_sched.cuh"
@@ -27,7 +32,8 @@ constexpr int kAbsorbVecs = 8;  // 16-byte vectors of M_h and q_c held per threa
 struct AbsorbArgs {
   const float* q_c;
   const float* q_r;
-  const int32_t* pos_q;
+  const int32_t* pos_q;     // null: position seq_lens[b] - 1
+  const int32_t* seq_lens;
   const float* M;
   float* q_abs;
   float* q_rot;
@@ -59,7 +65,7 @@ __global__ void __launch_bounds__(kAbsorbThreads) absorb_kernel(const AbsorbArgs
     const int bt = t / pairs;
     pi = t - bt * pairs;
     qrow = (static_cast<long long>(b0 + bt) * a.H + h) * a.d_r;
-    p = a.pos_q[b0 + bt];
+    p = a.pos_q ? static_cast<long long>(a.pos_q[b0 + bt]) : static_cast<long long>(a.seq_lens[b0 + bt]) - 1;
     x = *reinterpret_cast<const float2*>(a.q_r + qrow + 2 * pi);
   }
 
@@ -86,8 +92,7 @@ __global__ void __launch_bounds__(kAbsorbThreads) absorb_kernel(const AbsorbArgs
       else if (pi == 0)
         flag_error(a.err, GVA_DEVERR_POSITION);  // left unrotated
       float2 y;
-      y.x = fmaf(x.x, c, -x.y * s);
-      y.y = fmaf(x.x, s, x.y * c);
+      rope_rotate_f32(x.x, x.y, c, s, y.x, y.y);
       *reinterpret_cast<float2*>(a.q_rot + qrow + 2 * pi) = y;
     }
 #pragma unroll
@@ -107,42 +112,53 @@ __global__ void __launch_bounds__(kAbsorbThreads) absorb_kernel(const AbsorbArgs
   // Register tiles of 2 rows x 4 sequences per thread: rows i and i + d_v/2 (the two rows'
   // 16-byte reads stay conflict-free across a warp), sequences 4s..4s+3 (the warp shares s,
   // so the query reads are broadcasts).  6 shared-memory reads feed 32 FMAs; each output
-  // is one dot product in k order.
+  // keeps its four partial sums (chunk c of k into partial c mod 4).
   const int half = a.d_v / 2;
   const int nsb = (nb + 3) / 4;
+  const int nchunk = a.d_n / 4;
   for (int o = t; o < half * nsb; o += kAbsorbThreads) {
     const int i = o % half, sb = o / half;
     const float* m0 = Ms + i * ldm;
     const float* m1 = Ms + (i + half) * ldm;
-    float acc[2][4];
+    float acc[2][4][4];  // [row][sequence][partial]
 #pragma unroll
     for (int r = 0; r < 2; ++r)
 #pragma unroll
-      for (int j = 0; j < 4; ++j) acc[r][j] = 0.f;
-    for (int k = 0; k < a.d_n; k += 4) {
-      const float4 ma = *reinterpret_cast<const float4*>(m0 + k);
-      const float4 mb = *reinterpret_cast<const float4*>(m1 + k);
+      for (int j = 0; j < 4; ++j)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[r][j][e] = 0.f;
+    auto chunk = [&](int c, int e) {  // chunk c (elements 4c..4c+3) into partial e
+      const float4 ma = *reinterpret_cast<const float4*>(m0 + 4 * c);
+      const float4 mb = *reinterpret_cast<const float4*>(m1 + 4 * c);
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const int bt = min(4 * sb + j, nb - 1);  // rows past nb repeat a valid one, unused
-        const float4 q4 = *reinterpret_cast<const float4*>(qs + bt * ldm + k);
-        acc[0][j] = fmaf(ma.x, q4.x, acc[0][j]);
-        acc[0][j] = fmaf(ma.y, q4.y, acc[0][j]);
-        acc[0][j] = fmaf(ma.z, q4.z, acc[0][j]);
-        acc[0][j] = fmaf(ma.w, q4.w, acc[0][j]);
-        acc[1][j] = fmaf(mb.x, q4.x, acc[1][j]);
-        acc[1][j] = fmaf(mb.y, q4.y, acc[1][j]);
-        acc[1][j] = fmaf(mb.z, q4.z, acc[1][j]);
-        acc[1][j] = fmaf(mb.w, q4.w, acc[1][j]);
+        const float4 q4 = *reinterpret_cast<const float4*>(qs + bt * ldm + 4 * c);
+        acc[0][j][e] = fmaf(ma.x, q4.x, acc[0][j][e]);
+        acc[0][j][e] = fmaf(ma.y, q4.y, acc[0][j][e]);
+        acc[0][j][e] = fmaf(ma.z, q4.z, acc[0][j][e]);
+        acc[0][j][e] = fmaf(ma.w, q4.w, acc[0][j][e]);
+        acc[1][j][e] = fmaf(mb.x, q4.x, acc[1][j][e]);
+        acc[1][j][e] = fmaf(mb.y, q4.y, acc[1][j][e]);
+        acc[1][j][e] = fmaf(mb.z, q4.z, acc[1][j][e]);
+        acc[1][j][e] = fmaf(mb.w, q4.w, acc[1][j][e]);
       }
+    };
+    int c = 0;
+    for (; c + 4 <= nchunk; c += 4) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) chunk(c + e, e);
     }
+    if (c < nchunk) chunk(c, 0);
+    if (c + 1 < nchunk) chunk(c + 1, 1);
+    if (c + 2 < nchunk) chunk(c + 2, 2);
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const int bt = 4 * sb + j;
       if (bt < nb) {
         float* dst = a.q_abs + (static_cast<long long>(b0 + bt) * a.H + h) * a.d_v;
-        dst[i] = acc[0][j];
-        dst[i + half] = acc[1][j];
+        dst[i] = (acc[0][j][0] + acc[0][j][1]) + (acc[0][j][2] + acc[0][j][3]);
+        dst[i + half] = (acc[1][j][0] + acc[1][j][1]) + (acc[1][j][2] + acc[1][j][3]);
       }
     }
   }
@@ -152,11 +168,12 @@ __global__ void __launch_bounds__(kAbsorbThreads) absorb_kernel(const AbsorbArgs
 
 cudaError_t launch_absorb(const gva_ctx* ctx, int B, const float* q_c, const float* q_r,
                           const int32_t* pos_q, const float* M, float* q_abs, float* q_rot,
-                          cudaStream_t stream) {
+                          cudaStream_t stream, const int32_t* seq_lens) {
   AbsorbArgs a;
   a.q_c = q_c;
   a.q_r = q_r;
   a.pos_q = pos_q;
+  a.seq_lens = seq_lens;
   a.M = M;
   a.q_abs = q_abs;
   a.q_rot = q_rot;

@@ -8,7 +8,10 @@
 
 namespace {
 
-constexpr int kVersion = 100;  // 0.1.0
+constexpr int kVersion = 200;  // 0.2.0
+// Automatic step mode: fuse while the batch has at most this many (group, sequence) segments
+// per unit range.
+constexpr long long kStepAutoSegmentsPerRange = 2;
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -110,11 +113,37 @@ bool make_plan(const gva_ctx* ctx, int B, int max_seq_len, bool sep_k, gva::Plan
 constexpr int kPhasePartial = 1;
 constexpr int kPhaseCombine = 2;
 
+// Inputs of the fused decode step that the plain decode call does not take.
+struct StepInputs {
+  const float* q_c;
+  const float* q_r;
+  const float* M;
+  const void* v_new;
+  const void* kr_new;
+  void* v_pool;
+  void* kr_pool;
+};
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Bytes of the fused step's query stages for a plan: one per (range, segment) pair.
+size_t step_stage_bytes(const gva_ctx* ctx, int B, const gva::Plan& plan) {
+  const gva_dims& d = ctx->dims;
+  return sizeof(float) * (static_cast<size_t>(plan.n_groups) + static_cast<size_t>(B) * d.G) *
+         gva::step_stage_floats(d.H / d.G, d.d_v, d.d_r);
+}
+
+// Whether the fused step can run for this context (tensor-core path, d_n == d_v).
+bool step_fusable(const gva_ctx* ctx, const gva::Plan& plan) {
+  return plan.path == GVA_PATH_MMA && plan.nqp == 1 && ctx->dims.d_n == ctx->dims.d_v;
+}
+
 gva_status decode_common(gva_ctx* ctx, bool sep_k, int phases, int B, const float* q_abs,
                          const float* q_rot, const void* k_pool, const void* v_pool,
                          const void* kr_pool, const int32_t* block_table, int max_blocks,
                          int num_blocks, const int32_t* seq_lens, int max_seq_len, float* out,
-                         void* workspace, size_t ws_bytes, cudaStream_t stream, int nq = 1) {
+                         void* workspace, size_t ws_bytes, cudaStream_t stream, int nq = 1,
+                         const StepInputs* step = nullptr) {
   const bool partial = phases & kPhasePartial, combine = phases & kPhaseCombine;
   if (!ctx || B < 0 || max_seq_len < 1) return GVA_ERR_INVALID_ARG;
   if (partial && (max_blocks < 1 || num_blocks < 1)) return GVA_ERR_INVALID_ARG;
@@ -122,11 +151,11 @@ gva_status decode_common(gva_ctx* ctx, bool sep_k, int phases, int B, const floa
   if (B > gva::kMaxBatch) return GVA_ERR_UNSUPPORTED;  // prefix sums live in shared memory
   const gva_dims& d = ctx->dims;
   if (partial) {
-    if (!q_abs || !v_pool || !block_table || !seq_lens) return GVA_ERR_INVALID_ARG;
+    if ((!q_abs && !step) || !v_pool || !block_table || !seq_lens) return GVA_ERR_INVALID_ARG;
     if (sep_k && !k_pool) return GVA_ERR_INVALID_ARG;
-    if (!sep_k && d.d_r > 0 && (!q_rot || !kr_pool)) return GVA_ERR_INVALID_ARG;
+    if (!sep_k && d.d_r > 0 && ((!q_rot && !step) || !kr_pool)) return GVA_ERR_INVALID_ARG;
     if (static_cast<long long>(max_blocks) * GVA_BLOCK_TOKENS < max_seq_len) return GVA_ERR_INVALID_ARG;
-    if (!aligned16(q_abs) || !aligned16(v_pool) || (k_pool && !aligned16(k_pool)) ||
+    if ((q_abs && !aligned16(q_abs)) || !aligned16(v_pool) || (k_pool && !aligned16(k_pool)) ||
         (kr_pool && !aligned16(kr_pool)) || (q_rot && !aligned16(q_rot)))
       return GVA_ERR_INVALID_ARG;
   }
@@ -138,9 +167,12 @@ gva_status decode_common(gva_ctx* ctx, bool sep_k, int phases, int B, const floa
   if (partial && plan.path == GVA_PATH_MMA &&
       static_cast<long long>(num_blocks) * d.G * GVA_BLOCK_TOKENS >= (1LL << 31))
     return GVA_ERR_UNSUPPORTED;  // token rows are int32 tensor-copy coordinates
-  if (!workspace || ws_bytes < plan.ws_bytes || !aligned16(workspace)) return GVA_ERR_WORKSPACE;
+  if (step && (!step_fusable(ctx, plan) || sep_k || nq != 1)) return GVA_ERR_UNSUPPORTED;
+  const size_t stage_off = round_up(plan.ws_bytes, 256);
+  const size_t need = step ? stage_off + step_stage_bytes(ctx, B, plan) : plan.ws_bytes;
+  if (!workspace || ws_bytes < need || !aligned16(workspace)) return GVA_ERR_WORKSPACE;
 
-  gva::DecodeArgs a;
+  gva::DecodeArgs a{};
   a.q_abs = q_abs;
   a.q_rot = sep_k ? nullptr : q_rot;
   a.v_pool = v_pool;
@@ -165,6 +197,18 @@ gva_status decode_common(gva_ctx* ctx, bool sep_k, int phases, int B, const floa
   a.n_stages = plan.n_stages;
   a.scale_log2 = static_cast<float>(static_cast<double>(ctx->scale) * 1.4426950408889634);
   a.nq = nq;
+  if (step) {
+    a.fused = 1;
+    a.q_c = step->q_c;
+    a.q_r = step->q_r;
+    a.M = step->M;
+    a.v_new = step->v_new;
+    a.kr_new = step->kr_new;
+    a.v_pool_w = step->v_pool;
+    a.kr_pool_w = step->kr_pool;
+    a.rope32 = ctx->d_rope32;
+    a.qstage = reinterpret_cast<float*>(static_cast<char*>(workspace) + stage_off);
+  }
   // passes over the queries, each a partial pass and a combine: the largest power of two
   // that fits, then smaller ones for the rest (each pass reads the cache once more)
   for (a.q0 = 0; a.q0 < nq; a.q0 += a.nqp) {
@@ -206,6 +250,7 @@ gva_status gva_create(const gva_dims* dims, gva_ctx** out) {
   ctx->rope_base = d.rope_base > 0.0 ? d.rope_base : 10000.0;
   ctx->split_tokens = 0;
   ctx->path = GVA_PATH_AUTO;
+  ctx->step_mode = GVA_STEP_AUTO;
   if (cudaGetDevice(&ctx->device) != cudaSuccess ||
       cudaDeviceGetAttribute(&ctx->num_sms, cudaDevAttrMultiProcessorCount, ctx->device) != cudaSuccess ||
       cudaMalloc(reinterpret_cast<void**>(&ctx->d_err), sizeof(unsigned)) != cudaSuccess) {
@@ -318,6 +363,77 @@ size_t gva_decode_workspace_size_multi(const gva_ctx* ctx, int B, int n_q, int m
   gva::Plan plan;
   if (!make_plan(ctx, B, max_seq_len, false, &plan, n_q)) return 0;
   return plan.ws_bytes;
+}
+
+size_t gva_decode_step_workspace_size(const gva_ctx* ctx, int B, int max_seq_len) {
+  if (!ctx || B <= 0 || max_seq_len < 1) return 0;
+  gva::Plan plan;
+  if (!make_plan(ctx, B, max_seq_len, false, &plan)) return 0;
+  const gva_dims& d = ctx->dims;
+  const size_t off = round_up(plan.ws_bytes, 256);
+  // separate calls: the absorbed and rotated queries follow the decode workspace
+  const size_t separate = sizeof(float) * static_cast<size_t>(B) * d.H * (d.d_v + d.d_r) + 16;
+  const size_t fused = step_fusable(ctx, plan) ? step_stage_bytes(ctx, B, plan) : 0;
+  return off + (fused > separate ? fused : separate);
+}
+
+gva_status gva_decode_step(gva_ctx* ctx, int B, const float* q_c, const float* q_r, const float* M,
+                           const void* v_new, const void* kr_new, void* v_pool, void* kr_pool,
+                           const int32_t* block_table, int max_blocks, int num_blocks,
+                           const int32_t* seq_lens, int max_seq_len, float* out, void* workspace,
+                           size_t ws_bytes, gva_stream_t stream_) {
+  if (!ctx || B < 0 || max_seq_len < 1) return GVA_ERR_INVALID_ARG;
+  if (B == 0) return GVA_OK;
+  const gva_dims& d = ctx->dims;
+  if (!q_c || !M || !v_new || !v_pool || !block_table || !seq_lens || !out) return GVA_ERR_INVALID_ARG;
+  if (d.d_r > 0 && (!q_r || !kr_new || !kr_pool)) return GVA_ERR_INVALID_ARG;
+  if (!aligned16(q_c) || !aligned16(M) || !aligned16(v_new) || (q_r && !aligned16(q_r)) ||
+      (kr_new && (reinterpret_cast<uintptr_t>(kr_new) & 3u)))
+    return GVA_ERR_INVALID_ARG;
+  if (B > gva::kMaxBatch) return GVA_ERR_UNSUPPORTED;
+  if (!on_ctx_device(ctx)) return GVA_ERR_INVALID_ARG;
+  gva::Plan plan;
+  if (!make_plan(ctx, B, max_seq_len, false, &plan)) return GVA_ERR_UNSUPPORTED;
+  const cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  bool fuse = false;
+  switch (ctx->step_mode) {
+    case GVA_STEP_FUSED:
+      if (!step_fusable(ctx, plan)) return GVA_ERR_UNSUPPORTED;
+      fuse = true;
+      break;
+    case GVA_STEP_SEPARATE: fuse = false; break;
+    default:
+      // The prologue forms the queries of every segment a CTA's range meets; past a few
+      // segments per range the separate absorb kernel does that work faster.
+      fuse = step_fusable(ctx, plan) &&
+             static_cast<long long>(B) * d.G <= kStepAutoSegmentsPerRange * static_cast<long long>(plan.n_groups);
+  }
+  if (fuse) {
+    const StepInputs in{q_c, q_r, M, v_new, kr_new, v_pool, kr_pool};
+    return decode_common(ctx, false, kPhasePartial | kPhaseCombine, B, nullptr, nullptr, nullptr, v_pool,
+                         kr_pool, block_table, max_blocks, num_blocks, seq_lens, max_seq_len, out,
+                         workspace, ws_bytes, stream, 1, &in);
+  }
+  // Separate calls: append at position seq_lens[b] - 1, absorb at the same position, decode.
+  const size_t off = round_up(plan.ws_bytes, 256);
+  const size_t qbytes = sizeof(float) * static_cast<size_t>(B) * d.H * (d.d_v + d.d_r);
+  if (!workspace || !aligned16(workspace) || ws_bytes < off + qbytes) return GVA_ERR_WORKSPACE;
+  float* q_abs = reinterpret_cast<float*>(static_cast<char*>(workspace) + off);
+  float* q_rot = d.d_r > 0 ? q_abs + static_cast<size_t>(B) * d.H * d.d_v : nullptr;
+  if (gva::launch_append(ctx, B, 1, v_new, kr_new, nullptr, block_table, max_blocks, num_blocks, v_pool,
+                         kr_pool, stream, seq_lens) != cudaSuccess ||
+      gva::launch_absorb(ctx, B, q_c, q_r, nullptr, M, q_abs, q_rot, stream, seq_lens) != cudaSuccess)
+    return GVA_ERR_CUDA;
+  return decode_common(ctx, false, kPhasePartial | kPhaseCombine, B, q_abs, q_rot, nullptr, v_pool, kr_pool,
+                       block_table, max_blocks, num_blocks, seq_lens, max_seq_len, out, workspace, off,
+                       stream);
+}
+
+gva_status gva_set_step_mode(gva_ctx* ctx, gva_step_mode mode) {
+  if (!ctx || (mode != GVA_STEP_AUTO && mode != GVA_STEP_FUSED && mode != GVA_STEP_SEPARATE))
+    return GVA_ERR_INVALID_ARG;
+  ctx->step_mode = mode;
+  return GVA_OK;
 }
 
 gva_status gqa_decode_attention(gva_ctx* ctx, int B, const float* q, const void* k_pool,

@@ -19,7 +19,8 @@ namespace {
 struct AppendArgs {
   const void* v_new;
   const void* kr_new;
-  const int32_t* pos;
+  const int32_t* pos;       // null: position seq_lens[b] - 1
+  const int32_t* seq_lens;
   const int32_t* block_table;
   void* v_pool;
   void* kr_pool;
@@ -69,7 +70,8 @@ __global__ void __launch_bounds__(kAppendThreads) append_kernel(const AppendArgs
     x0 = static_cast<R>(CacheElem<T>::to_float(x[2 * lane]));
     x1 = static_cast<R>(CacheElem<T>::to_float(x[2 * lane + 1]));
   }
-  const long long p = static_cast<long long>(a.pos[b]) + t;
+  const long long p =
+      (a.pos ? static_cast<long long>(a.pos[b]) : static_cast<long long>(a.seq_lens[b]) - 1) + t;
 
   // Resolve the slot; an unresolvable one skips the token and is reported.
   if (p < 0 || (p >> 6) >= a.max_blocks || p >= (1LL << 32)) {
@@ -114,8 +116,10 @@ __global__ void __launch_bounds__(kAppendThreads) append_kernel(const AppendArgs
       y[2 * lane] = CacheElem<T>::from_double(y0);
       y[2 * lane + 1] = CacheElem<T>::from_double(y1);
     } else {
-      y[2 * lane] = __float2bfloat16_rn(fmaf(x0, c, -x1 * s));
-      y[2 * lane + 1] = __float2bfloat16_rn(fmaf(x0, s, x1 * c));
+      float y0, y1;
+      rope_rotate_f32(x0, x1, c, s, y0, y1);
+      y[2 * lane] = __float2bfloat16_rn(y0);
+      y[2 * lane + 1] = __float2bfloat16_rn(y1);
     }
   }
 }
@@ -125,11 +129,12 @@ __global__ void __launch_bounds__(kAppendThreads) append_kernel(const AppendArgs
 cudaError_t launch_append(const gva_ctx* ctx, int B, int n, const void* v_new,
                           const void* kr_new, const int32_t* pos, const int32_t* block_table,
                           int max_blocks, int num_blocks, void* v_pool, void* kr_pool,
-                          cudaStream_t stream) {
+                          cudaStream_t stream, const int32_t* seq_lens) {
   AppendArgs a;
   a.v_new = v_new;
   a.kr_new = kr_new;
   a.pos = pos;
+  a.seq_lens = seq_lens;
   a.block_table = block_table;
   a.v_pool = v_pool;
   a.kr_pool = kr_pool;

@@ -22,6 +22,16 @@
 // full (TMA), and the consumer warps take the range's tiles round-robin, each writing one
 // partial record per (sequence, group) it touched.  The matching GQA form (a separate key cache, no positional
 // slice) reuses the kernel with the key tile scored instead of the value tile.
+//
+// Fused decode step (FUSED instances): the absorption q' = M_h q_c and the rotation of the
+// positional query (the neighbouring step of the decode path) run in the kernel's prologue
+// instead of a kernel of their own.  The consumer warps, and the warps the launch has to spare
+// beside the pairs, compute them for every (group, sequence) segment of the CTA's range while
+// the copy warps fill the rings.  Each output is one fp32 dot product in k order, as in the
+// absorb kernel, so the results are bit-identical to it.  The new token of every sequence (the
+// last position of its context) is appended by the consumer that meets the sequence's last
+// tile: it writes the value row and the rotated positional key into the staged tile, before
+// any product reads it, and into the cache.
 #include <cuda.h>
 
 #include <algorithm>
@@ -89,6 +99,15 @@ __device__ __forceinline__ void mma_1688(float (&c)[4], uint32_t a0, uint32_t a1
       : "r"(a0), "r"(a1), "r"(b0));
 }
 
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
+__device__ __forceinline__ void st_shared_u32(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
 __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
   uint32_t y;
   asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
@@ -132,16 +151,19 @@ struct MmaLayout {
   static constexpr int kStageBytes = kOpBytes + kKrBytes;
 };
 
-// Shared memory: [alignment slack 1 KB][control 1 KB: full and empty mbarrier and valid
-// length of every stage][P*D operand tiles, 1 KB aligned for the swizzled boxes][P*D k_r
-// tiles][cum: B+1 ints].  Stage (c, slot) is index c*D + slot.
+// Shared memory: [alignment slack 1 KB][control 1 KB: full and empty mbarrier, valid length
+// and block id of every stage][P*D operand tiles, 1 KB aligned for the swizzled boxes][P*D
+// k_r tiles][cum: B+1 ints].  Stage (c, slot) is index c*D + slot.
 constexpr int kMaxStages = 40;
 constexpr int kCtrlBytes = 1024;
-static_assert(kMaxStages * (2 * 8 + 4) <= kCtrlBytes, "control block");
+static_assert(kMaxStages * (2 * 8 + 4 + 4) <= kCtrlBytes, "control block");
+constexpr int kStepBatch = 16;  // fused step: segments whose absorbed queries a warp forms at once
+constexpr int kStepBarrier = 1;  // fused step: named barrier that ends the prologue
+constexpr int kLookupBarrier = 2;  // fused step: the copy warps' first block-table reads are out
 // dynamic shared memory per CTA: the 227 KB opt-in limit less 1 KB for the kernel's static
 // shared memory (the prefix scan's scratch, placed ahead of the 1 KB aligned dynamic block)
 constexpr int kSmemLimit = 226 * 1024;
-inline int cum_bytes(int B) { return ((B + 1) * 4 + 15) / 16 * 16; }
+__host__ __device__ inline int cum_bytes(int B) { return ((B + 1) * 4 + 15) / 16 * 16; }
 inline int ring_fixed_bytes(int B) { return 1024 + kCtrlBytes + cum_bytes(B); }
 
 // One CTA streams one contiguous range of units (gva_sched.cuh) with P warp pairs.  Consumer
@@ -154,7 +176,10 @@ inline int ring_fixed_bytes(int B) { return 1024 + kCtrlBytes + cum_bytes(B); }
 // so phase parities are unambiguous, and about P*(D-1) tiles are in flight per SM while P
 // are being computed.  The copy warps take the issue work (a few hundred cycles per tile)
 // and the dependent block-table reads off the consumers' path.
-template <int DV, int DR, int R, int NQ, bool CAUSAL, bool SEPK>
+//
+// A FUSED launch adds E = (threads of the instance - 64*P)/32 prologue warps (warps 2P..2P+E-1)
+// that help form the queries and then exit.
+template <int DV, int DR, int R, int NQ, bool CAUSAL, bool SEPK, bool FUSED>
 __global__ void __launch_bounds__(mma_max_threads(DV, NQ), 1) decode_mma_kernel(const DecodeArgs a,
                                                                        const __grid_constant__ CUtensorMap tmv,
                                                                        const __grid_constant__ CUtensorMap tmk) {
@@ -167,6 +192,8 @@ __global__ void __launch_bounds__(mma_max_threads(DV, NQ), 1) decode_mma_kernel(
   constexpr int MD = DV / 16;           // m16 tiles over d_v in the output product
   static_assert(DR % 8 == 0, "positional width must be a multiple of 8 on this path");
   static_assert(!SEPK || DR == 0, "the key-cache form has no positional slice");
+  static_assert(!FUSED || (NQ == 1 && !CAUSAL && !SEPK), "the fused step is single-query GVA decode");
+  constexpr int QS = step_stage_floats(R, DV, DR);  // floats of one staged segment (fused step)
 
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
@@ -177,9 +204,13 @@ __global__ void __launch_bounds__(mma_max_threads(DV, NQ), 1) decode_mma_kernel(
   uint64_t* full = reinterpret_cast<uint64_t*>(smem);
   uint64_t* empty = full + kMaxStages;
   int* nvs = reinterpret_cast<int*>(empty + kMaxStages);  // tokens from each stage's tile to the end (0 = skip)
+  int* blks = nvs + kMaxStages;                            // block id of each stage's tile (fused step)
   unsigned char* tiles = smem + kCtrlBytes;
   unsigned char* krs = tiles + N * L::kOpBytes;
   int* cum = reinterpret_cast<int*>(krs + N * L::kKrBytes);
+  // fused step: the shared memory past the ring, [lengths: B ints][query stages]
+  unsigned char* spare = reinterpret_cast<unsigned char*>(cum) + cum_bytes(a.B);
+  int* lens_s = FUSED && a.spare_smem >= cum_bytes(a.B) ? reinterpret_cast<int*>(spare) : nullptr;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
@@ -195,13 +226,156 @@ __global__ void __launch_bounds__(mma_max_threads(DV, NQ), 1) decode_mma_kernel(
   }
   // Everything below may read what earlier work in the stream wrote.
   griddep_wait();
-  build_prefix<kMmaMaxThreads>(a, cum);  // ends with __syncthreads: the barriers are set up
+  build_prefix<kMmaMaxThreads>(a, cum, lens_s);  // ends with __syncthreads: the barriers are set up
   griddep_launch_dependents();
 
   const long long U = static_cast<long long>(a.G) * cum[a.B];
   const long long u0 = range_begin(blockIdx.x, U, a.n_groups);
   const int n = static_cast<int>(range_begin(blockIdx.x + 1, U, a.n_groups) - u0);
   if (n <= 0) return;  // CTA-uniform; no CTA-wide barrier follows
+
+  // ------------------------------------------------------------------ fused-step prologue
+  // Absorbed and rotated queries of every segment f_lo + j of this range into stage j (in the
+  // spare shared memory when they all fit, else stage c + f of the workspace), with the new
+  // token's rotated positional key.  Work items: (32 rows of one head, up to kStepBatch
+  // segments of one group); the item's M rows stay in registers while its segments' queries
+  // stream past.  A thread's positional pairs are rotated while its first item's loads are in
+  // flight, so the prologue costs about one memory round trip.
+  long long f_lo = 0;       // first segment of the range
+  int nseg = 0;             // segments of the range
+  float* stage = nullptr;   // stage of segment f_lo
+  if constexpr (FUSED) {
+    const UnitCursor first = cursor_at(u0, cum, a.B, a.G);
+    const UnitCursor last = cursor_at(u0 + n - 1, cum, a.B, a.G);
+    f_lo = segment_of(first.g, first.b, a.B);
+    nseg = static_cast<int>(segment_of(last.g, last.b, a.B) - f_lo) + 1;
+    const long long stage_smem = lens_s ? a.spare_smem - cum_bytes(a.B) : 0;
+    stage = static_cast<long long>(nseg) * QS * 4 <= stage_smem
+                ? reinterpret_cast<float*>(spare + cum_bytes(a.B))
+                : a.qstage + (static_cast<long long>(blockIdx.x) + f_lo) * QS;
+  }
+  auto absorb_segments = [&](int pw, int npw) {
+    // The prologue's loads go out after the copy warps' first block-table reads, which the
+    // first tile copies wait for (measured: 2.5 % of the long-context step; waiting until the
+    // rings are primed, or not at all, was slower).
+    named_barrier_sync(kLookupBarrier, static_cast<int>(blockDim.x));
+    // positional pairs: R query pairs and the new key's pair per (segment, pair index)
+    auto rotate_pairs = [&]() {
+      if constexpr (DR > 0) {
+        constexpr int PR = DR / 2;
+        const int nrot = nseg * (R + 1) * PR;
+        for (int it = pw * 32 + lane; it < nrot; it += npw * 32) {
+          const int sg = it / ((R + 1) * PR);
+          const int rem = it - sg * (R + 1) * PR;
+          const int r = rem / PR, pi = rem - r * PR;
+          const long long f = f_lo + sg;
+          const int g = static_cast<int>(f / a.B);
+          const int b = static_cast<int>(f - static_cast<long long>(g) * a.B);
+          int T;
+          if (lens_s) {
+            T = lens_s[b];  // 0 when out of range
+          } else {
+            T = a.seq_lens[b];
+            if (T > a.max_seq_len) T = 0;
+          }
+          if (T < 1) continue;  // no tile of this sequence is streamed
+          const long long xoff = r < R ? (static_cast<long long>(b) * a.H + g * R + r) * DR + 2 * pi : 0;
+          float2 x = make_float2(0.f, 0.f);
+          uint32_t w = 0;
+          if (r < R)
+            x = *reinterpret_cast<const float2*>(a.q_r + xoff);
+          else
+            w = *reinterpret_cast<const uint32_t*>(static_cast<const __nv_bfloat16*>(a.kr_new) +
+                                                   static_cast<long long>(b) * DR + 2 * pi);
+          float c, sn;
+          rope_cos_sin_f32(a.rope32, PR, static_cast<long long>(T) - 1, pi, c, sn);
+          float* slot = stage + static_cast<long long>(sg) * QS;
+          if (r < R) {
+            float2 y;
+            rope_rotate_f32(x.x, x.y, c, sn, y.x, y.y);
+            *reinterpret_cast<float2*>(slot + r * (DV + DR) + DV + 2 * pi) = y;
+          } else {
+            float x0, x1, y0, y1;
+            bf16x2_to_float2(w, x0, x1);
+            rope_rotate_f32(x0, x1, c, sn, y0, y1);
+            reinterpret_cast<uint32_t*>(slot + R * (DV + DR))[pi] = pack_bf16(y0, y1);
+          }
+        }
+      }
+    };
+    bool rotated = false;
+    // q' rows: four lanes per row, lane e of the quad accumulating chunks c = e, e+4, ... (the
+    // absorb kernel's summation order), so a warp's loads are 64 contiguous bytes per row
+    constexpr int RB = R * DV / 32;  // 32-row blocks of the group's R*d_v query rows
+    constexpr int XC = DV / 16;      // chunks per lane per row
+    const int rq = lane >> 2, e = lane & 3;
+    int item0 = 0;                   // item number of (this batch, block 0)
+    for (int s0 = 0; s0 < nseg; item0 += RB) {
+      const long long f0 = f_lo + s0;
+      const int g = static_cast<int>(f0 / a.B);
+      const int b0 = static_cast<int>(f0 - static_cast<long long>(g) * a.B);
+      const int cnt = min(min(kStepBatch, nseg - s0), a.B - b0);  // segments of group g
+      for (int rb = ((pw - item0) % npw + npw) % npw; rb < RB; rb += npw) {
+        const int h = (rb * 32) / DV;
+        const int head = g * R + h;
+        // rows i0 + 8*rnd of head h, RP of the four rounds at a time (16 vectors of M in registers)
+        const int i0 = rb * 32 - h * DV + rq;
+        constexpr int RP = 256 / DV;
+#pragma unroll 1
+        for (int r0 = 0; r0 < 4; r0 += RP) {
+        float4 m4[RP][XC];
+#pragma unroll
+        for (int rnd = 0; rnd < RP; ++rnd) {
+          const float4* mrow =
+              reinterpret_cast<const float4*>(a.M + (static_cast<long long>(head) * DV + i0 + 8 * (r0 + rnd)) * DV);
+#pragma unroll
+          for (int x = 0; x < XC; ++x) m4[rnd][x] = __ldg(mrow + 4 * x + e);
+        }
+        auto load_qc = [&](int j, float4 (&q4)[XC]) {
+          const float4* qrow = reinterpret_cast<const float4*>(a.q_c + (static_cast<long long>(b0 + j) * a.H + head) * DV);
+#pragma unroll
+          for (int x = 0; x < XC; ++x) q4[x] = __ldg(qrow + 4 * x + e);
+        };
+        float4 qn[XC];  // the next segment's query chunks, loaded one segment ahead
+        load_qc(0, qn);
+        if (!rotated) {  // while the loads above are in flight
+          rotate_pairs();
+          rotated = true;
+        }
+        for (int j = 0; j < cnt; ++j) {
+          float4 q4[XC];
+#pragma unroll
+          for (int x = 0; x < XC; ++x) q4[x] = qn[x];
+          if (j + 1 < cnt) load_qc(j + 1, qn);
+#pragma unroll
+          for (int rnd = 0; rnd < RP; ++rnd) {
+            float acc = 0.f;
+#pragma unroll
+            for (int x = 0; x < XC; ++x) {
+              acc = fmaf(m4[rnd][x].x, q4[x].x, acc);
+              acc = fmaf(m4[rnd][x].y, q4[x].y, acc);
+              acc = fmaf(m4[rnd][x].z, q4[x].z, acc);
+              acc = fmaf(m4[rnd][x].w, q4[x].w, acc);
+            }
+            acc += __shfl_xor_sync(kFullMask, acc, 1);  // p0 + p1, p2 + p3
+            acc += __shfl_xor_sync(kFullMask, acc, 2);  // (p0 + p1) + (p2 + p3)
+            if (e == 0) stage[static_cast<long long>(s0 + j) * QS + h * (DV + DR) + i0 + 8 * (r0 + rnd)] = acc;
+          }
+        }
+        }
+      }
+      s0 += cnt;
+    }
+    if (!rotated) rotate_pairs();
+  };
+  if constexpr (FUSED) {
+    const int E = static_cast<int>(blockDim.x / 32) - 2 * P;  // prologue-only warps
+    if (warp >= 2 * P) {
+      absorb_segments(P + (warp - 2 * P), P + E);
+      asm volatile("bar.arrive %0, %1;" ::"r"(kStepBarrier), "r"(32 * (P + E)) : "memory");
+      return;
+    }
+  }
 
   // ------------------------------------------------------------------ copy warps
   if (warp >= P) {
@@ -232,6 +406,7 @@ __global__ void __launch_bounds__(mma_max_threads(DV, NQ), 1) decode_mma_kernel(
     };
     int blk, grp, nv;
     lookup(0, blk, grp, nv);
+    if constexpr (FUSED) asm volatile("bar.arrive %0, %1;" ::"r"(kLookupBarrier), "r"(static_cast<int>(blockDim.x)) : "memory");
     int slot = 0, ph = 0, issued = 0;
     bool ok = true;
     for (int d0 = 0; d0 < n_mine && ok; d0 += 32) {
@@ -248,6 +423,7 @@ __global__ void __launch_bounds__(mma_max_threads(DV, NQ), 1) decode_mma_kernel(
           if (d0 + j >= D && !mbar_wait_bounded(&empty[s], ph ^ 1)) ok = false;
           if (ok) {
             nvs[s] = bj >= 0 ? vj : 0;  // published by the arrive below (release)
+            if (FUSED) blks[s] = bj;
             if (bj >= 0) {
               mbar_arrive_expect_tx(&full[s], L::kTx);
               unsigned char* st = tiles + s * L::kOpBytes;
@@ -288,6 +464,11 @@ __global__ void __launch_bounds__(mma_max_threads(DV, NQ), 1) decode_mma_kernel(
   }
 
   // ------------------------------------------------------------------ consumer warps
+  if constexpr (FUSED) {
+    const int E = static_cast<int>(blockDim.x / 32) - 2 * P;
+    absorb_segments(warp, P + E);
+    named_barrier_sync(kStepBarrier, 32 * (P + E));  // every stage of the range is written
+  }
   const int NC = P;  // consumer warps sharing the range
   int k = warp;
   if (k >= n) return;
@@ -301,6 +482,8 @@ __global__ void __launch_bounds__(mma_max_threads(DV, NQ), 1) decode_mma_kernel(
   // pass, head h of the group), part 0 = bf16(q), part 1 = bf16 remainder.
   uint32_t qb[NT][KSV + KSR][2];
   uint32_t qt[NT];
+  uint4 vnew = make_uint4(0, 0, 0, 0);  // fused step: a 16-byte piece of the new value row
+  uint32_t knew = 0;                    // fused step: a pair of the new rotated positional key
   auto load_q = [&](int b, int g) {
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
@@ -309,8 +492,8 @@ __global__ void __launch_bounds__(mma_max_threads(DV, NQ), 1) decode_mma_kernel(
       const bool valid = cp < RQ;
       const int qi = valid ? cp / R : 0, head = valid ? cp % R : 0;
       const long long row = (static_cast<long long>(b) * a.nq + a.q0 + qi) * a.H + g * R + head;
-      const float* qa = a.q_abs + row * DV;
-      const float* qr = a.q_rot + row * DR;
+      const float* qa = FUSED ? stage + (segment_of(g, b, a.B) - f_lo) * QS + head * (DV + DR) : a.q_abs + row * DV;
+      const float* qr = FUSED ? qa + DV : a.q_rot + row * DR;
       auto qv = [&](int kk) -> float {
         if (!valid) return 0.f;
         const float x = (kk < DV ? qa[kk] : qr[kk - DV]) * a.scale_log2;
@@ -326,6 +509,12 @@ __global__ void __launch_bounds__(mma_max_threads(DV, NQ), 1) decode_mma_kernel(
         const int k0 = 16 * (KSV + KSR) + 2 * tq;
         qt[nt] = pack_bf16(qv(k0), qv(k0 + 1));
       }
+    }
+    if constexpr (FUSED) {  // the new token's row, in case this warp meets the segment's last tile
+      if (lane < DV / 8)
+        vnew = __ldg(reinterpret_cast<const uint4*>(a.v_new) + (static_cast<long long>(b) * a.G + g) * (DV / 8) + lane);
+      if (DR > 0 && lane < DR / 2)
+        knew = reinterpret_cast<const uint32_t*>(stage + (segment_of(g, b, a.B) - f_lo) * QS + R * (DV + DR))[lane];
     }
   };
 
@@ -384,11 +573,29 @@ __global__ void __launch_bounds__(mma_max_threads(DV, NQ), 1) decode_mma_kernel(
       break;
     }
     const int nrem = nvs[s];
+    bool patched = false;
     if (nrem > 0) {
       const int nv = min(nrem, kBlockTokens);  // valid tokens of the tile
       const uint32_t vbase = smem_addr(tiles + s * L::kOpBytes);
       const uint32_t kbase = SEPK ? vbase + L::kVBytes : vbase;  // tile that is scored
       const uint32_t krbase = smem_addr(krs + s * L::kKrBytes);
+      if constexpr (FUSED) {
+        if (nrem <= kBlockTokens) {  // the sequence's last tile: the new token is row nrem - 1
+          const int o = nrem - 1;
+          const long long blk = blks[s];
+          if (lane < DV / 8) {
+            st_shared_v4(vbase + (lane >> 3) * kSubTileBytes + o * 128 + (((lane & 7) ^ (o & 7)) << 4), vnew);
+            reinterpret_cast<uint4*>(a.v_pool_w)[((blk * a.G + cc.g) * kBlockTokens + o) * (DV / 8) + lane] = vnew;
+          }
+          if (DR > 0 && lane < DR / 2) {
+            st_shared_u32(krbase + o * (2 * DR) + 4 * lane, knew);
+            if (cc.g == 0)  // one positional key per token, shared by the groups
+              reinterpret_cast<uint32_t*>(a.kr_pool_w)[(blk * kBlockTokens + o) * (DR / 2) + lane] = knew;
+          }
+          patched = true;
+          __syncwarp();
+        }
+      }
 
       // scores
       float sc[NT][4][4];
@@ -542,8 +749,11 @@ __global__ void __launch_bounds__(mma_max_threads(DV, NQ), 1) decode_mma_kernel(
         }
       }
     }
+    // the stage may be refilled (after this warp's own writes into it, if any, are ordered
+    // before the copy engine's)
+    if (FUSED && patched) fence_proxy_async_smem();
     __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[s]);  // the stage may be refilled
+    if (lane == 0) mbar_arrive(&empty[s]);
     k += NC;
     if (k >= n) break;
     const int pb_ = cc.b, pg = cc.g;
@@ -574,16 +784,22 @@ __global__ void __launch_bounds__(mma_max_threads(DV, NQ), 1) decode_mma_kernel(
   }
 }
 
-template <int DV, int DR, int R, int NQ, bool CAUSAL, bool SEPK>
+template <int DV, int DR, int R, int NQ, bool CAUSAL, bool SEPK, bool FUSED>
 cudaError_t launch_mma_t(const DecodeArgs& a, const CUtensorMap& mv, const CUtensorMap& mk, int grid,
                          cudaStream_t stream) {
   using L = MmaLayout<DV, DR, SEPK>;
   const int P = a.group_warps, D = a.n_stages;
   if (P < 1 || 64 * P > mma_max_threads(DV, NQ) || D < 1 || P * D > kMaxStages) return cudaErrorInvalidValue;
-  if (a.nqp != NQ || (a.nq > 1) != CAUSAL) return cudaErrorInvalidValue;
+  if (a.nqp != NQ || (a.nq > 1) != CAUSAL || (a.fused != 0) != FUSED) return cudaErrorInvalidValue;
   const int smem = ring_fixed_bytes(a.B) + P * D * L::kStageBytes;
   if (smem > kSmemLimit) return cudaErrorInvalidValue;
-  auto kern = decode_mma_kernel<DV, DR, R, NQ, CAUSAL, SEPK>;
+  // the fused step fills the instance's thread budget with prologue warps, and the shared
+  // memory budget with query stages
+  const int threads = FUSED ? mma_max_threads(DV, NQ) : 64 * P;
+  DecodeArgs args = a;
+  args.spare_smem = FUSED ? kSmemLimit - smem : 0;
+  const int dyn_smem = FUSED ? kSmemLimit : smem;
+  auto kern = decode_mma_kernel<DV, DR, R, NQ, CAUSAL, SEPK, FUSED>;
   static int configured[kMaxDevices] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -595,15 +811,15 @@ cudaError_t launch_mma_t(const DecodeArgs& a, const CUtensorMap& mv, const CUten
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(64 * P);
-  cfg.dynamicSmemBytes = smem;
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = dyn_smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, a, mv, mk);
+  return cudaLaunchKernelEx(&cfg, kern, args, mv, mk);
 }
 
 // Queries per pass: the instances built are NQ in {1, 2, 4} with R*NQ <= 8.
@@ -611,13 +827,18 @@ template <int DV, int DR, int R, bool SEPK>
 cudaError_t dispatch_nq(const DecodeArgs& a, const CUtensorMap& mv, const CUtensorMap& mk, int grid,
                         cudaStream_t stream) {
   if constexpr (!SEPK) {
+    if (a.fused) {
+      if (a.nqp == 1 && a.nq == 1 && a.d_v == DV) return launch_mma_t<DV, DR, R, 1, false, SEPK, true>(a, mv, mk, grid, stream);
+      return cudaErrorInvalidValue;
+    }
     if constexpr (R * 4 <= 8)
-      if (a.nqp == 4) return launch_mma_t<DV, DR, R, 4, true, SEPK>(a, mv, mk, grid, stream);
+      if (a.nqp == 4) return launch_mma_t<DV, DR, R, 4, true, SEPK, false>(a, mv, mk, grid, stream);
     if constexpr (R * 2 <= 8)
-      if (a.nqp == 2) return launch_mma_t<DV, DR, R, 2, true, SEPK>(a, mv, mk, grid, stream);
-    if (a.nqp == 1 && a.nq > 1) return launch_mma_t<DV, DR, R, 1, true, SEPK>(a, mv, mk, grid, stream);
+      if (a.nqp == 2) return launch_mma_t<DV, DR, R, 2, true, SEPK, false>(a, mv, mk, grid, stream);
+    if (a.nqp == 1 && a.nq > 1) return launch_mma_t<DV, DR, R, 1, true, SEPK, false>(a, mv, mk, grid, stream);
   }
-  if (a.nqp == 1 && a.nq == 1) return launch_mma_t<DV, DR, R, 1, false, SEPK>(a, mv, mk, grid, stream);
+  if (a.fused) return cudaErrorInvalidValue;
+  if (a.nqp == 1 && a.nq == 1) return launch_mma_t<DV, DR, R, 1, false, SEPK, false>(a, mv, mk, grid, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -196,6 +196,21 @@ __device__ __forceinline__ void rope_cos_sin_f32(const float2* __restrict__ tab,
   }
 }
 
+// Turns the pair (x0, x1) by the angle whose cosine and sine are (c, s), in fp32.  Every
+// fp32 rotation of this library (query and key) goes through this one expression, so a query
+// or key rotated by different kernels has the same bits.
+__device__ __forceinline__ void rope_rotate_f32(float x0, float x1, float c, float s, float& y0,
+                                                float& y1) {
+  y0 = fmaf(x0, c, -x1 * s);
+  y1 = fmaf(x0, s, x1 * c);
+}
+
+// Waits at CTA barrier `id` (1..15; 0 is __syncthreads) for `threads` threads (a multiple of
+// 32) and orders their earlier memory accesses before their later ones.
+__device__ __forceinline__ void named_barrier_sync(int id, int threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
 __device__ __forceinline__ void flag_error(unsigned* err, unsigned bit) {
   if (err) atomicOr(err, bit);
 }

@@ -19,6 +19,7 @@ struct gva_ctx {
   float2* d_rope32;     // the same table rounded to fp32
   int split_tokens;     // 0 = automatic
   gva_decode_path path;
+  gva_step_mode step_mode;
 };
 
 namespace gva {
@@ -50,7 +51,30 @@ struct DecodeArgs {
   int n_groups, group_warps;
   int n_stages;              // tensor-core kernel: ring depth of each warp pair (tiles)
   float scale_log2;          // softmax scale * log2(e)
+  // Fused decode step (tensor-core kernel, one query per sequence, d_n == d_v): the partial
+  // kernel absorbs and rotates the queries itself and appends the new token of every
+  // sequence, at position seq_lens[b] - 1, to the cache.  q_abs and q_rot are then unused.
+  int fused;
+  const float* q_c;          // [B,H,d_n] content query
+  const float* q_r;          // [B,H,d_r] positional query, unrotated
+  const float* M;            // [H,d_v,d_n] key maps
+  const void* v_new;         // [B,G,d_v] new values (bf16)
+  const void* kr_new;        // [B,d_r] new positional keys, unrotated (bf16)
+  void* v_pool_w;            // v_pool and kr_pool again, written at the new token's slot
+  void* kr_pool_w;
+  const float2* rope32;      // fp32 RoPE digit table
+  // Per (range c, segment f) at index c + f: step_stage_floats(R, d_v, d_r) floats holding
+  // the R absorbed queries [d_v] each followed by its rotated positional query [d_r], then the
+  // new token's rotated positional key as d_r/2 packed bf16 pairs.  A CTA keeps its stages in
+  // the shared memory the ring leaves over (spare_smem bytes) when they fit, here otherwise.
+  float* qstage;
+  int spare_smem;
 };
+
+// Floats of one fused-step query stage (a multiple of 4, so every stage is 16-byte aligned).
+__host__ __device__ constexpr int step_stage_floats(int R, int d_v, int d_r) {
+  return (R * (d_v + d_r) + d_r / 2 + 3) / 4 * 4;
+}
 
 // Record layout of one partial: m (log2 domain), l, two pad words, then d_v weighted sums.
 __host__ __device__ inline size_t partial_stride_floats(int d_v) { return static_cast<size_t>(d_v) + 4; }
@@ -69,13 +93,15 @@ struct Plan {
 };
 
 // Launchers (return cudaSuccess or the launch error).
+// With pos_q (pos) null, sequence b's position is seq_lens[b] - 1 (the last token of the
+// context: one decode step).
 cudaError_t launch_absorb(const gva_ctx* ctx, int B, const float* q_c, const float* q_r,
                           const int32_t* pos_q, const float* M, float* q_abs, float* q_rot,
-                          cudaStream_t stream);
+                          cudaStream_t stream, const int32_t* seq_lens = nullptr);
 cudaError_t launch_append(const gva_ctx* ctx, int B, int n, const void* v_new,
                           const void* kr_new, const int32_t* pos, const int32_t* block_table,
                           int max_blocks, int num_blocks, void* v_pool, void* kr_pool,
-                          cudaStream_t stream);
+                          cudaStream_t stream, const int32_t* seq_lens = nullptr);
 // Decode: partial kernel + combine.  sep_k selects the GQA form (k_pool used, d_r == 0).
 // Partial kernels: one CTA = 4 warps, each warp a balanced range of (b, g, tile) units.
 bool fma_supported(const gva_dims& d, bool sep_k);

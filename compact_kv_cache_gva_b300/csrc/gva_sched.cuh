@@ -58,9 +58,10 @@ __host__ __device__ inline bool warp_touched(long long a, long long e, int w, in
 // Per-CTA prologue: cum[0..B] in shared memory from seq_lens; lengths outside
 // [max(1, nq), max_seq_len] count as zero tiles (and are reported once by CTA 0).  Uses all
 // blockDim.x threads of the CTA (a multiple of 32, at most MAXT); ends with __syncthreads().
-// CTA 0 also publishes cum to the workspace header.
+// CTA 0 also publishes cum to the workspace header.  With `lens` (shared memory, B ints) the
+// lengths are kept too, 0 for a length outside that range.
 template <int MAXT>
-__device__ void build_prefix(const DecodeArgs& a, int* cum) {
+__device__ void build_prefix(const DecodeArgs& a, int* cum, int* lens = nullptr) {
   __shared__ int warp_tot[MAXT / 32];
   __shared__ int carry;
   const int nthr = blockDim.x;
@@ -72,10 +73,12 @@ __device__ void build_prefix(const DecodeArgs& a, int* cum) {
     int nt = 0;
     if (b < a.B) {
       const int T = a.seq_lens[b];
-      if (T >= a.nq && T >= 1 && T <= a.max_seq_len)
+      const bool valid = T >= a.nq && T >= 1 && T <= a.max_seq_len;
+      if (valid)
         nt = (T + kBlockTokens - 1) / kBlockTokens;
       else if (blockIdx.x == 0)
         flag_error(a.err, GVA_DEVERR_SEQ_LEN);
+      if (lens) lens[b] = valid ? T : 0;
     }
     // inclusive warp scan, then across warps
     int v = nt;

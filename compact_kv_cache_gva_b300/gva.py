@@ -17,6 +17,7 @@ LIB_PATH = os.path.join(_PKG, "libgva.so")
 GVA_OK, GVA_ERR_INVALID_ARG, GVA_ERR_UNSUPPORTED, GVA_ERR_WORKSPACE, GVA_ERR_CUDA, GVA_ERR_DEVICE_INDEX = range(6)
 GVA_F32, GVA_BF16 = 0, 1
 GVA_PATH_AUTO, GVA_PATH_FMA, GVA_PATH_MMA = 0, 1, 2
+GVA_STEP_AUTO, GVA_STEP_FUSED, GVA_STEP_SEPARATE = 0, 1, 2
 GVA_DEVERR_POSITION, GVA_DEVERR_BLOCK_ID, GVA_DEVERR_SEQ_LEN, GVA_DEVERR_TIMEOUT = 1, 2, 4, 8
 BLOCK_TOKENS = 64
 
@@ -25,7 +26,8 @@ EXPORTS = ("gva_create", "gva_destroy", "gva_absorb_query", "gva_cache_append", 
            "gva_decode_attention", "gqa_decode_attention", "gva_set_split_tokens", "gva_set_decode_path",
            "gva_decode_plan", "gva_get_device_error", "gva_status_string", "gva_version",
            "gva_decode_attention_noalloc", "gva_decode_partial", "gva_decode_combine",
-           "gva_decode_attention_multi", "gva_decode_workspace_size_multi")
+           "gva_decode_attention_multi", "gva_decode_workspace_size_multi", "gva_decode_step",
+           "gva_decode_step_workspace_size", "gva_set_step_mode")
 NOALLOC_SCRATCH_BYTES = 4 << 20
 
 
@@ -67,6 +69,10 @@ def load():
     L.gva_decode_attention_multi.argtypes = [vp, i, i, vp, vp, vp, vp, ip, i, i, ip, i, vp, vp, C.c_size_t, st]
     L.gva_decode_workspace_size_multi.argtypes = [vp, i, i, i]
     L.gva_decode_workspace_size_multi.restype = C.c_size_t
+    L.gva_decode_step.argtypes = [vp, i, vp, vp, vp, vp, vp, vp, vp, ip, i, i, ip, i, vp, vp, C.c_size_t, st]
+    L.gva_decode_step_workspace_size.argtypes = [vp, i, i]
+    L.gva_decode_step_workspace_size.restype = C.c_size_t
+    L.gva_set_step_mode.argtypes = [vp, i]
     L.gva_set_split_tokens.argtypes = [vp, i]
     L.gva_set_decode_path.argtypes = [vp, i]
     L.gva_decode_plan.argtypes = [vp, i, i, C.POINTER(C.c_int), C.POINTER(C.c_int)]
@@ -76,7 +82,7 @@ def load():
     L.gva_version.argtypes = []
     for name in EXPORTS:
         if name not in ("gva_destroy", "gva_decode_workspace_size", "gva_decode_workspace_size_multi",
-                        "gva_status_string", "gva_version"):
+                        "gva_decode_step_workspace_size", "gva_status_string", "gva_version"):
             getattr(L, name).restype = C.c_int
     _lib = L
     return L
@@ -326,6 +332,44 @@ def gva_decode_attention_noalloc(ctx, q_abs, q_rot, v_pool, kr_pool, block_table
                                                v_pool.shape[0], _ptr(seq_lens, torch.int32, "seq_lens"),
                                                int(max_seq_len), _ptr(out, torch.float32, "out"), _stream(stream)),
            "gva_decode_attention_noalloc")
+
+
+def gva_decode_step_workspace_size(ctx, B, max_seq_len):
+    return int(load().gva_decode_step_workspace_size(ctx.handle, int(B), int(max_seq_len)))
+
+
+def gva_decode_step(ctx, q_c, q_r, M, v_new, kr_new, v_pool, kr_pool, block_table, seq_lens, max_seq_len, out,
+                    workspace, stream=None):
+    """One decode step: appends each sequence's new token (v_new [B,G,d_v], kr_new [B,d_r], cache
+    dtype) at position seq_lens[b]-1, absorbs and rotates the query (q_c [B,H,d_n], q_r [B,H,d_r],
+    M [H,d_v,d_n]) at that position, and attends over the context including the new token
+    into out [B,H,d_v].  seq_lens already count the new token."""
+    d = ctx.dims
+    B = q_c.shape[0]
+    dt = ctx.cache_torch_dtype
+    has_r = d.d_r > 0
+    _shape(q_c, (B, d.H, d.d_n), "q_c")
+    _shape(M, (d.H, d.d_v, d.d_n), "M")
+    _shape(v_new, (B, d.G, d.d_v), "v_new")
+    _shape(out, (B, d.H, d.d_v), "out")
+    if has_r:
+        _shape(q_r, (B, d.H, d.d_r), "q_r")
+        _shape(kr_new, (B, d.d_r), "kr_new")
+    _check_table(block_table, B, seq_lens)
+    _check_pools(ctx, v_pool, kr_pool if has_r else None)
+    _check(load().gva_decode_step(ctx.handle, B, _ptr(q_c, torch.float32, "q_c"),
+                                  _ptr(q_r, torch.float32, "q_r", allow_none=not has_r), _ptr(M, torch.float32, "M"),
+                                  _ptr(v_new, dt, "v_new"), _ptr(kr_new, dt, "kr_new", allow_none=not has_r),
+                                  _ptr(v_pool, dt, "v_pool"), _ptr(kr_pool, dt, "kr_pool", allow_none=not has_r),
+                                  _ptr(block_table, torch.int32, "block_table"), block_table.shape[1],
+                                  v_pool.shape[0], _ptr(seq_lens, torch.int32, "seq_lens"), int(max_seq_len),
+                                  _ptr(out, torch.float32, "out"), _ptr(workspace, None, "workspace"),
+                                  workspace.numel() * workspace.element_size(), _stream(stream)),
+           "gva_decode_step")
+
+
+def gva_set_step_mode(ctx, mode):
+    _check(load().gva_set_step_mode(ctx.handle, int(mode)), "gva_set_step_mode")
 
 
 def gqa_decode_attention(ctx, q, k_pool, v_pool, block_table, seq_lens, max_seq_len, out, workspace, stream=None):

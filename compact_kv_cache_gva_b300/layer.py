@@ -1,4 +1,5 @@
-"""One decode step of one GVA layer through the C ABI: absorb -> append -> decode.
+"""One decode step of one GVA layer through the C ABI: absorb -> append -> decode, as three
+calls (step) or as the library's one-call step (fused_step).
 
 Holds the step's device buffers (absorbed/rotated queries, output, workspace) so a caller
 only passes the step's inputs and the cache.  Marshalling only; the work is in libgva.so.
@@ -13,18 +14,22 @@ class GVADecodeLayer:
     reading the cache through its own position): query rows are b*n_q + i, out is [B,n_q,H,d_v]."""
 
     def __init__(self, H, G, d_v, d_n, d_r, cache_dtype, B, max_seq_len, device="cuda", split_tokens=0,
-                 path=gva.GVA_PATH_AUTO, rope_base=10000.0, scale=0.0, n_q=1):
+                 path=gva.GVA_PATH_AUTO, rope_base=10000.0, scale=0.0, n_q=1, step_mode=gva.GVA_STEP_AUTO):
         self.ctx = gva.gva_create(H, G, d_v, d_n, d_r, cache_dtype, rope_base, scale)
         if split_tokens:
             gva.gva_set_split_tokens(self.ctx, split_tokens)
         if path != gva.GVA_PATH_AUTO:
             gva.gva_set_decode_path(self.ctx, path)
+        if step_mode != gva.GVA_STEP_AUTO:
+            gva.gva_set_step_mode(self.ctx, step_mode)
         self.B, self.max_seq_len, self.n_q = B, max_seq_len, n_q
         self.q_abs = torch.empty((B * n_q, H, d_v), dtype=torch.float32, device=device)
         self.q_rot = torch.empty((B * n_q, H, d_r), dtype=torch.float32, device=device)
         self.out = torch.empty((B, H, d_v) if n_q == 1 else (B, n_q, H, d_v), dtype=torch.float32, device=device)
         ws = max(16, gva.gva_decode_workspace_size(self.ctx, B, max_seq_len) if n_q == 1 else
                  gva.gva_decode_workspace_size_multi(self.ctx, B, n_q, max_seq_len))
+        if n_q == 1:
+            ws = max(ws, gva.gva_decode_step_workspace_size(self.ctx, B, max_seq_len))
         self.workspace = torch.empty(ws, dtype=torch.uint8, device=device)
         self._side = None  # side stream of step(overlap=True), created on first use
 
@@ -72,6 +77,19 @@ class GVADecodeLayer:
         self.absorb(q_c, q_r, pos_q, M, main)
         main.wait_stream(self._side)
         return self.attend(v_pool, kr_pool, block_table, seq_lens, stream=main)
+
+    def fused_step(self, q_c, q_r, M, v_new, kr_new, block_table, seq_lens, v_pool, kr_pool, stream=None):
+        """The whole step in one library call (gva_decode_step): the new token (v_new [B,1,G,d_v]
+        or [B,G,d_v], kr_new [B,1,d_r] or [B,d_r]) goes to position seq_lens[b]-1, which the
+        lengths already count, and the query sits there."""
+        if self.n_q != 1:
+            raise ValueError("fused_step decodes one query per sequence")
+        d = self.ctx.dims
+        has_r = d.d_r > 0
+        gva.gva_decode_step(self.ctx, q_c, q_r if has_r else None, M, v_new.reshape(self.B, d.G, d.d_v),
+                            kr_new.reshape(self.B, d.d_r) if has_r else None, v_pool, kr_pool if has_r else None,
+                            block_table, seq_lens, self.max_seq_len, self.out, self.workspace, stream)
+        return self.out
 
     def device_error(self):
         return gva.gva_get_device_error(self.ctx)

@@ -201,6 +201,43 @@ gva_status gva_decode_attention_multi(gva_ctx* ctx, int B, int n_q, const float*
                                       void* workspace, size_t ws_bytes, gva_stream_t stream);
 size_t gva_decode_workspace_size_multi(const gva_ctx* ctx, int B, int n_q, int max_seq_len);
 
+/* Step mode for gva_set_step_mode. */
+typedef enum {
+  GVA_STEP_AUTO = 0,     /* fused where it applies and the batch has few (group, sequence)
+                            segments per unit range, else the separate kernels */
+  GVA_STEP_FUSED = 1,    /* fused kernel (GVA_ERR_UNSUPPORTED where it does not apply) */
+  GVA_STEP_SEPARATE = 2  /* append, absorb and decode as separate kernels */
+} gva_step_mode;
+
+/* gva_decode_step -- one whole decode step of a layer: append each sequence's new token,
+ * absorb and rotate its query, and attend over the context including the new token.
+ * Sequence b's context length T = seq_lens[b] ALREADY COUNTS the new token, which goes to
+ * position p = T - 1, and its query sits at p (the decode lifecycle of the GQA explainer,
+ * section "与位置编码和 KV Cache 的关系": append the new token's state, then read the cache
+ * through the current position).  The result equals
+ *   gva_cache_append(ctx, B, 1, v_new, kr_new, pos = T - 1, ...);
+ *   gva_absorb_query(ctx, B, q_c, q_r, pos_q = T - 1, M, q_abs, q_rot, ...);
+ *   gva_decode_attention(ctx, B, q_abs, q_rot, ...);
+ * bit for bit, and the cache holds the new token afterwards in both forms.
+ *   q_c [B,H,d_n] f32, q_r [B,H,d_r] f32 (NULL when d_r == 0), M [H,d_v,d_n] f32
+ *   v_new [B,G,d_v] and kr_new [B,d_r] cache dtype (kr_new unrotated; 4-byte aligned)
+ *   v_pool, kr_pool, block_table, seq_lens, out: as gva_cache_append and gva_decode_attention
+ *   workspace: at least gva_decode_step_workspace_size(ctx, B, max_seq_len) bytes.
+ * The fused form (tensor-core path, d_n == d_v) is one partial kernel plus the combine: the
+ * partial kernel forms the absorbed queries in its prologue (the "extra query-side compute"
+ * of absorption, summary section 方法, done where the queries are used) and appends the new
+ * token while it streams the sequence's last block.  The separate form is the three calls
+ * above on `stream`.  gva_set_step_mode picks one; the default decides from the batch shape.
+ * A sequence whose length is outside [1, max_seq_len] sets GVA_DEVERR_SEQ_LEN, gets a zero
+ * output row, and its new slot's contents are unspecified. */
+gva_status gva_decode_step(gva_ctx* ctx, int B, const float* q_c, const float* q_r, const float* M,
+                           const void* v_new, const void* kr_new, void* v_pool, void* kr_pool,
+                           const int32_t* block_table, int max_blocks, int num_blocks,
+                           const int32_t* seq_lens, int max_seq_len, float* out, void* workspace,
+                           size_t ws_bytes, gva_stream_t stream);
+size_t gva_decode_step_workspace_size(const gva_ctx* ctx, int B, int max_seq_len);
+gva_status gva_set_step_mode(gva_ctx* ctx, gva_step_mode mode);
+
 /* gqa_decode_attention -- the matching grouped-query attention decode, built with the same
  * tiling and pools so that the cost of a key cache can be timed beside GVA (GQA explainer,
  * section "一次 GQA 计算如何展开": grouped keys and values, head h reads group g(h)).
