@@ -1,13 +1,15 @@
-"""Benchmark of the GVA decode hot path on B300: one step = absorb + append + decode.
+"""Benchmark of the GVA decode hot path on B300: one step = append + absorb + decode attention.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 4] [--path auto|fma|mma]
     python bench.py --impl reference ...     # the fp64 CPU oracle on a bounded sample
 
 Prints ONE JSON line (rank 0).  `value` is the cache bytes the step's decode attention must
 read (algorithmic: sum_b T_b * (G*d_v + d_r) * elem bytes) divided by the device time of the
-whole step, with every input resident in HBM.  `e2e` is the same metric through the same
-C-ABI calls when each step's inputs start in pinned host memory and its output returns to
-the host.  `roofline` is for the decode attention call (split-T partial kernel + combine).
+whole step, with every input resident in HBM.  The step is the library's one-call step,
+gva_decode_step (automatic mode: the fused kernel, or the three kernels where the batch has
+many segments per range); the same step as three calls is timed beside it.  `e2e` is the same
+metric through the same C-ABI call when each step's inputs start in pinned host memory and its
+output returns to the host.  `roofline` is for the step's split-T partial kernel.
 Under torchrun every rank runs its own replica of the workload (sequences are independent;
 no collective on the data path) and the line reports the total over ranks (weak scaling).
 """
@@ -30,9 +32,10 @@ from compact_kv_cache_gva_b300 import gva, synth  # noqa: E402
 from compact_kv_cache_gva_b300.layer import GVADecodeLayer  # noqa: E402
 
 METRIC = "GVA decode-attention cache-read GB/s (% of B300 HBM peak) and context tokens/s"
-# DRAM bytes (read + write) of one launch of the split-T partial kernel, from the ncu capture
-# summarised in profiles/ (None where no capture of the current kernel exists)
-TRAFFIC = {"long-context-bf16": 574_461_568}
+# DRAM bytes (read + write) of one launch of the step's split-T partial kernel (the fused one,
+# or the plain one), from the ncu captures summarised in profiles/ (absent where no capture of
+# the current kernel exists)
+TRAFFIC = {("long-context-bf16", "plain"): 574_461_568, ("long-context-bf16", "fused"): 572_635_264}
 L2_BYTES = 126 * 1024 * 1024
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 NVML_REASONS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap", 0x8: "hw_slowdown",
@@ -256,8 +259,35 @@ class Setup:
         self.decode_bytes = (self.cache_bytes + n_q * (w.B * w.H * (w.d_v + w.d_r) * 4 + w.B * w.H * w.d_v * 4) +
                              w.B * 4 + used_blocks * 4)
         self.decode_flops = self.sum_T * w.H * (2 * (w.d_v + w.d_r) + 2 * w.d_v)
+        # the fused partial pass reads the raw queries and the key maps instead of the absorbed
+        # queries, and reads and writes the new token
+        self.step_bytes = (self.cache_bytes + w.B * w.H * (w.d_n + w.d_r) * 4 + w.H * w.d_v * w.d_n * 4 +
+                           2 * w.B * (w.G * w.d_v + w.d_r) * w.elem_bytes + w.B * w.H * w.d_v * 4 + w.B * 4 +
+                           used_blocks * 4)
+
+        # one query per sequence: the library's one-call step; several: append + absorb + the
+        # multi-query decode
+        self.one_call = n_q == 1
+        self.fused = self.one_call and gva.gva_step_is_fused(self.layer.ctx, w.B, w.max_seq_len) == 1
+        R = w.H // w.G
+        nqp_max = 4 if R <= 2 else 2 if R == 4 else 1
+        passes, q = 0, 0
+        while q < n_q:  # the library's passes: the largest power of two that fits, then smaller
+            p = 1
+            while 2 * p <= min(nqp_max, n_q - q):
+                p *= 2
+            q += p
+            passes += 1
+        self.launches_per_step = 2 if self.fused else 2 + 2 * passes
 
     def step(self, stream=None):
+        if not self.one_call:
+            return self.three_call_step(stream)
+        r, i = self.raw, self.inp
+        return self.layer.fused_step(r.q_c, r.q_r, r.M, r.v_new, r.kr_new, i.block_table, i.seq_lens, i.v_pool,
+                                     i.kr_pool, stream)
+
+    def three_call_step(self, stream=None):
         r, i = self.raw, self.inp
         return self.layer.step(r.q_c, r.q_r, r.pos_q, r.M, r.v_new, r.kr_new, r.pos_new, i.block_table,
                                i.seq_lens, i.v_pool, i.kr_pool, stream)
@@ -347,7 +377,7 @@ def run_ours(args, rank, ws):
     if S.layer.device_error():
         raise RuntimeError("device reported an index error during warm-up")
     run_step = S.step
-    if args.graph:  # the three C-ABI calls of a step, replayed as one graph
+    if args.graph:  # the step's C-ABI call(s), replayed as one graph
         run_step = capture(S.step).replay
         for _ in range(3):
             run_step()
@@ -360,6 +390,17 @@ def run_ours(args, rank, ws):
         step_s = time_steps(run_step, K, flush)
     barrier(ws)
     total_s = max_over_ranks(step_s, ws)
+
+    # the same step as three calls (append on a side stream beside absorb, then decode), timed alike
+    three_s = None
+    if S.one_call:
+        for _ in range(3):
+            S.three_call_step()
+        three_run = capture(S.three_call_step).replay if args.graph else S.three_call_step
+        for _ in range(3):
+            three_run()
+        torch.cuda.synchronize()
+        three_s = max_over_ranks(time_steps(three_run, K, flush), ws)
 
     # the decode call alone (split-T partial + combine), timed the same way
     dec_s = max_over_ranks(time_steps(lambda: S.layer.attend(S.inp.v_pool, S.inp.kr_pool, S.inp.block_table,
@@ -385,14 +426,19 @@ def run_ours(args, rank, ws):
     pk, pk_kind = peaks()
     dec_us = dec_s * 1e6 / K
     part_us = part_s * 1e6
-    achieved = S.decode_bytes / part_s / 1e9
+    part_bytes = S.step_bytes if S.fused else S.decode_bytes
+    achieved = part_bytes / part_s / 1e9
     hbm_peak = pk["hbm_gbs"]
+    step_desc = ("gva_decode_step, fused: the split-T partial kernel absorbs and rotates the query in its "
+                 "prologue and appends the new token, then the combine" if S.fused else
+                 "gva_decode_step as separate kernels: append + absorb + split-T partial + combine" if S.one_call
+                 else "append + absorb + gva_decode_attention_multi")
 
     out = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws, "steps": K,
         "warmup": max(3, args.warmup), "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
-        "config": dict(w.describe(), step="absorb+append+decode", decode_path=args.path, n_q=S.n_q,
+        "config": dict(w.describe(), step=step_desc, decode_path=args.path, n_q=S.n_q,
                        cuda_graph=bool(args.graph),
                        split_plan=dict(zip(("split_tokens", "partial_warps"), S.layer.plan())),
                        l2="flushed before every step (252 MB write, then 252 MB read)" if need_flush else
@@ -401,16 +447,20 @@ def run_ours(args, rank, ws):
         "pct_of_hbm_peak": round(100 * value / ws / hbm_peak, 2),
         "context_tokens_per_s": round(tokens_per_s, 1),
         "decode_steps_per_s": round(K * ws / total_s, 2),
+        "three_call_step_us": round(three_s * 1e6 / K, 3) if three_s else None,
         "breakdown_us": br,
-        "roofline": {"kernel": "split-T partial pass of gva_decode_attention (gva_decode_partial)" if S.n_q == 1
-                     else f"gva_decode_attention_multi, {S.n_q} queries per sequence (partial and combine passes)",
+        "roofline": {"kernel": ("fused split-T partial kernel of gva_decode_step (gva_decode_step_partial)" if S.fused
+                                else "split-T partial pass of gva_decode_attention (gva_decode_partial)"
+                                if S.n_q == 1 else
+                                f"gva_decode_attention_multi, {S.n_q} queries per sequence (partial and combine "
+                                "passes)"),
                      "bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
                      "frac": round(achieved / hbm_peak, 4), "peak_kind": f"{pk_kind} copy bandwidth (burst)",
-                     "algorithmic_bytes_per_launch": S.decode_bytes, "partial_us": round(part_us, 3),
+                     "algorithmic_bytes_per_launch": part_bytes, "partial_us": round(part_us, 3),
                      "decode_call_us": round(dec_us, 3),
                      "decode_call_GBps": round(S.decode_bytes / (dec_s / K) / 1e9, 1),
-                     "traffic": TRAFFIC.get(w.name)},
-        "gpu_launches": 4 * K,
+                     "traffic": TRAFFIC.get((w.name, "fused" if S.fused else "plain"))},
+        "gpu_launches": S.launches_per_step * K,
         "clocks": clocks.summary(),
     }
     if rank == 0 and ws == 1:
@@ -423,13 +473,20 @@ def run_ours(args, rank, ws):
 
 
 def time_partial(S, K, flush):
-    """Average device seconds of one split-T partial pass (events on the launching stream)."""
-    L, i = S.layer, S.inp
+    """Average device seconds of the step's split-T partial pass (events on the launching stream):
+    the fused kernel (gva_decode_step_partial) when the step is fused, else gva_decode_partial."""
+    L, i, r, w = S.layer, S.inp, S.raw, S.w
 
     def partial():
-        gva.gva_decode_partial(L.ctx, L.q_abs, L.q_rot if S.w.d_r else None, i.v_pool,
-                               i.kr_pool if S.w.d_r else None, i.block_table, i.seq_lens, S.w.max_seq_len,
-                               L.workspace)
+        if S.fused:
+            gva.gva_decode_step_partial(L.ctx, r.q_c, r.q_r if w.d_r else None, r.M, r.v_new.reshape(w.B, w.G, w.d_v),
+                                        r.kr_new.reshape(w.B, w.d_r) if w.d_r else None, i.v_pool,
+                                        i.kr_pool if w.d_r else None, i.block_table, i.seq_lens, w.max_seq_len,
+                                        L.workspace)
+        else:
+            gva.gva_decode_partial(L.ctx, L.q_abs, L.q_rot if w.d_r else None, i.v_pool,
+                                   i.kr_pool if w.d_r else None, i.block_table, i.seq_lens, w.max_seq_len,
+                                   L.workspace)
 
     def combine():
         gva.gva_decode_combine(L.ctx, S.w.B, S.w.max_seq_len, L.out, L.workspace)
@@ -451,12 +508,14 @@ def time_partial(S, K, flush):
 def run_e2e(S, steps, flush, graph=True):
     """Same step, with the step's inputs copied from pinned host memory and the output read back.
 
-    The step's inputs (queries, the new tokens and their positions) sit in one pinned host
-    buffer, 256-byte aligned, and move with one copy; the output comes back with one copy.  With
+    The step's inputs (queries and new tokens; for the multi-query step also their positions)
+    sit in one pinned host buffer, 256-byte aligned, and move with one copy; the output comes
+    back with one copy.  With
     graph=True the copy in, the step's kernels and the copy out are one captured CUDA graph,
     replayed once per step, as a serving loop would run them."""
     r = S.raw
-    names = ("q_c", "q_r", "pos_q", "v_new", "kr_new", "pos_new")
+    # the one-call step takes no positions (the lengths imply them)
+    names = ("q_c", "q_r", "v_new", "kr_new") if S.one_call else ("q_c", "q_r", "pos_q", "v_new", "kr_new", "pos_new")
     offs, total = {}, 0
     for k in names:
         t = getattr(r, k)
@@ -478,8 +537,12 @@ def run_e2e(S, steps, flush, graph=True):
 
     def e2e_step():
         dev_buf.copy_(host_buf, non_blocking=True)
-        S.layer.step(dev_in["q_c"], dev_in["q_r"], dev_in["pos_q"], r.M, dev_in["v_new"], dev_in["kr_new"],
-                     dev_in["pos_new"], S.inp.block_table, S.inp.seq_lens, S.inp.v_pool, S.inp.kr_pool)
+        if S.one_call:
+            S.layer.fused_step(dev_in["q_c"], dev_in["q_r"], r.M, dev_in["v_new"], dev_in["kr_new"],
+                               S.inp.block_table, S.inp.seq_lens, S.inp.v_pool, S.inp.kr_pool)
+        else:
+            S.layer.step(dev_in["q_c"], dev_in["q_r"], dev_in["pos_q"], r.M, dev_in["v_new"], dev_in["kr_new"],
+                         dev_in["pos_new"], S.inp.block_table, S.inp.seq_lens, S.inp.v_pool, S.inp.kr_pool)
         host_out.copy_(S.layer.out, non_blocking=True)
     run = capture(e2e_step).replay if graph else e2e_step
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]

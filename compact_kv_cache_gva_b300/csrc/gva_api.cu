@@ -365,6 +365,52 @@ size_t gva_decode_workspace_size_multi(const gva_ctx* ctx, int B, int n_q, int m
   return plan.ws_bytes;
 }
 
+}  // extern "C"
+
+namespace {
+// Form gva_decode_step takes for this batch shape: 1 fused, 0 separate kernels, -1 the
+// context's mode asks for the fused form where it does not apply.
+int step_form(const gva_ctx* ctx, int B, const gva::Plan& plan) {
+  switch (ctx->step_mode) {
+    case GVA_STEP_FUSED: return step_fusable(ctx, plan) ? 1 : -1;
+    case GVA_STEP_SEPARATE: return 0;
+    default:
+      // The prologue forms the queries of every segment a CTA's range meets; past a few
+      // segments per range the separate absorb kernel does that work faster.
+      return step_fusable(ctx, plan) && static_cast<long long>(B) * ctx->dims.G <=
+                                            kStepAutoSegmentsPerRange * static_cast<long long>(plan.n_groups)
+                 ? 1
+                 : 0;
+  }
+}
+}  // namespace
+
+extern "C" {
+
+int gva_step_is_fused(const gva_ctx* ctx, int B, int max_seq_len) {
+  if (!ctx || B <= 0 || max_seq_len < 1) return -1;
+  gva::Plan plan;
+  if (!make_plan(ctx, B, max_seq_len, false, &plan)) return -1;
+  return step_form(ctx, B, plan);
+}
+
+gva_status gva_decode_step_partial(gva_ctx* ctx, int B, const float* q_c, const float* q_r, const float* M,
+                                   const void* v_new, const void* kr_new, void* v_pool, void* kr_pool,
+                                   const int32_t* block_table, int max_blocks, int num_blocks,
+                                   const int32_t* seq_lens, int max_seq_len, void* workspace, size_t ws_bytes,
+                                   gva_stream_t stream) {
+  if (!ctx || B < 0 || max_seq_len < 1) return GVA_ERR_INVALID_ARG;
+  if (B == 0) return GVA_OK;
+  if (!q_c || !M || !v_new || (ctx->dims.d_r > 0 && (!q_r || !kr_new))) return GVA_ERR_INVALID_ARG;
+  if (!aligned16(q_c) || !aligned16(M) || !aligned16(v_new) || (q_r && !aligned16(q_r)) ||
+      (kr_new && (reinterpret_cast<uintptr_t>(kr_new) & 3u)))
+    return GVA_ERR_INVALID_ARG;
+  const StepInputs in{q_c, q_r, M, v_new, kr_new, v_pool, kr_pool};
+  return decode_common(ctx, false, kPhasePartial, B, nullptr, nullptr, nullptr, v_pool, kr_pool, block_table,
+                       max_blocks, num_blocks, seq_lens, max_seq_len, nullptr, workspace, ws_bytes,
+                       reinterpret_cast<cudaStream_t>(stream), 1, &in);
+}
+
 size_t gva_decode_step_workspace_size(const gva_ctx* ctx, int B, int max_seq_len) {
   if (!ctx || B <= 0 || max_seq_len < 1) return 0;
   gva::Plan plan;
@@ -395,20 +441,9 @@ gva_status gva_decode_step(gva_ctx* ctx, int B, const float* q_c, const float* q
   gva::Plan plan;
   if (!make_plan(ctx, B, max_seq_len, false, &plan)) return GVA_ERR_UNSUPPORTED;
   const cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
-  bool fuse = false;
-  switch (ctx->step_mode) {
-    case GVA_STEP_FUSED:
-      if (!step_fusable(ctx, plan)) return GVA_ERR_UNSUPPORTED;
-      fuse = true;
-      break;
-    case GVA_STEP_SEPARATE: fuse = false; break;
-    default:
-      // The prologue forms the queries of every segment a CTA's range meets; past a few
-      // segments per range the separate absorb kernel does that work faster.
-      fuse = step_fusable(ctx, plan) &&
-             static_cast<long long>(B) * d.G <= kStepAutoSegmentsPerRange * static_cast<long long>(plan.n_groups);
-  }
-  if (fuse) {
+  const int form = step_form(ctx, B, plan);
+  if (form < 0) return GVA_ERR_UNSUPPORTED;
+  if (form == 1) {
     const StepInputs in{q_c, q_r, M, v_new, kr_new, v_pool, kr_pool};
     return decode_common(ctx, false, kPhasePartial | kPhaseCombine, B, nullptr, nullptr, nullptr, v_pool,
                          kr_pool, block_table, max_blocks, num_blocks, seq_lens, max_seq_len, out,

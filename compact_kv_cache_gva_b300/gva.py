@@ -27,7 +27,7 @@ EXPORTS = ("gva_create", "gva_destroy", "gva_absorb_query", "gva_cache_append", 
            "gva_decode_plan", "gva_get_device_error", "gva_status_string", "gva_version",
            "gva_decode_attention_noalloc", "gva_decode_partial", "gva_decode_combine",
            "gva_decode_attention_multi", "gva_decode_workspace_size_multi", "gva_decode_step",
-           "gva_decode_step_workspace_size", "gva_set_step_mode")
+           "gva_decode_step_workspace_size", "gva_set_step_mode", "gva_step_is_fused", "gva_decode_step_partial")
 NOALLOC_SCRATCH_BYTES = 4 << 20
 
 
@@ -73,6 +73,8 @@ def load():
     L.gva_decode_step_workspace_size.argtypes = [vp, i, i]
     L.gva_decode_step_workspace_size.restype = C.c_size_t
     L.gva_set_step_mode.argtypes = [vp, i]
+    L.gva_step_is_fused.argtypes = [vp, i, i]
+    L.gva_decode_step_partial.argtypes = [vp, i, vp, vp, vp, vp, vp, vp, vp, ip, i, i, ip, i, vp, C.c_size_t, st]
     L.gva_set_split_tokens.argtypes = [vp, i]
     L.gva_set_decode_path.argtypes = [vp, i]
     L.gva_decode_plan.argtypes = [vp, i, i, C.POINTER(C.c_int), C.POINTER(C.c_int)]
@@ -80,9 +82,11 @@ def load():
     L.gva_status_string.argtypes = [i]
     L.gva_status_string.restype = C.c_char_p
     L.gva_version.argtypes = []
+    L.gva_step_is_fused.restype = C.c_int
     for name in EXPORTS:
         if name not in ("gva_destroy", "gva_decode_workspace_size", "gva_decode_workspace_size_multi",
-                        "gva_decode_step_workspace_size", "gva_status_string", "gva_version"):
+                        "gva_decode_step_workspace_size", "gva_status_string", "gva_version",
+                        "gva_step_is_fused"):
             getattr(L, name).restype = C.c_int
     _lib = L
     return L
@@ -366,6 +370,39 @@ def gva_decode_step(ctx, q_c, q_r, M, v_new, kr_new, v_pool, kr_pool, block_tabl
                                   _ptr(out, torch.float32, "out"), _ptr(workspace, None, "workspace"),
                                   workspace.numel() * workspace.element_size(), _stream(stream)),
            "gva_decode_step")
+
+
+def gva_step_is_fused(ctx, B, max_seq_len):
+    """1 if gva_decode_step runs the fused kernel for this batch shape, 0 if the separate kernels,
+    -1 if neither applies."""
+    return int(load().gva_step_is_fused(ctx.handle, int(B), int(max_seq_len)))
+
+
+def gva_decode_step_partial(ctx, q_c, q_r, M, v_new, kr_new, v_pool, kr_pool, block_table, seq_lens, max_seq_len,
+                            workspace, stream=None):
+    """The fused step's split-T pass alone; gva_decode_combine completes it."""
+    d = ctx.dims
+    B = q_c.shape[0]
+    dt = ctx.cache_torch_dtype
+    has_r = d.d_r > 0
+    _shape(q_c, (B, d.H, d.d_n), "q_c")
+    _shape(M, (d.H, d.d_v, d.d_n), "M")
+    _shape(v_new, (B, d.G, d.d_v), "v_new")
+    if has_r:
+        _shape(q_r, (B, d.H, d.d_r), "q_r")
+        _shape(kr_new, (B, d.d_r), "kr_new")
+    _check_table(block_table, B, seq_lens)
+    _check_pools(ctx, v_pool, kr_pool if has_r else None)
+    _check(load().gva_decode_step_partial(ctx.handle, B, _ptr(q_c, torch.float32, "q_c"),
+                                          _ptr(q_r, torch.float32, "q_r", allow_none=not has_r),
+                                          _ptr(M, torch.float32, "M"), _ptr(v_new, dt, "v_new"),
+                                          _ptr(kr_new, dt, "kr_new", allow_none=not has_r),
+                                          _ptr(v_pool, dt, "v_pool"), _ptr(kr_pool, dt, "kr_pool", allow_none=not has_r),
+                                          _ptr(block_table, torch.int32, "block_table"), block_table.shape[1],
+                                          v_pool.shape[0], _ptr(seq_lens, torch.int32, "seq_lens"), int(max_seq_len),
+                                          _ptr(workspace, None, "workspace"),
+                                          workspace.numel() * workspace.element_size(), _stream(stream)),
+           "gva_decode_step_partial")
 
 
 def gva_set_step_mode(ctx, mode):

@@ -238,6 +238,23 @@ gva_status gva_decode_step(gva_ctx* ctx, int B, const float* q_c, const float* q
 size_t gva_decode_step_workspace_size(const gva_ctx* ctx, int B, int max_seq_len);
 gva_status gva_set_step_mode(gva_ctx* ctx, gva_step_mode mode);
 
+/* Which form gva_decode_step takes for this batch shape under the context's mode: 1 the fused
+ * kernel, 0 the separate kernels, -1 none (bad arguments, or fused mode where it does not
+ * apply). */
+int gva_step_is_fused(const gva_ctx* ctx, int B, int max_seq_len);
+
+/* The fused step's first pass alone (the split-T partial kernel with the absorption in its
+ * prologue and the append), for callers that schedule or time the passes apart:
+ * gva_decode_step in its fused form is exactly gva_decode_step_partial followed by
+ * gva_decode_combine (same context, B, max_seq_len and workspace, same stream).  Arguments as
+ * gva_decode_step without `out`; GVA_ERR_UNSUPPORTED where the fused form does not apply,
+ * whatever the step mode. */
+gva_status gva_decode_step_partial(gva_ctx* ctx, int B, const float* q_c, const float* q_r, const float* M,
+                                   const void* v_new, const void* kr_new, void* v_pool, void* kr_pool,
+                                   const int32_t* block_table, int max_blocks, int num_blocks,
+                                   const int32_t* seq_lens, int max_seq_len, void* workspace, size_t ws_bytes,
+                                   gva_stream_t stream);
+
 /* gqa_decode_attention -- the matching grouped-query attention decode, built with the same
  * tiling and pools so that the cost of a key cache can be timed beside GVA (GQA explainer,
  * section "一次 GQA 计算如何展开": grouped keys and values, head h reads group g(h)).

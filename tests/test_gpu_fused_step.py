@@ -204,3 +204,40 @@ def test_long_context_fused_step():
                                       h=h, d_n=w.d_n))
         have.append(o2[b, h].cpu().numpy())
     assert_bf16_parity(np.array(have), np.array(want), "long-context fused step")
+
+
+def test_step_partial_then_combine_equals_one_call():
+    """gva_decode_step (fused) is gva_decode_step_partial followed by gva_decode_combine."""
+    w = synth.custom(name="passes", dtype="bf16", B=5, H=16, G=4, d_v=64, d_r=16, T_range=(1, 2500), shuffled=True)
+    inp = synth.decode_inputs(w, seed=360, device="cuda")
+    raw = synth.raw_inputs(w, inp.seq_lens.cpu(), n_new=1, seed=361, device="cuda")
+    layer = make_layer(w, step_mode=gva.GVA_STEP_FUSED)
+    v1, k1 = inp.v_pool.clone(), inp.kr_pool.clone()
+    want = layer.fused_step(raw.q_c, raw.q_r, raw.M, raw.v_new, raw.kr_new, inp.block_table, inp.seq_lens,
+                            v1, k1).clone()
+    v2, k2 = inp.v_pool.clone(), inp.kr_pool.clone()
+    layer.out.fill_(float("nan"))
+    gva.gva_decode_step_partial(layer.ctx, raw.q_c, raw.q_r, raw.M, raw.v_new.reshape(w.B, w.G, w.d_v),
+                                raw.kr_new.reshape(w.B, w.d_r), v2, k2, inp.block_table, inp.seq_lens, w.max_seq_len,
+                                layer.workspace)
+    gva.gva_decode_combine(layer.ctx, w.B, w.max_seq_len, layer.out, layer.workspace)
+    torch.cuda.synchronize()
+    assert layer.device_error() == 0
+    assert torch.equal(layer.out, want) and torch.equal(v1, v2) and torch.equal(k1, k2)
+
+
+def test_step_form_query():
+    """gva_step_is_fused reports the form gva_decode_step takes."""
+    few = synth.custom(name="few", dtype="bf16", B=8, H=16, G=4, d_v=64, d_r=16, T=4096)
+    many = synth.custom(name="many", dtype="bf16", B=2048, H=16, G=4, d_v=64, d_r=16, T=256)
+    lf, lm = make_layer(few), make_layer(many)
+    assert gva.gva_step_is_fused(lf.ctx, few.B, few.max_seq_len) == 1
+    assert gva.gva_step_is_fused(lm.ctx, many.B, many.max_seq_len) == 0
+    gva.gva_set_step_mode(lm.ctx, gva.GVA_STEP_FUSED)
+    assert gva.gva_step_is_fused(lm.ctx, many.B, many.max_seq_len) == 1
+    gva.gva_set_step_mode(lf.ctx, gva.GVA_STEP_SEPARATE)
+    assert gva.gva_step_is_fused(lf.ctx, few.B, few.max_seq_len) == 0
+    f32 = make_layer(synth.WORKLOADS[1], step_mode=gva.GVA_STEP_FUSED)
+    assert gva.gva_step_is_fused(f32.ctx, 1, 256) == -1
+    gva.gva_set_step_mode(f32.ctx, gva.GVA_STEP_AUTO)
+    assert gva.gva_step_is_fused(f32.ctx, 1, 256) == 0
