@@ -51,6 +51,8 @@ def parse():
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--workload", type=int, default=4, choices=sorted(synth.WORKLOADS))
     p.add_argument("--path", default="auto", choices=["auto", "fma", "mma"])
+    p.add_argument("--step-mode", default="auto", choices=["auto", "fused", "separate"],
+                   help="form of the one-call step (gva_set_step_mode)")
     p.add_argument("--split-tokens", type=int, default=0)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-gqa", action="store_true")
@@ -240,7 +242,7 @@ SmiClockSampler.summary = ClockSampler.summary
 class Setup:
     """A resident workload: cache, block table, lengths, step inputs, layer buffers."""
 
-    def __init__(self, w, seed, path, split_tokens, device="cuda", n_q=1):
+    def __init__(self, w, seed, path, split_tokens, device="cuda", n_q=1, step_mode="auto"):
         self.w, self.n_q = w, n_q
         self.inp = synth.decode_inputs(w, seed=seed, device=device)
         self.lens_cpu = self.inp.seq_lens.cpu()
@@ -250,7 +252,9 @@ class Setup:
         self.layer = GVADecodeLayer(w.H, w.G, w.d_v, w.d_n, w.d_r, w.dtype, w.B, w.max_seq_len, device=device,
                                     split_tokens=split_tokens,
                                     path={"auto": gva.GVA_PATH_AUTO, "fma": gva.GVA_PATH_FMA,
-                                          "mma": gva.GVA_PATH_MMA}[path], n_q=n_q)
+                                          "mma": gva.GVA_PATH_MMA}[path], n_q=n_q,
+                                    step_mode={"auto": gva.GVA_STEP_AUTO, "fused": gva.GVA_STEP_FUSED,
+                                               "separate": gva.GVA_STEP_SEPARATE}[step_mode])
         self.sum_T = int(self.lens_cpu.sum())
         self.bytes_per_token = (w.G * w.d_v + w.d_r) * w.elem_bytes
         self.cache_bytes = self.sum_T * self.bytes_per_token
@@ -365,7 +369,7 @@ def workload(args):
 def run_ours(args, rank, ws):
     torch.cuda.init()
     w = workload(args)
-    S = Setup(w, seed=rank, path=args.path, split_tokens=args.split_tokens, n_q=args.nq)
+    S = Setup(w, seed=rank, path=args.path, split_tokens=args.split_tokens, n_q=args.nq, step_mode=args.step_mode)
     need_flush = S.cache_bytes < 2 * L2_BYTES
     flush = flusher() if need_flush else None
 
@@ -438,7 +442,7 @@ def run_ours(args, rank, ws):
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws, "steps": K,
         "warmup": max(3, args.warmup), "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
-        "config": dict(w.describe(), step=step_desc, decode_path=args.path, n_q=S.n_q,
+        "config": dict(w.describe(), step=step_desc, step_mode=args.step_mode, decode_path=args.path, n_q=S.n_q,
                        cuda_graph=bool(args.graph),
                        split_plan=dict(zip(("split_tokens", "partial_warps"), S.layer.plan())),
                        l2="flushed before every step (252 MB write, then 252 MB read)" if need_flush else
