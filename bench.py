@@ -548,21 +548,49 @@ def run_e2e(S, steps, flush, graph=True):
             S.layer.step(dev_in["q_c"], dev_in["q_r"], dev_in["pos_q"], r.M, dev_in["v_new"], dev_in["kr_new"],
                          dev_in["pos_new"], S.inp.block_table, S.inp.seq_lens, S.inp.v_pool, S.inp.kr_pool)
         host_out.copy_(S.layer.out, non_blocking=True)
-    run = capture(e2e_step).replay if graph else e2e_step
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
-    for k in range(steps + 3):
-        if flush:
-            flush()
-        e = ev[k - 3] if k >= 3 else None
-        if e:
-            e[0].record()
-        run()
-        if e:
-            e[1].record()
+    def timed(fn):
+        run = capture(fn).replay if graph else fn
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        for k in range(steps + 3):
+            if flush:
+                flush()
+            e = ev[k - 3] if k >= 3 else None
+            if e:
+                e[0].record()
+            run()
+            if e:
+                e[1].record()
+        torch.cuda.synchronize()
+        return sum(a.elapsed_time(b) for a, b in ev) / 1e3
+
+    t = timed(e2e_step)
+    copies = {"value": round(S.cache_bytes * steps / t / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+              "d2h_bytes_per_step": d2h, "ms_per_step": round(1e3 * t / steps, 5), "cuda_graph": bool(graph),
+              "transfer": "one copy of the packed inputs in, one copy of the output out, in the step's graph"}
+    if not S.one_call:
+        return copies
+    # The one-call step reads its inputs from, and writes its output to, pinned host memory
+    # directly (mapped under unified addressing): no copy before or after the kernels.
+    host_in = {k: view(host_buf, k) for k in names}
+
+    def zero_copy_step():
+        S.layer.fused_step(host_in["q_c"], host_in["q_r"], r.M, host_in["v_new"], host_in["kr_new"],
+                           S.inp.block_table, S.inp.seq_lens, S.inp.v_pool, S.inp.kr_pool, out=host_out)
+    zero_copy_step()
     torch.cuda.synchronize()
-    t = sum(a.elapsed_time(b) for a, b in ev) / 1e3
-    return {"value": round(S.cache_bytes * steps / t / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "ms_per_step": round(1e3 * t / steps, 5), "cuda_graph": bool(graph)}
+    host_out.fill_(float("nan"))
+    zero_copy_step()
+    torch.cuda.synchronize()
+    want = S.layer.fused_step(r.q_c, r.q_r, r.M, r.v_new, r.kr_new, S.inp.block_table, S.inp.seq_lens,
+                              S.inp.v_pool, S.inp.kr_pool).cpu()
+    if not torch.equal(host_out, want):
+        raise RuntimeError("the step through pinned host buffers differs from the step through device buffers")
+    t0 = timed(zero_copy_step)
+    zero = {"value": round(S.cache_bytes * steps / t0 / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": round(1e3 * t0 / steps, 5), "cuda_graph": bool(graph),
+            "transfer": "the kernels read the pinned host inputs and write the pinned host output across the "
+                        "bus (mapped memory, no copy)"}
+    return dict(zero, copies=copies)
 
 
 def run_gqa(S, flush, steps):

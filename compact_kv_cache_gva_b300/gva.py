@@ -112,15 +112,17 @@ def _stream(stream):
     return C.c_void_p(int(stream))
 
 
-def _ptr(t, dtype, name, allow_none=False):
+def _ptr(t, dtype, name, allow_none=False, allow_pinned=False):
+    """Pointer of a CUDA tensor (or, with allow_pinned, of a pinned host tensor, which the
+    kernels read or write directly through its mapped address)."""
     if t is None:
         if allow_none:
             return C.c_void_p(0)
         raise ValueError(f"{name} is required")
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
-    if not t.is_cuda:
-        raise ValueError(f"{name} must be a CUDA tensor")
+    if not (t.is_cuda or (allow_pinned and t.is_pinned())):
+        raise ValueError(f"{name} must be a CUDA tensor" + (" or pinned host memory" if allow_pinned else ""))
     if dtype is not None and t.dtype not in (dtype if isinstance(dtype, tuple) else (dtype,)):
         raise TypeError(f"{name} has dtype {t.dtype}, expected {dtype}")
     if not t.is_contiguous():
@@ -347,7 +349,8 @@ def gva_decode_step(ctx, q_c, q_r, M, v_new, kr_new, v_pool, kr_pool, block_tabl
     """One decode step: appends each sequence's new token (v_new [B,G,d_v], kr_new [B,d_r], cache
     dtype) at position seq_lens[b]-1, absorbs and rotates the query (q_c [B,H,d_n], q_r [B,H,d_r],
     M [H,d_v,d_n]) at that position, and attends over the context including the new token
-    into out [B,H,d_v].  seq_lens already count the new token."""
+    into out [B,H,d_v].  seq_lens already count the new token.  q_c, q_r, v_new, kr_new and out
+    may be pinned host tensors: the kernels then read and write them across the bus directly."""
     d = ctx.dims
     B = q_c.shape[0]
     dt = ctx.cache_torch_dtype
@@ -361,13 +364,16 @@ def gva_decode_step(ctx, q_c, q_r, M, v_new, kr_new, v_pool, kr_pool, block_tabl
         _shape(kr_new, (B, d.d_r), "kr_new")
     _check_table(block_table, B, seq_lens)
     _check_pools(ctx, v_pool, kr_pool if has_r else None)
-    _check(load().gva_decode_step(ctx.handle, B, _ptr(q_c, torch.float32, "q_c"),
-                                  _ptr(q_r, torch.float32, "q_r", allow_none=not has_r), _ptr(M, torch.float32, "M"),
-                                  _ptr(v_new, dt, "v_new"), _ptr(kr_new, dt, "kr_new", allow_none=not has_r),
+    _check(load().gva_decode_step(ctx.handle, B, _ptr(q_c, torch.float32, "q_c", allow_pinned=True),
+                                  _ptr(q_r, torch.float32, "q_r", allow_none=not has_r, allow_pinned=True),
+                                  _ptr(M, torch.float32, "M"),
+                                  _ptr(v_new, dt, "v_new", allow_pinned=True),
+                                  _ptr(kr_new, dt, "kr_new", allow_none=not has_r, allow_pinned=True),
                                   _ptr(v_pool, dt, "v_pool"), _ptr(kr_pool, dt, "kr_pool", allow_none=not has_r),
                                   _ptr(block_table, torch.int32, "block_table"), block_table.shape[1],
                                   v_pool.shape[0], _ptr(seq_lens, torch.int32, "seq_lens"), int(max_seq_len),
-                                  _ptr(out, torch.float32, "out"), _ptr(workspace, None, "workspace"),
+                                  _ptr(out, torch.float32, "out", allow_pinned=True),
+                                  _ptr(workspace, None, "workspace"),
                                   workspace.numel() * workspace.element_size(), _stream(stream)),
            "gva_decode_step")
 

@@ -78,18 +78,21 @@ class GVADecodeLayer:
         main.wait_stream(self._side)
         return self.attend(v_pool, kr_pool, block_table, seq_lens, stream=main)
 
-    def fused_step(self, q_c, q_r, M, v_new, kr_new, block_table, seq_lens, v_pool, kr_pool, stream=None):
+    def fused_step(self, q_c, q_r, M, v_new, kr_new, block_table, seq_lens, v_pool, kr_pool, stream=None,
+                   out=None):
         """The whole step in one library call (gva_decode_step): the new token (v_new [B,1,G,d_v]
         or [B,G,d_v], kr_new [B,1,d_r] or [B,d_r]) goes to position seq_lens[b]-1, which the
-        lengths already count, and the query sits there."""
+        lengths already count, and the query sits there.  The step's inputs and `out` (default:
+        the layer's device buffer) may be pinned host tensors."""
         if self.n_q != 1:
             raise ValueError("fused_step decodes one query per sequence")
         d = self.ctx.dims
         has_r = d.d_r > 0
         gva.gva_decode_step(self.ctx, q_c, q_r if has_r else None, M, v_new.reshape(self.B, d.G, d.d_v),
                             kr_new.reshape(self.B, d.d_r) if has_r else None, v_pool, kr_pool if has_r else None,
-                            block_table, seq_lens, self.max_seq_len, self.out, self.workspace, stream)
-        return self.out
+                            block_table, seq_lens, self.max_seq_len, self.out if out is None else out, self.workspace,
+                            stream)
+        return self.out if out is None else out
 
     def device_error(self):
         return gva.gva_get_device_error(self.ctx)

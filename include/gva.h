@@ -223,6 +223,10 @@ typedef enum {
  *   v_new [B,G,d_v] and kr_new [B,d_r] cache dtype (kr_new unrotated; 4-byte aligned)
  *   v_pool, kr_pool, block_table, seq_lens, out: as gva_cache_append and gva_decode_attention
  *   workspace: at least gva_decode_step_workspace_size(ctx, B, max_seq_len) bytes.
+ * q_c, q_r, v_new, kr_new and out may also point to page-locked host memory that the device
+ * can address (cudaHostAlloc, or cudaHostRegister with the mapped flag; under unified virtual
+ * addressing the host pointer itself): the kernels then read the step's inputs and write its
+ * output across the bus directly, with no copy before or after the step.
  * The fused form (tensor-core path, d_n == d_v) is one partial kernel plus the combine: the
  * partial kernel forms the absorbed queries in its prologue (the "extra query-side compute"
  * of absorption, summary section 方法, done where the queries are used) and appends the new

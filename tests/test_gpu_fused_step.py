@@ -241,3 +241,24 @@ def test_step_form_query():
     assert gva.gva_step_is_fused(f32.ctx, 1, 256) == -1
     gva.gva_set_step_mode(f32.ctx, gva.GVA_STEP_AUTO)
     assert gva.gva_step_is_fused(f32.ctx, 1, 256) == 0
+
+
+@pytest.mark.parametrize("mode", [gva.GVA_STEP_FUSED, gva.GVA_STEP_SEPARATE])
+def test_step_with_pinned_host_inputs_and_output(mode):
+    """The step's inputs read from, and its output written to, pinned host memory give the bits of
+    the step through device buffers."""
+    w = synth.custom(name="pinned", dtype="bf16", B=5, H=16, G=4, d_v=64, d_r=16, T_range=(1, 1500), shuffled=True)
+    inp = synth.decode_inputs(w, seed=370, device="cuda")
+    raw = synth.raw_inputs(w, inp.seq_lens.cpu(), n_new=1, seed=371, device="cuda")
+    layer = make_layer(w, step_mode=mode)
+    v1, k1 = inp.v_pool.clone(), inp.kr_pool.clone()
+    want = layer.fused_step(raw.q_c, raw.q_r, raw.M, raw.v_new, raw.kr_new, inp.block_table, inp.seq_lens,
+                            v1, k1).clone()
+    host = {k: getattr(raw, k).cpu().pin_memory() for k in ("q_c", "q_r", "v_new", "kr_new")}
+    out = torch.full((w.B, w.H, w.d_v), float("nan")).pin_memory()
+    v2, k2 = inp.v_pool.clone(), inp.kr_pool.clone()
+    layer.fused_step(host["q_c"], host["q_r"], raw.M, host["v_new"], host["kr_new"], inp.block_table, inp.seq_lens,
+                     v2, k2, out=out)
+    torch.cuda.synchronize()
+    assert layer.device_error() == 0
+    assert torch.equal(out, want.cpu()) and torch.equal(v1, v2) and torch.equal(k1, k2)
