@@ -77,6 +77,16 @@ def test_null_context_and_sizes_rejected(lib):
                                     None) == gva.GVA_ERR_INVALID_ARG
     assert lib.gva_decode_workspace_size(None, 1, 1) == 0
     assert lib.gva_set_split_tokens(None, 64) == gva.GVA_ERR_INVALID_ARG
+    # the one-call step and its helpers
+    assert lib.gva_decode_step(None, 1, None, None, None, None, None, None, None, None, 1, 1, None, 1, None, None,
+                               0, None) == gva.GVA_ERR_INVALID_ARG
+    assert lib.gva_decode_step_partial(None, 1, None, None, None, None, None, None, None, None, 1, 1, None, 1, None,
+                                       0, None) == gva.GVA_ERR_INVALID_ARG
+    assert lib.gva_decode_step_workspace_size(None, 1, 1) == 0
+    assert lib.gva_step_is_fused(None, 1, 1) == -1
+    assert lib.gva_set_step_mode(None, gva.GVA_STEP_FUSED) == gva.GVA_ERR_INVALID_ARG
+    assert lib.gva_decode_attention_multi(None, 1, 2, None, None, None, None, None, 1, 1, None, 2, None, None, 0,
+                                          None) == gva.GVA_ERR_INVALID_ARG
 
 
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU behaviour")
@@ -84,6 +94,14 @@ def test_create_without_gpu_reports_cuda_error(lib):
     dims = gva.gva_dims(16, 4, 64, 64, 16, 64, gva.GVA_BF16, 1e4, 0.0)
     h = C.c_void_p()
     assert lib.gva_create(C.byref(dims), C.byref(h)) == gva.GVA_ERR_CUDA
+
+
+def test_binding_takes_pinned_host_tensors_only_where_the_step_allows():
+    t = torch.zeros(1, 4, 32)  # ordinary pageable host memory is never accepted
+    with pytest.raises(ValueError, match="pinned"):
+        gva._ptr(t, torch.float32, "q_c", allow_pinned=True)
+    with pytest.raises(ValueError, match="CUDA"):
+        gva._ptr(t, torch.float32, "M")
 
 
 def test_binding_refuses_host_tensors():
