@@ -58,7 +58,10 @@ def parse():
     p.add_argument("--no-gqa", action="store_true")
     p.add_argument("--e2e-steps", type=int, default=200)
     p.add_argument("--cpu-sample-seqs", type=int, default=0, help="sequences in the CPU sample (0 = auto)")
-    p.add_argument("--graph", type=int, default=1, help="replay the step as a captured CUDA graph (1) or launch it (0)")
+    p.add_argument("--graph", type=int, default=0,
+                   help="launch the step's kernels directly (0: each is a programmatic dependent launch of the "
+                        "kernel before it, so a step's partial kernel is scheduled while the previous combine "
+                        "finishes) or replay the step as a captured CUDA graph (1: graph launches do not overlap)")
     p.add_argument("--nq", type=int, default=1,
                    help="query tokens per sequence per step (the last n_q positions: append n_q tokens, "
                         "absorb B*n_q query rows, gva_decode_attention_multi)")
@@ -566,7 +569,8 @@ def run_e2e(S, steps, flush, graph=True):
     t = timed(e2e_step)
     copies = {"value": round(S.cache_bytes * steps / t / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
               "d2h_bytes_per_step": d2h, "ms_per_step": round(1e3 * t / steps, 5), "cuda_graph": bool(graph),
-              "transfer": "one copy of the packed inputs in, one copy of the output out, in the step's graph"}
+              "transfer": "one copy of the packed inputs in, one copy of the output out" +
+                          (", in the step's graph" if graph else ", on the step's stream")}
     if not S.one_call:
         return copies
     # The one-call step reads its inputs from, and writes its output to, pinned host memory
