@@ -262,3 +262,99 @@ def test_step_with_pinned_host_inputs_and_output(mode):
     torch.cuda.synchronize()
     assert layer.device_error() == 0
     assert torch.equal(out, want.cpu()) and torch.equal(v1, v2) and torch.equal(k1, k2)
+
+
+def test_fused_step_bad_lengths_are_flagged_and_zeroed():
+    """A length of 0 or past max_seq_len sets GVA_DEVERR_SEQ_LEN and zeroes that row; the other
+    rows are unaffected, and the context stays usable."""
+    w = synth.custom(name="badlen", dtype="bf16", B=4, H=16, G=4, d_v=64, d_r=16, T_range=(64, 300), shuffled=True)
+    inp = synth.decode_inputs(w, seed=380, device="cuda")
+    raw = synth.raw_inputs(w, inp.seq_lens.cpu(), n_new=1, seed=381, device="cuda")
+    want, _, _ = oracle_step(w, inp, raw)
+    lens = inp.seq_lens.clone()
+    lens[1] = 0
+    lens[2] = w.max_seq_len + 1
+    layer = make_layer(w, step_mode=gva.GVA_STEP_FUSED)
+    out = layer.fused_step(raw.q_c, raw.q_r, raw.M, raw.v_new, raw.kr_new, inp.block_table, lens,
+                           inp.v_pool.clone(), inp.kr_pool.clone()).cpu().numpy()
+    assert layer.device_error() & gva.GVA_DEVERR_SEQ_LEN
+    assert np.all(out[1] == 0) and np.all(out[2] == 0)
+    assert_bf16_parity(out[[0, 3]], want[[0, 3]], "rows beside bad lengths")
+    layer.fused_step(raw.q_c, raw.q_r, raw.M, raw.v_new, raw.kr_new, inp.block_table, inp.seq_lens,
+                     inp.v_pool.clone(), inp.kr_pool.clone())
+    assert layer.device_error() == 0
+
+
+def test_fused_step_bad_block_id_is_flagged():
+    """A table entry outside the pool in a sequence's last block sets GVA_DEVERR_BLOCK_ID; that
+    tile (and its append) is skipped, the other sequences are unaffected."""
+    w = synth.custom(name="badblk", dtype="bf16", B=3, H=16, G=4, d_v=64, d_r=16, T_range=(100, 400), shuffled=True)
+    inp = synth.decode_inputs(w, seed=385, device="cuda")
+    raw = synth.raw_inputs(w, inp.seq_lens.cpu(), n_new=1, seed=386, device="cuda")
+    want, _, _ = oracle_step(w, inp, raw)
+    table = inp.block_table.clone()
+    last = (int(inp.seq_lens[1]) - 1) // 64
+    table[1, last] = inp.num_blocks + 5
+    layer = make_layer(w, step_mode=gva.GVA_STEP_FUSED)
+    out = layer.fused_step(raw.q_c, raw.q_r, raw.M, raw.v_new, raw.kr_new, table, inp.seq_lens,
+                           inp.v_pool.clone(), inp.kr_pool.clone()).cpu().numpy()
+    assert layer.device_error() & gva.GVA_DEVERR_BLOCK_ID
+    assert_bf16_parity(out[[0, 2]], want[[0, 2]], "rows beside a bad block id")
+
+
+def test_fused_step_with_stale_nan_workspace():
+    """Every stage the kernel reads is written in the same call: a workspace of NaN bytes gives the
+    three calls' bits."""
+    w = synth.custom(name="nanws", dtype="bf16", B=6, H=32, G=8, d_v=128, d_r=24, T_range=(1, 900), shuffled=True)
+    inp = synth.decode_inputs(w, seed=390, device="cuda")
+    raw = synth.raw_inputs(w, inp.seq_lens.cpu(), n_new=1, seed=391, device="cuda")
+    sep = make_layer(w)
+    v1, k1 = inp.v_pool.clone(), inp.kr_pool.clone()
+    want = sep.step(raw.q_c, raw.q_r, raw.pos_q, raw.M, raw.v_new, raw.kr_new, raw.pos_new, inp.block_table,
+                    inp.seq_lens, v1, k1, overlap=False).clone()
+    layer = make_layer(w, step_mode=gva.GVA_STEP_FUSED)
+    layer.workspace.fill_(0xFF)
+    v2, k2 = inp.v_pool.clone(), inp.kr_pool.clone()
+    out = layer.fused_step(raw.q_c, raw.q_r, raw.M, raw.v_new, raw.kr_new, inp.block_table, inp.seq_lens, v2, k2)
+    torch.cuda.synchronize()
+    assert layer.device_error() == 0
+    assert torch.equal(out, want) and torch.equal(v1, v2) and torch.equal(k1, k2)
+
+
+def test_fused_step_largest_batch():
+    """B = 8192: the lengths and the stages no longer fit beside the ring, so the prologue reads
+    the lengths and keeps the stages in the workspace.  Bit for bit against the three calls,
+    and against the oracle."""
+    w = synth.custom(name="maxb", dtype="bf16", B=8192, H=16, G=4, d_v=64, d_r=16, T_range=(1, 200), shuffled=True)
+    inp, raw, (o1, v1, k1), (o2, v2, k2) = run_both(w, seed=395)
+    assert torch.equal(o1, o2) and torch.equal(v1, v2) and torch.equal(k1, k2)
+    want, _, _ = oracle_step(w, inp, raw)
+    assert_bf16_parity(o2.cpu().numpy(), want, "B=8192")
+
+
+def test_fused_steps_on_two_streams():
+    """Two contexts' fused steps issued on two streams at once give their results one by one."""
+    wa = synth.custom(name="sa", dtype="bf16", B=6, H=16, G=4, d_v=64, d_r=16, T_range=(1, 3000), shuffled=True)
+    wb = synth.custom(name="sb", dtype="bf16", B=4, H=32, G=8, d_v=128, d_r=24, T_range=(1, 2000), shuffled=True)
+    runs = []
+    for w, seed in ((wa, 400), (wb, 402)):
+        inp = synth.decode_inputs(w, seed=seed, device="cuda")
+        raw = synth.raw_inputs(w, inp.seq_lens.cpu(), n_new=1, seed=seed + 1, device="cuda")
+        layer = make_layer(w, step_mode=gva.GVA_STEP_FUSED)
+        runs.append((layer, inp, raw))
+
+    def run(layer, inp, raw, stream=None):
+        return layer.fused_step(raw.q_c, raw.q_r, raw.M, raw.v_new, raw.kr_new, inp.block_table, inp.seq_lens,
+                                inp.v_pool, inp.kr_pool, stream=stream)
+    want = [run(*r).clone() for r in runs]
+    torch.cuda.synchronize()
+    sa, sb = torch.cuda.Stream(), torch.cuda.Stream()
+    for _ in range(3):
+        for layer, _, _ in runs:
+            layer.out.fill_(float("nan"))
+        torch.cuda.synchronize()
+        run(*runs[0], stream=sa)
+        run(*runs[1], stream=sb)
+        torch.cuda.synchronize()
+        assert torch.equal(runs[0][0].out, want[0]) and torch.equal(runs[1][0].out, want[1])
+    assert all(layer.device_error() == 0 for layer, _, _ in runs)
