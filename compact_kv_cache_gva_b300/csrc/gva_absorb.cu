@@ -40,6 +40,10 @@ struct AbsorbArgs {
   const float2* rope;  // fp32 RoPE digit table
   unsigned* err;
   int B, H, d_v, d_n, d_r;
+  // Set when the kernel directly follows the library's own append of the same step (which
+  // waits for all earlier work before it lets this kernel start): the wait for it is moved to
+  // the kernel's end, so the two overlap, and what follows still sees both done.
+  int defer_wait;
 };
 
 __global__ void __launch_bounds__(kAbsorbThreads) absorb_kernel(const AbsorbArgs a) {
@@ -51,7 +55,7 @@ __global__ void __launch_bounds__(kAbsorbThreads) absorb_kernel(const AbsorbArgs
   const int b0 = blockIdx.y * kAbsorbSeqs;
   const int nb = min(kAbsorbSeqs, a.B - b0);
   const int t = threadIdx.x;
-  griddep_wait();
+  if (!a.defer_wait) griddep_wait();
   griddep_launch_dependents();
 
   // positional slice: thread t < nb * pairs owns pair (t % pairs) of sequence b0 + t / pairs
@@ -162,14 +166,16 @@ __global__ void __launch_bounds__(kAbsorbThreads) absorb_kernel(const AbsorbArgs
       }
     }
   }
+  if (a.defer_wait) griddep_wait();
 }
 
 }  // namespace
 
 cudaError_t launch_absorb(const gva_ctx* ctx, int B, const float* q_c, const float* q_r,
                           const int32_t* pos_q, const float* M, float* q_abs, float* q_rot,
-                          cudaStream_t stream, const int32_t* seq_lens) {
+                          cudaStream_t stream, const int32_t* seq_lens, bool after_own_append) {
   AbsorbArgs a;
+  a.defer_wait = after_own_append ? 1 : 0;
   a.q_c = q_c;
   a.q_r = q_r;
   a.pos_q = pos_q;

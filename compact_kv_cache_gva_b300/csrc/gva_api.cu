@@ -457,7 +457,7 @@ gva_status gva_decode_step(gva_ctx* ctx, int B, const float* q_c, const float* q
   float* q_rot = d.d_r > 0 ? q_abs + static_cast<size_t>(B) * d.H * d.d_v : nullptr;
   if (gva::launch_append(ctx, B, 1, v_new, kr_new, nullptr, block_table, max_blocks, num_blocks, v_pool,
                          kr_pool, stream, seq_lens) != cudaSuccess ||
-      gva::launch_absorb(ctx, B, q_c, q_r, nullptr, M, q_abs, q_rot, stream, seq_lens) != cudaSuccess)
+      gva::launch_absorb(ctx, B, q_c, q_r, nullptr, M, q_abs, q_rot, stream, seq_lens, true) != cudaSuccess)
     return GVA_ERR_CUDA;
   return decode_common(ctx, false, kPhasePartial | kPhaseCombine, B, q_abs, q_rot, nullptr, v_pool, kr_pool,
                        block_table, max_blocks, num_blocks, seq_lens, max_seq_len, out, workspace, off,
