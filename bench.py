@@ -470,8 +470,7 @@ def run_ours(args, rank, ws):
         "gpu_launches": S.launches_per_step * K,
         "clocks": clocks.summary(),
     }
-    if rank == 0 and ws == 1:
-        out["e2e"] = run_e2e(S, args.e2e_steps, flush, graph=bool(args.graph))
+    out["e2e"] = run_e2e(S, args.e2e_steps, flush, graph=bool(args.graph), ws=ws)
     if not args.no_gqa and rank == 0:
         out["gqa_same_build"] = run_gqa(S, flush, min(K, 500))
     if rank == 0 and ws == 1 and not args.no_cpu_baseline and S.n_q == 1:
@@ -512,7 +511,7 @@ def time_partial(S, K, flush):
     return sum(a.elapsed_time(b) for a, b in evs) / 1e3 / K
 
 
-def run_e2e(S, steps, flush, graph=True):
+def run_e2e(S, steps, flush, graph=True, ws=1):
     """Same step, with the step's inputs copied from pinned host memory and the output read back.
 
     The step's inputs (queries and new tokens; for the multi-query step also their positions)
@@ -552,7 +551,9 @@ def run_e2e(S, steps, flush, graph=True):
                          dev_in["pos_new"], S.inp.block_table, S.inp.seq_lens, S.inp.v_pool, S.inp.kr_pool)
         host_out.copy_(S.layer.out, non_blocking=True)
     def timed(fn):
+        """Device seconds of `steps` steps on this rank; the slowest rank's under torchrun."""
         run = capture(fn).replay if graph else fn
+        barrier(ws)
         ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
         for k in range(steps + 3):
             if flush:
@@ -564,11 +565,14 @@ def run_e2e(S, steps, flush, graph=True):
             if e:
                 e[1].record()
         torch.cuda.synchronize()
-        return sum(a.elapsed_time(b) for a, b in ev) / 1e3
+        return max_over_ranks(sum(a.elapsed_time(b) for a, b in ev) / 1e3, ws)
 
+    # every rank moves its own replica's inputs and output: whole-job bytes and GB/s
+    h2d, d2h = h2d * ws, d2h * ws
     t = timed(e2e_step)
-    copies = {"value": round(S.cache_bytes * steps / t / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
-              "d2h_bytes_per_step": d2h, "ms_per_step": round(1e3 * t / steps, 5), "cuda_graph": bool(graph),
+    copies = {"value": round(whole_job(S.cache_bytes * steps, ws, t) / 1e9, 2), "unit": "GB/s",
+              "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(1e3 * t / steps, 5),
+              "cuda_graph": bool(graph),
               "transfer": "one copy of the packed inputs in, one copy of the output out" +
                           (", in the step's graph" if graph else ", on the step's stream")}
     if not S.one_call:
@@ -590,7 +594,7 @@ def run_e2e(S, steps, flush, graph=True):
     if not torch.equal(host_out, want):
         raise RuntimeError("the step through pinned host buffers differs from the step through device buffers")
     t0 = timed(zero_copy_step)
-    zero = {"value": round(S.cache_bytes * steps / t0 / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+    zero = {"value": round(whole_job(S.cache_bytes * steps, ws, t0) / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": round(1e3 * t0 / steps, 5), "cuda_graph": bool(graph),
             "transfer": "the kernels read the pinned host inputs and write the pinned host output across the "
                         "bus (mapped memory, no copy)"}
