@@ -151,12 +151,12 @@ struct MmaLayout {
   static constexpr int kStageBytes = kOpBytes + kKrBytes;
 };
 
-// Shared memory: [alignment slack 1 KB][control 1 KB: full and empty mbarrier, valid length
-// and block id of every stage][P*D operand tiles, 1 KB aligned for the swizzled boxes][P*D
-// k_r tiles][cum: B+1 ints].  Stage (c, slot) is index c*D + slot.
+// Shared memory: [alignment slack 1 KB][control 2 KB: full and empty mbarrier, valid length,
+// block id and (fused step) landing mbarrier of every stage][P*D operand tiles, 1 KB aligned
+// for the swizzled boxes][P*D k_r tiles][cum: B+1 ints].  Stage (c, slot) is index c*D + slot.
 constexpr int kMaxStages = 40;
-constexpr int kCtrlBytes = 1024;
-static_assert(kMaxStages * (2 * 8 + 4 + 4) <= kCtrlBytes, "control block");
+constexpr int kCtrlBytes = 2048;
+static_assert(kMaxStages * (3 * 8 + 4 + 4) <= kCtrlBytes, "control block");
 constexpr int kStepBatch = 16;  // fused step: segments whose absorbed queries a warp forms at once
 constexpr int kStepBarrier = 1;  // fused step: named barrier that ends the prologue
 constexpr int kLookupBarrier = 2;  // fused step: the copy warps' first block-table reads are out
@@ -205,6 +205,12 @@ __global__ void __launch_bounds__(mma_max_threads(DV, NQ), 1) decode_mma_kernel(
   uint64_t* empty = full + kMaxStages;
   int* nvs = reinterpret_cast<int*>(empty + kMaxStages);  // tokens from each stage's tile to the end (0 = skip)
   int* blks = nvs + kMaxStages;                            // block id of each stage's tile (fused step)
+  // fused step: a sequence's last tile lands on landed[s] instead of full[s]; the patcher warp
+  // writes the new token into it and then completes full[s]
+  uint64_t* landed = reinterpret_cast<uint64_t*>(blks + kMaxStages);
+  // Fused instances with a spare warp (all but the six-pair one) give the append to it: the
+  // consumers' loop is then the plain kernel's.
+  constexpr bool kPatcher = FUSED && !(DV == 64 && DR == 32);
   unsigned char* tiles = smem + kCtrlBytes;
   unsigned char* krs = tiles + N * L::kOpBytes;
   int* cum = reinterpret_cast<int*>(krs + N * L::kKrBytes);
@@ -217,6 +223,7 @@ __global__ void __launch_bounds__(mma_max_threads(DV, NQ), 1) decode_mma_kernel(
     for (int s = 0; s < N; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
+      if (kPatcher) mbar_init(&landed[s], 1);
     }
     mbar_init_fence();
   }
@@ -372,7 +379,62 @@ __global__ void __launch_bounds__(mma_max_threads(DV, NQ), 1) decode_mma_kernel(
     const int E = static_cast<int>(blockDim.x / 32) - 2 * P;  // prologue-only warps
     if (warp >= 2 * P) {
       absorb_segments(P + (warp - 2 * P), P + E);
-      asm volatile("bar.arrive %0, %1;" ::"r"(kStepBarrier), "r"(32 * (P + E)) : "memory");
+      if (!kPatcher || warp != 2 * P) {
+        asm volatile("bar.arrive %0, %1;" ::"r"(kStepBarrier), "r"(32 * (P + E)) : "memory");
+        return;
+      }
+      // ---------------------------------------------------------------- patcher warp
+      // For every sequence whose last tile lies in this range (in unit order, which is each
+      // copy warp's issue order): wait for the tile to land, write the new token's value row
+      // and rotated positional key into it and into the cache, then hand it to its consumer.
+      named_barrier_sync(kStepBarrier, 32 * (P + E));  // the rotated keys are staged
+      const long long tot = cum[a.B];
+      unsigned long long parity = 0;  // bit s: phase parity of landed[s]
+      for (int j = 0; j < nseg; ++j) {
+        const long long f = f_lo + j;
+        const int g = static_cast<int>(f / a.B);
+        const int b = static_cast<int>(f - static_cast<long long>(g) * a.B);
+        if (cum[b + 1] == cum[b]) continue;  // no tile (or an out-of-range length)
+        const long long kl = static_cast<long long>(g) * tot + cum[b + 1] - 1 - u0;  // its last unit
+        if (kl < 0 || kl >= n) continue;  // in another range
+        // the copy warp skips a tile whose block it cannot resolve (and completes full[s] itself)
+        const int t_last = cum[b + 1] - cum[b] - 1;
+        if (t_last >= a.max_blocks) continue;
+        const int id = a.block_table[static_cast<long long>(b) * a.max_blocks + t_last];
+        if (id < 0 || id >= a.num_blocks) continue;
+        const int w = static_cast<int>(kl % P), d = static_cast<int>(kl / P);
+        const int s = w * D + d % D;
+        uint4 vnew = make_uint4(0, 0, 0, 0);
+        uint32_t knew = 0;
+        if (lane < DV / 8)
+          vnew = __ldg(reinterpret_cast<const uint4*>(a.v_new) + (static_cast<long long>(b) * a.G + g) * (DV / 8) + lane);
+        if (DR > 0 && lane < DR / 2) knew = reinterpret_cast<const uint32_t*>(stage + static_cast<long long>(j) * QS + R * (DV + DR))[lane];
+        const bool got = mbar_wait_bounded(&landed[s], static_cast<uint32_t>((parity >> s) & 1));
+        parity ^= 1ull << s;
+        if (!__all_sync(kFullMask, got)) {
+          if (lane == 0) flag_error(a.err, GVA_DEVERR_TIMEOUT);
+        } else {
+          const int nrem = nvs[s];
+          if (nrem > 0) {
+            const int o = nrem - 1;
+            const long long blk = blks[s];
+            const uint32_t vbase = smem_addr(tiles + s * L::kOpBytes);
+            const uint32_t krbase = smem_addr(krs + s * L::kKrBytes);
+            if (lane < DV / 8) {
+              st_shared_v4(vbase + (lane >> 3) * kSubTileBytes + o * 128 + (((lane & 7) ^ (o & 7)) << 4), vnew);
+              reinterpret_cast<uint4*>(a.v_pool_w)[((blk * a.G + g) * kBlockTokens + o) * (DV / 8) + lane] = vnew;
+            }
+            if (DR > 0 && lane < DR / 2) {
+              st_shared_u32(krbase + o * (2 * DR) + 4 * lane, knew);
+              if (g == 0)  // one positional key per token, shared by the groups
+                reinterpret_cast<uint32_t*>(a.kr_pool_w)[(blk * kBlockTokens + o) * (DR / 2) + lane] = knew;
+            }
+          }
+        }
+        fence_proxy_async_smem();  // these writes come before the copy engine refills the stage
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&full[s]);  // the consumer may read the tile
+      }
       return;
     }
   }
@@ -425,18 +487,20 @@ __global__ void __launch_bounds__(mma_max_threads(DV, NQ), 1) decode_mma_kernel(
             nvs[s] = bj >= 0 ? vj : 0;  // published by the arrive below (release)
             if (FUSED) blks[s] = bj;
             if (bj >= 0) {
-              mbar_arrive_expect_tx(&full[s], L::kTx);
+              // fused step: a sequence's last tile goes to the patcher before the consumer
+              uint64_t* bar = kPatcher && vj <= kBlockTokens ? &landed[s] : &full[s];
+              mbar_arrive_expect_tx(bar, L::kTx);
               unsigned char* st = tiles + s * L::kOpBytes;
               const int y = (bj * a.G + gj) * kBlockTokens;
 #pragma unroll
               for (int sub = 0; sub < L::kSub; ++sub) {
-                tma_load_2d(st + sub * kSubTileBytes, &tmv, 64 * sub, y, &full[s]);
-                if (SEPK) tma_load_2d(st + L::kVBytes + sub * kSubTileBytes, &tmk, 64 * sub, y, &full[s]);
+                tma_load_2d(st + sub * kSubTileBytes, &tmv, 64 * sub, y, bar);
+                if (SEPK) tma_load_2d(st + L::kVBytes + sub * kSubTileBytes, &tmk, 64 * sub, y, bar);
               }
               if (!SEPK && DR > 0)
                 bulk_g2s(krs + s * L::kKrBytes,
                          static_cast<const __nv_bfloat16*>(a.kr_pool) + static_cast<size_t>(bj) * kBlockTokens * DR,
-                         L::kKrBytes, &full[s]);
+                         L::kKrBytes, bar);
             } else {
               mbar_arrive(&full[s]);  // completes the phase with no data; the tile is skipped
             }
@@ -510,7 +574,7 @@ __global__ void __launch_bounds__(mma_max_threads(DV, NQ), 1) decode_mma_kernel(
         qt[nt] = pack_bf16(qv(k0), qv(k0 + 1));
       }
     }
-    if constexpr (FUSED) {  // the new token's row, in case this warp meets the segment's last tile
+    if constexpr (FUSED && !kPatcher) {  // the new token's row, in case this warp meets the segment's last tile
       if (lane < DV / 8)
         vnew = __ldg(reinterpret_cast<const uint4*>(a.v_new) + (static_cast<long long>(b) * a.G + g) * (DV / 8) + lane);
       if (DR > 0 && lane < DR / 2)
@@ -579,7 +643,7 @@ __global__ void __launch_bounds__(mma_max_threads(DV, NQ), 1) decode_mma_kernel(
       const uint32_t vbase = smem_addr(tiles + s * L::kOpBytes);
       const uint32_t kbase = SEPK ? vbase + L::kVBytes : vbase;  // tile that is scored
       const uint32_t krbase = smem_addr(krs + s * L::kKrBytes);
-      if constexpr (FUSED) {
+      if constexpr (FUSED && !kPatcher) {
         if (nrem <= kBlockTokens) {  // the sequence's last tile: the new token is row nrem - 1
           const int o = nrem - 1;
           const long long blk = blks[s];
@@ -751,7 +815,7 @@ __global__ void __launch_bounds__(mma_max_threads(DV, NQ), 1) decode_mma_kernel(
     }
     // the stage may be refilled (after this warp's own writes into it, if any, are ordered
     // before the copy engine's)
-    if (FUSED && patched) fence_proxy_async_smem();
+    if (FUSED && !kPatcher && patched) fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[s]);
     k += NC;
@@ -794,8 +858,9 @@ cudaError_t launch_mma_t(const DecodeArgs& a, const CUtensorMap& mv, const CUten
   const int smem = ring_fixed_bytes(a.B) + P * D * L::kStageBytes;
   if (smem > kSmemLimit) return cudaErrorInvalidValue;
   // the fused step fills the instance's thread budget with prologue warps, and the shared
-  // memory budget with query stages
+  // memory budget with query stages; its patcher warp is the first prologue warp
   const int threads = FUSED ? mma_max_threads(DV, NQ) : 64 * P;
+  if (FUSED && !(DV == 64 && DR == 32) && threads <= 64 * P) return cudaErrorInvalidValue;
   DecodeArgs args = a;
   args.spare_smem = FUSED ? kSmemLimit - smem : 0;
   const int dyn_smem = FUSED ? kSmemLimit : smem;
