@@ -99,6 +99,18 @@ __device__ __forceinline__ void mma_1688(float (&c)[4], uint32_t a0, uint32_t a1
       : "r"(a0), "r"(a1), "r"(b0));
 }
 
+// Asks L2 to fetch [p, p + bytes) (bytes <= kMaxWarmBytes), spread over every thread of the
+// grid: one 128-byte line per request.
+constexpr long long kMaxWarmBytes = 4ll << 20;
+__device__ __forceinline__ void warm_l2(const void* p, long long bytes) {
+  if (!p || bytes <= 0 || bytes > kMaxWarmBytes) return;
+  const char* base = static_cast<const char*>(p);
+  const long long lines = (bytes + 127) / 128;
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < lines;
+       i += static_cast<long long>(gridDim.x) * blockDim.x)
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(base + i * 128));
+}
+
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
                : "memory");
@@ -233,6 +245,11 @@ __global__ void __launch_bounds__(mma_max_threads(DV, NQ), 1) decode_mma_kernel(
   }
   // Everything below may read what earlier work in the stream wrote.
   griddep_wait();
+  // The block table (and, for the fused step, the key maps) into L2 while the lengths are
+  // scanned: the first copies wait on table reads, and the cache stream of the previous call
+  // has evicted them.  (Both are device memory; the step's own inputs may be host memory.)
+  warm_l2(a.block_table, static_cast<long long>(a.B) * a.max_blocks * 4);
+  if constexpr (FUSED) warm_l2(a.M, static_cast<long long>(a.H) * DV * DV * 4);
   build_prefix<kMmaMaxThreads>(a, cum, lens_s);  // ends with __syncthreads: the barriers are set up
   griddep_launch_dependents();
 
