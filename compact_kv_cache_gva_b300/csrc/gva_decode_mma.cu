@@ -27,11 +27,12 @@
 // positional query (the neighbouring step of the decode path) run in the kernel's prologue
 // instead of a kernel of their own.  The consumer warps, and the warps the launch has to spare
 // beside the pairs, compute them for every (group, sequence) segment of the CTA's range while
-// the copy warps fill the rings.  Each output is one fp32 dot product in k order, as in the
-// absorb kernel, so the results are bit-identical to it.  The new token of every sequence (the
-// last position of its context) is appended by the consumer that meets the sequence's last
-// tile: it writes the value row and the rotated positional key into the staged tile, before
-// any product reads it, and into the cache.
+// the copy warps fill the rings.  Each output is an fp32 dot product in the absorb kernel's
+// summation order, so the results are bit-identical to it.  The new token of every sequence
+// (the last position of its context) is appended between the copy engine and the consumer:
+// the sequence's last tile lands on a barrier of its own, a patcher warp writes the value row
+// and the rotated positional key into the staged tile and into the cache, and only then hands
+// the tile to its consumer.
 #include <cuda.h>
 
 #include <algorithm>
@@ -190,7 +191,9 @@ inline int ring_fixed_bytes(int B) { return 1024 + kCtrlBytes + cum_bytes(B); }
 // and the dependent block-table reads off the consumers' path.
 //
 // A FUSED launch adds E = (threads of the instance - 64*P)/32 prologue warps (warps 2P..2P+E-1)
-// that help form the queries and then exit.
+// that help form the queries; the first of them then stays as the patcher warp, the others
+// exit.  (The six-pair instance, d_v = 64 with d_r = 32, has none to spare: its consumers
+// append themselves.)
 template <int DV, int DR, int R, int NQ, bool CAUSAL, bool SEPK, bool FUSED>
 __global__ void __launch_bounds__(mma_max_threads(DV, NQ), 1) decode_mma_kernel(const DecodeArgs a,
                                                                        const __grid_constant__ CUtensorMap tmv,
@@ -210,7 +213,7 @@ __global__ void __launch_bounds__(mma_max_threads(DV, NQ), 1) decode_mma_kernel(
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  const int P = a.group_warps;  // warp pairs; blockDim.x == 64 * P
+  const int P = a.group_warps;  // warp pairs; blockDim.x == 64 * P, plus the prologue warps of a fused launch
   const int D = a.n_stages;     // ring slots per pair
   const int N = P * D;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem);
