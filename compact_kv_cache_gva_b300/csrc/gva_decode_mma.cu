@@ -50,7 +50,8 @@ constexpr int kMmaMaxThreads = 64 * kMmaMaxPairs;  // consumer warps + as many c
 
 // Threads a kernel instance is compiled for: six warp pairs on the single-query d_v = 64
 // path, four elsewhere (d_v = 128 and several queries per pass hold twice the accumulators,
-// so they keep more registers per thread).
+// so they keep more registers per thread; five pairs at 320 threads squeezed the two-query
+// d_v = 64 instance from 194 to 168 registers and made it 11 % slower).
 __host__ __device__ constexpr int mma_max_threads(int dv, int nq) { return dv == 64 && nq == 1 ? 384 : 256; }
 constexpr int kSubTileBytes = kBlockTokens * 128;  // one [64 tokens][64 columns] bf16 swizzled box
 
@@ -1014,8 +1015,11 @@ bool mma_shape(const gva_dims& d, bool sep_k, int B, int nqp, int* pairs, int* s
   const int stage = op + (sep_k ? 0 : kBlockTokens * d.d_r * 2);
   const int avail = kSmemLimit - ring_fixed_bytes(B);
   auto depth = [&](int p) { return std::min(avail / (p * stage), kMaxStages / p); };
-  const int P = std::min(stage <= 11 * 1024 ? 4 : stage <= 12 * 1024 ? 6 : 3,
-                         mma_max_threads(d.d_v, nqp) / 64);
+  // Several queries per pass double the consumers' work per tile: as many pairs as fit (four
+  // rather than three at d_v = 128: the ragged batch's two-query decode 690 us against 817 us).
+  const int P = nqp > 1 ? mma_max_threads(d.d_v, nqp) / 64
+                        : std::min(stage <= 11 * 1024 ? 4 : stage <= 12 * 1024 ? 6 : 3,
+                                   mma_max_threads(d.d_v, nqp) / 64);
   const int D = depth(P);
   if (D < 1) return false;
   *pairs = P;
