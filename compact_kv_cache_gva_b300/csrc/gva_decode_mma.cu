@@ -122,6 +122,23 @@ __device__ __forceinline__ void st_shared_u32(uint32_t addr, uint32_t v) {
   asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
 
+// Fused step: the new token (row o of block blk) into the staged tile of its group g -- its
+// value row at the 128-byte-swizzled place the tensor copy gives it, its rotated positional
+// key in the plain k_r tile -- and into the cache (the key from group 0 only: one per token).
+// Lanes below d_v/8 move the value row (16 bytes each), lanes below d_r/2 a key pair.
+template <int DV, int DR>
+__device__ __forceinline__ void write_new_token(uint32_t vbase, uint32_t krbase, int o, uint4 vnew, uint32_t knew,
+                                                long long blk, int g, int G, void* v_pool, void* kr_pool, int lane) {
+  if (lane < DV / 8) {
+    st_shared_v4(vbase + (lane >> 3) * kSubTileBytes + o * 128 + (((lane & 7) ^ (o & 7)) << 4), vnew);
+    reinterpret_cast<uint4*>(v_pool)[((blk * G + g) * kBlockTokens + o) * (DV / 8) + lane] = vnew;
+  }
+  if (DR > 0 && lane < DR / 2) {
+    st_shared_u32(krbase + o * (2 * DR) + 4 * lane, knew);
+    if (g == 0) reinterpret_cast<uint32_t*>(kr_pool)[(blk * kBlockTokens + o) * (DR / 2) + lane] = knew;
+  }
+}
+
 __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
   uint32_t y;
   asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
@@ -436,21 +453,9 @@ __global__ void __launch_bounds__(mma_max_threads(DV, NQ), 1) decode_mma_kernel(
           if (lane == 0) flag_error(a.err, GVA_DEVERR_TIMEOUT);
         } else {
           const int nrem = nvs[s];
-          if (nrem > 0) {
-            const int o = nrem - 1;
-            const long long blk = blks[s];
-            const uint32_t vbase = smem_addr(tiles + s * L::kOpBytes);
-            const uint32_t krbase = smem_addr(krs + s * L::kKrBytes);
-            if (lane < DV / 8) {
-              st_shared_v4(vbase + (lane >> 3) * kSubTileBytes + o * 128 + (((lane & 7) ^ (o & 7)) << 4), vnew);
-              reinterpret_cast<uint4*>(a.v_pool_w)[((blk * a.G + g) * kBlockTokens + o) * (DV / 8) + lane] = vnew;
-            }
-            if (DR > 0 && lane < DR / 2) {
-              st_shared_u32(krbase + o * (2 * DR) + 4 * lane, knew);
-              if (g == 0)  // one positional key per token, shared by the groups
-                reinterpret_cast<uint32_t*>(a.kr_pool_w)[(blk * kBlockTokens + o) * (DR / 2) + lane] = knew;
-            }
-          }
+          if (nrem > 0)
+            write_new_token<DV, DR>(smem_addr(tiles + s * L::kOpBytes), smem_addr(krs + s * L::kKrBytes), nrem - 1,
+                                    vnew, knew, blks[s], g, a.G, a.v_pool_w, a.kr_pool_w, lane);
         }
         fence_proxy_async_smem();  // these writes come before the copy engine refills the stage
         __syncwarp();
@@ -666,17 +671,8 @@ __global__ void __launch_bounds__(mma_max_threads(DV, NQ), 1) decode_mma_kernel(
       const uint32_t krbase = smem_addr(krs + s * L::kKrBytes);
       if constexpr (FUSED && !kPatcher) {
         if (nrem <= kBlockTokens) {  // the sequence's last tile: the new token is row nrem - 1
-          const int o = nrem - 1;
-          const long long blk = blks[s];
-          if (lane < DV / 8) {
-            st_shared_v4(vbase + (lane >> 3) * kSubTileBytes + o * 128 + (((lane & 7) ^ (o & 7)) << 4), vnew);
-            reinterpret_cast<uint4*>(a.v_pool_w)[((blk * a.G + cc.g) * kBlockTokens + o) * (DV / 8) + lane] = vnew;
-          }
-          if (DR > 0 && lane < DR / 2) {
-            st_shared_u32(krbase + o * (2 * DR) + 4 * lane, knew);
-            if (cc.g == 0)  // one positional key per token, shared by the groups
-              reinterpret_cast<uint32_t*>(a.kr_pool_w)[(blk * kBlockTokens + o) * (DR / 2) + lane] = knew;
-          }
+          write_new_token<DV, DR>(vbase, krbase, nrem - 1, vnew, knew, blks[s], cc.g, a.G, a.v_pool_w, a.kr_pool_w,
+                                  lane);
           patched = true;
           __syncwarp();
         }
