@@ -138,6 +138,22 @@ bool step_fusable(const gva_ctx* ctx, const gva::Plan& plan) {
   return plan.path == GVA_PATH_MMA && plan.nqp == 1 && ctx->dims.d_n == ctx->dims.d_v;
 }
 
+// Form gva_decode_step takes for this batch shape: 1 fused, 0 separate kernels, -1 the
+// context's mode asks for the fused form where it does not apply.
+int step_form(const gva_ctx* ctx, int B, const gva::Plan& plan) {
+  switch (ctx->step_mode) {
+    case GVA_STEP_FUSED: return step_fusable(ctx, plan) ? 1 : -1;
+    case GVA_STEP_SEPARATE: return 0;
+    default:
+      // The prologue forms the queries of every segment a CTA's range meets; past a few
+      // segments per range the separate absorb kernel does that work faster.
+      return step_fusable(ctx, plan) && static_cast<long long>(B) * ctx->dims.G <=
+                                            kStepAutoSegmentsPerRange * static_cast<long long>(plan.n_groups)
+                 ? 1
+                 : 0;
+  }
+}
+
 gva_status decode_common(gva_ctx* ctx, bool sep_k, int phases, int B, const float* q_abs,
                          const float* q_rot, const void* k_pool, const void* v_pool,
                          const void* kr_pool, const int32_t* block_table, int max_blocks,
@@ -364,28 +380,6 @@ size_t gva_decode_workspace_size_multi(const gva_ctx* ctx, int B, int n_q, int m
   if (!make_plan(ctx, B, max_seq_len, false, &plan, n_q)) return 0;
   return plan.ws_bytes;
 }
-
-}  // extern "C"
-
-namespace {
-// Form gva_decode_step takes for this batch shape: 1 fused, 0 separate kernels, -1 the
-// context's mode asks for the fused form where it does not apply.
-int step_form(const gva_ctx* ctx, int B, const gva::Plan& plan) {
-  switch (ctx->step_mode) {
-    case GVA_STEP_FUSED: return step_fusable(ctx, plan) ? 1 : -1;
-    case GVA_STEP_SEPARATE: return 0;
-    default:
-      // The prologue forms the queries of every segment a CTA's range meets; past a few
-      // segments per range the separate absorb kernel does that work faster.
-      return step_fusable(ctx, plan) && static_cast<long long>(B) * ctx->dims.G <=
-                                            kStepAutoSegmentsPerRange * static_cast<long long>(plan.n_groups)
-                 ? 1
-                 : 0;
-  }
-}
-}  // namespace
-
-extern "C" {
 
 int gva_step_is_fused(const gva_ctx* ctx, int B, int max_seq_len) {
   if (!ctx || B <= 0 || max_seq_len < 1) return -1;
