@@ -10,8 +10,12 @@ namespace {
 
 constexpr int kVersion = 200;  // 0.2.0
 // Automatic step mode: fuse while the batch has at most this many (group, sequence) segments
-// per unit range.
-constexpr long long kStepAutoSegmentsPerRange = 2;
+// per unit range and a CTA's key maps (R*d_v*d_n fp32) are at most kStepAutoMapBytes.
+// Measured on B300 (one-call step, fused against separate kernels): d_v = d_n = 64, R = 4
+// (64 KB of maps) wins up to 7 segments per range (68.3 us against 73.6 us) and ties at 14;
+// d_v = d_n = 128 (256 KB) loses already at 1.8 (104.8 us against 102.9 us).
+constexpr long long kStepAutoSegmentsPerRange = 8;
+constexpr long long kStepAutoMapBytes = 64 * 1024;
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -144,13 +148,17 @@ int step_form(const gva_ctx* ctx, int B, const gva::Plan& plan) {
   switch (ctx->step_mode) {
     case GVA_STEP_FUSED: return step_fusable(ctx, plan) ? 1 : -1;
     case GVA_STEP_SEPARATE: return 0;
-    default:
-      // The prologue forms the queries of every segment a CTA's range meets; past a few
-      // segments per range the separate absorb kernel does that work faster.
-      return step_fusable(ctx, plan) && static_cast<long long>(B) * ctx->dims.G <=
-                                            kStepAutoSegmentsPerRange * static_cast<long long>(plan.n_groups)
+    default: {
+      // The prologue streams the group's key maps and forms the queries of every segment a
+      // CTA's range meets: with large maps or many segments per range the separate absorb
+      // kernel does that work faster.
+      const gva_dims& d = ctx->dims;
+      const long long map_bytes = 4ll * (d.H / d.G) * d.d_v * d.d_n;
+      return step_fusable(ctx, plan) && map_bytes <= kStepAutoMapBytes &&
+                     static_cast<long long>(B) * d.G <= kStepAutoSegmentsPerRange * plan.n_groups
                  ? 1
                  : 0;
+    }
   }
 }
 
