@@ -182,14 +182,16 @@ def test_fused_step_replays_in_a_cuda_graph():
 
 
 @pytest.mark.slow
-def test_long_context_fused_step():
-    """The long-context workload (B=8, T=131072): one call against three, bit for bit, and rows
-    sampled for the oracle."""
-    w = synth.WORKLOADS[4]
+@pytest.mark.parametrize("wid", [2, 3, 4])
+def test_full_size_fused_step(wid):
+    """The full-size workloads the automatic step mode fuses (350M layer, d_r = 24, long
+    context), in the benchmark's launch configuration: one call against three, bit for bit, and
+    rows sampled for the oracle."""
+    w = synth.WORKLOADS[wid]
     inp, raw, (o1, v1, k1), (o2, v2, k2) = run_both(w, seed=0)
     assert torch.equal(o1, o2) and torch.equal(v1, v2) and torch.equal(k1, k2)
     del v1, k1
-    rows = [(0, 0), (3, 9), (7, 15)]
+    rows = [(0, 0), (w.B // 2, w.H // 2 + 1), (w.B - 1, w.H - 1)]
     lens = inp.seq_lens.cpu().numpy()
     qa, qr = oracle.absorb(raw.q_c.double().cpu().numpy(), raw.q_r.double().cpu().numpy(),
                            (lens - 1).astype(np.int32), raw.M.double().cpu().numpy())
@@ -203,7 +205,7 @@ def test_long_context_fused_step():
         want.append(oracle.decode_one(qa[b:b + 1], qr[b:b + 1], vp, kp, tb, np.array([T], np.int32), G=w.G, b=0,
                                       h=h, d_n=w.d_n))
         have.append(o2[b, h].cpu().numpy())
-    assert_bf16_parity(np.array(have), np.array(want), "long-context fused step")
+    assert_bf16_parity(np.array(have), np.array(want), f"{w.name} fused step")
 
 
 def test_step_partial_then_combine_equals_one_call():
