@@ -32,8 +32,9 @@ constexpr int kAbsorbVecs = 8;  // 16-byte vectors of M_h and q_c held per threa
 struct AbsorbArgs {
   const float* q_c;
   const float* q_r;
-  const int32_t* pos_q;     // null: position seq_lens[b] - 1
+  const int32_t* pos_q;     // null: row b*n + i of n rows per sequence sits at seq_lens[b] - n + i
   const int32_t* seq_lens;
+  int rows_per_seq;
   const float* M;
   float* q_abs;
   float* q_rot;
@@ -69,7 +70,9 @@ __global__ void __launch_bounds__(kAbsorbThreads) absorb_kernel(const AbsorbArgs
     const int bt = t / pairs;
     pi = t - bt * pairs;
     qrow = (static_cast<long long>(b0 + bt) * a.H + h) * a.d_r;
-    p = a.pos_q ? static_cast<long long>(a.pos_q[b0 + bt]) : static_cast<long long>(a.seq_lens[b0 + bt]) - 1;
+    const int row = b0 + bt;
+    p = a.pos_q ? static_cast<long long>(a.pos_q[row])
+                : static_cast<long long>(a.seq_lens[row / a.rows_per_seq]) - a.rows_per_seq + row % a.rows_per_seq;
     x = *reinterpret_cast<const float2*>(a.q_r + qrow + 2 * pi);
   }
 
@@ -173,8 +176,10 @@ __global__ void __launch_bounds__(kAbsorbThreads) absorb_kernel(const AbsorbArgs
 
 cudaError_t launch_absorb(const gva_ctx* ctx, int B, const float* q_c, const float* q_r,
                           const int32_t* pos_q, const float* M, float* q_abs, float* q_rot,
-                          cudaStream_t stream, const int32_t* seq_lens, bool after_own_append) {
+                          cudaStream_t stream, const int32_t* seq_lens, bool after_own_append,
+                          int rows_per_seq) {
   AbsorbArgs a;
+  a.rows_per_seq = rows_per_seq;
   a.defer_wait = after_own_append ? 1 : 0;
   a.q_c = q_c;
   a.q_r = q_r;

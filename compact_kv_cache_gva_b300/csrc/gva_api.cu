@@ -466,6 +466,54 @@ gva_status gva_decode_step(gva_ctx* ctx, int B, const float* q_c, const float* q
                        stream);
 }
 
+size_t gva_decode_step_workspace_size_multi(const gva_ctx* ctx, int B, int n_q, int max_seq_len) {
+  if (!ctx || B <= 0 || n_q < 1 || max_seq_len < 1) return 0;
+  if (n_q == 1) return gva_decode_step_workspace_size(ctx, B, max_seq_len);
+  gva::Plan plan;
+  if (!make_plan(ctx, B, max_seq_len, false, &plan, n_q)) return 0;
+  const gva_dims& d = ctx->dims;
+  return round_up(plan.ws_bytes, 256) + sizeof(float) * static_cast<size_t>(B) * n_q * d.H * (d.d_v + d.d_r) + 16;
+}
+
+gva_status gva_decode_step_multi(gva_ctx* ctx, int B, int n_q, const float* q_c, const float* q_r,
+                                 const float* M, const void* v_new, const void* kr_new, void* v_pool,
+                                 void* kr_pool, const int32_t* block_table, int max_blocks, int num_blocks,
+                                 const int32_t* seq_lens, int max_seq_len, float* out, void* workspace,
+                                 size_t ws_bytes, gva_stream_t stream_) {
+  if (!ctx || B < 0 || n_q < 1 || max_seq_len < 1 || n_q > max_seq_len) return GVA_ERR_INVALID_ARG;
+  if (n_q == 1)
+    return gva_decode_step(ctx, B, q_c, q_r, M, v_new, kr_new, v_pool, kr_pool, block_table, max_blocks,
+                           num_blocks, seq_lens, max_seq_len, out, workspace, ws_bytes, stream_);
+  if (B == 0) return GVA_OK;
+  const gva_dims& d = ctx->dims;
+  if (!q_c || !M || !v_new || !v_pool || !block_table || !seq_lens || !out) return GVA_ERR_INVALID_ARG;
+  if (d.d_r > 0 && (!q_r || !kr_new || !kr_pool)) return GVA_ERR_INVALID_ARG;
+  if (!aligned16(q_c) || !aligned16(M) || !aligned16(v_new) || (q_r && !aligned16(q_r)) ||
+      (kr_new && (reinterpret_cast<uintptr_t>(kr_new) & 3u)))
+    return GVA_ERR_INVALID_ARG;
+  if (B > gva::kMaxBatch || static_cast<long long>(B) * n_q > (1LL << 30)) return GVA_ERR_UNSUPPORTED;
+  if (!on_ctx_device(ctx)) return GVA_ERR_INVALID_ARG;
+  gva::Plan plan;
+  if (!make_plan(ctx, B, max_seq_len, false, &plan, n_q)) return GVA_ERR_UNSUPPORTED;
+  const cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  // append the n_q tokens at the last n_q positions, absorb the B*n_q query rows at the same
+  // positions (overlapping the append), decode
+  const size_t off = round_up(plan.ws_bytes, 256);
+  const size_t rows = static_cast<size_t>(B) * n_q;
+  const size_t qbytes = sizeof(float) * rows * d.H * (d.d_v + d.d_r);
+  if (!workspace || !aligned16(workspace) || ws_bytes < off + qbytes) return GVA_ERR_WORKSPACE;
+  float* q_abs = reinterpret_cast<float*>(static_cast<char*>(workspace) + off);
+  float* q_rot = d.d_r > 0 ? q_abs + rows * d.H * d.d_v : nullptr;
+  if (gva::launch_append(ctx, B, n_q, v_new, kr_new, nullptr, block_table, max_blocks, num_blocks, v_pool,
+                         kr_pool, stream, seq_lens) != cudaSuccess ||
+      gva::launch_absorb(ctx, static_cast<int>(rows), q_c, q_r, nullptr, M, q_abs, q_rot, stream, seq_lens, true,
+                         n_q) != cudaSuccess)
+    return GVA_ERR_CUDA;
+  return decode_common(ctx, false, kPhasePartial | kPhaseCombine, B, q_abs, q_rot, nullptr, v_pool, kr_pool,
+                       block_table, max_blocks, num_blocks, seq_lens, max_seq_len, out, workspace, off, stream,
+                       n_q);
+}
+
 gva_status gva_set_step_mode(gva_ctx* ctx, gva_step_mode mode) {
   if (!ctx || (mode != GVA_STEP_AUTO && mode != GVA_STEP_FUSED && mode != GVA_STEP_SEPARATE))
     return GVA_ERR_INVALID_ARG;

@@ -19,7 +19,7 @@ namespace {
 struct AppendArgs {
   const void* v_new;
   const void* kr_new;
-  const int32_t* pos;       // null: position seq_lens[b] - 1
+  const int32_t* pos;       // null: the n new tokens are the last n positions, seq_lens[b] - n + t
   const int32_t* seq_lens;
   const int32_t* block_table;
   void* v_pool;
@@ -71,7 +71,7 @@ __global__ void __launch_bounds__(kAppendThreads) append_kernel(const AppendArgs
     x1 = static_cast<R>(CacheElem<T>::to_float(x[2 * lane + 1]));
   }
   const long long p =
-      (a.pos ? static_cast<long long>(a.pos[b]) : static_cast<long long>(a.seq_lens[b]) - 1) + t;
+      (a.pos ? static_cast<long long>(a.pos[b]) : static_cast<long long>(a.seq_lens[b]) - a.n) + t;
 
   // Resolve the slot; an unresolvable one skips the token and is reported.
   if (p < 0 || (p >> 6) >= a.max_blocks || p >= (1LL << 32)) {

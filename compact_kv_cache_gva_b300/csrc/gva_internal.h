@@ -93,14 +93,15 @@ struct Plan {
 };
 
 // Launchers (return cudaSuccess or the launch error).
-// With pos_q (pos) null, sequence b's position is seq_lens[b] - 1 (the last token of the
-// context: one decode step).  after_own_append: the absorb is launched right after
-// launch_append of the same step, on the same stream, and overlaps it (its inputs are not the
-// append's outputs).
+// With pos_q (pos) null, the positions come from the lengths: the n new tokens of sequence b
+// are its last n positions, seq_lens[b] - n + t, and query row b*n + i (rows_per_seq = n)
+// sits at seq_lens[b] - n + i (one decode step, or a step of n tokens).  after_own_append:
+// the absorb is launched right after launch_append of the same step, on the same stream, and
+// overlaps it (its inputs are not the append's outputs).
 cudaError_t launch_absorb(const gva_ctx* ctx, int B, const float* q_c, const float* q_r,
                           const int32_t* pos_q, const float* M, float* q_abs, float* q_rot,
                           cudaStream_t stream, const int32_t* seq_lens = nullptr,
-                          bool after_own_append = false);
+                          bool after_own_append = false, int rows_per_seq = 1);
 cudaError_t launch_append(const gva_ctx* ctx, int B, int n, const void* v_new,
                           const void* kr_new, const int32_t* pos, const int32_t* block_table,
                           int max_blocks, int num_blocks, void* v_pool, void* kr_pool,

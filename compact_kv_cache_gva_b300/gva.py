@@ -27,7 +27,8 @@ EXPORTS = ("gva_create", "gva_destroy", "gva_absorb_query", "gva_cache_append", 
            "gva_decode_plan", "gva_get_device_error", "gva_status_string", "gva_version",
            "gva_decode_attention_noalloc", "gva_decode_partial", "gva_decode_combine",
            "gva_decode_attention_multi", "gva_decode_workspace_size_multi", "gva_decode_step",
-           "gva_decode_step_workspace_size", "gva_set_step_mode", "gva_step_is_fused", "gva_decode_step_partial")
+           "gva_decode_step_workspace_size", "gva_set_step_mode", "gva_step_is_fused", "gva_decode_step_partial",
+           "gva_decode_step_multi", "gva_decode_step_workspace_size_multi")
 NOALLOC_SCRATCH_BYTES = 4 << 20
 
 
@@ -74,6 +75,9 @@ def load():
     L.gva_decode_step_workspace_size.restype = C.c_size_t
     L.gva_set_step_mode.argtypes = [vp, i]
     L.gva_step_is_fused.argtypes = [vp, i, i]
+    L.gva_decode_step_multi.argtypes = [vp, i, i, vp, vp, vp, vp, vp, vp, vp, ip, i, i, ip, i, vp, vp, C.c_size_t, st]
+    L.gva_decode_step_workspace_size_multi.argtypes = [vp, i, i, i]
+    L.gva_decode_step_workspace_size_multi.restype = C.c_size_t
     L.gva_decode_step_partial.argtypes = [vp, i, vp, vp, vp, vp, vp, vp, vp, ip, i, i, ip, i, vp, C.c_size_t, st]
     L.gva_set_split_tokens.argtypes = [vp, i]
     L.gva_set_decode_path.argtypes = [vp, i]
@@ -85,8 +89,8 @@ def load():
     L.gva_step_is_fused.restype = C.c_int
     for name in EXPORTS:
         if name not in ("gva_destroy", "gva_decode_workspace_size", "gva_decode_workspace_size_multi",
-                        "gva_decode_step_workspace_size", "gva_status_string", "gva_version",
-                        "gva_step_is_fused"):
+                        "gva_decode_step_workspace_size", "gva_decode_step_workspace_size_multi",
+                        "gva_status_string", "gva_version", "gva_step_is_fused"):
             getattr(L, name).restype = C.c_int
     _lib = L
     return L
@@ -409,6 +413,42 @@ def gva_decode_step_partial(ctx, q_c, q_r, M, v_new, kr_new, v_pool, kr_pool, bl
                                           _ptr(workspace, None, "workspace"),
                                           workspace.numel() * workspace.element_size(), _stream(stream)),
            "gva_decode_step_partial")
+
+
+def gva_decode_step_workspace_size_multi(ctx, B, n_q, max_seq_len):
+    return int(load().gva_decode_step_workspace_size_multi(ctx.handle, int(B), int(n_q), int(max_seq_len)))
+
+
+def gva_decode_step_multi(ctx, q_c, q_r, M, v_new, kr_new, v_pool, kr_pool, block_table, seq_lens, max_seq_len, out,
+                          workspace, stream=None):
+    """A decode step of n_q tokens per sequence: q_c [B,n_q,H,d_n], q_r [B,n_q,H,d_r],
+    v_new [B,n_q,G,d_v], kr_new [B,n_q,d_r] (the last n_q positions, which seq_lens already
+    count), out [B,n_q,H,d_v].  The step's inputs and out may be pinned host tensors."""
+    d = ctx.dims
+    B, n_q = q_c.shape[0], q_c.shape[1]
+    dt = ctx.cache_torch_dtype
+    has_r = d.d_r > 0
+    _shape(q_c, (B, n_q, d.H, d.d_n), "q_c")
+    _shape(M, (d.H, d.d_v, d.d_n), "M")
+    _shape(v_new, (B, n_q, d.G, d.d_v), "v_new")
+    _shape(out, (B, n_q, d.H, d.d_v), "out")
+    if has_r:
+        _shape(q_r, (B, n_q, d.H, d.d_r), "q_r")
+        _shape(kr_new, (B, n_q, d.d_r), "kr_new")
+    _check_table(block_table, B, seq_lens)
+    _check_pools(ctx, v_pool, kr_pool if has_r else None)
+    _check(load().gva_decode_step_multi(ctx.handle, B, n_q, _ptr(q_c, torch.float32, "q_c", allow_pinned=True),
+                                        _ptr(q_r, torch.float32, "q_r", allow_none=not has_r, allow_pinned=True),
+                                        _ptr(M, torch.float32, "M"), _ptr(v_new, dt, "v_new", allow_pinned=True),
+                                        _ptr(kr_new, dt, "kr_new", allow_none=not has_r, allow_pinned=True),
+                                        _ptr(v_pool, dt, "v_pool"),
+                                        _ptr(kr_pool, dt, "kr_pool", allow_none=not has_r),
+                                        _ptr(block_table, torch.int32, "block_table"), block_table.shape[1],
+                                        v_pool.shape[0], _ptr(seq_lens, torch.int32, "seq_lens"), int(max_seq_len),
+                                        _ptr(out, torch.float32, "out", allow_pinned=True),
+                                        _ptr(workspace, None, "workspace"),
+                                        workspace.numel() * workspace.element_size(), _stream(stream)),
+           "gva_decode_step_multi")
 
 
 def gva_set_step_mode(ctx, mode):

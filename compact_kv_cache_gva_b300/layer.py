@@ -28,8 +28,7 @@ class GVADecodeLayer:
         self.out = torch.empty((B, H, d_v) if n_q == 1 else (B, n_q, H, d_v), dtype=torch.float32, device=device)
         ws = max(16, gva.gva_decode_workspace_size(self.ctx, B, max_seq_len) if n_q == 1 else
                  gva.gva_decode_workspace_size_multi(self.ctx, B, n_q, max_seq_len))
-        if n_q == 1:
-            ws = max(ws, gva.gva_decode_step_workspace_size(self.ctx, B, max_seq_len))
+        ws = max(ws, gva.gva_decode_step_workspace_size_multi(self.ctx, B, n_q, max_seq_len))
         self.workspace = torch.empty(ws, dtype=torch.uint8, device=device)
         self._side = None  # side stream of step(overlap=True), created on first use
 
@@ -80,14 +79,21 @@ class GVADecodeLayer:
 
     def fused_step(self, q_c, q_r, M, v_new, kr_new, block_table, seq_lens, v_pool, kr_pool, stream=None,
                    out=None):
-        """The whole step in one library call (gva_decode_step): the new token (v_new [B,1,G,d_v]
-        or [B,G,d_v], kr_new [B,1,d_r] or [B,d_r]) goes to position seq_lens[b]-1, which the
-        lengths already count, and the query sits there.  The step's inputs and `out` (default:
-        the layer's device buffer) may be pinned host tensors."""
-        if self.n_q != 1:
-            raise ValueError("fused_step decodes one query per sequence")
+        """The whole step in one library call (gva_decode_step, or gva_decode_step_multi with
+        n_q > 1): the new tokens (v_new [B,n_q,G,d_v], kr_new [B,n_q,d_r]; [B,G,d_v] and [B,d_r]
+        also accepted when n_q == 1) go to the last n_q positions, which the lengths already
+        count, and the query rows (q_c [B*n_q,H,d_n]) sit there.  The step's inputs and `out`
+        (default: the layer's device buffer) may be pinned host tensors."""
         d = self.ctx.dims
         has_r = d.d_r > 0
+        if self.n_q > 1:
+            B, n = self.B, self.n_q
+            gva.gva_decode_step_multi(self.ctx, q_c.reshape(B, n, d.H, d.d_n),
+                                      q_r.reshape(B, n, d.H, d.d_r) if has_r else None, M,
+                                      v_new.reshape(B, n, d.G, d.d_v), kr_new.reshape(B, n, d.d_r) if has_r else None,
+                                      v_pool, kr_pool if has_r else None, block_table, seq_lens, self.max_seq_len,
+                                      self.out if out is None else out, self.workspace, stream)
+            return self.out if out is None else out
         gva.gva_decode_step(self.ctx, q_c, q_r if has_r else None, M, v_new.reshape(self.B, d.G, d.d_v),
                             kr_new.reshape(self.B, d.d_r) if has_r else None, v_pool, kr_pool if has_r else None,
                             block_table, seq_lens, self.max_seq_len, self.out if out is None else out, self.workspace,

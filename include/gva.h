@@ -243,6 +243,29 @@ gva_status gva_decode_step(gva_ctx* ctx, int B, const float* q_c, const float* q
 size_t gva_decode_step_workspace_size(const gva_ctx* ctx, int B, int max_seq_len);
 gva_status gva_set_step_mode(gva_ctx* ctx, gva_step_mode mode);
 
+/* gva_decode_step_multi -- a decode step of n_q tokens per sequence (drafts to verify in
+ * speculative decoding): the n_q new tokens go to the last n_q positions of each context,
+ * seq_lens[b] - n_q + i (the lengths already count them), their queries are absorbed and
+ * rotated at the same positions, and query i reads the cache through its own position (the
+ * decode lifecycle of the GQA explainer, section "与位置编码和 KV Cache 的关系").  Equals
+ *   gva_cache_append(ctx, B, n_q, v_new, kr_new, pos = T - n_q, ...);
+ *   gva_absorb_query(ctx, B*n_q, q_c, q_r, pos_q = T - n_q + i, M, q_abs, q_rot, ...);
+ *   gva_decode_attention_multi(ctx, B, n_q, q_abs, q_rot, ...);
+ * bit for bit.
+ *   q_c [B,n_q,H,d_n] f32, q_r [B,n_q,H,d_r] f32, M [H,d_v,d_n] f32
+ *   v_new [B,n_q,G,d_v] and kr_new [B,n_q,d_r] cache dtype (kr_new unrotated)
+ *   out [B,n_q,H,d_v] f32; seq_lens[b] in [n_q, max_seq_len]
+ *   workspace: at least gva_decode_step_workspace_size_multi(ctx, B, n_q, max_seq_len) bytes.
+ * The kernels run separately (append and absorb side by side, then the multi-query decode);
+ * q_c, q_r, v_new, kr_new and out may be pinned host memory as for gva_decode_step.  n_q == 1
+ * is gva_decode_step (whose fused form then applies). */
+gva_status gva_decode_step_multi(gva_ctx* ctx, int B, int n_q, const float* q_c, const float* q_r,
+                                 const float* M, const void* v_new, const void* kr_new, void* v_pool,
+                                 void* kr_pool, const int32_t* block_table, int max_blocks, int num_blocks,
+                                 const int32_t* seq_lens, int max_seq_len, float* out, void* workspace,
+                                 size_t ws_bytes, gva_stream_t stream);
+size_t gva_decode_step_workspace_size_multi(const gva_ctx* ctx, int B, int n_q, int max_seq_len);
+
 /* Which form gva_decode_step takes for this batch shape under the context's mode: 1 the fused
  * kernel, 0 the separate kernels, -1 none (bad arguments, or fused mode where it does not
  * apply). */

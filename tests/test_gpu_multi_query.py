@@ -161,3 +161,43 @@ def test_speculative_step_from_raw_inputs():
     want = oracle.decode_multi(qa.reshape(w.B, n_q, w.H, w.d_v), qr.reshape(w.B, n_q, w.H, w.d_r), ovp, okp,
                                table.numpy(), lens.numpy(), G=w.G, d_n=w.d_n)
     assert_bf16(out.cpu().numpy(), want, "speculative step")
+
+
+STEP_CASES = [
+    (dict(B=4, H=16, G=4, d_v=64, d_r=16, T_range=(3, 900)), 2),
+    (dict(B=3, H=8, G=4, d_v=64, d_r=24, T_range=(4, 500)), 4),
+    (dict(B=3, H=32, G=8, d_v=128, d_r=24, T_range=(3, 1200)), 3),
+    (dict(B=2, H=16, G=4, d_v=64, d_r=0, T_range=(2, 400)), 2),
+]
+
+
+@pytest.mark.parametrize("case", range(len(STEP_CASES)))
+def test_multi_query_one_call_step(case):
+    """gva_decode_step_multi: append n_q tokens at the last n_q positions, absorb the n_q query
+    rows there, decode -- bit for bit against the three calls, and against the oracle's append +
+    absorb + multi-query decode on a host copy of the cache."""
+    shape, n_q = STEP_CASES[case]
+    w = synth.custom(name=f"mstep{case}", dtype="bf16", shuffled=True, **shape)
+    lens = synth.seq_lens(w, seed_lens=60 + case)
+    lens[0] = n_q
+    inp = synth.decode_inputs(w, seed=70 + case, device="cuda", lens=lens)
+    raw = synth.raw_inputs(w, inp.seq_lens.cpu(), n_new=n_q, seed=80 + case, device="cuda", n_q=n_q)
+    mk = lambda: GVADecodeLayer(w.H, w.G, w.d_v, w.d_n, w.d_r, w.dtype, w.B, w.max_seq_len, n_q=n_q)
+    sep, one = mk(), mk()
+    v1, k1 = inp.v_pool.clone(), inp.kr_pool.clone()
+    want = sep.step(raw.q_c, raw.q_r, raw.pos_q, raw.M, raw.v_new, raw.kr_new, raw.pos_new, inp.block_table,
+                    inp.seq_lens, v1, k1, overlap=False).clone()
+    v2, k2 = inp.v_pool.clone(), inp.kr_pool.clone()
+    got = one.fused_step(raw.q_c, raw.q_r, raw.M, raw.v_new, raw.kr_new, inp.block_table, inp.seq_lens, v2, k2)
+    torch.cuda.synchronize()
+    assert sep.device_error() == 0 and one.device_error() == 0
+    assert torch.equal(got, want) and torch.equal(v1, v2) and torch.equal(k1, k2)
+    # the oracle: append, absorb at T - n_q + i, causal multi-query decode
+    vp, kp = synth.pool_bits(inp.v_pool).copy(), synth.pool_bits(inp.kr_pool).copy()
+    table, L = inp.block_table.cpu().numpy(), inp.seq_lens.cpu().numpy()
+    oracle.append(synth.pool_bits(raw.v_new), synth.pool_bits(raw.kr_new), (L - n_q).astype(np.int32), table, vp, kp)
+    qa, qr = oracle.absorb(raw.q_c.double().cpu().numpy(), raw.q_r.double().cpu().numpy(),
+                           raw.pos_q.cpu().numpy(), raw.M.double().cpu().numpy())
+    want_o = oracle.decode_multi(qa.reshape(w.B, n_q, w.H, w.d_v), qr.reshape(w.B, n_q, w.H, w.d_r), vp, kp, table,
+                                 L, G=w.G, d_n=w.d_n)
+    assert_bf16(got.cpu().numpy(), want_o, f"one-call step, case {case}")
