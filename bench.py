@@ -272,10 +272,9 @@ class Setup:
                            2 * w.B * (w.G * w.d_v + w.d_r) * w.elem_bytes + w.B * w.H * w.d_v * 4 + w.B * 4 +
                            used_blocks * 4)
 
-        # one query per sequence: the library's one-call step; several: append + absorb + the
-        # multi-query decode
-        self.one_call = n_q == 1
-        self.fused = self.one_call and gva.gva_step_is_fused(self.layer.ctx, w.B, w.max_seq_len) == 1
+        # the library's one-call step (gva_decode_step, or gva_decode_step_multi for n_q > 1)
+        self.one_call = True
+        self.fused = n_q == 1 and gva.gva_step_is_fused(self.layer.ctx, w.B, w.max_seq_len) == 1
         R = w.H // w.G
         nqp_max = 4 if R <= 2 else 2 if R == 4 else 1
         passes, q = 0, 0
@@ -288,8 +287,6 @@ class Setup:
         self.launches_per_step = 2 if self.fused else 2 + 2 * passes
 
     def step(self, stream=None):
-        if not self.one_call:
-            return self.three_call_step(stream)
         r, i = self.raw, self.inp
         return self.layer.fused_step(r.q_c, r.q_r, r.M, r.v_new, r.kr_new, i.block_table, i.seq_lens, i.v_pool,
                                      i.kr_pool, stream)
@@ -438,8 +435,9 @@ def run_ours(args, rank, ws):
     hbm_peak = pk["hbm_gbs"]
     step_desc = ("gva_decode_step, fused: the split-T partial kernel absorbs and rotates the query in its "
                  "prologue and appends the new token, then the combine" if S.fused else
-                 "gva_decode_step as separate kernels: append + absorb + split-T partial + combine" if S.one_call
-                 else "append + absorb + gva_decode_attention_multi")
+                 "gva_decode_step as separate kernels: append + absorb + split-T partial + combine" if S.n_q == 1
+                 else f"gva_decode_step_multi: append {S.n_q} tokens + absorb {S.n_q} query rows per sequence + "
+                      "the causal multi-query decode")
 
     out = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws, "steps": K,
