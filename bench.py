@@ -35,7 +35,7 @@ METRIC = "GVA decode-attention cache-read GB/s (% of B300 HBM peak) and context 
 # DRAM bytes (read + write) of one launch of the step's split-T partial kernel (the fused one,
 # or the plain one), from the ncu captures summarised in profiles/ (absent where no capture of
 # the current kernel exists)
-TRAFFIC = {("long-context-bf16", "plain"): 574_461_568, ("long-context-bf16", "fused"): 572_519_168}
+TRAFFIC = {("long-context-bf16", "plain"): 572_503_808, ("long-context-bf16", "fused"): 572_519_168}
 L2_BYTES = 126 * 1024 * 1024
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 NVML_REASONS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap", 0x8: "hw_slowdown",
