@@ -34,9 +34,13 @@ from compact_kv_cache_gva_b300.layer import GVADecodeLayer  # noqa: E402
 METRIC = "GVA decode-attention cache-read GB/s (% of B300 HBM peak) and context tokens/s"
 # DRAM bytes (read + write) of one launch of the step's split-T partial kernel (the fused one,
 # or the plain one), from the ncu captures summarised in profiles/ (absent where no capture of
-# the current kernel exists)
-TRAFFIC = {("long-context-bf16", "plain"): 572_503_808, ("long-context-bf16", "fused"): 572_519_168}
+# the current kernel exists).  The ragged batch's figure is the capture of its first 32
+# sequences (73,600 units) scaled to the full batch's 254,224 units.
+TRAFFIC = {("long-context-bf16", "plain"): 572_503_808, ("long-context-bf16", "fused"): 572_519_168,
+           ("layer-350m-bf16", "fused"): 71_833_088, ("dr24-bf16", "fused"): 296_072_704,
+           ("ragged-paged-bf16", "plain"): 4_272_515_956}
 L2_BYTES = 126 * 1024 * 1024
+NOMINAL_HBM_GBS = 8000.0  # B300 HBM3e, nominal
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 NVML_REASONS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap", 0x8: "hw_slowdown",
                 0x10: "sync_boost", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
@@ -65,6 +69,17 @@ def parse():
     p.add_argument("--nq", type=int, default=1,
                    help="query tokens per sequence per step (the last n_q positions: append n_q tokens, "
                         "absorb B*n_q query rows, gva_decode_attention_multi)")
+    p.add_argument("--batch", type=int, default=0,
+                   help="keep only the first N sequences of the workload (named <name>-b<N>), e.g. for a "
+                        "profiler capture small enough to hold on the device twice")
+    p.add_argument("--profile", action="store_true",
+                   help="run only the step's split-T partial pass: --warmup launches, then --steps more, "
+                        "and print one line (for a profiler's launch filter; no timing is reported)")
+    p.add_argument("--workloads", default="2,3,5",
+                   help="other configurations measured after the headline, in the same process "
+                        "(comma-separated workload ids; empty for none)")
+    p.add_argument("--workload-steps", type=int, default=200,
+                   help="timed steps of each of those configurations (at least --steps)")
     p.add_argument("--dr", type=int, default=-1,
                    help="override the workload's positional width d_r (0 = no positional slice, the Shared-KV "
                         "cache layout); the workload is then named <name>-dr<d_r>")
@@ -163,6 +178,9 @@ class SmiClockSampler:
             self.max_mhz = mx
             self.samples.append((sm, reasons))
 
+    def sample(self):
+        pass  # the nvidia-smi process polls on its own
+
     summary = None  # set below
 
 
@@ -198,18 +216,25 @@ class ClockSampler:
         except Exception as e:  # no NVML: report that instead of guessing
             self.err = repr(e)
 
-    def _run(self):
+    def sample(self):
+        """One reading now (also called from the timing loop while the device is busy, so that
+        a timed region shorter than the polling period still has samples)."""
+        if not self.ok:
+            return
         nv = self.nv
-        while not self._stop.is_set():
+        try:
+            sm = nv.nvmlDeviceGetClockInfo(self.h, nv.NVML_CLOCK_SM)
             try:
-                sm = nv.nvmlDeviceGetClockInfo(self.h, nv.NVML_CLOCK_SM)
-                try:
-                    reasons = nv.nvmlDeviceGetCurrentClocksEventReasons(self.h)
-                except Exception:
-                    reasons = nv.nvmlDeviceGetCurrentClocksThrottleReasons(self.h)
-                self.samples.append((sm, int(reasons)))
+                reasons = nv.nvmlDeviceGetCurrentClocksEventReasons(self.h)
             except Exception:
-                pass
+                reasons = nv.nvmlDeviceGetCurrentClocksThrottleReasons(self.h)
+            self.samples.append((sm, int(reasons)))
+        except Exception:
+            pass
+
+    def _run(self):
+        while not self._stop.is_set():
+            self.sample()
             time.sleep(self.period)
 
     def __enter__(self):
@@ -286,6 +311,12 @@ class Setup:
             passes += 1
         self.launches_per_step = 2 if self.fused else 2 + 2 * passes
 
+    def prime_queries(self):
+        """The layer's absorbed and rotated queries (what gva_decode_partial reads when it is
+        timed alone) from this step's raw queries."""
+        r = self.raw
+        self.layer.absorb(r.q_c, r.q_r, r.pos_q, r.M)
+
     def step(self, stream=None):
         r, i = self.raw, self.inp
         return self.layer.fused_step(r.q_c, r.q_r, r.M, r.v_new, r.kr_new, i.block_table, i.seq_lens, i.v_pool,
@@ -322,23 +353,31 @@ def flusher():
     return flush
 
 
-def time_steps(run_step, K, flush):
+def time_steps(run_step, K, flush, clocks=None):
     """Device seconds for K steps.  Inputs larger than L2: one event pair around the K
-    back-to-back steps.  Otherwise L2 is flushed before every step, outside per-step events."""
+    back-to-back steps.  Otherwise L2 is flushed before every step, outside per-step events.
+    With `clocks`, one clock reading is taken after the first step is enqueued and one after
+    the last (the device is then still working through the queue)."""
+    tick = clocks.sample if clocks is not None else (lambda: None)
     if flush is None:
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
-        for _ in range(K):
+        for k in range(K):
             run_step()
+            if k == 0:
+                tick()
         e1.record()
+        tick()
         torch.cuda.synchronize()
         return e0.elapsed_time(e1) / 1e3
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
-    for a, b in evs:
+    for k, (a, b) in enumerate(evs):
         flush()
         a.record()
         run_step()
         b.record()
+        if k == 0 or k == K - 1:
+            tick()
     torch.cuda.synchronize()
     return sum(a.elapsed_time(b) for a, b in evs) / 1e3
 
@@ -363,7 +402,27 @@ def workload(args):
         w = dataclasses.replace(w, d_r=args.dr, name=f"{w.name}-dr{args.dr}")
     if args.nq > 1:
         w = dataclasses.replace(w, name=f"{w.name}-nq{args.nq}")
+    if args.batch and args.batch < w.B:
+        w = dataclasses.replace(w, B=args.batch, name=f"{w.name}-b{args.batch}")
     return w
+
+
+def run_profile(args):
+    """The step's split-T partial pass alone, launched --warmup + --steps times, for a profiler."""
+    torch.cuda.init()
+    w = workload(args)
+    S = Setup(w, seed=0, path=args.path, split_tokens=args.split_tokens, step_mode=args.step_mode)
+    S.prime_queries()
+    partial, _ = partial_calls(S)
+    for _ in range(args.warmup + args.steps):
+        partial()
+    torch.cuda.synchronize()
+    if S.layer.device_error():
+        raise RuntimeError("device reported an index error")
+    units = int(((S.lens_cpu + 63) // 64).sum()) * w.G
+    print(json.dumps({"profile": w.name, "kernel": "fused" if S.fused else "plain", "launches": args.warmup + args.steps,
+                      "units_per_launch": units, "cache_bytes": S.cache_bytes,
+                      "algorithmic_bytes_per_launch": S.step_bytes if S.fused else S.decode_bytes}), flush=True)
 
 
 def run_ours(args, rank, ws):
@@ -391,7 +450,7 @@ def run_ours(args, rank, ws):
     barrier(ws)
     torch.cuda.synchronize()
     with ClockSampler() as clocks:
-        step_s = time_steps(run_step, K, flush)
+        step_s = time_steps(run_step, K, flush, clocks)
     barrier(ws)
     total_s = max_over_ranks(step_s, ws)
 
@@ -449,7 +508,11 @@ def run_ours(args, rank, ws):
                        l2="flushed before every step (252 MB write, then 252 MB read)" if need_flush else
                        f"inputs larger than L2 ({S.cache_bytes / 1e6:.0f} MB cache)",
                        parallelism=f"replicas x{ws}" if ws > 1 else "single GPU"),
-        "pct_of_hbm_peak": round(100 * value / ws / hbm_peak, 2),
+        # against the B300's nominal ~8 TB/s HBM3e peak (the target's denominator); the
+        # fraction of this machine's measured copy bandwidth is reported beside it
+        "pct_of_hbm_peak": round(100 * value / ws / NOMINAL_HBM_GBS, 2),
+        "hbm_peak_basis": f"nominal {NOMINAL_HBM_GBS:.0f} GB/s",
+        "pct_of_measured_copy_bw": round(100 * value / ws / hbm_peak, 2),
         "context_tokens_per_s": round(tokens_per_s, 1),
         "decode_steps_per_s": round(K * ws / total_s, 2),
         "three_call_step_us": round(three_s * 1e6 / K, 3) if three_s else None,
@@ -464,10 +527,15 @@ def run_ours(args, rank, ws):
                      "algorithmic_bytes_per_launch": part_bytes, "partial_us": round(part_us, 3),
                      "decode_call_us": round(dec_us, 3),
                      "decode_call_GBps": round(S.decode_bytes / (dec_s / K) / 1e9, 1),
-                     "traffic": TRAFFIC.get((w.name, "fused" if S.fused else "plain"))},
+                     "traffic": TRAFFIC.get((w.name, "fused" if S.fused else "plain")),
+                     "traffic_ratio": (round(TRAFFIC[(w.name, "fused" if S.fused else "plain")] / part_bytes, 4)
+                                       if (w.name, "fused" if S.fused else "plain") in TRAFFIC else None)},
         "gpu_launches": S.launches_per_step * K,
         "clocks": clocks.summary(),
     }
+    if args.workloads and S.n_q == 1 and args.dr < 0:
+        out["workloads"] = [run_workload_line(int(x), args, rank, ws) for x in args.workloads.split(",")
+                            if int(x) != args.workload]
     out["e2e"] = run_e2e(S, args.e2e_steps, flush, graph=bool(args.graph), ws=ws)
     if not args.no_gqa and rank == 0:
         out["gqa_same_build"] = run_gqa(S, flush, min(K, 500))
@@ -476,9 +544,62 @@ def run_ours(args, rank, ws):
     return out
 
 
-def time_partial(S, K, flush):
-    """Average device seconds of the step's split-T partial pass (events on the launching stream):
-    the fused kernel (gva_decode_step_partial) when the step is fused, else gva_decode_partial."""
+def run_workload_line(wid, args, rank, ws):
+    """Another configuration measured in the same process as the headline, the same way: the
+    one-call step, the decode call (partial + combine) and the split-T partial pass alone, each
+    timed with CUDA events over K steps (L2 flushed before every step when the cache is smaller
+    than twice L2), with the clocks sampled during the step's timed region."""
+    w = synth.WORKLOADS[wid]
+    S = Setup(w, seed=rank, path=args.path, split_tokens=args.split_tokens, step_mode=args.step_mode)
+    flush = flusher() if S.cache_bytes < 2 * L2_BYTES else None
+    K = max(args.steps, args.workload_steps)
+    S.prime_queries()
+    for _ in range(max(3, args.warmup)):
+        if flush:
+            flush()
+        S.step()
+    torch.cuda.synchronize()
+    if S.layer.device_error():
+        raise RuntimeError(f"{w.name}: device reported an index error during warm-up")
+    barrier(ws)
+    torch.cuda.synchronize()
+    with ClockSampler() as clocks:
+        step_s = time_steps(S.step, K, flush, clocks)
+    barrier(ws)
+    step_s = max_over_ranks(step_s, ws)
+    dec_s = max_over_ranks(time_steps(lambda: S.layer.attend(S.inp.v_pool, S.inp.kr_pool, S.inp.block_table,
+                                                             S.inp.seq_lens), K, flush), ws)
+    part_s = max_over_ranks(time_partial(S, K, flush), ws)
+    pk, pk_kind = peaks()
+    part_bytes = S.step_bytes if S.fused else S.decode_bytes
+    achieved = part_bytes / part_s / 1e9
+    traffic = TRAFFIC.get((w.name, "fused" if S.fused else "plain"))
+    line = {
+        "workload": w.name, "config": w.describe(), "steps": K,
+        "step_form": "fused" if S.fused else "separate",
+        "l2": "flushed before every step" if flush else "inputs larger than L2",
+        "value": round(whole_job(S.cache_bytes * K, ws, step_s) / 1e9, 2), "unit": "GB/s",
+        "step_us": round(step_s * 1e6 / K, 3),
+        "decode_call_us": round(dec_s * 1e6 / K, 3),
+        "partial_us": round(part_s * 1e6, 3),
+        "context_tokens_per_s": round(whole_job(S.sum_T * K, ws, step_s), 1),
+        "pct_of_hbm_peak": round(100 * S.cache_bytes / (step_s / K) / 1e9 / NOMINAL_HBM_GBS, 2),
+        "roofline": {"kernel": "fused split-T partial kernel (gva_decode_step_partial)" if S.fused else
+                     "split-T partial pass (gva_decode_partial)", "bound": "hbm", "achieved": round(achieved, 1),
+                     "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": round(achieved / pk["hbm_gbs"], 4),
+                     "peak_kind": f"{pk_kind} copy bandwidth (burst)", "algorithmic_bytes_per_launch": part_bytes,
+                     "traffic": traffic,
+                     "traffic_ratio": round(traffic / part_bytes, 4) if traffic else None},
+        "clocks": clocks.summary(),
+    }
+    del S
+    torch.cuda.empty_cache()
+    return line
+
+
+def partial_calls(S):
+    """(partial, combine): the step's split-T partial pass (the fused kernel,
+    gva_decode_step_partial, when the step is fused, else gva_decode_partial) and its combine."""
     L, i, r, w = S.layer, S.inp, S.raw, S.w
 
     def partial():
@@ -494,6 +615,12 @@ def time_partial(S, K, flush):
 
     def combine():
         gva.gva_decode_combine(L.ctx, S.w.B, S.w.max_seq_len, L.out, L.workspace)
+    return partial, combine
+
+
+def time_partial(S, K, flush):
+    """Average device seconds of the step's split-T partial pass (events on the launching stream)."""
+    partial, combine = partial_calls(S)
     for _ in range(3):
         partial()
         combine()
@@ -736,6 +863,9 @@ def main():
         return
     if not torch.cuda.is_available():
         raise SystemExit("bench.py needs a CUDA device (no CPU fallback)")
+    if args.profile:
+        run_profile(args)
+        return
     out = run_ours(args, rank, ws)
     if rank == 0:
         print(json.dumps(out), flush=True)

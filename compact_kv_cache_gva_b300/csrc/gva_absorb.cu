@@ -28,6 +28,7 @@ namespace {
 constexpr int kAbsorbThreads = 256;
 constexpr int kAbsorbSeqs = 16;
 constexpr int kAbsorbVecs = 8;  // 16-byte vectors of M_h and q_c held per thread per pass
+constexpr long long kMaxGridY = 65535;  // largest y extent of a grid
 
 struct AbsorbArgs {
   const float* q_c;
@@ -47,17 +48,14 @@ struct AbsorbArgs {
   int defer_wait;
 };
 
-__global__ void __launch_bounds__(kAbsorbThreads) absorb_kernel(const AbsorbArgs a) {
-  extern __shared__ __align__(16) float sm[];
+// Rows b0 .. b0 + 15 (those below B) of head blockIdx.x.
+__device__ __forceinline__ void absorb_rows(const AbsorbArgs& a, float* sm, int b0) {
   const int ldm = a.d_n + 4;     // padded rows: conflict-free 16-byte reads by row
   float* Ms = sm;                // [d_v][d_n + 4]
   float* qs = sm + a.d_v * ldm;  // [kAbsorbSeqs][d_n + 4]
   const int h = blockIdx.x;
-  const int b0 = blockIdx.y * kAbsorbSeqs;
   const int nb = min(kAbsorbSeqs, a.B - b0);
   const int t = threadIdx.x;
-  if (!a.defer_wait) griddep_wait();
-  griddep_launch_dependents();
 
   // positional slice: thread t < nb * pairs owns pair (t % pairs) of sequence b0 + t / pairs
   const int pairs = a.d_r / 2;
@@ -169,6 +167,18 @@ __global__ void __launch_bounds__(kAbsorbThreads) absorb_kernel(const AbsorbArgs
       }
     }
   }
+}
+
+// One CTA per (head, block of 16 rows); a grid narrower than the row blocks (its y extent
+// is capped at 65535) takes them in strides, so any row count runs.
+__global__ void __launch_bounds__(kAbsorbThreads) absorb_kernel(const AbsorbArgs a) {
+  extern __shared__ __align__(16) float sm[];
+  if (!a.defer_wait) griddep_wait();
+  griddep_launch_dependents();
+  for (long long yb = blockIdx.y; yb * kAbsorbSeqs < a.B; yb += gridDim.y) {
+    if (yb != blockIdx.y) __syncthreads();  // the previous rows' shared memory has been read
+    absorb_rows(a, sm, static_cast<int>(yb * kAbsorbSeqs));
+  }
   if (a.defer_wait) griddep_wait();
 }
 
@@ -208,7 +218,8 @@ cudaError_t launch_absorb(const gva_ctx* ctx, int B, const float* q_c, const flo
     if (dev < kMaxDevicesHost) configured[dev] = static_cast<int>(smem);
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(a.H, (B + kAbsorbSeqs - 1) / kAbsorbSeqs);
+  const long long row_blocks = (static_cast<long long>(B) + kAbsorbSeqs - 1) / kAbsorbSeqs;
+  cfg.gridDim = dim3(a.H, static_cast<unsigned>(row_blocks < kMaxGridY ? row_blocks : kMaxGridY));
   cfg.blockDim = dim3(kAbsorbThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;

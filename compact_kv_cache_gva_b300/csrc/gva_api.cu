@@ -19,6 +19,29 @@ constexpr long long kStepAutoMapBytes = 64 * 1024;
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Whether the kernels may read or write p: device or managed memory, or page-locked host
+// memory mapped into the device's address space at the same address (cudaHostAlloc, or
+// cudaHostRegister with the mapped flag, under unified addressing).  Pageable host memory
+// (malloc, the stack) is not: a kernel touching it would fault.  Null passes (the caller
+// checks required pointers itself).
+bool device_addressable(const void* p) {
+  if (!p) return true;
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    (void)cudaGetLastError();  // clear the error the query left behind
+    return false;
+  }
+  if (at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged) return true;
+  return at.type == cudaMemoryTypeHost && at.devicePointer == p;
+}
+
+// The step's per-call inputs and output, which may be pinned host memory.
+bool step_buffers_addressable(const void* q_c, const void* q_r, const void* v_new, const void* kr_new,
+                              const void* out) {
+  return device_addressable(q_c) && device_addressable(q_r) && device_addressable(v_new) &&
+         device_addressable(kr_new) && device_addressable(out);
+}
+
 bool on_ctx_device(const gva_ctx* ctx) {
   int dev = -1;
   return cudaGetDevice(&dev) == cudaSuccess && dev == ctx->device;
@@ -407,6 +430,7 @@ gva_status gva_decode_step_partial(gva_ctx* ctx, int B, const float* q_c, const 
   if (!aligned16(q_c) || !aligned16(M) || !aligned16(v_new) || (q_r && !aligned16(q_r)) ||
       (kr_new && (reinterpret_cast<uintptr_t>(kr_new) & 3u)))
     return GVA_ERR_INVALID_ARG;
+  if (!step_buffers_addressable(q_c, q_r, v_new, kr_new, nullptr)) return GVA_ERR_INVALID_ARG;
   const StepInputs in{q_c, q_r, M, v_new, kr_new, v_pool, kr_pool};
   return decode_common(ctx, false, kPhasePartial, B, nullptr, nullptr, nullptr, v_pool, kr_pool, block_table,
                        max_blocks, num_blocks, seq_lens, max_seq_len, nullptr, workspace, ws_bytes,
@@ -440,6 +464,7 @@ gva_status gva_decode_step(gva_ctx* ctx, int B, const float* q_c, const float* q
     return GVA_ERR_INVALID_ARG;
   if (B > gva::kMaxBatch) return GVA_ERR_UNSUPPORTED;
   if (!on_ctx_device(ctx)) return GVA_ERR_INVALID_ARG;
+  if (!step_buffers_addressable(q_c, q_r, v_new, kr_new, out)) return GVA_ERR_INVALID_ARG;
   gva::Plan plan;
   if (!make_plan(ctx, B, max_seq_len, false, &plan)) return GVA_ERR_UNSUPPORTED;
   const cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
@@ -493,6 +518,7 @@ gva_status gva_decode_step_multi(gva_ctx* ctx, int B, int n_q, const float* q_c,
     return GVA_ERR_INVALID_ARG;
   if (B > gva::kMaxBatch || static_cast<long long>(B) * n_q > (1LL << 30)) return GVA_ERR_UNSUPPORTED;
   if (!on_ctx_device(ctx)) return GVA_ERR_INVALID_ARG;
+  if (!step_buffers_addressable(q_c, q_r, v_new, kr_new, out)) return GVA_ERR_INVALID_ARG;
   gva::Plan plan;
   if (!make_plan(ctx, B, max_seq_len, false, &plan, n_q)) return GVA_ERR_UNSUPPORTED;
   const cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);

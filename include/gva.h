@@ -227,7 +227,9 @@ typedef enum {
  * q_c, q_r, v_new, kr_new and out may also point to page-locked host memory that the device
  * can address (cudaHostAlloc, or cudaHostRegister with the mapped flag; under unified virtual
  * addressing the host pointer itself): the kernels then read the step's inputs and write its
- * output across the bus directly, with no copy before or after the step.
+ * output across the bus directly, with no copy before or after the step.  Any other host
+ * memory (pageable: malloc, the stack) is rejected with GVA_ERR_INVALID_ARG before anything
+ * is enqueued, as it is by gva_decode_step_multi and gva_decode_step_partial.
  * The fused form (tensor-core path, d_n == d_v) is one partial kernel plus the combine: the
  * partial kernel forms the absorbed queries in its prologue (the "extra query-side compute"
  * of absorption, summary section 方法, done where the queries are used) and appends the new
@@ -326,7 +328,10 @@ gva_status gva_decode_plan(const gva_ctx* ctx, int B, int max_seq_len, int* spli
  *   - Batches whose gva_decode_workspace_size() exceeds GVA_NOALLOC_SCRATCH_BYTES are
  *     rejected with GVA_ERR_WORKSPACE before anything is enqueued.
  *   - The first call on each device looks up the array's device address (with that device
- *     current); make that first call before any stream capture.
+ *     current); make that first call before any stream capture.  The address is kept for
+ *     the life of the process: after cudaDeviceReset (or anything else that destroys the
+ *     device's primary context) it no longer names the array, so do not call this entry
+ *     point on that device again in the same process.
  *   - Every call on a device shares the one array, and it keeps the previous call's
  *     contents.  Calls whose work can overlap on the GPU (different streams without
  *     ordering between them) race on it and give wrong results; order them on one stream. */

@@ -192,6 +192,15 @@ def test_multi_query_one_call_step(case):
     torch.cuda.synchronize()
     assert sep.device_error() == 0 and one.device_error() == 0
     assert torch.equal(got, want) and torch.equal(v1, v2) and torch.equal(k1, k2)
+    # the step's inputs read from, and its output written to, pinned host memory: same bits
+    host = {k: getattr(raw, k).cpu().pin_memory() for k in ("q_c", "q_r", "v_new", "kr_new")}
+    out_h = torch.full(tuple(want.shape), float("nan")).pin_memory()
+    v3, k3 = inp.v_pool.clone(), inp.kr_pool.clone()
+    one.fused_step(host["q_c"], host["q_r"], raw.M, host["v_new"], host["kr_new"], inp.block_table, inp.seq_lens,
+                   v3, k3, out=out_h)
+    torch.cuda.synchronize()
+    assert one.device_error() == 0
+    assert torch.equal(out_h, want.cpu()) and torch.equal(v3, v1) and torch.equal(k3, k1)
     # the oracle: append, absorb at T - n_q + i, causal multi-query decode
     vp, kp = synth.pool_bits(inp.v_pool).copy(), synth.pool_bits(inp.kr_pool).copy()
     table, L = inp.block_table.cpu().numpy(), inp.seq_lens.cpu().numpy()
