@@ -2,8 +2,9 @@
 
 TEST INFRASTRUCTURE ONLY: imported by the test suite, the package smoke check and the
 benchmark's CPU-baseline leg, never by the library.  Arrays are numpy; pools are raw
-cache-dtype arrays (float32, or uint16 holding bf16 bit patterns), exactly the bytes a
-cache would hold.  Every call checks shapes and raises on a non-zero oracle status.
+cache-dtype arrays (float32, uint16 holding bf16 bit patterns, or for the fp8 cache's value
+pool uint8: the E4M3 codes followed by the int8 exponents), exactly the bytes a cache would
+hold.  Every call checks shapes and raises on a non-zero oracle status.
 """
 import ctypes as C
 import os
@@ -12,7 +13,7 @@ import numpy as np
 
 from .build import build as _build
 
-F32, BF16 = 0, 1
+F32, BF16, FP8 = 0, 1, 2
 BLOCK = 64
 
 _lib = None
@@ -24,6 +25,16 @@ def lib():
         path = _build()
         L = C.CDLL(path)
         dp, ip, vp = C.POINTER(C.c_double), C.POINTER(C.c_int32), C.c_void_p
+        L.oracle_e4m3_to_double.restype = C.c_double
+        L.oracle_e4m3_to_double.argtypes = [C.c_uint8]
+        L.oracle_double_to_e4m3.restype = C.c_uint8
+        L.oracle_double_to_e4m3.argtypes = [C.c_double]
+        L.oracle_fp8_exponent.restype = C.c_int
+        L.oracle_fp8_exponent.argtypes = [C.c_double]
+        L.oracle_fp8_exp_offset.restype = C.c_int64
+        L.oracle_fp8_exp_offset.argtypes = [C.c_int, C.c_int, C.c_int, C.c_int64, C.c_int, C.c_int]
+        L.oracle_cache_bytes_per_token.restype = C.c_double
+        L.oracle_cache_bytes_per_token.argtypes = [C.c_int] * 4
         L.oracle_bf16_to_double.restype = C.c_double
         L.oracle_bf16_to_double.argtypes = [C.c_uint16]
         L.oracle_double_to_bf16.restype = C.c_uint16
@@ -80,11 +91,40 @@ def _pool(a):
         code = F32
     elif a.dtype == np.uint16:
         code = BF16
+    elif a.dtype == np.uint8:
+        code = FP8  # value pool of the fp8 cache: E4M3 codes, then the int8 exponents
     else:
-        raise TypeError("pool arrays are float32 or uint16 (bf16 bits)")
+        raise TypeError("pool arrays are float32, uint16 (bf16 bits) or uint8 (fp8 value pool)")
     if not a.flags.c_contiguous:
         raise ValueError("pool must be contiguous")
     return code, C.c_void_p(a.ctypes.data)
+
+
+def num_blocks_of(v_pool, G, d_v):
+    """Blocks in a value pool: [NB][G][64][d_v] elements, or for the fp8 cache NB*G*64*d_v
+    codes followed by NB*G*64 exponents."""
+    per_block = G * BLOCK * d_v + (G * BLOCK if v_pool.dtype == np.uint8 else 0)
+    return v_pool.size // per_block
+
+
+def e4m3_to_double(code):
+    return lib().oracle_e4m3_to_double(int(code))
+
+
+def double_to_e4m3(x):
+    return lib().oracle_double_to_e4m3(float(x))
+
+
+def fp8_exponent(amax):
+    return lib().oracle_fp8_exponent(float(amax))
+
+
+def fp8_exp_offset(G, d_v, num_blocks, blk, g, o):
+    return lib().oracle_fp8_exp_offset(G, d_v, num_blocks, blk, g, o)
+
+
+def cache_bytes_per_token(dtype, G, d_v, d_r):
+    return lib().oracle_cache_bytes_per_token({"f32": F32, "bf16": BF16, "fp8": FP8}.get(dtype, dtype), G, d_v, d_r)
 
 
 def bf16_to_double(bits):
@@ -129,11 +169,15 @@ def kr_offset(d_r, blk, o, c):
 
 
 def append(v_new, kr_new, pos, block_table, v_pool, kr_pool, base=10000.0, raise_on_index=True):
-    """In place on host pools.  v_new [B,n,G,d_v], kr_new [B,n,d_r] in the pool's dtype.
+    """In place on host pools.  v_new [B,n,G,d_v], kr_new [B,n,d_r] in the pool's dtype (for the
+    fp8 cache, whose value pool is uint8, both are bf16 bits and the values are quantised).
     Returns the oracle status (0, or 5 when some slot could not be resolved)."""
     code, pv = _pool(v_pool)
     code2, pk = _pool(kr_pool)
-    assert code == code2 and v_new.dtype == v_pool.dtype and kr_new.dtype == kr_pool.dtype
+    if code == FP8:
+        assert code2 == BF16 and v_new.dtype == np.uint16 and kr_new.dtype == np.uint16
+    else:
+        assert code == code2 and v_new.dtype == v_pool.dtype and kr_new.dtype == kr_pool.dtype
     v_new = np.ascontiguousarray(v_new)
     kr_new = np.ascontiguousarray(kr_new)
     B, n, G, d_v = v_new.shape
@@ -141,7 +185,7 @@ def append(v_new, kr_new, pos, block_table, v_pool, kr_pool, base=10000.0, raise
     pos, ppos = _i(pos)
     bt, pbt = _i(block_table)
     max_blocks = bt.shape[1]
-    num_blocks = v_pool.size // (G * BLOCK * d_v)
+    num_blocks = num_blocks_of(v_pool, G, d_v)
     st = lib().oracle_append(code, B, n, G, d_v, d_r, float(base), C.c_void_p(v_new.ctypes.data),
                              C.c_void_p(kr_new.ctypes.data), ppos, pbt, max_blocks, num_blocks, pv, pk)
     if raise_on_index:
@@ -159,10 +203,10 @@ def _decode_common(v_pool, kr_pool, block_table, seq_lens, G, d_v):
         pk = C.c_void_p(v_pool.ctypes.data)  # never read when d_r == 0
     else:
         code2, pk = _pool(kr_pool)
-        assert code2 == code
+        assert code2 == (BF16 if code == FP8 else code)
     bt, pbt = _i(block_table)
     sl, psl = _i(seq_lens)
-    num_blocks = v_pool.size // (G * BLOCK * d_v)
+    num_blocks = num_blocks_of(v_pool, G, d_v)
     return code, pv, pk, bt, pbt, sl, psl, num_blocks
 
 

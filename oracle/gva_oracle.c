@@ -40,6 +40,16 @@
  *   - Paged layout, 64-token blocks:  V element (blk, g, o, i) at ((blk*G+g)*64+o)*d_v+i,
  *     k_r element (blk, o, c) at (blk*64+o)*d_r+c, blk = table[b][p/64], o = p%64.
  *
+ * Low-precision value cache (not on the pages; a reading of this library's own): the
+ * value heads may be stored as OCP FP8 E4M3 codes (1 sign, 4 exponent bits with bias 7,
+ * 3 mantissa bits; no infinities; S.1111.111 is NaN; largest finite 448), with one
+ * power-of-two scale 2^e per (token, group).  e is the smallest integer with
+ * max_i |v_i| <= 448 * 2^e, clamped to [-126, 120] (e = -126 for an all-zero row); each code
+ * is v_i * 2^-e rounded once to the nearest E4M3 value (ties to even, magnitudes beyond 448
+ * clamped to 448).  The stored value is code * 2^e, exact in fp64.  Pool layout: the codes
+ * [NB][G][64][d_v] (one byte each) followed by the exponents [NB][G][64] (int8); the
+ * positional keys stay bf16.
+ *
  * Every function below is pinned by a CPU test against something other than itself
  * (closed forms, hand cases, library routines, invariants); see tests/test_oracle_pins.py.
  */
@@ -54,7 +64,11 @@
 
 #define OR_F32 0
 #define OR_BF16 1
+#define OR_FP8 2 /* E4M3 value codes + per-(token, group) exponents; bf16 positional keys */
 #define OR_BLOCK 64
+#define OR_E4M3_MAX 448.0
+#define OR_FP8_EMIN (-126)
+#define OR_FP8_EMAX 120
 
 #define OR_OK 0
 #define OR_ERR_ARG 1
@@ -97,9 +111,67 @@ uint16_t oracle_double_to_bf16(double x) {
   return (uint16_t)(u >> 16);
 }
 
+/* E4M3 code -> value (exact).  Normal: (-1)^s (1 + m/8) 2^(E-7); subnormal (E = 0):
+ * (-1)^s m 2^-9; S.1111.111 is NaN. */
+double oracle_e4m3_to_double(uint8_t c) {
+  int sgn = c >> 7, E = (c >> 3) & 15, m = c & 7;
+  if (E == 15 && m == 7) return NAN;
+  double mag = E == 0 ? ldexp((double)m, -9) : ldexp(1.0 + m / 8.0, E - 7);
+  return sgn ? -mag : mag;
+}
+
+/* Value -> E4M3 code, one rounding to nearest (ties to even); magnitudes that round beyond
+ * 448 give +-448 (saturation), NaN gives 0x7F. */
+uint8_t oracle_double_to_e4m3(double x) {
+  if (isnan(x)) return 0x7F;
+  uint8_t sgn = signbit(x) ? 0x80 : 0x00;
+  double a = fabs(x);
+  if (a == 0.0) return sgn;
+  if (a > OR_E4M3_MAX) return (uint8_t)(sgn | 0x7E);  /* saturates (also infinities) */
+  int e;
+  frexp(a, &e);                      /* a = f * 2^e, f in [0.5, 1): spacing 2^(e-4) */
+  int ulp_exp = e - 4;
+  if (ulp_exp < -9) ulp_exp = -9;    /* subnormal spacing */
+  int old = fegetround();
+  fesetround(FE_TONEAREST);
+  double r = nearbyint(ldexp(a, -ulp_exp)); /* exact scaling, then round half to even */
+  fesetround(old);
+  double y = ldexp(r, ulp_exp);
+  if (y > OR_E4M3_MAX) y = OR_E4M3_MAX;
+  if (y < ldexp(1.0, -6)) return (uint8_t)(sgn | (uint8_t)ldexp(y, 9)); /* subnormal or 0 */
+  int ey;
+  double fy = frexp(y, &ey);         /* y = fy * 2^ey: E = ey + 6, mantissa (2 fy - 1) * 8 */
+  return (uint8_t)(sgn | ((ey + 6) << 3) | (int)((2.0 * fy - 1.0) * 8.0));
+}
+
+/* Exponent of the power-of-two scale of a row whose largest magnitude is amax: the smallest
+ * e with amax <= 448 * 2^e, clamped to [-126, 120]; -126 for amax = 0. */
+int oracle_fp8_exponent(double amax) {
+  if (!(amax > 0.0)) return OR_FP8_EMIN;
+  int E;
+  double f = frexp(amax, &E);        /* amax = f * 2^E; 448 = 0.875 * 2^9 */
+  int e = E - 9 + (f > 0.875 ? 1 : 0);
+  if (e < OR_FP8_EMIN) e = OR_FP8_EMIN;
+  if (e > OR_FP8_EMAX) e = OR_FP8_EMAX;
+  return e;
+}
+
 static double load_elem(const void* base, int dtype, int64_t idx) {
   if (dtype == OR_F32) return (double)((const float*)base)[idx];
   return oracle_bf16_to_double(((const uint16_t*)base)[idx]);
+}
+
+/* Dtype of the positional-key pool: the fp8 cache keeps its keys in bf16. */
+static int kr_dtype(int dtype) { return dtype == OR_FP8 ? OR_BF16 : dtype; }
+
+/* Value element (blk, g, o, i) of a pool of num_blocks blocks. */
+static double load_v(const void* v_pool, int dtype, int G, int d_v, int num_blocks, int64_t blk,
+                     int g, int o, int i) {
+  int64_t idx = (((blk * G + g) * OR_BLOCK) + o) * (int64_t)d_v + i;
+  if (dtype != OR_FP8) return load_elem(v_pool, dtype, idx);
+  const uint8_t* codes = (const uint8_t*)v_pool;
+  const int8_t* exps = (const int8_t*)(codes + (int64_t)num_blocks * G * OR_BLOCK * d_v);
+  return ldexp(oracle_e4m3_to_double(codes[idx]), exps[(blk * G + g) * OR_BLOCK + o]);
 }
 
 static void store_elem(void* base, int dtype, int64_t idx, double v) {
@@ -110,6 +182,11 @@ static void store_elem(void* base, int dtype, int64_t idx, double v) {
 }
 
 static int elem_size(int dtype) { return dtype == OR_F32 ? 4 : 2; }
+
+/* Offset of the exponent of (blk, g, o) in an fp8 value pool (after all the codes). */
+int64_t oracle_fp8_exp_offset(int G, int d_v, int num_blocks, int64_t blk, int g, int o) {
+  return (int64_t)num_blocks * G * OR_BLOCK * d_v + (blk * G + g) * OR_BLOCK + o;
+}
 
 /* ------------------------------------------------------------------------------------ */
 /* Decoupled RoPE on the positional slice  [REV §3 Decoupled RoPE; EXP §位置信息怎么办]     */
@@ -188,10 +265,10 @@ int oracle_append(int dtype, int B, int n, int G, int d_v, int d_r, double base,
                   const void* v_new, const void* kr_new, const int32_t* pos,
                   const int32_t* block_table, int max_blocks, int num_blocks, void* v_pool,
                   void* kr_pool) {
-  if ((dtype != OR_F32 && dtype != OR_BF16) || B < 0 || n < 0 || G <= 0 || d_v <= 0 ||
-      d_r < 0 || (d_r % 2) != 0)
+  if ((dtype != OR_F32 && dtype != OR_BF16 && dtype != OR_FP8) || B < 0 || n < 0 || G <= 0 ||
+      d_v <= 0 || d_r < 0 || (d_r % 2) != 0)
     return OR_ERR_ARG;
-  int es = elem_size(dtype);
+  int es = elem_size(kr_dtype(dtype)); /* the fp8 cache takes its new values in bf16 */
   int status = OR_OK;
   double* x = (double*)malloc(sizeof(double) * (d_r > 0 ? d_r : 1));
   for (int b = 0; b < B; ++b) {
@@ -204,15 +281,32 @@ int oracle_append(int dtype, int B, int n, int G, int d_v, int d_r, double base,
       }
       int o = (int)(p % OR_BLOCK);
       for (int g = 0; g < G; ++g) {
-        const char* src = (const char*)v_new + ((((int64_t)b * n + t) * G + g) * d_v) * es;
-        char* dst = (char*)v_pool + oracle_v_offset(G, d_v, blk, g, o, 0) * es;
-        memcpy(dst, src, (size_t)d_v * es);
+        int64_t src_idx = (((int64_t)b * n + t) * G + g) * d_v;
+        if (dtype == OR_FP8) {
+          /* quantise the row: the scale exponent from its largest magnitude, then each value
+           * times 2^-e (exact) rounded once to E4M3 */
+          double amax = 0.0;
+          for (int i = 0; i < d_v; ++i) {
+            double v = fabs(load_elem(v_new, OR_BF16, src_idx + i));
+            if (v > amax) amax = v;
+          }
+          int e = oracle_fp8_exponent(amax);
+          uint8_t* codes = (uint8_t*)v_pool;
+          for (int i = 0; i < d_v; ++i)
+            codes[oracle_v_offset(G, d_v, blk, g, o, i)] =
+                oracle_double_to_e4m3(ldexp(load_elem(v_new, OR_BF16, src_idx + i), -e));
+          ((int8_t*)v_pool)[oracle_fp8_exp_offset(G, d_v, num_blocks, blk, g, o)] = (int8_t)e;
+        } else {
+          const char* src = (const char*)v_new + src_idx * es;
+          char* dst = (char*)v_pool + oracle_v_offset(G, d_v, blk, g, o, 0) * es;
+          memcpy(dst, src, (size_t)d_v * es);
+        }
       }
       for (int c = 0; c < d_r; ++c)
-        x[c] = load_elem(kr_new, dtype, ((int64_t)b * n + t) * d_r + c);
+        x[c] = load_elem(kr_new, kr_dtype(dtype), ((int64_t)b * n + t) * d_r + c);
       oracle_rope(x, d_r, (double)p, base, x);
       for (int c = 0; c < d_r; ++c)
-        store_elem(kr_pool, dtype, oracle_kr_offset(d_r, blk, o, c), x[c]);
+        store_elem(kr_pool, kr_dtype(dtype), oracle_kr_offset(d_r, blk, o, c), x[c]);
     }
   }
   free(x);
@@ -223,6 +317,13 @@ int oracle_append(int dtype, int B, int n, int G, int d_v, int d_r, double base,
  * [EXP §省下来的到底是多少]: (G*d_v + d_r) / (2*G*d_v). */
 double oracle_cache_ratio(int G, int d_v, int d_r) {
   return ((double)G * d_v + d_r) / (2.0 * G * d_v);
+}
+
+/* Persistent cache bytes per token per layer: values and positional key in the cache dtype;
+ * the fp8 cache holds G*d_v codes, G exponents and d_r bf16 key elements. */
+double oracle_cache_bytes_per_token(int dtype, int G, int d_v, int d_r) {
+  if (dtype == OR_FP8) return (double)G * d_v + G + 2.0 * d_r;
+  return (double)elem_size(dtype) * ((double)G * d_v + d_r);
 }
 
 /* ------------------------------------------------------------------------------------ */
@@ -249,9 +350,9 @@ static int partial_bh(int dtype, int H, int G, int d_v, int d_r, double scale,
     int o = (int)(j % OR_BLOCK);
     double content = 0.0, positional = 0.0;
     for (int i = 0; i < d_v; ++i)
-      content += qa[i] * load_elem(v_pool, dtype, oracle_v_offset(G, d_v, blk, g, o, i));
+      content += qa[i] * load_v(v_pool, dtype, G, d_v, num_blocks, blk, g, o, i);
     for (int c = 0; c < d_r; ++c)
-      positional += qr[c] * load_elem(kr_pool, dtype, oracle_kr_offset(d_r, blk, o, c));
+      positional += qr[c] * load_elem(kr_pool, kr_dtype(dtype), oracle_kr_offset(d_r, blk, o, c));
     s[j - j0] = scale * (content + positional);
   }
   double m = -INFINITY;
@@ -265,7 +366,7 @@ static int partial_bh(int dtype, int H, int G, int d_v, int d_r, double scale,
     int64_t blk = oracle_block_of(block_table, max_blocks, num_blocks, b, j);
     int o = (int)(j % OR_BLOCK);
     for (int i = 0; i < d_v; ++i)
-      u[i] += w * load_elem(v_pool, dtype, oracle_v_offset(G, d_v, blk, g, o, i));
+      u[i] += w * load_v(v_pool, dtype, G, d_v, num_blocks, blk, g, o, i);
   }
   free(s);
   *m_out = m;
@@ -428,7 +529,7 @@ int oracle_decode_unabsorbed(int dtype, int B, int H, int G, int d_v, int d_n, i
         int64_t blk = oracle_block_of(block_table, max_blocks, num_blocks, b, j);
         if (blk < 0) { status = OR_ERR_INDEX; break; }
         int o = (int)(j % OR_BLOCK);
-        for (int i = 0; i < d_v; ++i) v[i] = load_elem(v_pool, dtype, oracle_v_offset(G, d_v, blk, g, o, i));
+        for (int i = 0; i < d_v; ++i) v[i] = load_v(v_pool, dtype, G, d_v, num_blocks, blk, g, o, i);
         /* row vector k_c = v^T M_h, i.e. kc[k] = sum_i v[i] M_h[i][k] */
         for (int k = 0; k < d_n; ++k) {
           double acc = 0.0;
@@ -437,7 +538,8 @@ int oracle_decode_unabsorbed(int dtype, int B, int H, int G, int d_v, int d_n, i
         }
         double dot = 0.0;
         for (int k = 0; k < d_n; ++k) dot += qc[k] * kc[k];
-        for (int c = 0; c < d_r; ++c) dot += qrot[c] * load_elem(kr_pool, dtype, oracle_kr_offset(d_r, blk, o, c));
+        for (int c = 0; c < d_r; ++c)
+          dot += qrot[c] * load_elem(kr_pool, kr_dtype(dtype), oracle_kr_offset(d_r, blk, o, c));
         s[j] = sc * dot;
         if (s[j] > m) m = s[j];
       }
@@ -450,7 +552,7 @@ int oracle_decode_unabsorbed(int dtype, int B, int H, int G, int d_v, int d_n, i
         l += w;
         int64_t blk = oracle_block_of(block_table, max_blocks, num_blocks, b, j);
         int o = (int)(j % OR_BLOCK);
-        for (int i = 0; i < d_v; ++i) orow[i] += w * load_elem(v_pool, dtype, oracle_v_offset(G, d_v, blk, g, o, i));
+        for (int i = 0; i < d_v; ++i) orow[i] += w * load_v(v_pool, dtype, G, d_v, num_blocks, blk, g, o, i);
       }
       for (int i = 0; i < d_v; ++i) orow[i] /= l;
     }
@@ -471,7 +573,7 @@ int oracle_gqa_decode_one(int dtype, int H, int G, int d, double scale, const vo
                           const void* v_pool, const int32_t* block_table, int max_blocks,
                           int num_blocks, const int32_t* seq_lens, int b, int h, const double* q,
                           double* out_row) {
-  if (H <= 0 || G <= 0 || H % G != 0 || d <= 0) return OR_ERR_ARG;
+  if (H <= 0 || G <= 0 || H % G != 0 || d <= 0 || (dtype != OR_F32 && dtype != OR_BF16)) return OR_ERR_ARG;
   int64_t T = seq_lens[b];
   if (T <= 0) return OR_ERR_ARG;
   double sc = scale > 0.0 ? scale : 1.0 / sqrt((double)d);

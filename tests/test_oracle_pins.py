@@ -7,7 +7,10 @@ Each pin is chosen so that a plausible slip in the oracle fails it:
     torch's scaled_dot_product_attention (Shared KV = M_h = I with no positional slice,
     plain GQA, the key materialised from the page's K_h = V_g M_h);
   * head->group map, split-T invariance, ragged tails, the paged layout and the
-    cache-size closed form against the figures the pages print.
+    cache-size closed form against the figures the pages print;
+  * the fp8 value cache (a reading of this library's, not the pages'): torch's E4M3 format
+    on every code and on every tie, the scale exponent's closed form, the quantised append,
+    and decode over fp8 codes equal to decode over the values torch dequantises from them.
 """
 import math
 import os
@@ -435,3 +438,177 @@ def test_cache_ratio_equals_counted_pool_scalars(oracle_mod):
         used = int((vp != 0xFFFF).sum() + (kp != 0xFFFF).sum())
         gqa = 2 * G * d_v  # key and value rows for each of the G groups
         assert used / gqa == oracle_mod.cache_ratio(G, d_v, d_r)
+
+
+# ---------------------------------------------------------------- fp8 (E4M3) value cache
+#
+# Not on the pages: the library's low-precision value cache.  E4M3 codes (OCP FP8: 4 exponent
+# bits with bias 7, 3 mantissa bits, S.1111.111 = NaN, largest finite 448) with one
+# power-of-two scale 2^e per (token, group); e is the smallest integer with
+# max|v| <= 448 * 2^e (clamped to [-126, 120]); codes are v * 2^-e rounded once to nearest
+# even, saturating at 448.  torch's float8_e4m3fn pins the format; closed forms pin the rest.
+
+def e4m3_values_torch(codes):
+    return torch.tensor(np.asarray(codes, np.uint8)).view(torch.float8_e4m3fn).float().numpy().astype(np.float64)
+
+
+def e4m3_codes_torch(x):
+    return torch.tensor(np.asarray(x, np.float32)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+
+def test_e4m3_decode_matches_torch_on_every_code(oracle_mod):
+    codes = np.arange(256, dtype=np.uint8)
+    want = e4m3_values_torch(codes)
+    got = np.array([oracle_mod.e4m3_to_double(int(c)) for c in codes])
+    assert np.array_equal(np.isnan(got), np.isnan(want)) and np.isnan(got).sum() == 2  # 0x7F, 0xFF
+    ok = ~np.isnan(want)
+    assert np.array_equal(got[ok], want[ok])
+    assert got[0x7E] == 448.0 and got[0x08] == 2.0 ** -6 and got[0x01] == 2.0 ** -9 and got[0x38] == 1.0
+
+
+def test_e4m3_encode_matches_torch_in_range(oracle_mod):
+    rng = np.random.default_rng(8)
+    finite = e4m3_values_torch(np.arange(0, 0x7F, dtype=np.uint8))   # 0 .. 448, increasing
+    mids = (finite[:-1] + finite[1:]) / 2                                # every tie, exact in fp32
+    x = np.concatenate([rng.standard_normal(3000) * 40, rng.standard_normal(1000) * 2.0 ** -7,
+                        mids, -mids, finite, -finite, rng.uniform(-463.9, 463.9, 1000)]).astype(np.float32)
+    got = np.array([oracle_mod.double_to_e4m3(float(v)) for v in x], dtype=np.uint8)
+    assert np.array_equal(got, e4m3_codes_torch(x))
+
+
+def test_e4m3_ties_saturation_and_specials(oracle_mod):
+    enc = oracle_mod.double_to_e4m3
+    assert enc(1.0) == 0x38 and enc(1.0625) == 0x38 and enc(1.1875) == 0x3A    # ties to the even code
+    assert enc(2.0 ** -10) == 0x00 and enc(3 * 2.0 ** -11) == 0x01             # subnormal tie, round up
+    assert enc(15 * 2.0 ** -10) == 0x08                                         # subnormal rounds to 2^-6
+    assert enc(448.0) == 0x7E and enc(449.0) == 0x7E and enc(470.0) == 0x7E    # saturation, not NaN
+    assert enc(1e30) == 0x7E and enc(-1e30) == 0xFE and enc(float("inf")) == 0x7E
+    assert enc(float("nan")) == 0x7F and enc(0.0) == 0x00 and enc(-0.0) == 0x80
+
+
+def test_fp8_exponent_closed_form(oracle_mod):
+    e = oracle_mod.fp8_exponent
+    assert e(448.0) == 0 and e(450.0) == 1 and e(1.0) == -8 and e(0.875) == -9 and e(0.0) == -126
+    assert e(1e-40) == -126 and e(3.0e38) == 120
+    rng = np.random.default_rng(9)
+    for a in np.exp(rng.uniform(-80, 80, 2000)):
+        k = e(float(a))
+        assert 448.0 * 2.0 ** (k - 1) < a <= 448.0 * 2.0 ** k
+
+
+def test_fp8_append_quantises_each_row(oracle_mod):
+    """Each (token, group) row: the exponent from its largest magnitude, the codes torch's E4M3
+    rounding of v * 2^-e; untouched slots keep their sentinel bytes; keys rotate as in bf16."""
+    G, d_v, d_r, NB = 2, 64, 16, 3
+    rng = np.random.default_rng(10)
+    n = 70
+    scale = np.exp(rng.uniform(-6, 6, (1, n, G, 1)))                 # rows of very different sizes
+    v = (rng.standard_normal((1, n, G, d_v)) * scale).astype(np.float32)
+    v[0, 3, 1] = 0.0                                                   # an all-zero row
+    v_bits = bf16_bits(v)
+    kr = bf16_bits(rng.standard_normal((1, n, d_r)))
+    table = np.array([[2, 0]], np.int32)
+    vp = np.full(NB * G * 64 * (d_v + 1), 0xA5, np.uint8)
+    kp = np.full((NB, 64, d_r), 0xFFFF, np.uint16)
+    assert oracle_mod.append(v_bits, kr, [0], table, vp, kp) == 0
+    codes = vp[:NB * G * 64 * d_v].reshape(NB, G, 64, d_v)
+    exps = vp[NB * G * 64 * d_v:].view(np.int8).reshape(NB, G, 64)
+    vv = bits_to_f(v_bits)
+    for t in range(n):
+        blk, o = table[0, t // 64], t % 64
+        for g in range(G):
+            row = vv[0, t, g]
+            amax = np.abs(row).max()
+            k = -126 if amax == 0 else int(np.ceil(np.log2(amax / 448.0)))  # smallest k: amax <= 448 2^k
+            assert exps[blk, g, o] == k
+            assert oracle_mod.fp8_exp_offset(G, d_v, NB, blk, g, o) == NB * G * 64 * d_v + (blk * G + g) * 64 + o
+            assert np.array_equal(codes[blk, g, o], e4m3_codes_torch(np.ldexp(row, -k)))
+        # the positional key is the bf16 cache's: rotated at its position, rounded once
+        want = np.array([oracle_mod.double_to_bf16(x) for x in oracle_mod.rope(bits_to_f(kr[0, t]), t)], np.uint16)
+        assert np.array_equal(kp[blk, o], want)
+    used_rows = {(table[0, t // 64], t % 64) for t in range(n)}
+    for blk in range(NB):
+        for o in range(64):
+            if (blk, o) not in used_rows:
+                assert (codes[blk, :, o] == 0xA5).all() and (exps[blk, :, o] == np.int8(-91)).all()
+                assert (kp[blk, o] == 0xFFFF).all()
+
+
+def test_fp8_round_trip_error_within_half_a_code(oracle_mod):
+    """Dequantised values are within half an E4M3 spacing of the bf16 input, scaled by 2^e."""
+    G, d_v, d_r = 1, 128, 2
+    rng = np.random.default_rng(11)
+    v = (rng.standard_normal((1, 64, G, d_v)) * np.exp(rng.uniform(-4, 4, (1, 64, G, 1)))).astype(np.float32)
+    v_bits = bf16_bits(v)
+    vp = np.zeros(G * 64 * (d_v + 1), np.uint8)
+    kp = np.zeros((1, 64, d_r), np.uint16)
+    oracle_mod.append(v_bits, bf16_bits(np.zeros((1, 64, d_r))), [0], np.array([[0]]), vp, kp)
+    codes = vp[:64 * d_v].reshape(64, d_v)
+    exps = vp[64 * d_v:].view(np.int8)
+    x = bits_to_f(v_bits)[0, :, 0]
+    deq = e4m3_values_torch(codes) * np.exp2(exps.astype(np.float64))[:, None]
+    # spacing of E4M3 around |y| (y = x 2^-e): 2^(floor(log2|y|) - 3) for normals, 2^-9 below 2^-6
+    y = np.abs(x) * np.exp2(-exps.astype(np.float64))[:, None]
+    expo = np.floor(np.log2(np.maximum(y, 2.0 ** -6)))
+    half = 0.5 * np.exp2(expo - 3) * np.exp2(exps.astype(np.float64))[:, None]
+    assert (np.abs(deq - x) <= half).all()
+
+
+def fp8_pool(rng, NB, G, d_v, emin=-12, emax=2):
+    """Random fp8 value pool (no NaN codes) and the same values dequantised by torch into fp32."""
+    codes = rng.integers(0, 256, (NB, G, 64, d_v)).astype(np.uint8)
+    codes[(codes & 0x7F) == 0x7F] ^= 0x01                       # no NaN codes
+    exps = rng.integers(emin, emax + 1, (NB, G, 64)).astype(np.int8)
+    pool = np.concatenate([codes.reshape(-1), exps.view(np.uint8).reshape(-1)])
+    vals = torch.ldexp(torch.tensor(codes).view(torch.float8_e4m3fn).double(),
+                       torch.tensor(exps.astype(np.int64))[..., None].double())
+    return pool, vals.float().numpy()
+
+
+def test_fp8_decode_equals_decode_of_the_dequantised_values(oracle_mod):
+    """Decode over the fp8 pool equals decode over an fp32 pool holding the values torch
+    dequantises from the same codes and exponents (single-query, multi-query, unabsorbed)."""
+    rng = np.random.default_rng(12)
+    B, H, G, d_v, d_r = 3, 8, 2, 64, 16
+    lens = np.array([1, 70, 130], np.int32)
+    NB = 6
+    table = np.array([[4, -1, -1], [0, 2, -1], [5, 1, 3]], np.int32)
+    vp8, vp32 = fp8_pool(rng, NB, G, d_v)
+    kp = bf16_bits(rng.standard_normal((NB, 64, d_r)))
+    kp32 = bits_to_f(kp).astype(np.float32)
+    qa = rng.standard_normal((B, H, d_v)) * 0.05
+    qr = rng.standard_normal((B, H, d_r))
+    got = oracle_mod.decode(qa, qr, vp8, kp, table, lens, G=G)
+    want = oracle_mod.decode(qa, qr, vp32, kp32, table, lens, G=G)
+    assert np.abs(got - want).max() <= 1e-12 * max(1.0, np.abs(want).max())
+    qam = rng.standard_normal((B, 2, H, d_v)) * 0.05
+    qrm = rng.standard_normal((B, 2, H, d_r))
+    lens2 = np.maximum(lens, 2)
+    got = oracle_mod.decode_multi(qam, qrm, vp8, kp, table, lens2, G=G)
+    want = oracle_mod.decode_multi(qam, qrm, vp32, kp32, table, lens2, G=G)
+    assert np.abs(got - want).max() <= 1e-12 * max(1.0, np.abs(want).max())
+    q_c = rng.standard_normal((B, H, d_v))
+    q_r = rng.standard_normal((B, H, d_r))
+    M = rng.standard_normal((H, d_v, d_v)) / 8
+    pos = lens - 1
+    got = oracle_mod.decode_unabsorbed(q_c, q_r, pos, M, vp8, kp, table, lens, G=G)
+    want = oracle_mod.decode_unabsorbed(q_c, q_r, pos, M, vp32, kp32, table, lens, G=G)
+    assert np.abs(got - want).max() <= 1e-12 * max(1.0, np.abs(want).max())
+
+
+def test_fp8_cache_bytes_per_token_counted_from_the_pools(oracle_mod):
+    """Bytes one appended token occupies: G*d_v codes, G exponents and d_r bf16 key elements,
+    against the bf16 cache and the matching bf16 K+V cache."""
+    for G, d_v, d_r in [(4, 64, 16), (4, 64, 24), (8, 128, 24)]:
+        vp = np.full(G * 64 * (d_v + 1), 0xA5, np.uint8)
+        kp = np.full((1, 64, d_r), 0xFFFF, np.uint16)
+        v = bf16_bits(np.full((1, 1, G, d_v), 0.75))          # exponent -9, code 0x7C (384)
+        oracle_mod.append(v, bf16_bits(np.ones((1, 1, d_r))), [5], np.array([[0]]), vp, kp)
+        codes, exps = vp[:G * 64 * d_v].reshape(G, 64, d_v), vp[G * 64 * d_v:].reshape(G, 64)
+        used = int((codes[:, 5] != 0xA5).sum() + (exps[:, 5] != 0xA5).sum()) + 2 * int((kp[0, 5] != 0xFFFF).sum())
+        assert used == G * d_v + G + 2 * d_r == oracle_mod.cache_bytes_per_token("fp8", G, d_v, d_r)
+        assert oracle_mod.cache_bytes_per_token("bf16", G, d_v, d_r) == 2 * (G * d_v + d_r)
+        gqa = 2 * (2 * G * d_v)
+        assert (G * d_v + G + 2 * d_r) / gqa == pytest.approx((G * d_v + G + 2 * d_r) / (4 * G * d_v))
+    # long-context layer: 292 bytes per token against 544 (bf16 GVA) and 1024 (bf16 GQA)
+    assert oracle_mod.cache_bytes_per_token("fp8", 4, 64, 16) == 292
