@@ -153,6 +153,11 @@ struct StepInputs {
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// Bytes of E4M3 codes in an fp8 value pool of num_blocks blocks (its exponents follow them).
+size_t fp8_code_bytes(int num_blocks, const gva_dims& d) {
+  return static_cast<size_t>(num_blocks) * d.G * GVA_BLOCK_TOKENS * d.d_v;
+}
+
 // Bytes of the fused step's query stages for a plan: one per (range, segment) pair.
 size_t step_stage_bytes(const gva_ctx* ctx, int B, const gva::Plan& plan) {
   const gva_dims& d = ctx->dims;
@@ -223,6 +228,8 @@ gva_status decode_common(gva_ctx* ctx, bool sep_k, int phases, int B, const floa
   a.q_abs = q_abs;
   a.q_rot = sep_k ? nullptr : q_rot;
   a.v_pool = v_pool;
+  if (d.cache_dtype == GVA_FP8_E4M3 && v_pool)  // the exponents follow the codes
+    a.v_exp = static_cast<const signed char*>(v_pool) + fp8_code_bytes(num_blocks, d);
   a.k_pool = k_pool;
   a.kr_pool = sep_k ? nullptr : kr_pool;
   a.block_table = block_table;
@@ -252,6 +259,8 @@ gva_status decode_common(gva_ctx* ctx, bool sep_k, int phases, int B, const floa
     a.v_new = step->v_new;
     a.kr_new = step->kr_new;
     a.v_pool_w = step->v_pool;
+    if (d.cache_dtype == GVA_FP8_E4M3)
+      a.v_exp_w = static_cast<signed char*>(step->v_pool) + fp8_code_bytes(num_blocks, d);
     a.kr_pool_w = step->kr_pool;
     a.rope32 = ctx->d_rope32;
     a.qstage = reinterpret_cast<float*>(static_cast<char*>(workspace) + stage_off);
@@ -285,7 +294,8 @@ gva_status gva_create(const gva_dims* dims, gva_ctx** out) {
   if (d.H <= 0 || d.G <= 0 || d.H % d.G != 0 || d.d_v <= 0 || d.d_n <= 0 || d.d_r < 0 ||
       (d.d_r & 1) || d.d_v % 32 != 0 || d.d_n % 4 != 0 || d.block_size != GVA_BLOCK_TOKENS)
     return GVA_ERR_INVALID_ARG;
-  if (d.cache_dtype != GVA_F32 && d.cache_dtype != GVA_BF16) return GVA_ERR_INVALID_ARG;
+  if (d.cache_dtype != GVA_F32 && d.cache_dtype != GVA_BF16 && d.cache_dtype != GVA_FP8_E4M3)
+    return GVA_ERR_INVALID_ARG;
   if (d.d_r > 32) return GVA_ERR_UNSUPPORTED;
   if (!gva::fma_supported(d, false) && !gva::mma_supported(d, false) &&
       !(d.d_r == 0 && (gva::fma_supported(d, true) || gva::mma_supported(d, true))))

@@ -378,6 +378,7 @@ int fma_smem_bytes(const gva_dims& d, bool sep_k) {
 }  // namespace
 
 bool fma_supported(const gva_dims& d, bool sep_k) {
+  if (d.cache_dtype != GVA_F32 && d.cache_dtype != GVA_BF16) return false;  // fp8: tensor-core path only
   const int r = d.H / d.G;
   if (!(d.d_v == 32 || d.d_v == 64 || d.d_v == 128)) return false;
   if (!(r == 1 || r == 2 || r == 4 || r == 8)) return false;

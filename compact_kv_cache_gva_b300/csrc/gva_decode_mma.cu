@@ -1,910 +1,10 @@
-// gva_decode_mma.cu -- split-T decode attention over a bf16 GVA cache on the tensor cores.
-//
-// Same contract and partial records as the CUDA-core kernel (gva_decode_fma.cu): for head h
-// of value group g, s_j = scale * (q'_h . v_j + q~_r,h . k_r,j), online softmax, o_h =
-// sum_j p_j v_j (ai-feeds.com summary "Grouped Value Attention:通过按需 key 重建实现高效 KV
-// 缓存", section 方法; review "[논문리뷰] Grouped Value Attention", section 3).
-//
-// Per 64-token tile of group g, with the r = H/G heads of the group packed into the N=8
-// columns of a warp-level bf16 MMA (m16n8k16 / m16n8k8, fp32 accumulate):
-//   scores  S^T[64 tok x 8] = [V | k_r][64 x (d_v+d_r)] . [q'_hi | q'_lo]^T
-//   output  O^T[d_v x 8]   += V^T[d_v x 64] . [p_hi | p_lo][64 x 8]
-// Each head occupies two columns: its query (and later its probabilities) split into a
-// bf16 high part and a bf16 remainder, so both products keep about 16 significant bits
-// while using columns that the 4-head group would leave empty anyway.  The V tile arrives
-// by TMA (tensor copy, 128-byte swizzle) so that ldmatrix reads it without bank conflicts,
-// both as V (scores) and transposed as V^T (output); k_r arrives by a plain bulk copy.
-// Probabilities never leave registers: movmatrix turns the score fragment (tokens on rows)
-// into the B fragment of the output product (tokens on k).
-//
-// Work split (gva_sched.cuh): one CTA per SM streams a balanced range of (sequence, group,
-// tile) units with a few warp pairs: a copy warp keeps its consumer's private ring of tiles
-// full (TMA), and the consumer warps take the range's tiles round-robin, each writing one
-// partial record per (sequence, group) it touched.  The matching GQA form (a separate key cache, no positional
-// slice) reuses the kernel with the key tile scored instead of the value tile.
-//
-// Fused decode step (FUSED instances): the absorption q' = M_h q_c and the rotation of the
-// positional query (the neighbouring step of the decode path) run in the kernel's prologue
-// instead of a kernel of their own.  The consumer warps, and the warps the launch has to spare
-// beside the pairs, compute them for every (group, sequence) segment of the CTA's range while
-// the copy warps fill the rings.  Each output is an fp32 dot product in the absorb kernel's
-// summation order, so the results are bit-identical to it.  The new token of every sequence
-// (the last position of its context) is appended between the copy engine and the consumer:
-// the sequence's last tile lands on a barrier of its own, a patcher warp writes the value row
-// and the rotated positional key into the staged tile and into the cache, and only then hands
-// the tile to its consumer.
-#include <cuda.h>
-
-#include <algorithm>
-#include <type_traits>
-#include <math.h>
-
-#include "gva_device.cuh"
-#include "gva_internal.h"
-#include "gva_sched.cuh"
+// gva_decode_mma.cu -- the tensor-core decode kernel's bf16 instances, its plan (warp pairs and
+// ring depth) and the launch entry point; the kernel itself is in gva_decode_mma.cuh.
+#include "gva_decode_mma.cuh"
 
 namespace gva {
 namespace {
 
-constexpr int kMmaMaxThreads = 64 * kMmaMaxPairs;  // consumer warps + as many copy warps
-
-// Threads a kernel instance is compiled for: six warp pairs on the single-query d_v = 64
-// path, four elsewhere (d_v = 128 and several queries per pass hold twice the accumulators,
-// so they keep more registers per thread; five pairs at 320 threads squeezed the two-query
-// d_v = 64 instance from 194 to 168 registers and made it 11 % slower).
-__host__ __device__ constexpr int mma_max_threads(int dv, int nq) { return dv == 64 && nq == 1 ? 384 : 256; }
-constexpr int kSubTileBytes = kBlockTokens * 128;  // one [64 tokens][64 columns] bf16 swizzled box
-
-// ---- PTX wrappers ------------------------------------------------------------------------
-
-__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y,
-                                            uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_addr(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar))
-      : "memory");
-}
-
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(addr));
-}
-
-__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t (&r)[4]) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(addr));
-}
-
-__device__ __forceinline__ void ldsm_x2(uint32_t addr, uint32_t& r0, uint32_t& r1) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0, %1}, [%2];"
-               : "=r"(r0), "=r"(r1)
-               : "r"(addr));
-}
-
-__device__ __forceinline__ void mma_16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
-                                          uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
-      "{%8, %9}, {%0, %1, %2, %3};"
-      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
-__device__ __forceinline__ void mma_1688(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t b0) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k8.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5}, {%6}, "
-      "{%0, %1, %2, %3};"
-      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-      : "r"(a0), "r"(a1), "r"(b0));
-}
-
-// Asks L2 to fetch [p, p + bytes) (bytes <= kMaxWarmBytes), spread over every thread of the
-// grid: one 128-byte line per request.
-constexpr long long kMaxWarmBytes = 4ll << 20;
-__device__ __forceinline__ void warm_l2(const void* p, long long bytes) {
-  if (!p || bytes <= 0 || bytes > kMaxWarmBytes) return;
-  const char* base = static_cast<const char*>(p);
-  const long long lines = (bytes + 127) / 128;
-  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < lines;
-       i += static_cast<long long>(gridDim.x) * blockDim.x)
-    asm volatile("prefetch.global.L2 [%0];" ::"l"(base + i * 128));
-}
-
-__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
-  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
-               : "memory");
-}
-
-__device__ __forceinline__ void st_shared_u32(uint32_t addr, uint32_t v) {
-  asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
-}
-
-// Fused step: the new token (row o of block blk) into the staged tile of its group g -- its
-// value row at the 128-byte-swizzled place the tensor copy gives it, its rotated positional
-// key in the plain k_r tile -- and into the cache (the key from group 0 only: one per token).
-// Lanes below d_v/8 move the value row (16 bytes each), lanes below d_r/2 a key pair.
-template <int DV, int DR>
-__device__ __forceinline__ void write_new_token(uint32_t vbase, uint32_t krbase, int o, uint4 vnew, uint32_t knew,
-                                                long long blk, int g, int G, void* v_pool, void* kr_pool, int lane) {
-  if (lane < DV / 8) {
-    st_shared_v4(vbase + (lane >> 3) * kSubTileBytes + o * 128 + (((lane & 7) ^ (o & 7)) << 4), vnew);
-    reinterpret_cast<uint4*>(v_pool)[((blk * G + g) * kBlockTokens + o) * (DV / 8) + lane] = vnew;
-  }
-  if (DR > 0 && lane < DR / 2) {
-    st_shared_u32(krbase + o * (2 * DR) + 4 * lane, knew);
-    if (g == 0) reinterpret_cast<uint32_t*>(kr_pool)[(blk * kBlockTokens + o) * (DR / 2) + lane] = knew;
-  }
-}
-
-__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
-  uint32_t y;
-  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
-  return y;
-}
-
-// Packs two floats as bf16 (first in the low half).
-__device__ __forceinline__ uint32_t pack_bf16(float lo_half, float hi_half) {
-  const uint32_t a = __bfloat16_as_ushort(__float2bfloat16_rn(lo_half));
-  const uint32_t b = __bfloat16_as_ushort(__float2bfloat16_rn(hi_half));
-  return a | (b << 16);
-}
-
-// x = hi + lo with hi = bf16(x) and lo = bf16(x - hi); returns (hi, lo) packed.
-__device__ __forceinline__ uint32_t split_pack(float x) {
-  const __nv_bfloat16 hi = __float2bfloat16_rn(x);
-  const __nv_bfloat16 lo = __float2bfloat16_rn(x - __bfloat162float(hi));
-  return static_cast<uint32_t>(__bfloat16_as_ushort(hi)) |
-         (static_cast<uint32_t>(__bfloat16_as_ushort(lo)) << 16);
-}
-
-__device__ __forceinline__ float split_part(float x, int part) {
-  const __nv_bfloat16 hi = __float2bfloat16_rn(x);
-  return part == 0 ? __bfloat162float(hi) : x - __bfloat162float(hi);
-}
-
-// Zeroes the bf16 halves of a fragment register whose token index is >= nv.
-__device__ __forceinline__ uint32_t mask_pair(uint32_t v, int tok, int nv) {
-  const uint32_t lo = tok < nv ? 0x0000ffffu : 0u;
-  const uint32_t hi = tok + 1 < nv ? 0xffff0000u : 0u;
-  return v & (lo | hi);
-}
-
-template <int DV, int DR, bool SEPK>
-struct MmaLayout {
-  static constexpr int kSub = DV / 64;                        // 64-column swizzled boxes
-  static constexpr int kVBytes = kSub * kSubTileBytes;        // one operand tile
-  static constexpr int kOpBytes = kVBytes * (SEPK ? 2 : 1);   // operand tiles of a stage (1 KB multiple)
-  static constexpr int kKrBytes = SEPK ? 0 : kBlockTokens * DR * 2;
-  static constexpr int kTx = kOpBytes + kKrBytes;             // bytes landing per stage
-  static constexpr int kStageBytes = kOpBytes + kKrBytes;
-};
-
-// Shared memory: [alignment slack 1 KB][control 2 KB: full and empty mbarrier, valid length,
-// block id and (fused step) landing mbarrier of every stage][P*D operand tiles, 1 KB aligned
-// for the swizzled boxes][P*D k_r tiles][cum: B+1 ints].  Stage (c, slot) is index c*D + slot.
-constexpr int kMaxStages = 40;
-constexpr int kCtrlBytes = 2048;
-static_assert(kMaxStages * (3 * 8 + 4 + 4) <= kCtrlBytes, "control block");
-constexpr int kStepBatch = 16;  // fused step: segments whose absorbed queries a warp forms at once
-constexpr int kStepBarrier = 1;  // fused step: named barrier that ends the prologue
-constexpr int kLookupBarrier = 2;  // fused step: the copy warps' first block-table reads are out
-// dynamic shared memory per CTA: the 227 KB opt-in limit less 1 KB for the kernel's static
-// shared memory (the prefix scan's scratch, placed ahead of the 1 KB aligned dynamic block)
-constexpr int kSmemLimit = 226 * 1024;
-__host__ __device__ inline int cum_bytes(int B) { return ((B + 1) * 4 + 15) / 16 * 16; }
-inline int ring_fixed_bytes(int B) { return 1024 + kCtrlBytes + cum_bytes(B); }
-
-// One CTA streams one contiguous range of units (gva_sched.cuh) with P warp pairs.  Consumer
-// warp c (warps 0..P-1) takes units k = c, c + P, c + 2P, ... of the range; its d-th unit
-// lands in its private ring slot d % D.  Copy warp c (warp P + c) serves consumer c alone:
-// its lanes look up the block ids of the consumer's next 32 units at once, one batch ahead,
-// and lane 0 issues each unit's copies (TMA for the value (and key) tile, a bulk copy for
-// the positional-key tile) as soon as the consumer has released the slot.  Every barrier
-// has one waiter that waits in order (the consumer on "full", the copy warp on "empty"),
-// so phase parities are unambiguous, and about P*(D-1) tiles are in flight per SM while P
-// are being computed.  The copy warps take the issue work (a few hundred cycles per tile)
-// and the dependent block-table reads off the consumers' path.
-//
-// A FUSED launch adds E = (threads of the instance - 64*P)/32 prologue warps (warps 2P..2P+E-1)
-// that help form the queries; the first of them then stays as the patcher warp, the others
-// exit.  (The six-pair instance, d_v = 64 with d_r = 32, has none to spare: its consumers
-// append themselves.)
-template <int DV, int DR, int R, int NQ, bool CAUSAL, bool SEPK, bool FUSED>
-__global__ void __launch_bounds__(mma_max_threads(DV, NQ), 1) decode_mma_kernel(const DecodeArgs a,
-                                                                       const __grid_constant__ CUtensorMap tmv,
-                                                                       const __grid_constant__ CUtensorMap tmk) {
-  using L = MmaLayout<DV, DR, SEPK>;
-  constexpr int RQ = R * NQ;            // (query, head) column pairs of a group: c = i*R + h
-  constexpr int NT = (2 * RQ + 7) / 8;  // n-tiles of 8 columns (4 column pairs each)
-  constexpr int KSV = DV / 16;          // k16 steps over the value (key) columns
-  constexpr int KSR = DR / 16;          // k16 steps over the positional columns
-  constexpr bool KR8 = (DR % 16) != 0;  // one trailing k8 step
-  constexpr int MD = DV / 16;           // m16 tiles over d_v in the output product
-  static_assert(DR % 8 == 0, "positional width must be a multiple of 8 on this path");
-  static_assert(!SEPK || DR == 0, "the key-cache form has no positional slice");
-  static_assert(!FUSED || (NQ == 1 && !CAUSAL && !SEPK), "the fused step is single-query GVA decode");
-  constexpr int QS = step_stage_floats(R, DV, DR);  // floats of one staged segment (fused step)
-
-  extern __shared__ __align__(1024) unsigned char smem_raw[];
-  unsigned char* smem = reinterpret_cast<unsigned char*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  const int P = a.group_warps;  // warp pairs; blockDim.x == 64 * P, plus the prologue warps of a fused launch
-  const int D = a.n_stages;     // ring slots per pair
-  const int N = P * D;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem);
-  uint64_t* empty = full + kMaxStages;
-  int* nvs = reinterpret_cast<int*>(empty + kMaxStages);  // tokens from each stage's tile to the end (0 = skip)
-  int* blks = nvs + kMaxStages;                            // block id of each stage's tile (fused step)
-  // fused step: a sequence's last tile lands on landed[s] instead of full[s]; the patcher warp
-  // writes the new token into it and then completes full[s]
-  uint64_t* landed = reinterpret_cast<uint64_t*>(blks + kMaxStages);
-  // Fused instances with a spare warp (all but the six-pair one) give the append to it: the
-  // consumers' loop is then the plain kernel's.
-  constexpr bool kPatcher = FUSED && !(DV == 64 && DR == 32);
-  unsigned char* tiles = smem + kCtrlBytes;
-  unsigned char* krs = tiles + N * L::kOpBytes;
-  int* cum = reinterpret_cast<int*>(krs + N * L::kKrBytes);
-  // fused step: the shared memory past the ring, [lengths: B ints][query stages]
-  unsigned char* spare = reinterpret_cast<unsigned char*>(cum) + cum_bytes(a.B);
-  int* lens_s = FUSED && a.spare_smem >= cum_bytes(a.B) ? reinterpret_cast<int*>(spare) : nullptr;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < N; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
-      if (kPatcher) mbar_init(&landed[s], 1);
-    }
-    mbar_init_fence();
-  }
-  if (warp == P && lane == 0) {
-    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmv)) : "memory");
-    if (SEPK) asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmk)) : "memory");
-  }
-  // Everything below may read what earlier work in the stream wrote.
-  griddep_wait();
-  // The block table (and, for the fused step, the key maps) into L2 while the lengths are
-  // scanned: the first copies wait on table reads, and the cache stream of the previous call
-  // has evicted them.  (Both are device memory; the step's own inputs may be host memory.)
-  warm_l2(a.block_table, static_cast<long long>(a.B) * a.max_blocks * 4);
-  if constexpr (FUSED) warm_l2(a.M, static_cast<long long>(a.H) * DV * DV * 4);
-  build_prefix<kMmaMaxThreads>(a, cum, lens_s);  // ends with __syncthreads: the barriers are set up
-  griddep_launch_dependents();
-
-  const long long U = static_cast<long long>(a.G) * cum[a.B];
-  const long long u0 = range_begin(blockIdx.x, U, a.n_groups);
-  const int n = static_cast<int>(range_begin(blockIdx.x + 1, U, a.n_groups) - u0);
-  if (n <= 0) return;  // CTA-uniform; no CTA-wide barrier follows
-
-  // ------------------------------------------------------------------ fused-step prologue
-  // Absorbed and rotated queries of every segment f_lo + j of this range into stage j (in the
-  // spare shared memory when they all fit, else stage c + f of the workspace), with the new
-  // token's rotated positional key.  Work items: (32 rows of one head, up to kStepBatch
-  // segments of one group); the item's M rows stay in registers while its segments' queries
-  // stream past.  A thread's positional pairs are rotated while its first item's loads are in
-  // flight, so the prologue costs about one memory round trip.
-  long long f_lo = 0;       // first segment of the range
-  int nseg = 0;             // segments of the range
-  float* stage = nullptr;   // stage of segment f_lo
-  if constexpr (FUSED) {
-    const UnitCursor first = cursor_at(u0, cum, a.B, a.G);
-    const UnitCursor last = cursor_at(u0 + n - 1, cum, a.B, a.G);
-    f_lo = segment_of(first.g, first.b, a.B);
-    nseg = static_cast<int>(segment_of(last.g, last.b, a.B) - f_lo) + 1;
-    const long long stage_smem = lens_s ? a.spare_smem - cum_bytes(a.B) : 0;
-    stage = static_cast<long long>(nseg) * QS * 4 <= stage_smem
-                ? reinterpret_cast<float*>(spare + cum_bytes(a.B))
-                : a.qstage + (static_cast<long long>(blockIdx.x) + f_lo) * QS;
-  }
-  auto absorb_segments = [&](int pw, int npw) {
-    // The prologue's loads go out after the copy warps' first block-table reads, which the
-    // first tile copies wait for (measured: 2.5 % of the long-context step; waiting until the
-    // rings are primed, or not at all, was slower).
-    named_barrier_sync(kLookupBarrier, static_cast<int>(blockDim.x));
-    // positional pairs: R query pairs and the new key's pair per (segment, pair index)
-    auto rotate_pairs = [&]() {
-      if constexpr (DR > 0) {
-        constexpr int PR = DR / 2;
-        const int nrot = nseg * (R + 1) * PR;
-        for (int it = pw * 32 + lane; it < nrot; it += npw * 32) {
-          const int sg = it / ((R + 1) * PR);
-          const int rem = it - sg * (R + 1) * PR;
-          const int r = rem / PR, pi = rem - r * PR;
-          const long long f = f_lo + sg;
-          const int g = static_cast<int>(f / a.B);
-          const int b = static_cast<int>(f - static_cast<long long>(g) * a.B);
-          int T;
-          if (lens_s) {
-            T = lens_s[b];  // 0 when out of range
-          } else {
-            T = a.seq_lens[b];
-            if (T > a.max_seq_len) T = 0;
-          }
-          if (T < 1) continue;  // no tile of this sequence is streamed
-          const long long xoff = r < R ? (static_cast<long long>(b) * a.H + g * R + r) * DR + 2 * pi : 0;
-          float2 x = make_float2(0.f, 0.f);
-          uint32_t w = 0;
-          if (r < R)
-            x = *reinterpret_cast<const float2*>(a.q_r + xoff);
-          else
-            w = *reinterpret_cast<const uint32_t*>(static_cast<const __nv_bfloat16*>(a.kr_new) +
-                                                   static_cast<long long>(b) * DR + 2 * pi);
-          float c, sn;
-          rope_cos_sin_f32(a.rope32, PR, static_cast<long long>(T) - 1, pi, c, sn);
-          float* slot = stage + static_cast<long long>(sg) * QS;
-          if (r < R) {
-            float2 y;
-            rope_rotate_f32(x.x, x.y, c, sn, y.x, y.y);
-            *reinterpret_cast<float2*>(slot + r * (DV + DR) + DV + 2 * pi) = y;
-          } else {
-            float x0, x1, y0, y1;
-            bf16x2_to_float2(w, x0, x1);
-            rope_rotate_f32(x0, x1, c, sn, y0, y1);
-            reinterpret_cast<uint32_t*>(slot + R * (DV + DR))[pi] = pack_bf16(y0, y1);
-          }
-        }
-      }
-    };
-    bool rotated = false;
-    // q' rows: four lanes per row, lane e of the quad accumulating chunks c = e, e+4, ... (the
-    // absorb kernel's summation order), so a warp's loads are 64 contiguous bytes per row
-    constexpr int RB = R * DV / 32;  // 32-row blocks of the group's R*d_v query rows
-    constexpr int XC = DV / 16;      // chunks per lane per row
-    const int rq = lane >> 2, e = lane & 3;
-    int item0 = 0;                   // item number of (this batch, block 0)
-    for (int s0 = 0; s0 < nseg; item0 += RB) {
-      const long long f0 = f_lo + s0;
-      const int g = static_cast<int>(f0 / a.B);
-      const int b0 = static_cast<int>(f0 - static_cast<long long>(g) * a.B);
-      const int cnt = min(min(kStepBatch, nseg - s0), a.B - b0);  // segments of group g
-      for (int rb = ((pw - item0) % npw + npw) % npw; rb < RB; rb += npw) {
-        const int h = (rb * 32) / DV;
-        const int head = g * R + h;
-        // rows i0 + 8*rnd of head h, RP of the four rounds at a time (16 vectors of M in registers)
-        const int i0 = rb * 32 - h * DV + rq;
-        constexpr int RP = 256 / DV;
-#pragma unroll 1
-        for (int r0 = 0; r0 < 4; r0 += RP) {
-        float4 m4[RP][XC];
-#pragma unroll
-        for (int rnd = 0; rnd < RP; ++rnd) {
-          const float4* mrow =
-              reinterpret_cast<const float4*>(a.M + (static_cast<long long>(head) * DV + i0 + 8 * (r0 + rnd)) * DV);
-#pragma unroll
-          for (int x = 0; x < XC; ++x) m4[rnd][x] = __ldg(mrow + 4 * x + e);
-        }
-        auto load_qc = [&](int j, float4 (&q4)[XC]) {
-          const float4* qrow = reinterpret_cast<const float4*>(a.q_c + (static_cast<long long>(b0 + j) * a.H + head) * DV);
-#pragma unroll
-          for (int x = 0; x < XC; ++x) q4[x] = __ldg(qrow + 4 * x + e);
-        };
-        float4 qn[XC];  // the next segment's query chunks, loaded one segment ahead
-        load_qc(0, qn);
-        if (!rotated) {  // while the loads above are in flight
-          rotate_pairs();
-          rotated = true;
-        }
-        for (int j = 0; j < cnt; ++j) {
-          float4 q4[XC];
-#pragma unroll
-          for (int x = 0; x < XC; ++x) q4[x] = qn[x];
-          if (j + 1 < cnt) load_qc(j + 1, qn);
-#pragma unroll
-          for (int rnd = 0; rnd < RP; ++rnd) {
-            float acc = 0.f;
-#pragma unroll
-            for (int x = 0; x < XC; ++x) {
-              acc = fmaf(m4[rnd][x].x, q4[x].x, acc);
-              acc = fmaf(m4[rnd][x].y, q4[x].y, acc);
-              acc = fmaf(m4[rnd][x].z, q4[x].z, acc);
-              acc = fmaf(m4[rnd][x].w, q4[x].w, acc);
-            }
-            acc += __shfl_xor_sync(kFullMask, acc, 1);  // p0 + p1, p2 + p3
-            acc += __shfl_xor_sync(kFullMask, acc, 2);  // (p0 + p1) + (p2 + p3)
-            if (e == 0) stage[static_cast<long long>(s0 + j) * QS + h * (DV + DR) + i0 + 8 * (r0 + rnd)] = acc;
-          }
-        }
-        }
-      }
-      s0 += cnt;
-    }
-    if (!rotated) rotate_pairs();
-  };
-  if constexpr (FUSED) {
-    const int E = static_cast<int>(blockDim.x / 32) - 2 * P;  // prologue-only warps
-    if (warp >= 2 * P) {
-      absorb_segments(P + (warp - 2 * P), P + E);
-      if (!kPatcher || warp != 2 * P) {
-        asm volatile("bar.arrive %0, %1;" ::"r"(kStepBarrier), "r"(32 * (P + E)) : "memory");
-        return;
-      }
-      // ---------------------------------------------------------------- patcher warp
-      // For every sequence whose last tile lies in this range (in unit order, which is each
-      // copy warp's issue order): wait for the tile to land, write the new token's value row
-      // and rotated positional key into it and into the cache, then hand it to its consumer.
-      named_barrier_sync(kStepBarrier, 32 * (P + E));  // the rotated keys are staged
-      const long long tot = cum[a.B];
-      unsigned long long parity = 0;  // bit s: phase parity of landed[s]
-      for (int j = 0; j < nseg; ++j) {
-        const long long f = f_lo + j;
-        const int g = static_cast<int>(f / a.B);
-        const int b = static_cast<int>(f - static_cast<long long>(g) * a.B);
-        if (cum[b + 1] == cum[b]) continue;  // no tile (or an out-of-range length)
-        const long long kl = static_cast<long long>(g) * tot + cum[b + 1] - 1 - u0;  // its last unit
-        if (kl < 0 || kl >= n) continue;  // in another range
-        // the copy warp skips a tile whose block it cannot resolve (and completes full[s] itself)
-        const int t_last = cum[b + 1] - cum[b] - 1;
-        if (t_last >= a.max_blocks) continue;
-        const int id = a.block_table[static_cast<long long>(b) * a.max_blocks + t_last];
-        if (id < 0 || id >= a.num_blocks) continue;
-        const int w = static_cast<int>(kl % P), d = static_cast<int>(kl / P);
-        const int s = w * D + d % D;
-        uint4 vnew = make_uint4(0, 0, 0, 0);
-        uint32_t knew = 0;
-        if (lane < DV / 8)
-          vnew = __ldg(reinterpret_cast<const uint4*>(a.v_new) + (static_cast<long long>(b) * a.G + g) * (DV / 8) + lane);
-        if (DR > 0 && lane < DR / 2) knew = reinterpret_cast<const uint32_t*>(stage + static_cast<long long>(j) * QS + R * (DV + DR))[lane];
-        const bool got = mbar_wait_bounded(&landed[s], static_cast<uint32_t>((parity >> s) & 1));
-        parity ^= 1ull << s;
-        if (!__all_sync(kFullMask, got)) {
-          if (lane == 0) flag_error(a.err, GVA_DEVERR_TIMEOUT);
-        } else {
-          const int nrem = nvs[s];
-          if (nrem > 0)
-            write_new_token<DV, DR>(smem_addr(tiles + s * L::kOpBytes), smem_addr(krs + s * L::kKrBytes), nrem - 1,
-                                    vnew, knew, blks[s], g, a.G, a.v_pool_w, a.kr_pool_w, lane);
-        }
-        fence_proxy_async_smem();  // these writes come before the copy engine refills the stage
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&full[s]);  // the consumer may read the tile
-      }
-      return;
-    }
-  }
-
-  // ------------------------------------------------------------------ copy warps
-  if (warp >= P) {
-    const int c = warp - P;                        // the consumer this warp serves
-    const int n_mine = n > c ? (n - c + P - 1) / P : 0;  // its units: k = c + P*d, d < n_mine
-    // lane i: block id (or -1), group and valid tokens of the consumer's unit d0 + i
-    auto lookup = [&](int d0, int& blk, int& grp, int& nv) {
-      blk = -1;
-      grp = 0;
-      nv = 0;
-      const int d = d0 + lane;
-      if (d < n_mine) {
-        const UnitCursor cu = cursor_at(u0 + c + static_cast<long long>(P) * d, cum, a.B, a.G);
-        grp = cu.g;
-        const int T = a.seq_lens[cu.b];  // issued beside the table read: one round trip
-        if (cu.t >= a.max_blocks) {
-          flag_error(a.err, GVA_DEVERR_POSITION);
-        } else {
-          const int id = a.block_table[static_cast<long long>(cu.b) * a.max_blocks + cu.t];
-          if (id >= 0 && id < a.num_blocks) {
-            blk = id;
-            nv = T - cu.t * kBlockTokens;  // tokens from the tile's start to the end (>= 1)
-          } else {
-            flag_error(a.err, GVA_DEVERR_BLOCK_ID);
-          }
-        }
-      }
-    };
-    int blk, grp, nv;
-    lookup(0, blk, grp, nv);
-    if constexpr (FUSED) asm volatile("bar.arrive %0, %1;" ::"r"(kLookupBarrier), "r"(static_cast<int>(blockDim.x)) : "memory");
-    int slot = 0, ph = 0, issued = 0;
-    bool ok = true;
-    for (int d0 = 0; d0 < n_mine && ok; d0 += 32) {
-      int nblk, ngrp, nnv;
-      lookup(d0 + 32, nblk, ngrp, nnv);  // next batch: loads in flight while this one issues
-      const int cnt = min(32, n_mine - d0);
-      for (int j = 0; j < cnt; ++j) {
-        const int bj = __shfl_sync(kFullMask, blk, j);
-        const int gj = __shfl_sync(kFullMask, grp, j);
-        const int vj = __shfl_sync(kFullMask, nv, j);
-        if (lane == 0) {
-          const int s = c * D + slot;
-          // the slot's previous unit must have been released by the consumer
-          if (d0 + j >= D && !mbar_wait_bounded(&empty[s], ph ^ 1)) ok = false;
-          if (ok) {
-            nvs[s] = bj >= 0 ? vj : 0;  // published by the arrive below (release)
-            if (FUSED) blks[s] = bj;
-            if (bj >= 0) {
-              // fused step: a sequence's last tile goes to the patcher before the consumer
-              uint64_t* bar = kPatcher && vj <= kBlockTokens ? &landed[s] : &full[s];
-              mbar_arrive_expect_tx(bar, L::kTx);
-              unsigned char* st = tiles + s * L::kOpBytes;
-              const int y = (bj * a.G + gj) * kBlockTokens;
-#pragma unroll
-              for (int sub = 0; sub < L::kSub; ++sub) {
-                tma_load_2d(st + sub * kSubTileBytes, &tmv, 64 * sub, y, bar);
-                if (SEPK) tma_load_2d(st + L::kVBytes + sub * kSubTileBytes, &tmk, 64 * sub, y, bar);
-              }
-              if (!SEPK && DR > 0)
-                bulk_g2s(krs + s * L::kKrBytes,
-                         static_cast<const __nv_bfloat16*>(a.kr_pool) + static_cast<size_t>(bj) * kBlockTokens * DR,
-                         L::kKrBytes, bar);
-            } else {
-              mbar_arrive(&full[s]);  // completes the phase with no data; the tile is skipped
-            }
-            ++issued;
-          }
-        }
-        ok = __shfl_sync(kFullMask, ok, 0);
-        if (!ok) break;
-        if (++slot == D) {
-          slot = 0;
-          ph ^= 1;
-        }
-      }
-      blk = nblk;
-      grp = ngrp;
-      nv = nnv;
-    }
-    if (lane == 0) {
-      if (!ok) flag_error(a.err, GVA_DEVERR_TIMEOUT);
-      // no copy may still be landing in shared memory when the CTA exits
-      for (int d = max(0, issued - D); d < issued; ++d)
-        if (!mbar_wait_bounded(&full[c * D + d % D], (d / D) & 1)) flag_error(a.err, GVA_DEVERR_TIMEOUT);
-    }
-    return;
-  }
-
-  // ------------------------------------------------------------------ consumer warps
-  if constexpr (FUSED) {
-    const int E = static_cast<int>(blockDim.x / 32) - 2 * P;
-    absorb_segments(warp, P + E);
-    named_barrier_sync(kStepBarrier, 32 * (P + E));  // every stage of the range is written
-  }
-  const int NC = P;  // consumer warps sharing the range
-  int k = warp;
-  if (k >= n) return;
-  float* recs = a.part + header_bytes(a.B) / 4;
-  constexpr int rec_floats = DV + 4;
-  UnitCursor cc = cursor_at(u0 + k, cum, a.B, a.G);
-  int slot = 0, ph = 0;  // ring slot and phase parity of this warp's next unit
-
-  // query fragments (B operand of the score product) of the current (b, g), pre-scaled by
-  // scale*log2(e); column n = 2*c + part for column pair c = i*R + h (query q0 + i of this
-  // pass, head h of the group), part 0 = bf16(q), part 1 = bf16 remainder.
-  uint32_t qb[NT][KSV + KSR][2];
-  uint32_t qt[NT];
-  uint4 vnew = make_uint4(0, 0, 0, 0);  // fused step: a 16-byte piece of the new value row
-  uint32_t knew = 0;                    // fused step: a pair of the new rotated positional key
-  auto load_q = [&](int b, int g) {
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      const int cp = nt * 4 + ((lane >> 2) >> 1), part = (lane >> 2) & 1;
-      const int tq = lane & 3;
-      const bool valid = cp < RQ;
-      const int qi = valid ? cp / R : 0, head = valid ? cp % R : 0;
-      const long long row = (static_cast<long long>(b) * a.nq + a.q0 + qi) * a.H + g * R + head;
-      const float* qa = FUSED ? stage + (segment_of(g, b, a.B) - f_lo) * QS + head * (DV + DR) : a.q_abs + row * DV;
-      const float* qr = FUSED ? qa + DV : a.q_rot + row * DR;
-      auto qv = [&](int kk) -> float {
-        if (!valid) return 0.f;
-        const float x = (kk < DV ? qa[kk] : qr[kk - DV]) * a.scale_log2;
-        return split_part(x, part);
-      };
-#pragma unroll
-      for (int ks = 0; ks < KSV + KSR; ++ks) {
-        const int k0 = 16 * ks + 2 * tq;
-        qb[nt][ks][0] = pack_bf16(qv(k0), qv(k0 + 1));
-        qb[nt][ks][1] = pack_bf16(qv(k0 + 8), qv(k0 + 9));
-      }
-      if (KR8) {
-        const int k0 = 16 * (KSV + KSR) + 2 * tq;
-        qt[nt] = pack_bf16(qv(k0), qv(k0 + 1));
-      }
-    }
-    if constexpr (FUSED && !kPatcher) {  // the new token's row, in case this warp meets the segment's last tile
-      if (lane < DV / 8)
-        vnew = __ldg(reinterpret_cast<const uint4*>(a.v_new) + (static_cast<long long>(b) * a.G + g) * (DV / 8) + lane);
-      if (DR > 0 && lane < DR / 2)
-        knew = reinterpret_cast<const uint32_t*>(stage + (segment_of(g, b, a.B) - f_lo) * QS + R * (DV + DR))[lane];
-    }
-  };
-
-  float m[NT], l[NT], o[NT][MD][4];
-  auto reset_state = [&]() {
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      m[nt] = -INFINITY;
-      l[nt] = 0.f;
-#pragma unroll
-      for (int md = 0; md < MD; ++md)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) o[nt][md][e] = 0.f;
-    }
-  };
-  const int gid = lane >> 2, tq = lane & 3;
-  // Partial record of segment f for this warp: per column pair (m, l, 0, 0, o[0..DV)).
-  auto flush = [&](long long f) {
-    float* rec = recs + ((static_cast<long long>(blockIdx.x) + f) * NC + warp) * RQ * rec_floats;
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      float lt = l[nt];
-      lt += __shfl_xor_sync(kFullMask, lt, 4);
-      lt += __shfl_xor_sync(kFullMask, lt, 8);
-      lt += __shfl_xor_sync(kFullMask, lt, 16);
-      const int cp = nt * 4 + tq;
-      if (cp < RQ) {
-        float* r = rec + cp * rec_floats;
-        if (gid == 0) {
-          r[0] = m[nt];
-          r[1] = lt;
-        }
-#pragma unroll
-        for (int md = 0; md < MD; ++md) {
-          r[4 + 16 * md + gid] = o[nt][md][0] + o[nt][md][1];
-          r[4 + 16 * md + gid + 8] = o[nt][md][2] + o[nt][md][3];
-        }
-      }
-    }
-  };
-
-  // lane-dependent parts of the ldmatrix addresses
-  const int ld_row = (lane & 7) + ((lane >> 3) & 1) * 8;  // non-transposed: row within m16
-  const int ld_kc = lane >> 4;                             // non-transposed: 8-column chunk
-  const int tr_tok = (lane & 7) + ((lane >> 4) & 1) * 8;   // transposed: token within k16
-  const int tr_dc = (lane >> 3) & 1;                       // transposed: 8-column chunk
-
-  reset_state();
-  load_q(cc.b, cc.g);
-  bool ok = true;
-  while (true) {
-    const int s = warp * D + slot;
-    const bool got = mbar_wait_bounded(&full[s], ph);
-    if (!__all_sync(kFullMask, got)) {
-      ok = false;
-      break;
-    }
-    const int nrem = nvs[s];
-    bool patched = false;
-    if (nrem > 0) {
-      const int nv = min(nrem, kBlockTokens);  // valid tokens of the tile
-      const uint32_t vbase = smem_addr(tiles + s * L::kOpBytes);
-      const uint32_t kbase = SEPK ? vbase + L::kVBytes : vbase;  // tile that is scored
-      const uint32_t krbase = smem_addr(krs + s * L::kKrBytes);
-      if constexpr (FUSED && !kPatcher) {
-        if (nrem <= kBlockTokens) {  // the sequence's last tile: the new token is row nrem - 1
-          write_new_token<DV, DR>(vbase, krbase, nrem - 1, vnew, knew, blks[s], cc.g, a.G, a.v_pool_w, a.kr_pool_w,
-                                  lane);
-          patched = true;
-          __syncwarp();
-        }
-      }
-
-      // scores
-      float sc[NT][4][4];
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-        for (int mt = 0; mt < 4; ++mt)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) sc[nt][mt][e] = 0.f;
-#pragma unroll
-      for (int mt = 0; mt < 4; ++mt) {
-        const int row = 16 * mt + ld_row;
-#pragma unroll
-        for (int ks = 0; ks < KSV; ++ks) {
-          const int kc = 2 * ks + ld_kc;
-          const uint32_t addr = kbase + (kc >> 3) * kSubTileBytes + row * 128 + (((kc & 7) ^ (row & 7)) << 4);
-          uint32_t af[4];
-          ldsm_x4(addr, af);
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt) mma_16816(sc[nt][mt], af, qb[nt][ks][0], qb[nt][ks][1]);
-        }
-#pragma unroll
-        for (int ks = 0; ks < KSR; ++ks) {
-          uint32_t af[4];
-          ldsm_x4(krbase + row * (2 * DR) + (2 * ks + ld_kc) * 16, af);
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt) mma_16816(sc[nt][mt], af, qb[nt][KSV + ks][0], qb[nt][KSV + ks][1]);
-        }
-        if (KR8) {
-          uint32_t a0, a1;
-          ldsm_x2(krbase + row * (2 * DR) + (2 * KSR) * 16, a0, a1);
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt) mma_1688(sc[nt][mt], a0, a1, qt[nt]);
-        }
-      }
-
-      // online softmax (log2 domain); thread holds column pair c = nt*4 + tq (query q0 + c/R,
-      // head c%R) for tokens 16*mt + gid and 16*mt + gid + 8.  Query q of nq reads positions
-      // up to T - nq + q: in this tile, tokens j < nrem - (nq - 1 - q).  Most tiles are seen
-      // whole by every query of the pass (the earliest one is q0) and take the unmasked form;
-      // the masked form also keeps the state of a query that sees no token of the tile (its
-      // position precedes the tile) unchanged.
-      uint32_t pb[NT][4][2];
-      auto softmax = [&](auto masked) {
-        constexpr bool kMasked = decltype(masked)::value;
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          float sv[4][2];
-          float mx = -INFINITY;
-          if constexpr (kMasked) {
-            const int cp = nt * 4 + tq;
-            const int lim = min(nv, nrem - (a.nq - 1 - (a.q0 + (cp < RQ ? cp / R : 0))));
-#pragma unroll
-            for (int mt = 0; mt < 4; ++mt) {
-              const int j0 = 16 * mt + gid;
-              sv[mt][0] = j0 < lim ? sc[nt][mt][0] + sc[nt][mt][1] : -INFINITY;
-              sv[mt][1] = j0 + 8 < lim ? sc[nt][mt][2] + sc[nt][mt][3] : -INFINITY;
-              mx = fmaxf(mx, fmaxf(sv[mt][0], sv[mt][1]));
-            }
-          } else {
-#pragma unroll
-            for (int mt = 0; mt < 4; ++mt) {
-              sv[mt][0] = sc[nt][mt][0] + sc[nt][mt][1];
-              sv[mt][1] = sc[nt][mt][2] + sc[nt][mt][3];
-              mx = fmaxf(mx, fmaxf(sv[mt][0], sv[mt][1]));
-            }
-          }
-          mx = fmaxf(mx, __shfl_xor_sync(kFullMask, mx, 4));
-          mx = fmaxf(mx, __shfl_xor_sync(kFullMask, mx, 8));
-          mx = fmaxf(mx, __shfl_xor_sync(kFullMask, mx, 16));
-          const float mn = fmaxf(m[nt], mx);
-          const bool none = kMasked && mn == -INFINITY;
-          const float alpha = none ? 1.f : exp2f(m[nt] - mn);
-          m[nt] = mn;
-          float ps = 0.f;
-#pragma unroll
-          for (int mt = 0; mt < 4; ++mt) {
-            const float p0 = none ? 0.f : exp2f(sv[mt][0] - mn);
-            const float p1 = none ? 0.f : exp2f(sv[mt][1] - mn);
-            ps += p0 + p1;
-            pb[nt][mt][0] = movmatrix_trans(split_pack(p0));
-            pb[nt][mt][1] = movmatrix_trans(split_pack(p1));
-          }
-          l[nt] = fmaf(l[nt], alpha, ps);
-#pragma unroll
-          for (int md = 0; md < MD; ++md)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) o[nt][md][e] *= alpha;
-        }
-      };
-      if constexpr (!CAUSAL) {
-        // one query per sequence at its last position: only the tokens past the end of the
-        // context are masked
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          float sv[4][2];
-          float mx = -INFINITY;
-#pragma unroll
-          for (int mt = 0; mt < 4; ++mt) {
-            const int j0 = 16 * mt + gid;
-            sv[mt][0] = j0 < nv ? sc[nt][mt][0] + sc[nt][mt][1] : -INFINITY;
-            sv[mt][1] = j0 + 8 < nv ? sc[nt][mt][2] + sc[nt][mt][3] : -INFINITY;
-            mx = fmaxf(mx, fmaxf(sv[mt][0], sv[mt][1]));
-          }
-          mx = fmaxf(mx, __shfl_xor_sync(kFullMask, mx, 4));
-          mx = fmaxf(mx, __shfl_xor_sync(kFullMask, mx, 8));
-          mx = fmaxf(mx, __shfl_xor_sync(kFullMask, mx, 16));
-          const float mn = fmaxf(m[nt], mx);
-          const float alpha = exp2f(m[nt] - mn);
-          m[nt] = mn;
-          float ps = 0.f;
-#pragma unroll
-          for (int mt = 0; mt < 4; ++mt) {
-            const float p0 = exp2f(sv[mt][0] - mn);
-            const float p1 = exp2f(sv[mt][1] - mn);
-            ps += p0 + p1;
-            pb[nt][mt][0] = movmatrix_trans(split_pack(p0));
-            pb[nt][mt][1] = movmatrix_trans(split_pack(p1));
-          }
-          l[nt] = fmaf(l[nt], alpha, ps);
-#pragma unroll
-          for (int md = 0; md < MD; ++md)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) o[nt][md][e] *= alpha;
-        }
-      } else if (nrem - (a.nq - 1 - a.q0) >= kBlockTokens) {
-        softmax(std::false_type{});
-      } else {
-        softmax(std::true_type{});
-      }
-
-      // output: O^T[d x n] += V^T[d x tok] P[tok x n]
-#pragma unroll
-      for (int kt = 0; kt < 4; ++kt) {
-        const int tok = 16 * kt + tr_tok;
-        const int jt = 16 * kt + 2 * tq;  // tokens of this thread's A-fragment halves
-#pragma unroll
-        for (int md = 0; md < MD; ++md) {
-          const int dc = 2 * md + tr_dc;
-          const uint32_t addr = vbase + (dc >> 3) * kSubTileBytes + tok * 128 + (((dc & 7) ^ (tok & 7)) << 4);
-          uint32_t af[4];
-          ldsm_x4_trans(addr, af);
-          if (nv < kBlockTokens) {  // slots past the context may hold anything: zero them
-            af[0] = mask_pair(af[0], jt, nv);
-            af[1] = mask_pair(af[1], jt, nv);
-            af[2] = mask_pair(af[2], jt + 8, nv);
-            af[3] = mask_pair(af[3], jt + 8, nv);
-          }
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt) mma_16816(o[nt][md], af, pb[nt][kt][0], pb[nt][kt][1]);
-        }
-      }
-    }
-    // the stage may be refilled (after this warp's own writes into it, if any, are ordered
-    // before the copy engine's)
-    if (FUSED && !kPatcher && patched) fence_proxy_async_smem();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[s]);
-    k += NC;
-    if (k >= n) break;
-    const int pb_ = cc.b, pg = cc.g;
-    cursor_advance(cc, NC, cum, a.B, a.G);
-    if (cc.b != pb_ || cc.g != pg) {  // segment boundary: emit, start the next (b, g)
-      flush(segment_of(pg, pb_, a.B));
-      reset_state();
-      load_q(cc.b, cc.g);
-    }
-    if (++slot == D) {
-      slot = 0;
-      ph ^= 1;
-    }
-  }
-  if (ok) {
-    flush(segment_of(cc.g, cc.b, a.B));
-    return;
-  }
-  // A copy never arrived: report, and leave empty records for every segment still owed so
-  // the combine reads defined values.  (The copy warp waits for its copies in flight.)
-  if (lane == 0) flag_error(a.err, GVA_DEVERR_TIMEOUT);
-  reset_state();
-  flush(segment_of(cc.g, cc.b, a.B));
-  for (k += NC; k < n; k += NC) {
-    const int pb_ = cc.b, pg = cc.g;
-    cursor_advance(cc, NC, cum, a.B, a.G);
-    if (cc.b != pb_ || cc.g != pg) flush(segment_of(cc.g, cc.b, a.B));
-  }
-}
-
-template <int DV, int DR, int R, int NQ, bool CAUSAL, bool SEPK, bool FUSED>
-cudaError_t launch_mma_t(const DecodeArgs& a, const CUtensorMap& mv, const CUtensorMap& mk, int grid,
-                         cudaStream_t stream) {
-  using L = MmaLayout<DV, DR, SEPK>;
-  const int P = a.group_warps, D = a.n_stages;
-  if (P < 1 || 64 * P > mma_max_threads(DV, NQ) || D < 1 || P * D > kMaxStages) return cudaErrorInvalidValue;
-  if (a.nqp != NQ || (a.nq > 1) != CAUSAL || (a.fused != 0) != FUSED) return cudaErrorInvalidValue;
-  const int smem = ring_fixed_bytes(a.B) + P * D * L::kStageBytes;
-  if (smem > kSmemLimit) return cudaErrorInvalidValue;
-  // the fused step fills the instance's thread budget with prologue warps, and the shared
-  // memory budget with query stages; its patcher warp is the first prologue warp
-  const int threads = FUSED ? mma_max_threads(DV, NQ) : 64 * P;
-  if (FUSED && !(DV == 64 && DR == 32) && threads <= 64 * P) return cudaErrorInvalidValue;
-  DecodeArgs args = a;
-  args.spare_smem = FUSED ? kSmemLimit - smem : 0;
-  const int dyn_smem = FUSED ? kSmemLimit : smem;
-  auto kern = decode_mma_kernel<DV, DR, R, NQ, CAUSAL, SEPK, FUSED>;
-  static int configured[kMaxDevices] = {};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev >= kMaxDevices || !configured[dev]) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
-    if (e != cudaSuccess) return e;
-    if (dev < kMaxDevices) configured[dev] = 1;
-  }
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(threads);
-  cfg.dynamicSmemBytes = dyn_smem;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, args, mv, mk);
-}
-
-// Queries per pass: the instances built are NQ in {1, 2, 4} with R*NQ <= 8.
 template <int DV, int DR, int R, bool SEPK>
 cudaError_t dispatch_nq(const DecodeArgs& a, const CUtensorMap& mv, const CUtensorMap& mk, int grid,
                         cudaStream_t stream) {
@@ -951,25 +51,6 @@ cudaError_t dispatch_dr(const DecodeArgs& a, const CUtensorMap& mv, const CUtens
 }
 
 // cuTensorMapEncodeTiled through the runtime's driver entry point (no libcuda link).
-using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  if (!fn) {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(p);
-  }
-  return fn;
-}
-
-// A pool seen as a 2-D bf16 tensor: rows = NB*G*64 token rows of d_v columns; one box = 64
 // columns x 64 rows, swizzled in 128-byte rows.
 bool make_pool_map(CUtensorMap* map, const void* pool, int num_blocks, int G, int d_v) {
   EncodeTiledFn fn = encode_fn();
@@ -987,7 +68,7 @@ bool make_pool_map(CUtensorMap* map, const void* pool, int num_blocks, int G, in
 }  // namespace
 
 bool mma_supported(const gva_dims& d, bool sep_k) {
-  if (d.cache_dtype != GVA_BF16) return false;
+  if (d.cache_dtype != GVA_BF16 && !(d.cache_dtype == GVA_FP8_E4M3 && !sep_k)) return false;
   if (!(d.d_v == 64 || d.d_v == 128)) return false;
   if (sep_k) {
     if (d.d_r != 0) return false;
@@ -1007,13 +88,18 @@ bool mma_supported(const gva_dims& d, bool sep_k) {
 int mma_max_queries_per_pass(int R) { return R <= 2 ? 4 : R == 4 ? 2 : 1; }
 
 bool mma_shape(const gva_dims& d, bool sep_k, int B, int nqp, int* pairs, int* stages) {
-  const int op = (d.d_v / 64) * kSubTileBytes * (sep_k ? 2 : 1);
-  const int stage = op + (sep_k ? 0 : kBlockTokens * d.d_r * 2);
+  const bool f8 = d.cache_dtype == GVA_FP8_E4M3;
+  if (f8 && (sep_k || nqp > 1)) return false;
+  const int op = f8 ? kBlockTokens * d.d_v : (d.d_v / 64) * kSubTileBytes * (sep_k ? 2 : 1);
+  const int stage = op + (sep_k ? 0 : kBlockTokens * d.d_r * 2) + (f8 ? kBlockTokens : 0);
   const int avail = kSmemLimit - ring_fixed_bytes(B);
   auto depth = [&](int p) { return std::min(avail / (p * stage), kMaxStages / p); };
   // Several queries per pass double the consumers' work per tile: as many pairs as fit (four
   // rather than three at d_v = 128: the ragged batch's two-query decode 690 us against 817 us).
+  // The fp8 cache's smaller stages keep the bf16 counts of pairs: four at d_v = 64 (so its fused
+  // step keeps a patcher warp at every d_r), three at d_v = 128.
   const int P = nqp > 1 ? mma_max_threads(d.d_v, nqp) / 64
+                : f8    ? (d.d_v == 64 ? 4 : 3)
                         : std::min(stage <= 11 * 1024 ? 4 : stage <= 12 * 1024 ? 6 : 3,
                                    mma_max_threads(d.d_v, nqp) / 64);
   const int D = depth(P);
@@ -1024,6 +110,7 @@ bool mma_shape(const gva_dims& d, bool sep_k, int B, int nqp, int* pairs, int* s
 }
 
 cudaError_t launch_decode_mma(const DecodeArgs& a, bool sep_k, int grid, cudaStream_t stream) {
+  if (a.v_exp) return sep_k ? cudaErrorInvalidValue : launch_decode_mma_fp8(a, grid, stream);
   CUtensorMap mv, mk;
   if (!make_pool_map(&mv, a.v_pool, a.num_blocks, a.G, a.d_v)) return cudaErrorInvalidValue;
   if (sep_k) {
@@ -1039,3 +126,4 @@ cudaError_t launch_decode_mma(const DecodeArgs& a, bool sep_k, int grid, cudaStr
 }
 
 }  // namespace gva
+

@@ -143,6 +143,39 @@ struct CacheElem<__nv_bfloat16> {
   static __device__ __forceinline__ float to_float(__nv_bfloat16 v) { return __bfloat162float(v); }
 };
 
+// ---- fp8 value cache (E4M3 codes with a power-of-two scale per (token, group)) ----------
+
+// Two E4M3 codes (the low 16 bits of x, the first in the low byte) -> two f16 (exact: every
+// E4M3 value is an f16 value), the first in the low half.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t x) {
+  uint32_t d;
+  const unsigned short h = static_cast<unsigned short>(x & 0xffffu);
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(d) : "h"(h));
+  return d;
+}
+
+// Two floats -> two E4M3 codes (round to nearest even, magnitudes past 448 clamped to 448),
+// the first in the low byte of the result.
+__device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float first, float second) {
+  unsigned short d;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(d) : "f"(second), "f"(first));
+  return d;
+}
+
+// 2^e as a float for -126 <= e <= 127 (exact, from the exponent field).
+__device__ __forceinline__ float exp2_int(int e) { return __int_as_float((e + 127) << 23); }
+
+// Scale exponent of a row of the fp8 value cache whose largest magnitude is amax (a bf16
+// value): the smallest e with amax <= 448 * 2^e, clamped to [-126, 120].  From the bits: a
+// normal amax = 1.m 2^(E-127) needs e = E - 135, one more when 1.m > 1.75; an amax below
+// 2^-126 (or 0) takes the clamp.
+__device__ __forceinline__ int fp8_row_exponent(float amax) {
+  const uint32_t u = __float_as_uint(amax) & 0x7fffffffu;
+  if (u < 0x00800000u) return -126;
+  int e = static_cast<int>(u >> 23) - 135 + ((u & 0x7fffffu) > 0x600000u ? 1 : 0);
+  return e < -126 ? -126 : (e > 120 ? 120 : e);
+}
+
 // RoPE rotation of pair i at position p >= 0: (cos, sin) of p * theta_i, theta_i =
 // base^(-2i/d_r).  The context holds, per 8-bit digit of the position, the fp64 cos/sin of
 // digit * 256^k * theta_i (computed on the host); the angle of p is the sum of its digits'

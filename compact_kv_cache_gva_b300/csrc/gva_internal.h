@@ -30,7 +30,8 @@ constexpr int kMaxDevicesHost = 64;  // per-device host caches (function attribu
 struct DecodeArgs {
   const float* q_abs;        // [B,H,d_v] absorbed query (GQA: the plain query)
   const float* q_rot;        // [B,H,d_r] rotated positional query (nullptr when d_r == 0)
-  const void* v_pool;        // [NB][G][64][d_v]
+  const void* v_pool;        // [NB][G][64][d_v] (fp8 cache: the E4M3 codes)
+  const signed char* v_exp;  // fp8 cache: the scale exponents [NB][G][64], after the codes
   const void* k_pool;        // GQA only: [NB][G][64][d_v]
   const void* kr_pool;       // [NB][64][d_r]
   const int32_t* block_table;
@@ -61,6 +62,7 @@ struct DecodeArgs {
   const void* v_new;         // [B,G,d_v] new values (bf16)
   const void* kr_new;        // [B,d_r] new positional keys, unrotated (bf16)
   void* v_pool_w;            // v_pool and kr_pool again, written at the new token's slot
+  signed char* v_exp_w;      // (fp8 cache: and the exponents)
   void* kr_pool_w;
   const float2* rope32;      // fp32 RoPE digit table
   // Per (range c, segment f) at index c + f: step_stage_floats(R, d_v, d_r) floats holding
@@ -121,6 +123,8 @@ bool mma_shape(const gva_dims& d, bool sep_k, int B, int nqp, int* pairs, int* s
 // Queries per pass of the tensor-core kernel (its (query, head) column pairs: R*nqp <= 8).
 int mma_max_queries_per_pass(int R);
 cudaError_t launch_decode_mma(const DecodeArgs& a, bool sep_k, int grid, cudaStream_t stream);
+// The same kernel over the fp8 value cache (single query per sequence, plain or fused step).
+cudaError_t launch_decode_mma_fp8(const DecodeArgs& a, int grid, cudaStream_t stream);
 // Merges the partial records of each (b, g) into out; launched as a programmatic dependent
 // of the partial kernel.
 cudaError_t launch_combine(const DecodeArgs& a, cudaStream_t stream);

@@ -15,7 +15,7 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libgva.so")
 
 GVA_OK, GVA_ERR_INVALID_ARG, GVA_ERR_UNSUPPORTED, GVA_ERR_WORKSPACE, GVA_ERR_CUDA, GVA_ERR_DEVICE_INDEX = range(6)
-GVA_F32, GVA_BF16 = 0, 1
+GVA_F32, GVA_BF16, GVA_FP8_E4M3 = 0, 1, 2
 GVA_PATH_AUTO, GVA_PATH_FMA, GVA_PATH_MMA = 0, 1, 2
 GVA_STEP_AUTO, GVA_STEP_FUSED, GVA_STEP_SEPARATE = 0, 1, 2
 GVA_DEVERR_POSITION, GVA_DEVERR_BLOCK_ID, GVA_DEVERR_SEQ_LEN, GVA_DEVERR_TIMEOUT = 1, 2, 4, 8
@@ -138,9 +138,14 @@ class Context:
     """Owns one gva_ctx (bound to the device current at creation)."""
 
     def __init__(self, H, G, d_v, d_n, d_r, cache_dtype, rope_base=10000.0, scale=0.0):
-        self.dims = gva_dims(H, G, d_v, d_n, d_r, BLOCK_TOKENS,
-                             GVA_F32 if cache_dtype in ("f32", torch.float32) else GVA_BF16, rope_base, scale)
-        self.cache_torch_dtype = torch.float32 if self.dims.cache_dtype == GVA_F32 else torch.bfloat16
+        code = {"f32": GVA_F32, torch.float32: GVA_F32, "bf16": GVA_BF16, torch.bfloat16: GVA_BF16,
+                "fp8": GVA_FP8_E4M3}[cache_dtype]
+        self.dims = gva_dims(H, G, d_v, d_n, d_r, BLOCK_TOKENS, code, rope_base, scale)
+        self.fp8 = code == GVA_FP8_E4M3
+        # dtype of the new values and keys, and of the positional-key pool (bf16 for the fp8 cache)
+        self.cache_torch_dtype = torch.float32 if code == GVA_F32 else torch.bfloat16
+        # dtype of the value pool: the fp8 cache's is bytes (E4M3 codes, then int8 exponents)
+        self.v_pool_dtype = torch.uint8 if self.fp8 else self.cache_torch_dtype
         h = C.c_void_p()
         _check(load().gva_create(C.byref(self.dims), C.byref(h)), "gva_create")
         self.handle = h
@@ -174,10 +179,36 @@ def _shape(t, shape, name):
         raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
 
 
+def fp8_value_pool_bytes(num_blocks, G, d_v):
+    """Bytes of an fp8 value pool of num_blocks blocks: the E4M3 codes [NB][G][64][d_v], then the
+    int8 scale exponents [NB][G][64]."""
+    return num_blocks * G * BLOCK_TOKENS * (d_v + 1)
+
+
+def fp8_pool_views(v_pool, G, d_v):
+    """(codes [NB,G,64,d_v] uint8, exponents [NB,G,64] int8): views of an fp8 value pool."""
+    NB = v_pool.numel() // (G * BLOCK_TOKENS * (d_v + 1))
+    flat = v_pool.reshape(-1)
+    n = NB * G * BLOCK_TOKENS * d_v
+    return flat[:n].view(NB, G, BLOCK_TOKENS, d_v), flat[n:n + NB * G * BLOCK_TOKENS].view(torch.int8).view(
+        NB, G, BLOCK_TOKENS)
+
+
+def _num_blocks(ctx, v_pool):
+    d = ctx.dims
+    if ctx.fp8:
+        per = d.G * BLOCK_TOKENS * (d.d_v + 1)
+        if v_pool.numel() % per:
+            raise ValueError(f"fp8 value pool of {v_pool.numel()} bytes is not a whole number of {per}-byte blocks")
+        return v_pool.numel() // per
+    return v_pool.shape[0]
+
+
 def _check_pools(ctx, v_pool, kr_pool, k_pool=None):
     d = ctx.dims
-    NB = v_pool.shape[0]
-    _shape(v_pool, (NB, d.G, BLOCK_TOKENS, d.d_v), "v_pool")
+    NB = _num_blocks(ctx, v_pool)
+    if not ctx.fp8:
+        _shape(v_pool, (NB, d.G, BLOCK_TOKENS, d.d_v), "v_pool")
     if k_pool is not None:
         _shape(k_pool, (NB, d.G, BLOCK_TOKENS, d.d_v), "k_pool")
     if d.d_r > 0 and kr_pool is not None:
@@ -225,7 +256,7 @@ def gva_cache_append(ctx, v_new, kr_new, pos, block_table, v_pool, kr_pool, stre
     _check(load().gva_cache_append(ctx.handle, B, n, _ptr(v_new, dt, "v_new"),
                                    _ptr(kr_new, dt, "kr_new", allow_none=not has_r), _ptr(pos, torch.int32, "pos"),
                                    _ptr(block_table, torch.int32, "block_table"), block_table.shape[1],
-                                   v_pool.shape[0], _ptr(v_pool, dt, "v_pool"),
+                                   _num_blocks(ctx, v_pool), _ptr(v_pool, ctx.v_pool_dtype, "v_pool"),
                                    _ptr(kr_pool, dt, "kr_pool", allow_none=not has_r), _stream(stream)),
            "gva_cache_append")
 
@@ -248,9 +279,9 @@ def gva_decode_attention(ctx, q_abs, q_rot, v_pool, kr_pool, block_table, seq_le
     _check_pools(ctx, v_pool, kr_pool if has_r else None)
     _check(load().gva_decode_attention(ctx.handle, B, _ptr(q_abs, torch.float32, "q_abs"),
                                        _ptr(q_rot, torch.float32, "q_rot", allow_none=not has_r),
-                                       _ptr(v_pool, dt, "v_pool"), _ptr(kr_pool, dt, "kr_pool", allow_none=not has_r),
+                                       _ptr(v_pool, ctx.v_pool_dtype, "v_pool"), _ptr(kr_pool, dt, "kr_pool", allow_none=not has_r),
                                        _ptr(block_table, torch.int32, "block_table"), block_table.shape[1],
-                                       v_pool.shape[0], _ptr(seq_lens, torch.int32, "seq_lens"), int(max_seq_len),
+                                       _num_blocks(ctx, v_pool), _ptr(seq_lens, torch.int32, "seq_lens"), int(max_seq_len),
                                        _ptr(out, torch.float32, "out"), _ptr(workspace, None, "workspace"),
                                        workspace.numel() * workspace.element_size(), _stream(stream)),
            "gva_decode_attention")
@@ -270,9 +301,9 @@ def gva_decode_partial(ctx, q_abs, q_rot, v_pool, kr_pool, block_table, seq_lens
     _check_pools(ctx, v_pool, kr_pool if has_r else None)
     _check(load().gva_decode_partial(ctx.handle, B, _ptr(q_abs, torch.float32, "q_abs"),
                                      _ptr(q_rot, torch.float32, "q_rot", allow_none=not has_r),
-                                     _ptr(v_pool, dt, "v_pool"), _ptr(kr_pool, dt, "kr_pool", allow_none=not has_r),
+                                     _ptr(v_pool, ctx.v_pool_dtype, "v_pool"), _ptr(kr_pool, dt, "kr_pool", allow_none=not has_r),
                                      _ptr(block_table, torch.int32, "block_table"), block_table.shape[1],
-                                     v_pool.shape[0], _ptr(seq_lens, torch.int32, "seq_lens"), int(max_seq_len),
+                                     _num_blocks(ctx, v_pool), _ptr(seq_lens, torch.int32, "seq_lens"), int(max_seq_len),
                                      _ptr(workspace, None, "workspace"), workspace.numel() * workspace.element_size(),
                                      _stream(stream)),
            "gva_decode_partial")
@@ -308,10 +339,10 @@ def gva_decode_attention_multi(ctx, q_abs, q_rot, v_pool, kr_pool, block_table, 
     _check_pools(ctx, v_pool, kr_pool if has_r else None)
     _check(load().gva_decode_attention_multi(ctx.handle, B, n_q, _ptr(q_abs, torch.float32, "q_abs"),
                                              _ptr(q_rot, torch.float32, "q_rot", allow_none=not has_r),
-                                             _ptr(v_pool, dt, "v_pool"),
+                                             _ptr(v_pool, ctx.v_pool_dtype, "v_pool"),
                                              _ptr(kr_pool, dt, "kr_pool", allow_none=not has_r),
                                              _ptr(block_table, torch.int32, "block_table"), block_table.shape[1],
-                                             v_pool.shape[0], _ptr(seq_lens, torch.int32, "seq_lens"),
+                                             _num_blocks(ctx, v_pool), _ptr(seq_lens, torch.int32, "seq_lens"),
                                              int(max_seq_len), _ptr(out, torch.float32, "out"),
                                              _ptr(workspace, None, "workspace"),
                                              workspace.numel() * workspace.element_size(), _stream(stream)),
@@ -336,10 +367,10 @@ def gva_decode_attention_noalloc(ctx, q_abs, q_rot, v_pool, kr_pool, block_table
     _check_pools(ctx, v_pool, kr_pool if has_r else None)
     _check(load().gva_decode_attention_noalloc(ctx.handle, B, _ptr(q_abs, torch.float32, "q_abs"),
                                                _ptr(q_rot, torch.float32, "q_rot", allow_none=not has_r),
-                                               _ptr(v_pool, dt, "v_pool"),
+                                               _ptr(v_pool, ctx.v_pool_dtype, "v_pool"),
                                                _ptr(kr_pool, dt, "kr_pool", allow_none=not has_r),
                                                _ptr(block_table, torch.int32, "block_table"), block_table.shape[1],
-                                               v_pool.shape[0], _ptr(seq_lens, torch.int32, "seq_lens"),
+                                               _num_blocks(ctx, v_pool), _ptr(seq_lens, torch.int32, "seq_lens"),
                                                int(max_seq_len), _ptr(out, torch.float32, "out"), _stream(stream)),
            "gva_decode_attention_noalloc")
 
@@ -373,9 +404,9 @@ def gva_decode_step(ctx, q_c, q_r, M, v_new, kr_new, v_pool, kr_pool, block_tabl
                                   _ptr(M, torch.float32, "M"),
                                   _ptr(v_new, dt, "v_new", allow_pinned=True),
                                   _ptr(kr_new, dt, "kr_new", allow_none=not has_r, allow_pinned=True),
-                                  _ptr(v_pool, dt, "v_pool"), _ptr(kr_pool, dt, "kr_pool", allow_none=not has_r),
+                                  _ptr(v_pool, ctx.v_pool_dtype, "v_pool"), _ptr(kr_pool, dt, "kr_pool", allow_none=not has_r),
                                   _ptr(block_table, torch.int32, "block_table"), block_table.shape[1],
-                                  v_pool.shape[0], _ptr(seq_lens, torch.int32, "seq_lens"), int(max_seq_len),
+                                  _num_blocks(ctx, v_pool), _ptr(seq_lens, torch.int32, "seq_lens"), int(max_seq_len),
                                   _ptr(out, torch.float32, "out", allow_pinned=True),
                                   _ptr(workspace, None, "workspace"),
                                   workspace.numel() * workspace.element_size(), _stream(stream)),
@@ -407,9 +438,9 @@ def gva_decode_step_partial(ctx, q_c, q_r, M, v_new, kr_new, v_pool, kr_pool, bl
                                           _ptr(q_r, torch.float32, "q_r", allow_none=not has_r),
                                           _ptr(M, torch.float32, "M"), _ptr(v_new, dt, "v_new"),
                                           _ptr(kr_new, dt, "kr_new", allow_none=not has_r),
-                                          _ptr(v_pool, dt, "v_pool"), _ptr(kr_pool, dt, "kr_pool", allow_none=not has_r),
+                                          _ptr(v_pool, ctx.v_pool_dtype, "v_pool"), _ptr(kr_pool, dt, "kr_pool", allow_none=not has_r),
                                           _ptr(block_table, torch.int32, "block_table"), block_table.shape[1],
-                                          v_pool.shape[0], _ptr(seq_lens, torch.int32, "seq_lens"), int(max_seq_len),
+                                          _num_blocks(ctx, v_pool), _ptr(seq_lens, torch.int32, "seq_lens"), int(max_seq_len),
                                           _ptr(workspace, None, "workspace"),
                                           workspace.numel() * workspace.element_size(), _stream(stream)),
            "gva_decode_step_partial")
@@ -441,10 +472,10 @@ def gva_decode_step_multi(ctx, q_c, q_r, M, v_new, kr_new, v_pool, kr_pool, bloc
                                         _ptr(q_r, torch.float32, "q_r", allow_none=not has_r, allow_pinned=True),
                                         _ptr(M, torch.float32, "M"), _ptr(v_new, dt, "v_new", allow_pinned=True),
                                         _ptr(kr_new, dt, "kr_new", allow_none=not has_r, allow_pinned=True),
-                                        _ptr(v_pool, dt, "v_pool"),
+                                        _ptr(v_pool, ctx.v_pool_dtype, "v_pool"),
                                         _ptr(kr_pool, dt, "kr_pool", allow_none=not has_r),
                                         _ptr(block_table, torch.int32, "block_table"), block_table.shape[1],
-                                        v_pool.shape[0], _ptr(seq_lens, torch.int32, "seq_lens"), int(max_seq_len),
+                                        _num_blocks(ctx, v_pool), _ptr(seq_lens, torch.int32, "seq_lens"), int(max_seq_len),
                                         _ptr(out, torch.float32, "out", allow_pinned=True),
                                         _ptr(workspace, None, "workspace"),
                                         workspace.numel() * workspace.element_size(), _stream(stream)),
@@ -464,8 +495,8 @@ def gqa_decode_attention(ctx, q, k_pool, v_pool, block_table, seq_lens, max_seq_
     _check_table(block_table, B, seq_lens)
     _check_pools(ctx, v_pool, None, k_pool)
     _check(load().gqa_decode_attention(ctx.handle, B, _ptr(q, torch.float32, "q"), _ptr(k_pool, dt, "k_pool"),
-                                       _ptr(v_pool, dt, "v_pool"), _ptr(block_table, torch.int32, "block_table"),
-                                       block_table.shape[1], v_pool.shape[0], _ptr(seq_lens, torch.int32, "seq_lens"),
+                                       _ptr(v_pool, ctx.v_pool_dtype, "v_pool"), _ptr(block_table, torch.int32, "block_table"),
+                                       block_table.shape[1], _num_blocks(ctx, v_pool), _ptr(seq_lens, torch.int32, "seq_lens"),
                                        int(max_seq_len), _ptr(out, torch.float32, "out"),
                                        _ptr(workspace, None, "workspace"),
                                        workspace.numel() * workspace.element_size(), _stream(stream)),

@@ -20,6 +20,7 @@ Distributions: V, q_c, q_r and the raw positional key ~ N(0,1); M_h ~ N(0, 1/d_v
 Ragged lengths come from a second generator seeded with 1 (randint(512, 32769)), and the
 block shuffle is the next draw (randperm) from that same generator.
 """
+import dataclasses
 from dataclasses import dataclass, field
 import math
 
@@ -32,7 +33,7 @@ BLOCK = 64
 class Workload:
     id: int
     name: str
-    dtype: str  # "f32" | "bf16"
+    dtype: str  # "f32" | "bf16" | "fp8" (E4M3 value cache, bf16 positional keys)
     B: int
     H: int
     G: int
@@ -46,11 +47,20 @@ class Workload:
 
     @property
     def torch_dtype(self):
+        """dtype of new values and keys, and of the positional-key pool (bf16 for the fp8 cache)."""
         return torch.float32 if self.dtype == "f32" else torch.bfloat16
 
     @property
     def elem_bytes(self):
         return 4 if self.dtype == "f32" else 2
+
+    @property
+    def bytes_per_token(self):
+        """Cache bytes of one token of one layer: values and positional key in the cache dtype;
+        the fp8 cache holds G*d_v codes, G scale exponents and d_r bf16 key elements."""
+        if self.dtype == "fp8":
+            return self.G * self.d_v + self.G + 2 * self.d_r
+        return (self.G * self.d_v + self.d_r) * self.elem_bytes
 
     @property
     def r(self):
@@ -79,6 +89,12 @@ WORKLOADS = {
     5: Workload(5, "ragged-paged-bf16", "bf16", B=128, H=32, G=8, d_v=128, d_n=128, d_r=24,
                 T_range=(512, 32768), shuffled=True),
 }
+
+
+def with_cache(w: Workload, dtype: str):
+    """The same workload over another cache dtype, named for it (e.g. long-context-fp8)."""
+    name = w.name.replace(w.dtype, dtype) if w.dtype in w.name else f"{w.name}-{dtype}"
+    return dataclasses.replace(w, dtype=dtype, name=name)
 
 
 def custom(name="custom", dtype="bf16", B=2, H=4, G=2, d_v=64, d_n=None, d_r=16, T=0, T_range=(), shuffled=False):
@@ -174,7 +190,10 @@ def decode_inputs(w: Workload, seed=0, device="cpu", lens=None, spare_blocks=0, 
     lens = seq_lens(w) if lens is None else torch.as_tensor(lens, dtype=torch.int32)
     table, nb = block_table(w, lens, spare_blocks=spare_blocks)
     g = torch.Generator(device=device).manual_seed(seed)
-    v_pool = torch.randn((nb, w.G, BLOCK, w.d_v), generator=g, device=device).to(w.torch_dtype)
+    if w.dtype == "fp8":
+        v_pool = fp8_value_pool(w, nb, g, device)
+    else:
+        v_pool = torch.randn((nb, w.G, BLOCK, w.d_v), generator=g, device=device).to(w.torch_dtype)
     kr_pool = torch.randn((nb, BLOCK, w.d_r), generator=g, device=device).to(w.torch_dtype)
     q_abs = torch.randn((w.B, w.H, w.d_v), generator=g, device=device)
     q_rot = torch.randn((w.B, w.H, w.d_r), generator=g, device=device)
@@ -186,6 +205,17 @@ def decode_inputs(w: Workload, seed=0, device="cpu", lens=None, spare_blocks=0, 
     return DecodeInputs(v_pool, kr_pool, table.to(device), lens.to(device), q_abs, q_rot, nb, extra)
 
 
+def fp8_value_pool(w: Workload, nb, g, device):
+    """A filled fp8 value pool: the E4M3 codes [nb][G][64][d_v] followed by the int8 exponents
+    [nb][G][64].  Values are N(0,1) draws; each row's exponent is drawn from {-8, -7, -6} (the
+    exponent a row of 64 or 128 such values needs is about -7) and the codes are torch's E4M3
+    cast of the draws times 2^-e, clamped to the format's range."""
+    x = torch.randn((nb, w.G, BLOCK, w.d_v), generator=g, device=device)
+    e = torch.randint(-8, -5, (nb, w.G, BLOCK), generator=g, device=device)
+    codes = (x * torch.exp2(-e.float())[..., None]).clamp(-448.0, 448.0).to(torch.float8_e4m3fn).view(torch.uint8)
+    return torch.cat([codes.reshape(-1), e.to(torch.int8).view(torch.uint8).reshape(-1)])
+
+
 def pool_bits(t: torch.Tensor):
     """Host numpy view of a cache tensor as the oracle reads it (float32, or uint16 bf16 bits)."""
     t = t.detach().contiguous().cpu()
@@ -193,4 +223,6 @@ def pool_bits(t: torch.Tensor):
         return t.view(torch.int16).numpy().view("uint16")
     if t.dtype == torch.float32:
         return t.numpy()
+    if t.dtype == torch.uint8:  # fp8 value pool: codes, then exponents (flat)
+        return t.reshape(-1).numpy()
     raise TypeError(t.dtype)

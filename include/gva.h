@@ -32,6 +32,9 @@
  *       V pool   [NB][G][64][d_v]   element (blk, g, o, i) at ((blk*G + g)*64 + o)*d_v + i
  *       k_r pool [NB][64][d_r]      element (blk, o, c)    at (blk*64 + o)*d_r + c
  *     Position p of sequence b lives in block block_table[b*max_blocks + p/64], slot p%64.
+ *     The fp8 value cache (GVA_FP8_E4M3) stores in the V pool NB*G*64*d_v one-byte E4M3 codes
+ *     in the layout above, followed by NB*G*64 int8 scale exponents, exponent (blk, g, o) at
+ *     byte NB*G*64*d_v + (blk*G + g)*64 + o: value = code * 2^exponent.  Its k_r pool is bf16.
  *   - Head h reads value group g(h) = h / (H/G) (contiguous head blocks, as in grouped-
  *     query attention).  RoPE turns pair (2i, 2i+1) by p * base^(-2i/d_r).  The softmax
  *     scale defaults to 1/sqrt(d_n + d_r).
@@ -60,7 +63,16 @@ typedef enum {
   GVA_ERR_DEVICE_INDEX = 5  /* gva_get_device_error found a device-side error bit set */
 } gva_status;
 
-typedef enum { GVA_F32 = 0, GVA_BF16 = 1 } gva_dtype;
+/* Cache dtypes.  GVA_FP8_E4M3 is a low-precision value cache of this library (the paper
+ * stores values in the model's precision): each (token, group) value row is kept as E4M3
+ * codes (OCP FP8: 4 exponent bits with bias 7, 3 mantissa bits, largest finite 448) times
+ * one power-of-two scale 2^e, e the smallest integer with max|v| <= 448 * 2^e (clamped to
+ * [-126, 120]); each code is v * 2^-e rounded to nearest even, saturating at 448.  The
+ * positional keys stay bf16; new values and keys are given in bf16.  G*d_v + G + 2*d_r
+ * bytes per token (292 at G = 4, d_v = 64, d_r = 16, against 544 for bf16).  Tensor-core
+ * path only: d_v 64 or 128, one query per sequence (gva_decode_attention, _partial,
+ * _combine, _noalloc, gva_decode_step and its parts), no gqa_decode_attention. */
+typedef enum { GVA_F32 = 0, GVA_BF16 = 1, GVA_FP8_E4M3 = 2 } gva_dtype;
 
 /* Bits of the device error word. */
 #define GVA_DEVERR_POSITION 1u /* position < 0, or position/64 >= max_blocks */
@@ -82,7 +94,7 @@ typedef struct {
   int d_n;               /* content query width (absorbed query input); multiple of 4 */
   int d_r;               /* positional width; even, 0 <= d_r <= 32 (0 = no positional slice) */
   int block_size;        /* tokens per cache block; must be 64 */
-  gva_dtype cache_dtype; /* GVA_F32 or GVA_BF16 */
+  gva_dtype cache_dtype; /* GVA_F32, GVA_BF16 or GVA_FP8_E4M3 */
   double rope_base;      /* <= 0 selects 10000 */
   float scale;           /* softmax scale; <= 0 selects 1/sqrt(d_n + d_r) */
 } gva_dims;
@@ -122,10 +134,12 @@ gva_status gva_absorb_query(gva_ctx* ctx, int B, const float* q_c, const float* 
  * "append the new token's state, then read through the current position" step of the
  * decode lifecycle, GQA explainer section "与位置编码和 KV Cache 的关系"; cache content per
  * the abstract and the review's section 3: grouped values plus one rotated positional key).
- *   v_new  [B,n,G,d_v] cache dtype   new values, copied bit for bit
+ *   v_new  [B,n,G,d_v] cache dtype   new values, copied bit for bit (fp8 cache: bf16
+ *                                    values, quantised row by row as GVA_FP8_E4M3 states)
  *   kr_new [B,n,d_r]   cache dtype   new positional keys, UNROTATED; each is rotated to its
- *                                    own position (fp64 for fp32 caches, fp32 for bf16
- *                                    caches) and rounded once to nearest even
+ *                                    own position (fp64 for fp32 caches, fp32 for bf16 and
+ *                                    fp8 caches) and rounded once to nearest even (fp8
+ *                                    cache: bf16 keys)
  *   pos    [B] int32                 position of the first new token of each sequence
  *   block_table [B,max_blocks] int32, pools as in the layout above (NB = num_blocks)
  * Token t of sequence b goes to position pos[b]+t.  A position beyond the table or a block
