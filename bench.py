@@ -69,15 +69,19 @@ def parse():
     p.add_argument("--nq", type=int, default=1,
                    help="query tokens per sequence per step (the last n_q positions: append n_q tokens, "
                         "absorb B*n_q query rows, gva_decode_attention_multi)")
+    p.add_argument("--cache", default="default", choices=["default", "bf16", "fp8"],
+                   help="cache dtype of the workload (default: its own; fp8 = E4M3 value cache with a "
+                        "power-of-two scale per token and group, bf16 positional keys)")
     p.add_argument("--batch", type=int, default=0,
                    help="keep only the first N sequences of the workload (named <name>-b<N>), e.g. for a "
                         "profiler capture small enough to hold on the device twice")
     p.add_argument("--profile", action="store_true",
                    help="run only the step's split-T partial pass: --warmup launches, then --steps more, "
                         "and print one line (for a profiler's launch filter; no timing is reported)")
-    p.add_argument("--workloads", default="2,3,5",
+    p.add_argument("--workloads", default="2,3,5,4:fp8",
                    help="other configurations measured after the headline, in the same process "
-                        "(comma-separated workload ids; empty for none)")
+                        "(comma-separated workload ids, each optionally :fp8 for the fp8 value cache; "
+                        "empty for none)")
     p.add_argument("--workload-steps", type=int, default=200,
                    help="timed steps of each of those configurations (at least --steps)")
     p.add_argument("--dr", type=int, default=-1,
@@ -284,7 +288,7 @@ class Setup:
                                     step_mode={"auto": gva.GVA_STEP_AUTO, "fused": gva.GVA_STEP_FUSED,
                                                "separate": gva.GVA_STEP_SEPARATE}[step_mode])
         self.sum_T = int(self.lens_cpu.sum())
-        self.bytes_per_token = (w.G * w.d_v + w.d_r) * w.elem_bytes
+        self.bytes_per_token = w.bytes_per_token
         self.cache_bytes = self.sum_T * self.bytes_per_token
         # algorithmic bytes of the decode call: cache + queries + output + lengths + table rows used
         used_blocks = int(((self.lens_cpu + 63) // 64).sum())
@@ -292,9 +296,10 @@ class Setup:
                              w.B * 4 + used_blocks * 4)
         self.decode_flops = self.sum_T * w.H * (2 * (w.d_v + w.d_r) + 2 * w.d_v)
         # the fused partial pass reads the raw queries and the key maps instead of the absorbed
-        # queries, and reads and writes the new token
+        # queries, and reads the new token (cache dtype; bf16 for the fp8 cache) and writes it
         self.step_bytes = (self.cache_bytes + w.B * w.H * (w.d_n + w.d_r) * 4 + w.H * w.d_v * w.d_n * 4 +
-                           2 * w.B * (w.G * w.d_v + w.d_r) * w.elem_bytes + w.B * w.H * w.d_v * 4 + w.B * 4 +
+                           w.B * ((w.G * w.d_v + w.d_r) * w.elem_bytes + w.bytes_per_token) +
+                           w.B * w.H * w.d_v * 4 + w.B * 4 +
                            used_blocks * 4)
 
         # the library's one-call step (gva_decode_step, or gva_decode_step_multi for n_q > 1)
@@ -398,6 +403,8 @@ def capture(fn):
 
 def workload(args):
     w = synth.WORKLOADS[args.workload]
+    if args.cache != "default" and args.cache != w.dtype:
+        w = synth.with_cache(w, args.cache)
     if args.dr >= 0 and args.dr != w.d_r:
         w = dataclasses.replace(w, d_r=args.dr, name=f"{w.name}-dr{args.dr}")
     if args.nq > 1:
@@ -534,22 +541,27 @@ def run_ours(args, rank, ws):
         "clocks": clocks.summary(),
     }
     if args.workloads and S.n_q == 1 and args.dr < 0:
-        out["workloads"] = [run_workload_line(int(x), args, rank, ws) for x in args.workloads.split(",")
-                            if int(x) != args.workload]
+        lines = []
+        for x in args.workloads.split(","):
+            wid, _, cache = x.partition(":")
+            other = synth.WORKLOADS[int(wid)]
+            other = synth.with_cache(other, cache) if cache and cache != other.dtype else other
+            if other.name != w.name:
+                lines.append(run_workload_line(other, args, rank, ws))
+        out["workloads"] = lines
     out["e2e"] = run_e2e(S, args.e2e_steps, flush, graph=bool(args.graph), ws=ws)
-    if not args.no_gqa and rank == 0:
+    if not args.no_gqa and rank == 0 and w.dtype == "bf16":
         out["gqa_same_build"] = run_gqa(S, flush, min(K, 500))
     if rank == 0 and ws == 1 and not args.no_cpu_baseline and S.n_q == 1:
         out["cpu_baseline"] = cpu_baseline(S, args)
     return out
 
 
-def run_workload_line(wid, args, rank, ws):
+def run_workload_line(w, args, rank, ws):
     """Another configuration measured in the same process as the headline, the same way: the
     one-call step, the decode call (partial + combine) and the split-T partial pass alone, each
     timed with CUDA events over K steps (L2 flushed before every step when the cache is smaller
     than twice L2), with the clocks sampled during the step's timed region."""
-    w = synth.WORKLOADS[wid]
     S = Setup(w, seed=rank, path=args.path, split_tokens=args.split_tokens, step_mode=args.step_mode)
     flush = flusher() if S.cache_bytes < 2 * L2_BYTES else None
     K = max(args.steps, args.workload_steps)
@@ -584,6 +596,8 @@ def run_workload_line(wid, args, rank, ws):
         "partial_us": round(part_s * 1e6, 3),
         "context_tokens_per_s": round(whole_job(S.sum_T * K, ws, step_s), 1),
         "pct_of_hbm_peak": round(100 * S.cache_bytes / (step_s / K) / 1e9 / NOMINAL_HBM_GBS, 2),
+        "bytes_per_token": w.bytes_per_token,
+        "bf16_bytes_per_token": synth.with_cache(w, "bf16").bytes_per_token,
         "roofline": {"kernel": "fused split-T partial kernel (gva_decode_step_partial)" if S.fused else
                      "split-T partial pass (gva_decode_partial)", "bound": "hbm", "achieved": round(achieved, 1),
                      "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": round(achieved / pk["hbm_gbs"], 4),
@@ -761,8 +775,13 @@ def cpu_sample(S, nseq, max_tokens=None):
         T = int(S.lens_cpu[b]) if max_tokens is None else min(int(S.lens_cpu[b]), max_tokens)
         nblk = (T + 63) // 64
         ids = inp.block_table[b, :nblk].long()
-        seqs.append((b, T, synth.pool_bits(inp.v_pool.index_select(0, ids)),
-                     synth.pool_bits(inp.kr_pool.index_select(0, ids))))
+        if w.dtype == "fp8":  # the blocks' codes, then their exponents
+            codes, exps = gva.fp8_pool_views(inp.v_pool, w.G, w.d_v)
+            vsel = torch.cat([codes.index_select(0, ids).reshape(-1),
+                              exps.index_select(0, ids).view(torch.uint8).reshape(-1)])
+        else:
+            vsel = inp.v_pool.index_select(0, ids)
+        seqs.append((b, T, synth.pool_bits(vsel), synth.pool_bits(inp.kr_pool.index_select(0, ids))))
         raw["pos_q"][b] = T - 1
         raw["pos_new"][b] = T - 1
     return seqs, raw
@@ -784,7 +803,7 @@ def oracle_step(w, seqs, raw):
         oracle.append(synth.pool_bits(raw["v_new"][b:b + 1]), synth.pool_bits(raw["kr_new"][b:b + 1]),
                       raw["pos_new"][b:b + 1].numpy(), table, vp, kp)
         oracle.decode(qa, qr, vp, kp, table, np.array([T], np.int32), G=w.G, d_n=w.d_n)
-        nbytes += T * (w.G * w.d_v + w.d_r) * w.elem_bytes
+        nbytes += T * w.bytes_per_token
     return time.perf_counter() - t0, nbytes
 
 

@@ -57,6 +57,11 @@ constexpr int kMmaMaxThreads = 64 * kMmaMaxPairs;  // consumer warps + as many c
 // so they keep more registers per thread; five pairs at 320 threads squeezed the two-query
 // d_v = 64 instance from 194 to 168 registers and made it 11 % slower).
 __host__ __device__ constexpr int mma_max_threads(int dv, int nq) { return dv == 64 && nq == 1 ? 384 : 256; }
+// Consumers a copy warp fills: one (warp pairs), or two for the fp8 value cache at d_v = 64,
+// whose small tiles come fast enough that its consumers are what limits (8 consumers and 4
+// copy warps fill the 384 threads; a copy warp issues a tile in a small fraction of the
+// time a consumer computes one).
+__host__ __device__ constexpr int mma_consumers_per_copy_warp(int dv, bool f8) { return f8 && dv == 64 ? 2 : 1; }
 constexpr int kSubTileBytes = kBlockTokens * 128;  // one [64 tokens][64 columns] bf16 swizzled box
 
 // ---- PTX wrappers ------------------------------------------------------------------------
@@ -335,12 +340,14 @@ __global__ void __launch_bounds__(mma_max_threads(DV, NQ), 1) decode_mma_kernel(
   static_assert(!SEPK || DR == 0, "the key-cache form has no positional slice");
   static_assert(!FUSED || (NQ == 1 && !CAUSAL && !SEPK), "the fused step is single-query GVA decode");
   static_assert(!F8 || (NQ == 1 && !CAUSAL && !SEPK), "the fp8 value cache is read by single-query GVA decode");
+  constexpr int CPC = mma_consumers_per_copy_warp(DV, F8);
   constexpr int QS = step_stage_floats(R, DV, DR);  // floats of one staged segment (fused step)
 
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  const int P = a.group_warps;  // warp pairs; blockDim.x == 64 * P, plus the prologue warps of a fused launch
+  const int P = a.group_warps;  // consumer warps
+  const int PC = P / CPC;       // copy warps; blockDim.x == 32 * (P + PC), plus the prologue warps of a fused launch
   const int D = a.n_stages;     // ring slots per pair
   const int N = P * D;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem);
@@ -352,7 +359,7 @@ __global__ void __launch_bounds__(mma_max_threads(DV, NQ), 1) decode_mma_kernel(
   uint64_t* landed = reinterpret_cast<uint64_t*>(blks + kMaxStages);
   // Fused instances with a spare warp (all but the bf16 six-pair one) give the append to it: the
   // consumers' loop is then the plain kernel's.
-  constexpr bool kPatcher = FUSED && (F8 || !(DV == 64 && DR == 32));
+  constexpr bool kPatcher = FUSED && !(DV == 64 && (DR == 32 || F8));
   unsigned char* tiles = smem + kCtrlBytes;
   unsigned char* krs = tiles + N * L::kOpBytes;
   unsigned char* exs = krs + N * L::kKrBytes;  // fp8 cache: the scale exponents of each stage's tile
@@ -524,10 +531,10 @@ __global__ void __launch_bounds__(mma_max_threads(DV, NQ), 1) decode_mma_kernel(
     if (!rotated) rotate_pairs();
   };
   if constexpr (FUSED) {
-    const int E = static_cast<int>(blockDim.x / 32) - 2 * P;  // prologue-only warps
-    if (warp >= 2 * P) {
-      absorb_segments(P + (warp - 2 * P), P + E);
-      if (!kPatcher || warp != 2 * P) {
+    const int E = static_cast<int>(blockDim.x / 32) - P - PC;  // prologue-only warps
+    if (warp >= P + PC) {
+      absorb_segments(P + (warp - P - PC), P + E);
+      if (!kPatcher || warp != P + PC) {
         asm volatile("bar.arrive %0, %1;" ::"r"(kStepBarrier), "r"(32 * (P + E)) : "memory");
         return;
       }
@@ -583,16 +590,18 @@ __global__ void __launch_bounds__(mma_max_threads(DV, NQ), 1) decode_mma_kernel(
 
   // ------------------------------------------------------------------ copy warps
   if (warp >= P) {
-    const int c = warp - P;                        // the consumer this warp serves
-    const int n_mine = n > c ? (n - c + P - 1) / P : 0;  // its units: k = c + P*d, d < n_mine
-    // lane i: block id (or -1), group and valid tokens of the consumer's unit d0 + i
+    // copy warp c serves the units k = c + PC*i of the range (i < n_mine): CPC consumers, unit
+    // k going to consumer k % P as its (k / P)-th unit
+    const int c = warp - P;
+    const int n_mine = n > c ? (n - c + PC - 1) / PC : 0;
+    // lane i: block id (or -1), group and valid tokens of this warp's unit d0 + i
     auto lookup = [&](int d0, int& blk, int& grp, int& nv) {
       blk = -1;
       grp = 0;
       nv = 0;
       const int d = d0 + lane;
       if (d < n_mine) {
-        const UnitCursor cu = cursor_at(u0 + c + static_cast<long long>(P) * d, cum, a.B, a.G);
+        const UnitCursor cu = cursor_at(u0 + c + static_cast<long long>(PC) * d, cum, a.B, a.G);
         grp = cu.g;
         const int T = a.seq_lens[cu.b];  // issued beside the table read: one round trip
         if (cu.t >= a.max_blocks) {
@@ -611,8 +620,13 @@ __global__ void __launch_bounds__(mma_max_threads(DV, NQ), 1) decode_mma_kernel(
     int blk, grp, nv;
     lookup(0, blk, grp, nv);
     if constexpr (FUSED) asm volatile("bar.arrive %0, %1;" ::"r"(kLookupBarrier), "r"(static_cast<int>(blockDim.x)) : "memory");
-    int slot = 0, ph = 0, issued = 0;
+    int issued = 0;
     bool ok = true;
+    auto stage_of = [&](int i, int& dd) {  // ring stage of this warp's i-th unit; dd = its index at its consumer
+      const int k = c + PC * i;
+      dd = k / P;
+      return (k - dd * P) * D + dd % D;
+    };
     for (int d0 = 0; d0 < n_mine && ok; d0 += 32) {
       int nblk, ngrp, nnv;
       lookup(d0 + 32, nblk, ngrp, nnv);  // next batch: loads in flight while this one issues
@@ -622,9 +636,10 @@ __global__ void __launch_bounds__(mma_max_threads(DV, NQ), 1) decode_mma_kernel(
         const int gj = __shfl_sync(kFullMask, grp, j);
         const int vj = __shfl_sync(kFullMask, nv, j);
         if (lane == 0) {
-          const int s = c * D + slot;
+          int dd;
+          const int s = stage_of(d0 + j, dd);
           // the slot's previous unit must have been released by the consumer
-          if (d0 + j >= D && !mbar_wait_bounded(&empty[s], ph ^ 1)) ok = false;
+          if (dd >= D && !mbar_wait_bounded(&empty[s], ((dd / D) & 1) ^ 1)) ok = false;
           if (ok) {
             nvs[s] = bj >= 0 ? vj : 0;  // published by the arrive below (release)
             if (FUSED) blks[s] = bj;
@@ -658,10 +673,6 @@ __global__ void __launch_bounds__(mma_max_threads(DV, NQ), 1) decode_mma_kernel(
         }
         ok = __shfl_sync(kFullMask, ok, 0);
         if (!ok) break;
-        if (++slot == D) {
-          slot = 0;
-          ph ^= 1;
-        }
       }
       blk = nblk;
       grp = ngrp;
@@ -669,16 +680,20 @@ __global__ void __launch_bounds__(mma_max_threads(DV, NQ), 1) decode_mma_kernel(
     }
     if (lane == 0) {
       if (!ok) flag_error(a.err, GVA_DEVERR_TIMEOUT);
-      // no copy may still be landing in shared memory when the CTA exits
-      for (int d = max(0, issued - D); d < issued; ++d)
-        if (!mbar_wait_bounded(&full[c * D + d % D], (d / D) & 1)) flag_error(a.err, GVA_DEVERR_TIMEOUT);
+      // no copy may still be landing in shared memory when the CTA exits (the last D units of
+      // each consumer served are the last CPC*D issued)
+      for (int i = max(0, issued - CPC * D); i < issued; ++i) {
+        int dd;
+        const int s = stage_of(i, dd);
+        if (!mbar_wait_bounded(&full[s], (dd / D) & 1)) flag_error(a.err, GVA_DEVERR_TIMEOUT);
+      }
     }
     return;
   }
 
   // ------------------------------------------------------------------ consumer warps
   if constexpr (FUSED) {
-    const int E = static_cast<int>(blockDim.x / 32) - 2 * P;
+    const int E = static_cast<int>(blockDim.x / 32) - P - PC;
     absorb_segments(warp, P + E);
     named_barrier_sync(kStepBarrier, 32 * (P + E));  // every stage of the range is written
   }
@@ -1104,14 +1119,17 @@ cudaError_t launch_mma_t(const DecodeArgs& a, const CUtensorMap& mv, const CUten
                          cudaStream_t stream) {
   using L = MmaLayout<DV, DR, SEPK, F8>;
   const int P = a.group_warps, D = a.n_stages;
-  if (P < 1 || 64 * P > mma_max_threads(DV, NQ) || D < 1 || P * D > kMaxStages) return cudaErrorInvalidValue;
+  constexpr int CPC = mma_consumers_per_copy_warp(DV, F8);
+  const int warps = P + P / CPC;
+  if (P < 1 || P % CPC || 32 * warps > mma_max_threads(DV, NQ) || D < 1 || P * D > kMaxStages)
+    return cudaErrorInvalidValue;
   if (a.nqp != NQ || (a.nq > 1) != CAUSAL || (a.fused != 0) != FUSED) return cudaErrorInvalidValue;
   const int smem = ring_fixed_bytes(a.B) + P * D * L::kStageBytes;
   if (smem > kSmemLimit) return cudaErrorInvalidValue;
   // the fused step fills the instance's thread budget with prologue warps, and the shared
   // memory budget with query stages; its patcher warp is the first prologue warp
-  const int threads = FUSED ? mma_max_threads(DV, NQ) : 64 * P;
-  if (FUSED && (F8 || !(DV == 64 && DR == 32)) && threads <= 64 * P) return cudaErrorInvalidValue;
+  const int threads = FUSED ? mma_max_threads(DV, NQ) : 32 * warps;
+  if (FUSED && !(DV == 64 && (DR == 32 || F8)) && threads <= 32 * warps) return cudaErrorInvalidValue;
   DecodeArgs args = a;
   args.spare_smem = FUSED ? kSmemLimit - smem : 0;
   const int dyn_smem = FUSED ? kSmemLimit : smem;
