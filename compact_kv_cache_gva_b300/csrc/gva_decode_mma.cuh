@@ -220,6 +220,14 @@ __device__ __forceinline__ void write_new_token_f8(uint32_t vbase, uint32_t krba
   }
 }
 
+// 2^x by the special-function unit (relative error about 2^-22; results below 2^-126 flush to
+// zero, 2^-inf = 0): softmax weights of the fp8 value cache.
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
   uint32_t y;
   asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
@@ -251,12 +259,6 @@ __device__ __forceinline__ uint32_t pack_f16(float lo_half, float hi_half) {
   const uint32_t a = __half_as_ushort(__float2half_rn(lo_half));
   const uint32_t b = __half_as_ushort(__float2half_rn(hi_half));
   return a | (b << 16);
-}
-
-__device__ __forceinline__ uint32_t split_pack_f16(float x) {
-  const __half hi = __float2half_rn(x);
-  const __half lo = __float2half_rn(x - __half2float(hi));
-  return static_cast<uint32_t>(__half_as_ushort(hi)) | (static_cast<uint32_t>(__half_as_ushort(lo)) << 16);
 }
 
 __device__ __forceinline__ float split_part_f16(float x, int part) {
@@ -798,6 +800,13 @@ __global__ void __launch_bounds__(mma_max_threads(DV, NQ), 1) decode_mma_kernel(
   // lane-dependent parts of the ldmatrix addresses
   const int ld_row = (lane & 7) + ((lane >> 3) & 1) * 8;  // non-transposed: row within m16
   const int ld_kc = lane >> 4;                             // non-transposed: 8-column chunk
+  // fp8 cache: offset of this lane's row address in 16-column chunk pair cc of a code tile
+  // (tokens ld_row of the first 16; the next 16 tokens are 16 DV bytes on, same swizzle)
+  uint32_t f8_off[F8 ? DV / 32 : 1];
+  if constexpr (F8) {
+#pragma unroll
+    for (int cc = 0; cc < DV / 32; ++cc) f8_off[cc] = f8_addr<DV>(0, ld_row, 2 * cc + ld_kc);
+  }
   const int tr_tok = (lane & 7) + ((lane >> 4) & 1) * 8;   // transposed: token within k16
   const int tr_dc = (lane >> 3) & 1;                       // transposed: 8-column chunk
 
@@ -832,11 +841,13 @@ __global__ void __launch_bounds__(mma_max_threads(DV, NQ), 1) decode_mma_kernel(
         }
       }
       // fp8 cache: the scale 2^e of the tokens this thread's score rows hold (16mt + gid and
-      // 16mt + gid + 8) and E, the largest exponent among the tile's valid tokens (slots past
-      // the context may hold any byte: clamped, and left out of E)
+      // 16mt + gid + 8); E, the largest exponent among the tile's valid tokens, no lower than
+      // -112 (so that 2^(14 - E) and 2^(E - 14) are normal floats); and each token's factor
+      // 2^(e - E + 14) for its probability, 0 for slots past the context (they may hold any
+      // byte: their exponent is clamped and left out of E)
       float fsc[4][2];
-      int eex[4][2];
-      int emax = -127;
+      float pfac[4][2];
+      int emax = -112;
       if constexpr (F8) {
 #pragma unroll
         for (int mt = 0; mt < 4; ++mt)
@@ -844,13 +855,17 @@ __global__ void __launch_bounds__(mma_max_threads(DV, NQ), 1) decode_mma_kernel(
           for (int hh = 0; hh < 2; ++hh) {
             const int tok = 16 * mt + gid + 8 * hh;
             const int e = max(ld_shared_s8(exbase + tok), -126);
-            eex[mt][hh] = e;
             fsc[mt][hh] = exp2_int(e);
             if (tok < nv) emax = max(emax, e);
           }
         emax = max(emax, __shfl_xor_sync(kFullMask, emax, 4));
         emax = max(emax, __shfl_xor_sync(kFullMask, emax, 8));
         emax = max(emax, __shfl_xor_sync(kFullMask, emax, 16));
+        const float pscale = exp2_int(14 - emax);
+#pragma unroll
+        for (int mt = 0; mt < 4; ++mt)
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) pfac[mt][hh] = 16 * mt + gid + 8 * hh < nv ? fsc[mt][hh] * pscale : 0.f;
       }
 
       // scores
@@ -869,13 +884,14 @@ __global__ void __launch_bounds__(mma_max_threads(DV, NQ), 1) decode_mma_kernel(
           for (int kp = 0; kp < KSV / 2; ++kp) {
             // matrices: (tokens +0..7, chunk 2kp), (+8..15, 2kp), (+0..7, 2kp+1), (+8..15, 2kp+1)
             uint32_t r4[4];
-            ldsm_x4(f8_addr<DV>(kbase, row, 2 * kp + ld_kc), r4);
-            const uint32_t af[4] = {e4m3x2_to_f16x2(r4[0]), e4m3x2_to_f16x2(r4[1]), e4m3x2_to_f16x2(r4[0] >> 16),
-                                    e4m3x2_to_f16x2(r4[1] >> 16)};
+            ldsm_x4(kbase + 16 * DV * mt + f8_off[kp], r4);
+            uint32_t af[4], ag[4];
+            e4m3x4_to_f16x2x2(r4[0], af[0], af[2]);
+            e4m3x4_to_f16x2x2(r4[1], af[1], af[3]);
+            e4m3x4_to_f16x2x2(r4[2], ag[0], ag[2]);
+            e4m3x4_to_f16x2x2(r4[3], ag[1], ag[3]);
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) mma_16816_f16(sc[nt][mt], af, qb[nt][2 * kp][0], qb[nt][2 * kp][1]);
-            const uint32_t ag[4] = {e4m3x2_to_f16x2(r4[2]), e4m3x2_to_f16x2(r4[3]), e4m3x2_to_f16x2(r4[2] >> 16),
-                                    e4m3x2_to_f16x2(r4[3] >> 16)};
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt)
               mma_16816_f16(sc[nt][mt], ag, qb[nt][2 * kp + 1][0], qb[nt][2 * kp + 1][1]);
@@ -985,17 +1001,19 @@ __global__ void __launch_bounds__(mma_max_threads(DV, NQ), 1) decode_mma_kernel(
           mx = fmaxf(mx, __shfl_xor_sync(kFullMask, mx, 8));
           mx = fmaxf(mx, __shfl_xor_sync(kFullMask, mx, 16));
           const float mn = fmaxf(m[nt], mx);
-          const float alpha = exp2f(m[nt] - mn);
+          const float alpha = F8 ? fast_exp2(m[nt] - mn) : exp2f(m[nt] - mn);
           m[nt] = mn;
           float ps = 0.f;
 #pragma unroll
           for (int mt = 0; mt < 4; ++mt) {
-            const float p0 = exp2f(sv[mt][0] - mn);
-            const float p1 = exp2f(sv[mt][1] - mn);
+            const float p0 = F8 ? fast_exp2(sv[mt][0] - mn) : exp2f(sv[mt][0] - mn);
+            const float p1 = F8 ? fast_exp2(sv[mt][1] - mn) : exp2f(sv[mt][1] - mn);
             ps += p0 + p1;
-            if constexpr (F8) {  // p_j 2^(e_j - E + 14) in f16 parts (slots past the context: p = 0)
-              pb[nt][mt][0] = movmatrix_trans(split_pack_f16(p0 * exp2_int(min(max(eex[mt][0] - emax + 14, -126), 14))));
-              pb[nt][mt][1] = movmatrix_trans(split_pack_f16(p1 * exp2_int(min(max(eex[mt][1] - emax + 14, -126), 14))));
+            if constexpr (F8) {
+              // p_j 2^(e_j - E + 14) as one f16 (11 bits, far beyond the codes' 4; the second
+              // column of the head stays 0)
+              pb[nt][mt][0] = movmatrix_trans(__half_as_ushort(__float2half_rn(p0 * pfac[mt][0])));
+              pb[nt][mt][1] = movmatrix_trans(__half_as_ushort(__float2half_rn(p1 * pfac[mt][1])));
             } else {
               pb[nt][mt][0] = movmatrix_trans(split_pack(p0));
               pb[nt][mt][1] = movmatrix_trans(split_pack(p1));
@@ -1024,7 +1042,6 @@ __global__ void __launch_bounds__(mma_max_threads(DV, NQ), 1) decode_mma_kernel(
             for (int e = 0; e < 4; ++e) ot[nt][md][e] = 0.f;
 #pragma unroll
         for (int kt = 0; kt < 4; ++kt) {
-          const int tok = 16 * kt + ld_row;
           const int jt = 16 * kt + 2 * tq;
 #pragma unroll
           for (int cp = 0; cp < MD / 2; ++cp) {
@@ -1032,12 +1049,12 @@ __global__ void __launch_bounds__(mma_max_threads(DV, NQ), 1) decode_mma_kernel(
             // transposed: a lane gets bytes (d, d+1) of tokens (t, t+1), d = 2gid, t = 2tq; the
             // permutation makes the low half tokens (t, t+1) of row d and the high half of row d+1
             uint32_t x4[4];
-            ldsm_x4_trans(f8_addr<DV>(vbase, tok, 2 * cp + ld_kc), x4);
+            ldsm_x4_trans(vbase + 16 * DV * kt + f8_off[cp], x4);
 #pragma unroll
             for (int h2 = 0; h2 < 2; ++h2) {
-              const uint32_t y0 = byte_perm(x4[2 * h2], 0x3120), y1 = byte_perm(x4[2 * h2 + 1], 0x3120);
-              uint32_t af[4] = {e4m3x2_to_f16x2(y0), e4m3x2_to_f16x2(y0 >> 16), e4m3x2_to_f16x2(y1),
-                                e4m3x2_to_f16x2(y1 >> 16)};
+              uint32_t af[4];
+              e4m3x4_to_f16x2x2(byte_perm(x4[2 * h2], 0x3120), af[0], af[1]);
+              e4m3x4_to_f16x2x2(byte_perm(x4[2 * h2 + 1], 0x3120), af[2], af[3]);
               if (nv < kBlockTokens) {  // slots past the context may hold any byte: zero them
                 af[0] = mask_pair(af[0], jt, nv);
                 af[1] = mask_pair(af[1], jt, nv);
@@ -1049,7 +1066,7 @@ __global__ void __launch_bounds__(mma_max_threads(DV, NQ), 1) decode_mma_kernel(
             }
           }
         }
-        const float unit = exp2_int(emax) * 0x1p-14f;  // exact: a power of two
+        const float unit = exp2_int(emax - 14);  // exact: a power of two
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll

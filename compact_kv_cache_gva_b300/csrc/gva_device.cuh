@@ -154,6 +154,15 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t x) {
   return d;
 }
 
+// Four E4M3 codes (a 32-bit word, the first in the low byte) -> two f16 pairs: lo holds codes
+// 0 and 1, hi codes 2 and 3 (the halves are taken by a register split, not by shifts).
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t x, uint32_t& lo, uint32_t& hi) {
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, l;\n\tcvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(x));
+}
+
 // Two floats -> two E4M3 codes (round to nearest even, magnitudes past 448 clamped to 448),
 // the first in the low byte of the result.
 __device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float first, float second) {

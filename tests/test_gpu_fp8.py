@@ -264,3 +264,13 @@ def test_fp8_cache_against_the_bf16_cache_of_the_same_values():
     d = (outs[1] - outs[0]).double()
     rel = (d.pow(2).mean().sqrt() / outs[0].double().pow(2).mean().sqrt()).item()
     assert rel < 0.05, f"fp8 against bf16 cache: relative RMS {rel:.3e}"
+
+
+def test_fp8_step_form_query():
+    """The automatic step mode keeps the fp8 cache at d_v = 64 on the separate kernels (its
+    fused kernel has no spare warp for the append); the fused mode still applies."""
+    w = synth.custom(dtype="fp8", B=8, H=16, G=4, d_v=64, d_r=16, T=4096)
+    layer = make_layer(w)
+    assert gva.gva_step_is_fused(layer.ctx, w.B, w.max_seq_len) == 0
+    gva.gva_set_step_mode(layer.ctx, gva.GVA_STEP_FUSED)
+    assert gva.gva_step_is_fused(layer.ctx, w.B, w.max_seq_len) == 1
