@@ -306,7 +306,10 @@ class Setup:
         self.one_call = True
         self.fused = n_q == 1 and gva.gva_step_is_fused(self.layer.ctx, w.B, w.max_seq_len) == 1
         R = w.H // w.G
-        nqp_max = 4 if R <= 2 else 2 if R == 4 else 1
+        cols = 16 if w.d_v == 64 else 8  # (query, head) column pairs of a pass
+        nqp_max = 1
+        while 2 * nqp_max <= 4 and 2 * nqp_max * R <= cols:
+            nqp_max *= 2
         passes, q = 0, 0
         while q < n_q:  # the library's passes: the largest power of two that fits, then smaller
             p = 1

@@ -100,7 +100,7 @@ bool make_plan(const gva_ctx* ctx, int B, int max_seq_len, bool sep_k, gva::Plan
   if (nq > 1 && (path != GVA_PATH_MMA || sep_k)) return false;  // several queries: tensor-core path
   const int R = ctx->dims.H / ctx->dims.G;
   int nqp = 1;  // queries per pass: powers of two up to the kernel's limit
-  while (2 * nqp <= nq && 2 * nqp <= gva::mma_max_queries_per_pass(R)) nqp *= 2;
+  while (2 * nqp <= nq && 2 * nqp <= gva::mma_max_queries_per_pass(R, ctx->dims.d_v)) nqp *= 2;
   const long long nt_max = (max_seq_len + GVA_BLOCK_TOKENS - 1) / GVA_BLOCK_TOKENS;
   const long long units_max = static_cast<long long>(B) * ctx->dims.G * nt_max;
   const bool mma = path == GVA_PATH_MMA;

@@ -13,9 +13,10 @@ cudaError_t dispatch_nq(const DecodeArgs& a, const CUtensorMap& mv, const CUtens
       if (a.nqp == 1 && a.nq == 1 && a.d_v == DV) return launch_mma_t<DV, DR, R, 1, false, SEPK, true>(a, mv, mk, grid, stream);
       return cudaErrorInvalidValue;
     }
-    if constexpr (R * 4 <= 8)
+    constexpr int kCols = mma_max_column_pairs(DV);  // (query, head) column pairs of a pass
+    if constexpr (R * 4 <= kCols)
       if (a.nqp == 4) return launch_mma_t<DV, DR, R, 4, true, SEPK, false>(a, mv, mk, grid, stream);
-    if constexpr (R * 2 <= 8)
+    if constexpr (R * 2 <= kCols)
       if (a.nqp == 2) return launch_mma_t<DV, DR, R, 2, true, SEPK, false>(a, mv, mk, grid, stream);
     if (a.nqp == 1 && a.nq > 1) return launch_mma_t<DV, DR, R, 1, true, SEPK, false>(a, mv, mk, grid, stream);
   }
@@ -85,7 +86,16 @@ bool mma_supported(const gva_dims& d, bool sep_k) {
 // 11 KB; five or six were 2-8 % slower) and six at d_r = 32 (12 KB stages, 12 % faster than
 // four); the 19 KB stages of d_v = 128 use three pairs (four give the same time with half
 // the depth).  D takes the rest of shared memory.
-int mma_max_queries_per_pass(int R) { return R <= 2 ? 4 : R == 4 ? 2 : 1; }
+// Queries per pass: the largest power of two up to 4 whose (query, head) column pairs fit,
+// 16 at d_v = 64 (four n-tiles of hi/lo columns, 251-255 registers at 256 threads; the
+// long-context four-query decode in one pass instead of two) and 8 at d_v = 128 (sixteen
+// spilled 508 bytes).
+int mma_max_queries_per_pass(int R, int d_v) {
+  const int cols = mma_max_column_pairs(d_v);
+  int q = 1;
+  while (2 * q <= 4 && 2 * q * R <= cols) q *= 2;
+  return q;
+}
 
 bool mma_shape(const gva_dims& d, bool sep_k, int B, int nqp, int* pairs, int* stages) {
   const bool f8 = d.cache_dtype == GVA_FP8_E4M3;

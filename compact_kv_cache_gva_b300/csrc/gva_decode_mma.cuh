@@ -57,6 +57,8 @@ constexpr int kMmaMaxThreads = 64 * kMmaMaxPairs;  // consumer warps + as many c
 // so they keep more registers per thread; five pairs at 320 threads squeezed the two-query
 // d_v = 64 instance from 194 to 168 registers and made it 11 % slower).
 __host__ __device__ constexpr int mma_max_threads(int dv, int nq) { return dv == 64 && nq == 1 ? 384 : 256; }
+// (query, head) column pairs a multi-query pass may hold: 16 at d_v = 64, 8 at d_v = 128.
+__host__ __device__ constexpr int mma_max_column_pairs(int dv) { return dv == 64 ? 16 : 8; }
 // Consumers a copy warp fills: one (warp pairs), or two for the fp8 value cache at d_v = 64,
 // whose small tiles come fast enough that its consumers are what limits (8 consumers and 4
 // copy warps fill the 384 threads; a copy warp issues a tile in a small fraction of the

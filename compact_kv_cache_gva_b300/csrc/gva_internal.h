@@ -120,8 +120,9 @@ bool mma_supported(const gva_dims& d, bool sep_k);
 // range.  mma_shape picks P and D for the dims (0 if no ring fits).
 constexpr int kMmaMaxPairs = 6;
 bool mma_shape(const gva_dims& d, bool sep_k, int B, int nqp, int* pairs, int* stages);
-// Queries per pass of the tensor-core kernel (its (query, head) column pairs: R*nqp <= 8).
-int mma_max_queries_per_pass(int R);
+// Queries per pass of the tensor-core kernel (its (query, head) column pairs: R*nqp <= 16 at
+// d_v = 64, 8 at d_v = 128; at most 4).
+int mma_max_queries_per_pass(int R, int d_v);
 cudaError_t launch_decode_mma(const DecodeArgs& a, bool sep_k, int grid, cudaStream_t stream);
 // The same kernel over the fp8 value cache (single query per sequence, plain or fused step).
 cudaError_t launch_decode_mma_fp8(const DecodeArgs& a, int grid, cudaStream_t stream);

@@ -66,6 +66,10 @@ CASES = [
     (dict(B=3, H=32, G=8, d_v=128, d_r=24, T_range=(2, 1200)), 2, 0),   # d_v = 128
     (dict(B=2, H=16, G=4, d_v=64, d_r=0, T_range=(2, 400)), 2, 0),       # no positional slice
     (dict(B=2, H=8, G=1, d_v=128, d_r=32, T_range=(8, 200)), 8, 0),      # R=8: 8 passes of 1
+    (dict(B=4, H=16, G=4, d_v=64, d_r=16, T_range=(4, 3000)), 4, 0),     # R=4, d_v=64: one pass of 4
+    (dict(B=3, H=16, G=4, d_v=64, d_r=24, T_range=(6, 900)), 6, 64 * 4),  # passes of 4 + 2
+    (dict(B=3, H=16, G=2, d_v=64, d_r=16, T_range=(2, 700)), 2, 0),      # R=8, d_v=64: one pass of 2
+    (dict(B=2, H=16, G=4, d_v=64, d_r=32, T_range=(4, 500)), 4, 0),      # d_r = 32, one pass of 4
 ]
 
 
