@@ -80,12 +80,13 @@ bool mma_supported(const gva_dims& d, bool sep_k) {
   return r == 1 || r == 2 || r == 4 || r == 8;
 }
 
-// Warp pairs and ring depth, from measurements on B300 (the d_r sweep of the long-context
-// workload, 0 <= d_r <= 32, and the ragged batch): fewer than four pairs lose throughput
+// Consumer warps and ring depth, from measurements on B300 (the d_r sweep of the long-context
+// workload, 0 <= d_r <= 32, and the ragged batch): fewer than four consumers lose throughput
 // even with deeper rings; with d_v = 64, four pairs are best up to d_r = 24 (stages up to
-// 11 KB; five or six were 2-8 % slower) and six at d_r = 32 (12 KB stages, 12 % faster than
-// four); the 19 KB stages of d_v = 128 use three pairs (four give the same time with half
-// the depth).  D takes the rest of shared memory.
+// 11 KB; five or six were 2-8 % slower) and six consumers at d_r = 32 (12 KB stages, 12 %
+// faster than four; three copy warps fill them, mma_consumers_per_copy_warp); the 19 KB stages
+// of d_v = 128 use three pairs (four give the same time with half the depth).  D takes the
+// rest of shared memory.
 // Queries per pass: the largest power of two up to 4 whose (query, head) column pairs fit,
 // 16 at d_v = 64 (four n-tiles of hi/lo columns, 251-255 registers at 256 threads; the
 // long-context four-query decode in one pass instead of two) and 8 at d_v = 128 (sixteen

@@ -59,11 +59,14 @@ constexpr int kMmaMaxThreads = 64 * kMmaMaxPairs;  // consumer warps + as many c
 __host__ __device__ constexpr int mma_max_threads(int dv, int nq) { return dv == 64 && nq == 1 ? 384 : 256; }
 // (query, head) column pairs a multi-query pass may hold: 16 at d_v = 64, 8 at d_v = 128.
 __host__ __device__ constexpr int mma_max_column_pairs(int dv) { return dv == 64 ? 16 : 8; }
-// Consumers a copy warp fills: one (warp pairs), or two for the fp8 value cache at d_v = 64,
-// whose small tiles come fast enough that its consumers are what limits (8 consumers and 4
-// copy warps fill the 384 threads; a copy warp issues a tile in a small fraction of the
-// time a consumer computes one).
-__host__ __device__ constexpr int mma_consumers_per_copy_warp(int dv, bool f8) { return f8 && dv == 64 ? 2 : 1; }
+// Consumers a copy warp fills: one (warp pairs), or two where a CTA wants more consumers than
+// pairs fit (a copy warp issues a tile in a small fraction of the time a consumer computes
+// one): the fp8 value cache at d_v = 64, whose small tiles make its consumers what limits (8
+// consumers and 4 copy warps fill the 384 threads), and the bf16 cache at d_v = 64, d_r = 32
+// (6 consumers and 3 copy warps, which leaves the fused step a patcher and two helpers).
+__host__ __device__ constexpr int mma_consumers_per_copy_warp(int dv, int dr, bool f8) {
+  return dv == 64 && (f8 || dr == 32) ? 2 : 1;
+}
 constexpr int kSubTileBytes = kBlockTokens * 128;  // one [64 tokens][64 columns] bf16 swizzled box
 
 // ---- PTX wrappers ------------------------------------------------------------------------
@@ -301,21 +304,23 @@ constexpr int kSmemLimit = 226 * 1024;
 __host__ __device__ inline int cum_bytes(int B) { return ((B + 1) * 4 + 15) / 16 * 16; }
 inline int ring_fixed_bytes(int B) { return 1024 + kCtrlBytes + cum_bytes(B); }
 
-// One CTA streams one contiguous range of units (gva_sched.cuh) with P warp pairs.  Consumer
-// warp c (warps 0..P-1) takes units k = c, c + P, c + 2P, ... of the range; its d-th unit
-// lands in its private ring slot d % D.  Copy warp c (warp P + c) serves consumer c alone:
-// its lanes look up the block ids of the consumer's next 32 units at once, one batch ahead,
-// and lane 0 issues each unit's copies (TMA for the value (and key) tile, a bulk copy for
-// the positional-key tile) as soon as the consumer has released the slot.  Every barrier
-// has one waiter that waits in order (the consumer on "full", the copy warp on "empty"),
-// so phase parities are unambiguous, and about P*(D-1) tiles are in flight per SM while P
-// are being computed.  The copy warps take the issue work (a few hundred cycles per tile)
-// and the dependent block-table reads off the consumers' path.
+// One CTA streams one contiguous range of units (gva_sched.cuh) with P consumer warps and
+// P/CPC copy warps (CPC = mma_consumers_per_copy_warp: 1, warp pairs, or 2).  Consumer warp
+// c (warps 0..P-1) takes units k = c, c + P, c + 2P, ... of the range; its d-th unit lands
+// in its private ring slot d % D.  Copy warp c (warp P + c) serves the units k = c, c + P/CPC,
+// ... in unit order (with CPC = 1, exactly consumer c's): its lanes look up the block ids of
+// its next 32 units at once, one batch ahead, and lane 0 issues each unit's copies (TMA for
+// the value (and key) tile, a bulk copy for the positional-key tile) as soon as the unit's
+// consumer has released the slot.  Every barrier has one waiter that waits in order (the
+// consumer on "full", the copy warp on "empty"), so phase parities are unambiguous, and about
+// P*(D-1) tiles are in flight per SM while P are being computed.  The copy warps take the
+// issue work (a few hundred cycles per tile) and the dependent block-table reads off the
+// consumers' path.
 //
-// A FUSED launch adds E = (threads of the instance - 64*P)/32 prologue warps (warps 2P..2P+E-1)
-// that help form the queries; the first of them then stays as the patcher warp, the others
-// exit.  (The six-pair instance, d_v = 64 with d_r = 32, has none to spare: its consumers
-// append themselves.)
+// A FUSED launch adds E = (threads of the instance)/32 - P - P/CPC prologue warps that help
+// form the queries; the first of them then stays as the patcher warp, the others exit.  (The
+// fp8 instances at d_v = 64, 8 consumers and 4 copy warps, have none to spare: their
+// consumers append themselves.)
 //
 // F8 instances read the fp8 value cache: the value tile is E4M3 codes (a tensor copy of
 // 64 x DV bytes) plus its 64 scale exponents (a bulk copy), converted to f16 in registers for
@@ -344,7 +349,7 @@ __global__ void __launch_bounds__(mma_max_threads(DV, NQ), 1) decode_mma_kernel(
   static_assert(!SEPK || DR == 0, "the key-cache form has no positional slice");
   static_assert(!FUSED || (NQ == 1 && !CAUSAL && !SEPK), "the fused step is single-query GVA decode");
   static_assert(!F8 || (NQ == 1 && !CAUSAL && !SEPK), "the fp8 value cache is read by single-query GVA decode");
-  constexpr int CPC = mma_consumers_per_copy_warp(DV, F8);
+  constexpr int CPC = mma_consumers_per_copy_warp(DV, DR, F8);
   constexpr int QS = step_stage_floats(R, DV, DR);  // floats of one staged segment (fused step)
 
   extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -361,9 +366,9 @@ __global__ void __launch_bounds__(mma_max_threads(DV, NQ), 1) decode_mma_kernel(
   // fused step: a sequence's last tile lands on landed[s] instead of full[s]; the patcher warp
   // writes the new token into it and then completes full[s]
   uint64_t* landed = reinterpret_cast<uint64_t*>(blks + kMaxStages);
-  // Fused instances with a spare warp (all but the bf16 six-pair one) give the append to it: the
+  // Fused instances with a spare warp (all but the fp8 ones at d_v = 64) give the append to it: the
   // consumers' loop is then the plain kernel's.
-  constexpr bool kPatcher = FUSED && !(DV == 64 && (DR == 32 || F8));
+  constexpr bool kPatcher = FUSED && !(DV == 64 && F8);
   unsigned char* tiles = smem + kCtrlBytes;
   unsigned char* krs = tiles + N * L::kOpBytes;
   unsigned char* exs = krs + N * L::kKrBytes;  // fp8 cache: the scale exponents of each stage's tile
@@ -1138,7 +1143,7 @@ cudaError_t launch_mma_t(const DecodeArgs& a, const CUtensorMap& mv, const CUten
                          cudaStream_t stream) {
   using L = MmaLayout<DV, DR, SEPK, F8>;
   const int P = a.group_warps, D = a.n_stages;
-  constexpr int CPC = mma_consumers_per_copy_warp(DV, F8);
+  constexpr int CPC = mma_consumers_per_copy_warp(DV, DR, F8);
   const int warps = P + P / CPC;
   if (P < 1 || P % CPC || 32 * warps > mma_max_threads(DV, NQ) || D < 1 || P * D > kMaxStages)
     return cudaErrorInvalidValue;
@@ -1148,7 +1153,7 @@ cudaError_t launch_mma_t(const DecodeArgs& a, const CUtensorMap& mv, const CUten
   // the fused step fills the instance's thread budget with prologue warps, and the shared
   // memory budget with query stages; its patcher warp is the first prologue warp
   const int threads = FUSED ? mma_max_threads(DV, NQ) : 32 * warps;
-  if (FUSED && !(DV == 64 && (DR == 32 || F8)) && threads <= 32 * warps) return cudaErrorInvalidValue;
+  if (FUSED && !(DV == 64 && F8) && threads <= 32 * warps) return cudaErrorInvalidValue;
   DecodeArgs args = a;
   args.spare_smem = FUSED ? kSmemLimit - smem : 0;
   const int dyn_smem = FUSED ? kSmemLimit : smem;
