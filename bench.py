@@ -361,6 +361,14 @@ def flusher():
     return flush
 
 
+def head_start():
+    """Keeps the device busy (a spin kernel of about 25 ms) while the host enqueues a flushed
+    loop, so that the device never waits for the host between a step's two events: a flushed
+    step is short, and a host thread slowed by the clock-sampling thread could otherwise fall
+    behind it and put its own latency inside the timed region."""
+    torch.cuda._sleep(50_000_000)
+
+
 def time_steps(run_step, K, flush, clocks=None):
     """Device seconds for K steps.  Inputs larger than L2: one event pair around the K
     back-to-back steps.  Otherwise L2 is flushed before every step, outside per-step events.
@@ -379,6 +387,7 @@ def time_steps(run_step, K, flush, clocks=None):
         torch.cuda.synchronize()
         return e0.elapsed_time(e1) / 1e3
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    head_start()
     for k, (a, b) in enumerate(evs):
         flush()
         a.record()
@@ -421,9 +430,10 @@ def run_profile(args):
     """The step's split-T partial pass alone, launched --warmup + --steps times, for a profiler."""
     torch.cuda.init()
     w = workload(args)
-    S = Setup(w, seed=0, path=args.path, split_tokens=args.split_tokens, step_mode=args.step_mode)
+    S = Setup(w, seed=0, path=args.path, split_tokens=args.split_tokens, step_mode=args.step_mode, n_q=args.nq)
     S.prime_queries()
-    partial, _ = partial_calls(S)
+    # multi-query: the one-call step (append, absorb, then the multi-query partial pass and combine)
+    partial = partial_calls(S)[0] if S.n_q == 1 else S.step
     for _ in range(args.warmup + args.steps):
         partial()
     torch.cuda.synchronize()
@@ -485,6 +495,8 @@ def run_ours(args, rank, ws):
     # per-call breakdown (events between calls; informative only, they stop launch overlap)
     nb = min(K, 100)
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(nb)]
+    if flush:
+        head_start()
     for k in range(nb):
         if flush:
             flush()
@@ -642,6 +654,8 @@ def time_partial(S, K, flush):
         partial()
         combine()
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    if flush:
+        head_start()
     for a, b in evs:
         if flush:
             flush()
@@ -697,6 +711,8 @@ def run_e2e(S, steps, flush, graph=True, ws=1):
         run = capture(fn).replay if graph else fn
         barrier(ws)
         ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        if flush:
+            head_start()
         for k in range(steps + 3):
             if flush:
                 flush()

@@ -110,7 +110,7 @@ bool mma_shape(const gva_dims& d, bool sep_k, int B, int nqp, int* pairs, int* s
   // The fp8 cache's consumers do more work per byte than the bf16 ones: at d_v = 64 eight
   // consumers, two per copy warp (mma_consumers_per_copy_warp), fill the 384 threads (the
   // long-context step: 6 pairs 119 us, 4 pairs 155 us); at d_v = 128 three pairs.
-  const int P = nqp > 1 ? mma_max_threads(d.d_v, nqp) / 64
+  const int P = nqp > 1 ? (d.d_v == 64 ? 8 : mma_max_threads(d.d_v, nqp) / 64)
                 : f8    ? (d.d_v == 64 ? 8 : 3)
                         : std::min(stage <= 11 * 1024 ? 4 : stage <= 12 * 1024 ? 6 : 3,
                                    mma_max_threads(d.d_v, nqp) / 64);

@@ -52,21 +52,28 @@ namespace {
 
 constexpr int kMmaMaxThreads = 64 * kMmaMaxPairs;  // consumer warps + as many copy warps
 
-// Threads a kernel instance is compiled for: six warp pairs on the single-query d_v = 64
-// path, four elsewhere (d_v = 128 and several queries per pass hold twice the accumulators,
-// so they keep more registers per thread; five pairs at 320 threads squeezed the two-query
-// d_v = 64 instance from 194 to 168 registers and made it 11 % slower).
+// Threads a kernel instance is compiled for: twelve warps on the single-query d_v = 64 path,
+// eight elsewhere.  A warp's registers come from its sub-partition's quarter of the register
+// file, so the per-thread limit follows the warps a sub-partition hosts: up to 255 with eight
+// warps (two each), 168 with nine to twelve.  Several queries per pass and d_v = 128 hold
+// twice the accumulators and keep eight warps.
 __host__ __device__ constexpr int mma_max_threads(int dv, int nq) { return dv == 64 && nq == 1 ? 384 : 256; }
 // (query, head) column pairs a multi-query pass may hold: 16 at d_v = 64, 8 at d_v = 128.
 __host__ __device__ constexpr int mma_max_column_pairs(int dv) { return dv == 64 ? 16 : 8; }
-// Consumers a copy warp fills: one (warp pairs), or two where a CTA wants more consumers than
+// Consumers a copy warp fills: one (warp pairs), or more where a CTA wants more consumers than
 // pairs fit (a copy warp issues a tile in a small fraction of the time a consumer computes
 // one): the fp8 value cache at d_v = 64, whose small tiles make its consumers what limits (8
-// consumers and 4 copy warps fill the 384 threads), and the bf16 cache at d_v = 64, d_r = 32
+// consumers and 4 copy warps fill the 384 threads), the bf16 cache at d_v = 64, d_r = 32
 // (6 consumers and 3 copy warps, which leaves the fused step a patcher and two helpers).
 __host__ __device__ constexpr int mma_consumers_per_copy_warp(int dv, int dr, bool f8) {
   return dv == 64 && (f8 || dr == 32) ? 2 : 1;
 }
+// The passes of a multi-query call at d_v = 64 (and a call's single-query remainder pass, which
+// shares their plan) have no copy warps: 8 consumers, two per sub-partition so that one
+// computes while the other waits on its dependent products, each issuing the copies of its own
+// ring.  A tile costs them over ten times longer to compute than its copies take to issue, and
+// one copy warp for seven consumers left them waiting for tiles.
+__host__ __device__ constexpr bool mma_self_fed(int dv, bool multi) { return dv == 64 && multi; }
 constexpr int kSubTileBytes = kBlockTokens * 128;  // one [64 tokens][64 columns] bf16 swizzled box
 
 // ---- PTX wrappers ------------------------------------------------------------------------
@@ -246,6 +253,12 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo_half, float hi_half) {
   return a | (b << 16);
 }
 
+// Packs two floats as bf16 with one conversion (first in the low half).
+__device__ __forceinline__ uint32_t pack2_bf16(float lo_half, float hi_half) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo_half, hi_half);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
 // x = hi + lo with hi = bf16(x) and lo = bf16(x - hi); returns (hi, lo) packed.
 __device__ __forceinline__ uint32_t split_pack(float x) {
   const __nv_bfloat16 hi = __float2bfloat16_rn(x);
@@ -305,7 +318,7 @@ __host__ __device__ inline int cum_bytes(int B) { return ((B + 1) * 4 + 15) / 16
 inline int ring_fixed_bytes(int B) { return 1024 + kCtrlBytes + cum_bytes(B); }
 
 // One CTA streams one contiguous range of units (gva_sched.cuh) with P consumer warps and
-// P/CPC copy warps (CPC = mma_consumers_per_copy_warp: 1, warp pairs, or 2).  Consumer warp
+// P/CPC copy warps (CPC = mma_consumers_per_copy_warp: 1, warp pairs, 2 or 7).  Consumer warp
 // c (warps 0..P-1) takes units k = c, c + P, c + 2P, ... of the range; its d-th unit lands
 // in its private ring slot d % D.  Copy warp c (warp P + c) serves the units k = c, c + P/CPC,
 // ... in unit order (with CPC = 1, exactly consumer c's): its lanes look up the block ids of
@@ -356,7 +369,8 @@ __global__ void __launch_bounds__(mma_max_threads(DV, NQ), 1) decode_mma_kernel(
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const int P = a.group_warps;  // consumer warps
-  const int PC = P / CPC;       // copy warps; blockDim.x == 32 * (P + PC), plus the prologue warps of a fused launch
+  constexpr bool kSelfFed = mma_self_fed(DV, CAUSAL);
+  const int PC = kSelfFed ? 0 : P / CPC;  // copy warps; blockDim.x == 32 * (P + PC), plus the prologue warps of a fused launch
   const int D = a.n_stages;     // ring slots per pair
   const int N = P * D;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem);
@@ -386,7 +400,7 @@ __global__ void __launch_bounds__(mma_max_threads(DV, NQ), 1) decode_mma_kernel(
     }
     mbar_init_fence();
   }
-  if (warp == P && lane == 0) {
+  if (warp == (kSelfFed ? 0 : P) && lane == 0) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmv)) : "memory");
     if (SEPK) asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmk)) : "memory");
   }
@@ -598,36 +612,68 @@ __global__ void __launch_bounds__(mma_max_threads(DV, NQ), 1) decode_mma_kernel(
   }
 
   // ------------------------------------------------------------------ copy warps
-  if (warp >= P) {
+  // Lane i of a warp that issues the copies of the units base + stride*d (d < n_mine): block id
+  // (or -1), group and valid tokens of unit d0 + i.
+  auto lookup = [&](int base, int stride, int n_mine, int d0, int& blk, int& grp, int& nv) {
+    blk = -1;
+    grp = 0;
+    nv = 0;
+    const int d = d0 + lane;
+    if (d < n_mine) {
+      const UnitCursor cu = cursor_at(u0 + base + static_cast<long long>(stride) * d, cum, a.B, a.G);
+      grp = cu.g;
+      const int T = a.seq_lens[cu.b];  // issued beside the table read: one round trip
+      if (cu.t >= a.max_blocks) {
+        flag_error(a.err, GVA_DEVERR_POSITION);
+      } else {
+        const int id = a.block_table[static_cast<long long>(cu.b) * a.max_blocks + cu.t];
+        if (id >= 0 && id < a.num_blocks) {
+          blk = id;
+          nv = T - cu.t * kBlockTokens;  // tokens from the tile's start to the end (>= 1)
+        } else {
+          flag_error(a.err, GVA_DEVERR_BLOCK_ID);
+        }
+      }
+    }
+  };
+  // One thread: the copies of a unit (block bj, group gj, vj tokens to the end) into stage s,
+  // completing full[s] (or, for a sequence's last tile in a fused step, landed[s]).
+  auto issue = [&](int s, int bj, int gj, int vj) {
+    nvs[s] = bj >= 0 ? vj : 0;  // published by the arrive below (release)
+    if (FUSED) blks[s] = bj;
+    if (bj >= 0) {
+      // fused step: a sequence's last tile goes to the patcher before the consumer
+      uint64_t* bar = kPatcher && vj <= kBlockTokens ? &landed[s] : &full[s];
+      mbar_arrive_expect_tx(bar, L::kTx);
+      unsigned char* st = tiles + s * L::kOpBytes;
+      if constexpr (F8) {
+        // the tile's codes as DV/2 rows of 128 bytes, and its 64 exponents
+        tma_load_2d(st, &tmv, 0, (bj * a.G + gj) * (DV / 2), bar);
+        bulk_g2s(exs + s * L::kExBytes, a.v_exp + (static_cast<long long>(bj) * a.G + gj) * kBlockTokens,
+                 L::kExBytes, bar);
+      } else {
+        const int y = (bj * a.G + gj) * kBlockTokens;
+#pragma unroll
+        for (int sub = 0; sub < L::kSub; ++sub) {
+          tma_load_2d(st + sub * kSubTileBytes, &tmv, 64 * sub, y, bar);
+          if (SEPK) tma_load_2d(st + L::kVBytes + sub * kSubTileBytes, &tmk, 64 * sub, y, bar);
+        }
+      }
+      if (!SEPK && DR > 0)
+        bulk_g2s(krs + s * L::kKrBytes,
+                 static_cast<const __nv_bfloat16*>(a.kr_pool) + static_cast<size_t>(bj) * kBlockTokens * DR,
+                 L::kKrBytes, bar);
+    } else {
+      mbar_arrive(&full[s]);  // completes the phase with no data; the tile is skipped
+    }
+  };
+  if (!kSelfFed && warp >= P) {
     // copy warp c serves the units k = c + PC*i of the range (i < n_mine): CPC consumers, unit
     // k going to consumer k % P as its (k / P)-th unit
     const int c = warp - P;
     const int n_mine = n > c ? (n - c + PC - 1) / PC : 0;
-    // lane i: block id (or -1), group and valid tokens of this warp's unit d0 + i
-    auto lookup = [&](int d0, int& blk, int& grp, int& nv) {
-      blk = -1;
-      grp = 0;
-      nv = 0;
-      const int d = d0 + lane;
-      if (d < n_mine) {
-        const UnitCursor cu = cursor_at(u0 + c + static_cast<long long>(PC) * d, cum, a.B, a.G);
-        grp = cu.g;
-        const int T = a.seq_lens[cu.b];  // issued beside the table read: one round trip
-        if (cu.t >= a.max_blocks) {
-          flag_error(a.err, GVA_DEVERR_POSITION);
-        } else {
-          const int id = a.block_table[static_cast<long long>(cu.b) * a.max_blocks + cu.t];
-          if (id >= 0 && id < a.num_blocks) {
-            blk = id;
-            nv = T - cu.t * kBlockTokens;  // tokens from the tile's start to the end (>= 1)
-          } else {
-            flag_error(a.err, GVA_DEVERR_BLOCK_ID);
-          }
-        }
-      }
-    };
     int blk, grp, nv;
-    lookup(0, blk, grp, nv);
+    lookup(c, PC, n_mine, 0, blk, grp, nv);
     if constexpr (FUSED) asm volatile("bar.arrive %0, %1;" ::"r"(kLookupBarrier), "r"(static_cast<int>(blockDim.x)) : "memory");
     int issued = 0;
     bool ok = true;
@@ -638,7 +684,7 @@ __global__ void __launch_bounds__(mma_max_threads(DV, NQ), 1) decode_mma_kernel(
     };
     for (int d0 = 0; d0 < n_mine && ok; d0 += 32) {
       int nblk, ngrp, nnv;
-      lookup(d0 + 32, nblk, ngrp, nnv);  // next batch: loads in flight while this one issues
+      lookup(c, PC, n_mine, d0 + 32, nblk, ngrp, nnv);  // next batch: loads in flight while this one issues
       const int cnt = min(32, n_mine - d0);
       for (int j = 0; j < cnt; ++j) {
         const int bj = __shfl_sync(kFullMask, blk, j);
@@ -650,33 +696,7 @@ __global__ void __launch_bounds__(mma_max_threads(DV, NQ), 1) decode_mma_kernel(
           // the slot's previous unit must have been released by the consumer
           if (dd >= D && !mbar_wait_bounded(&empty[s], ((dd / D) & 1) ^ 1)) ok = false;
           if (ok) {
-            nvs[s] = bj >= 0 ? vj : 0;  // published by the arrive below (release)
-            if (FUSED) blks[s] = bj;
-            if (bj >= 0) {
-              // fused step: a sequence's last tile goes to the patcher before the consumer
-              uint64_t* bar = kPatcher && vj <= kBlockTokens ? &landed[s] : &full[s];
-              mbar_arrive_expect_tx(bar, L::kTx);
-              unsigned char* st = tiles + s * L::kOpBytes;
-              if constexpr (F8) {
-                // the tile's codes as DV/2 rows of 128 bytes, and its 64 exponents
-                tma_load_2d(st, &tmv, 0, (bj * a.G + gj) * (DV / 2), bar);
-                bulk_g2s(exs + s * L::kExBytes, a.v_exp + (static_cast<long long>(bj) * a.G + gj) * kBlockTokens,
-                         L::kExBytes, bar);
-              } else {
-                const int y = (bj * a.G + gj) * kBlockTokens;
-#pragma unroll
-                for (int sub = 0; sub < L::kSub; ++sub) {
-                  tma_load_2d(st + sub * kSubTileBytes, &tmv, 64 * sub, y, bar);
-                  if (SEPK) tma_load_2d(st + L::kVBytes + sub * kSubTileBytes, &tmk, 64 * sub, y, bar);
-                }
-              }
-              if (!SEPK && DR > 0)
-                bulk_g2s(krs + s * L::kKrBytes,
-                         static_cast<const __nv_bfloat16*>(a.kr_pool) + static_cast<size_t>(bj) * kBlockTokens * DR,
-                         L::kKrBytes, bar);
-            } else {
-              mbar_arrive(&full[s]);  // completes the phase with no data; the tile is skipped
-            }
+            issue(s, bj, gj, vj);
             ++issued;
           }
         }
@@ -713,6 +733,23 @@ __global__ void __launch_bounds__(mma_max_threads(DV, NQ), 1) decode_mma_kernel(
   constexpr int rec_floats = DV + 4;
   UnitCursor cc = cursor_at(u0 + k, cum, a.B, a.G);
   int slot = 0, ph = 0;  // ring slot and phase parity of this warp's next unit
+  // Self-fed consumer: its units are k = warp + P*i (i < n_own), unit i in slot i % D.  Lanes
+  // hold the block ids of units [f0, f0 + 32) and of the next 32 (looked up a batch ahead); the
+  // first D units' copies go out before the query is loaded, unit i + D's once unit i is done.
+  int n_own = 0, f0 = 0, i_own = 0;
+  int fb = -1, fg = 0, fv = 0, xb = -1, xg = 0, xv = 0;
+  if constexpr (kSelfFed) {
+    n_own = (n - warp + P - 1) / P;
+    lookup(warp, P, n_own, 0, fb, fg, fv);
+    lookup(warp, P, n_own, 32, xb, xg, xv);
+    const int first = min(D, n_own);
+    for (int j = 0; j < first; ++j) {
+      const int bj = __shfl_sync(kFullMask, fb, j);
+      const int gj = __shfl_sync(kFullMask, fg, j);
+      const int vj = __shfl_sync(kFullMask, fv, j);
+      if (lane == 0) issue(warp * D + j, bj, gj, vj);
+    }
+  }
 
   // query fragments (B operand of the score product) of the current (b, g), pre-scaled by
   // scale*log2(e); column n = 2*c + part for column pair c = i*R + h (query q0 + i of this
@@ -765,17 +802,29 @@ __global__ void __launch_bounds__(mma_max_threads(DV, NQ), 1) decode_mma_kernel(
     }
   };
 
-  float m[NT], l[NT], o[NT][MD][4];
+  // Wide instances (an even number of n-tiles: several queries per pass, or 8 heads a group)
+  // give each accumulator column a column pair of its own: the probabilities' bf16 high parts
+  // of n-tiles 2i and 2i+1 form one B operand and their remainders another, two products into
+  // the same accumulator, whose column 2q + j then holds column pair (2i + j)*4 + q.  That
+  // halves the output accumulators (the narrow form keeps a pair's high and low products in
+  // two columns and adds them at the end).  They also take 2^x from the special-function
+  // unit directly (relative error about 2^-22).
+  constexpr bool kWide = !F8 && NT % 2 == 0;
+  constexpr int NO = kWide ? NT / 2 : NT;  // accumulator n-tiles
+  constexpr bool kFastExp = F8 || kWide;
+  float m[NT], l[NT], o[NO][MD][4];
   auto reset_state = [&]() {
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       m[nt] = -INFINITY;
       l[nt] = 0.f;
+    }
+#pragma unroll
+    for (int no = 0; no < NO; ++no)
 #pragma unroll
       for (int md = 0; md < MD; ++md)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) o[nt][md][e] = 0.f;
-    }
+        for (int e = 0; e < 4; ++e) o[no][md][e] = 0.f;
   };
   const int gid = lane >> 2, tq = lane & 3;
   // Partial record of segment f for this warp: per column pair (m, l, 0, 0, o[0..DV)).
@@ -797,8 +846,13 @@ __global__ void __launch_bounds__(mma_max_threads(DV, NQ), 1) decode_mma_kernel(
 #pragma unroll
         for (int md = 0; md < MD; ++md) {
           // fp8 cache: A-fragment rows gid and gid + 8 of chunk md are value rows 2gid, 2gid + 1
-          r[4 + 16 * md + (F8 ? 2 * gid : gid)] = o[nt][md][0] + o[nt][md][1];
-          r[4 + 16 * md + (F8 ? 2 * gid + 1 : gid + 8)] = o[nt][md][2] + o[nt][md][3];
+          if constexpr (kWide) {
+            r[4 + 16 * md + gid] = o[nt / 2][md][nt % 2];
+            r[4 + 16 * md + gid + 8] = o[nt / 2][md][2 + nt % 2];
+          } else {
+            r[4 + 16 * md + (F8 ? 2 * gid : gid)] = o[nt][md][0] + o[nt][md][1];
+            r[4 + 16 * md + (F8 ? 2 * gid + 1 : gid + 8)] = o[nt][md][2] + o[nt][md][3];
+          }
         }
       }
     }
@@ -942,7 +996,16 @@ __global__ void __launch_bounds__(mma_max_threads(DV, NQ), 1) decode_mma_kernel(
       // whole by every query of the pass (the earliest one is q0) and take the unmasked form;
       // the masked form also keeps the state of a query that sees no token of the tile (its
       // position precedes the tile) unchanged.
-      uint32_t pb[NT][4][2];
+      uint32_t pb[NO][4][2];               // B operands: the probabilities (wide: their high parts)
+      uint32_t pl[kWide ? NO : 1][4][2];   // wide: the remainders
+      float pr[kWide ? NT : 1][4][2];      // wide: this tile's probabilities, packed below
+      float al[NT];                        // wide: each column pair's rescale factor
+      auto ex2 = [&](float x) {
+        if constexpr (kFastExp)
+          return fast_exp2(x);
+        else
+          return exp2f(x);
+      };
       auto softmax = [&](auto masked) {
         constexpr bool kMasked = decltype(masked)::value;
 #pragma unroll
@@ -972,22 +1035,31 @@ __global__ void __launch_bounds__(mma_max_threads(DV, NQ), 1) decode_mma_kernel(
           mx = fmaxf(mx, __shfl_xor_sync(kFullMask, mx, 16));
           const float mn = fmaxf(m[nt], mx);
           const bool none = kMasked && mn == -INFINITY;
-          const float alpha = none ? 1.f : exp2f(m[nt] - mn);
+          const float alpha = none || (kWide && mn == m[nt]) ? 1.f : ex2(m[nt] - mn);
           m[nt] = mn;
           float ps = 0.f;
 #pragma unroll
           for (int mt = 0; mt < 4; ++mt) {
-            const float p0 = none ? 0.f : exp2f(sv[mt][0] - mn);
-            const float p1 = none ? 0.f : exp2f(sv[mt][1] - mn);
+            const float p0 = none ? 0.f : ex2(sv[mt][0] - mn);
+            const float p1 = none ? 0.f : ex2(sv[mt][1] - mn);
             ps += p0 + p1;
-            pb[nt][mt][0] = movmatrix_trans(split_pack(p0));
-            pb[nt][mt][1] = movmatrix_trans(split_pack(p1));
+            if constexpr (kWide) {
+              pr[nt][mt][0] = p0;
+              pr[nt][mt][1] = p1;
+            } else {
+              pb[nt][mt][0] = movmatrix_trans(split_pack(p0));
+              pb[nt][mt][1] = movmatrix_trans(split_pack(p1));
+            }
           }
           l[nt] = fmaf(l[nt], alpha, ps);
+          if constexpr (kWide) {
+            al[nt] = alpha;
+          } else {
 #pragma unroll
-          for (int md = 0; md < MD; ++md)
+            for (int md = 0; md < MD; ++md)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) o[nt][md][e] *= alpha;
+              for (int e = 0; e < 4; ++e) o[nt][md][e] *= alpha;
+          }
         }
       };
       if constexpr (!CAUSAL) {
@@ -1008,15 +1080,18 @@ __global__ void __launch_bounds__(mma_max_threads(DV, NQ), 1) decode_mma_kernel(
           mx = fmaxf(mx, __shfl_xor_sync(kFullMask, mx, 8));
           mx = fmaxf(mx, __shfl_xor_sync(kFullMask, mx, 16));
           const float mn = fmaxf(m[nt], mx);
-          const float alpha = F8 ? fast_exp2(m[nt] - mn) : exp2f(m[nt] - mn);
+          const float alpha = kWide && mn == m[nt] ? 1.f : ex2(m[nt] - mn);
           m[nt] = mn;
           float ps = 0.f;
 #pragma unroll
           for (int mt = 0; mt < 4; ++mt) {
-            const float p0 = F8 ? fast_exp2(sv[mt][0] - mn) : exp2f(sv[mt][0] - mn);
-            const float p1 = F8 ? fast_exp2(sv[mt][1] - mn) : exp2f(sv[mt][1] - mn);
+            const float p0 = ex2(sv[mt][0] - mn);
+            const float p1 = ex2(sv[mt][1] - mn);
             ps += p0 + p1;
-            if constexpr (F8) {
+            if constexpr (kWide) {
+              pr[nt][mt][0] = p0;
+              pr[nt][mt][1] = p1;
+            } else if constexpr (F8) {
               // p_j 2^(e_j - E + 14) as one f16 (11 bits, far beyond the codes' 4; the second
               // column of the head stays 0)
               pb[nt][mt][0] = movmatrix_trans(__half_as_ushort(__float2half_rn(p0 * pfac[mt][0])));
@@ -1027,15 +1102,50 @@ __global__ void __launch_bounds__(mma_max_threads(DV, NQ), 1) decode_mma_kernel(
             }
           }
           l[nt] = fmaf(l[nt], alpha, ps);
+          if constexpr (kWide) {
+            al[nt] = alpha;
+          } else {
 #pragma unroll
-          for (int md = 0; md < MD; ++md)
+            for (int md = 0; md < MD; ++md)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) o[nt][md][e] *= alpha;
+              for (int e = 0; e < 4; ++e) o[nt][md][e] *= alpha;
+          }
         }
       } else if (nrem - (a.nq - 1 - a.q0) >= kBlockTokens) {
         softmax(std::false_type{});
       } else {
         softmax(std::true_type{});
+      }
+      if constexpr (kWide) {
+        // rescale the accumulators, skipped by the whole warp when no running maximum moved
+        bool moved = false;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) moved |= al[nt] != 1.f;
+        if (__any_sync(kFullMask, moved)) {
+#pragma unroll
+          for (int no = 0; no < NO; ++no)
+#pragma unroll
+            for (int md = 0; md < MD; ++md) {
+              o[no][md][0] *= al[2 * no];
+              o[no][md][1] *= al[2 * no + 1];
+              o[no][md][2] *= al[2 * no];
+              o[no][md][3] *= al[2 * no + 1];
+            }
+        }
+        // high parts and remainders of n-tiles 2no and 2no+1 (columns 2tq and 2tq+1 of the
+        // 8x8 blocks that movmatrix turns into B fragments)
+#pragma unroll
+        for (int no = 0; no < NO; ++no)
+#pragma unroll
+          for (int mt = 0; mt < 4; ++mt)
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+              const float x0 = pr[2 * no][mt][hh], x1 = pr[2 * no + 1][mt][hh];
+              const uint32_t hi = pack2_bf16(x0, x1);
+              pb[no][mt][hh] = movmatrix_trans(hi);
+              pl[no][mt][hh] = movmatrix_trans(pack2_bf16(x0 - __uint_as_float(hi << 16),
+                                                          x1 - __uint_as_float(hi & 0xffff0000u)));
+            }
       }
 
       // output: O^T[d x n] += V^T[d x tok] P[tok x n]
@@ -1097,17 +1207,45 @@ __global__ void __launch_bounds__(mma_max_threads(DV, NQ), 1) decode_mma_kernel(
             af[2] = mask_pair(af[2], jt + 8, nv);
             af[3] = mask_pair(af[3], jt + 8, nv);
           }
+          if constexpr (kWide) {
 #pragma unroll
-          for (int nt = 0; nt < NT; ++nt) mma_16816(o[nt][md], af, pb[nt][kt][0], pb[nt][kt][1]);
+            for (int no = 0; no < NO; ++no) {
+              mma_16816(o[no][md], af, pb[no][kt][0], pb[no][kt][1]);
+              mma_16816(o[no][md], af, pl[no][kt][0], pl[no][kt][1]);
+            }
+          } else {
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) mma_16816(o[nt][md], af, pb[nt][kt][0], pb[nt][kt][1]);
+          }
         }
       }
       }
     }
     // the stage may be refilled (after this warp's own writes into it, if any, are ordered
     // before the copy engine's)
-    if (FUSED && !kPatcher && patched) fence_proxy_async_smem();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[s]);
+    if constexpr (kSelfFed) {
+      const int inext = i_own + D;
+      if (inext < n_own) {
+        if (inext - f0 >= 32) {  // the next batch of block ids becomes current
+          f0 += 32;
+          fb = xb;
+          fg = xg;
+          fv = xv;
+          lookup(warp, P, n_own, f0 + 32, xb, xg, xv);
+        }
+        const int bj = __shfl_sync(kFullMask, fb, inext - f0);
+        const int gj = __shfl_sync(kFullMask, fg, inext - f0);
+        const int vj = __shfl_sync(kFullMask, fv, inext - f0);
+        fence_proxy_async_smem();  // this warp's reads of the stage come before the copy's writes
+        __syncwarp();
+        if (lane == 0) issue(s, bj, gj, vj);
+      }
+      ++i_own;
+    } else {
+      if (FUSED && !kPatcher && patched) fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
+    }
     k += NC;
     if (k >= n) break;
     const int pb_ = cc.b, pg = cc.g;
@@ -1127,8 +1265,13 @@ __global__ void __launch_bounds__(mma_max_threads(DV, NQ), 1) decode_mma_kernel(
     return;
   }
   // A copy never arrived: report, and leave empty records for every segment still owed so
-  // the combine reads defined values.  (The copy warp waits for its copies in flight.)
-  if (lane == 0) flag_error(a.err, GVA_DEVERR_TIMEOUT);
+  // the combine reads defined values.  (The copy warp waits for its copies in flight; a
+  // self-fed consumer waits for its own: units i_own .. i_own + D - 1.)
+  if (lane == 0) {
+    flag_error(a.err, GVA_DEVERR_TIMEOUT);
+    if constexpr (kSelfFed)
+      for (int j = i_own; j < min(i_own + D, n_own); ++j) (void)mbar_wait_bounded(&full[warp * D + j % D], (j / D) & 1);
+  }
   reset_state();
   flush(segment_of(cc.g, cc.b, a.B));
   for (k += NC; k < n; k += NC) {
@@ -1144,7 +1287,7 @@ cudaError_t launch_mma_t(const DecodeArgs& a, const CUtensorMap& mv, const CUten
   using L = MmaLayout<DV, DR, SEPK, F8>;
   const int P = a.group_warps, D = a.n_stages;
   constexpr int CPC = mma_consumers_per_copy_warp(DV, DR, F8);
-  const int warps = P + P / CPC;
+  const int warps = P + (mma_self_fed(DV, CAUSAL) ? 0 : P / CPC);
   if (P < 1 || P % CPC || 32 * warps > mma_max_threads(DV, NQ) || D < 1 || P * D > kMaxStages)
     return cudaErrorInvalidValue;
   if (a.nqp != NQ || (a.nq > 1) != CAUSAL || (a.fused != 0) != FUSED) return cudaErrorInvalidValue;
@@ -1180,8 +1323,6 @@ cudaError_t launch_mma_t(const DecodeArgs& a, const CUtensorMap& mv, const CUten
   return cudaLaunchKernelEx(&cfg, kern, args, mv, mk);
 }
 
-// Queries per pass: the instances built are NQ in {1, 2, 4} with R*NQ <= 8.
-
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                    const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
                                    const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
@@ -1199,8 +1340,6 @@ EncodeTiledFn encode_fn() {
   }
   return fn;
 }
-
-// A pool seen as a 2-D bf16 tensor: rows = NB*G*64 token rows of d_v columns; one box = 64
 
 }  // namespace
 }  // namespace gva
