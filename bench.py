@@ -36,9 +36,11 @@ METRIC = "GVA decode-attention cache-read GB/s (% of B300 HBM peak) and context 
 # or the plain one), from the ncu captures summarised in profiles/ (absent where no capture of
 # the current kernel exists).  The ragged batch's figure is the capture of its first 32
 # sequences (73,600 units) scaled to the full batch's 254,224 units.
-TRAFFIC = {("long-context-bf16", "plain"): 572_503_808, ("long-context-bf16", "fused"): 572_519_168,
-           ("layer-350m-bf16", "fused"): 71_833_088, ("dr24-bf16", "fused"): 296_072_704,
-           ("ragged-paged-bf16", "plain"): 4_272_515_956}
+TRAFFIC = {("long-context-bf16", "plain"): 570_841_344, ("long-context-bf16", "fused"): 571_154_944,
+           ("long-context-bf16-dr32", "fused"): 604_714_240,
+           ("layer-350m-bf16", "fused"): 71_829_504, ("dr24-bf16", "fused"): 296_206_848,
+           ("ragged-paged-bf16", "plain"): 4_271_621_972,
+           ("long-context-fp8", "plain"): 306_742_016, ("long-context-fp8", "fused"): 306_979_840}
 L2_BYTES = 126 * 1024 * 1024
 NOMINAL_HBM_GBS = 8000.0  # B300 HBM3e, nominal
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
@@ -188,36 +190,73 @@ class SmiClockSampler:
     summary = None  # set below
 
 
+class _Nvml:
+    """The few NVML reads the clock record needs, through the driver's libnvidia-ml by ctypes
+    (read-only queries: SM clock, maximum SM clock, active clock-event reasons)."""
+    NVML_CLOCK_SM = 1
+
+    def __init__(self):
+        import ctypes
+        self.c = ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        self._ok(self.lib.nvmlInit_v2(), "nvmlInit_v2")
+        self.h = ctypes.c_void_p()
+        uuid = str(torch.cuda.get_device_properties(torch.cuda.current_device()).uuid)
+        uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+        if self.lib.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(self.h)) != 0:
+            self._ok(self.lib.nvmlDeviceGetHandleByIndex_v2(torch.cuda.current_device(), ctypes.byref(self.h)),
+                     "nvmlDeviceGetHandleByIndex_v2")
+        try:
+            self._reasons_fn = self.lib.nvmlDeviceGetCurrentClocksEventReasons
+        except AttributeError:
+            self._reasons_fn = self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+
+    @staticmethod
+    def _ok(rc, what):
+        if rc != 0:
+            raise RuntimeError(f"{what} returned {rc}")
+
+    def _clock(self, fn):
+        v = self.c.c_uint()
+        self._ok(fn(self.h, self.NVML_CLOCK_SM, self.c.byref(v)), fn.__name__)
+        return int(v.value)
+
+    def max_sm(self):
+        return self._clock(self.lib.nvmlDeviceGetMaxClockInfo)
+
+    def sm(self):
+        return self._clock(self.lib.nvmlDeviceGetClockInfo)
+
+    def reasons(self):
+        v = self.c.c_ulonglong()
+        self._ok(self._reasons_fn(self.h, self.c.byref(v)), "clock-event reasons")
+        return int(v.value)
+
+
 class ClockSampler:
-    """Samples SM clock and clock-event reasons through NVML while the timed region runs."""
+    """Samples SM clock and clock-event reasons through NVML while the timed region runs: a
+    polling thread, plus readings that the timing loop takes while the device is busy."""
 
     def __new__(cls, period_s=0.01):
         try:
-            import pynvml  # noqa: F401
-        except ImportError:
+            nv = _Nvml()
+        except Exception:
             return SmiClockSampler()
-        return super().__new__(cls)
+        self = super().__new__(cls)
+        self.nv = nv
+        return self
 
     def __init__(self, period_s=0.01):
         self.period = period_s
         self.samples = []
         self.max_mhz = None
         self.ok = False
+        self.err = ""
         self._stop = threading.Event()
         try:
-            import pynvml
-            pynvml.nvmlInit()
-            self.nv = pynvml
-            h = None
-            try:
-                uuid = str(torch.cuda.get_device_properties(torch.cuda.current_device()).uuid)
-                h = pynvml.nvmlDeviceGetHandleByUUID(("GPU-" + uuid) if not uuid.startswith("GPU-") else uuid)
-            except Exception:
-                h = pynvml.nvmlDeviceGetHandleByIndex(torch.cuda.current_device())
-            self.h = h
-            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(h, pynvml.NVML_CLOCK_SM)
+            self.max_mhz = self.nv.max_sm()
             self.ok = True
-        except Exception as e:  # no NVML: report that instead of guessing
+        except Exception as e:  # report that instead of guessing
             self.err = repr(e)
 
     def sample(self):
@@ -225,14 +264,8 @@ class ClockSampler:
         a timed region shorter than the polling period still has samples)."""
         if not self.ok:
             return
-        nv = self.nv
         try:
-            sm = nv.nvmlDeviceGetClockInfo(self.h, nv.NVML_CLOCK_SM)
-            try:
-                reasons = nv.nvmlDeviceGetCurrentClocksEventReasons(self.h)
-            except Exception:
-                reasons = nv.nvmlDeviceGetCurrentClocksThrottleReasons(self.h)
-            self.samples.append((sm, int(reasons)))
+            self.samples.append((self.nv.sm(), self.nv.reasons()))
         except Exception:
             pass
 
@@ -362,39 +395,42 @@ def flusher():
 
 
 def head_start():
-    """Keeps the device busy (a spin kernel of about 25 ms) while the host enqueues a flushed
-    loop, so that the device never waits for the host between a step's two events: a flushed
+    """Keeps the device busy (a spin kernel of about 25 ms) while the host starts enqueueing a
+    timed loop, so that the device never waits for the host inside the timed region: a flushed
     step is short, and a host thread slowed by the clock-sampling thread could otherwise fall
-    behind it and put its own latency inside the timed region."""
+    behind it; and an unflushed loop would otherwise start with the device idle until the host
+    has enqueued its first step."""
     torch.cuda._sleep(50_000_000)
 
 
 def time_steps(run_step, K, flush, clocks=None):
     """Device seconds for K steps.  Inputs larger than L2: one event pair around the K
     back-to-back steps.  Otherwise L2 is flushed before every step, outside per-step events.
-    With `clocks`, one clock reading is taken after the first step is enqueued and one after
-    the last (the device is then still working through the queue)."""
+    With `clocks`, two clock readings are taken once every step is enqueued, while the device
+    is still working through the queue (the host enqueues a step in a fraction of its device
+    time), beside the sampler's polling thread; a reading inside the loop could stall the
+    enqueueing host and leave the device idle inside the timed region."""
     tick = clocks.sample if clocks is not None else (lambda: None)
     if flush is None:
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        head_start()  # the first step's launch is queued before the device reaches e0
         e0.record()
-        for k in range(K):
+        for _ in range(K):
             run_step()
-            if k == 0:
-                tick()
         e1.record()
+        tick()
         tick()
         torch.cuda.synchronize()
         return e0.elapsed_time(e1) / 1e3
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     head_start()
-    for k, (a, b) in enumerate(evs):
+    for a, b in evs:
         flush()
         a.record()
         run_step()
         b.record()
-        if k == 0 or k == K - 1:
-            tick()
+    tick()
+    tick()
     torch.cuda.synchronize()
     return sum(a.elapsed_time(b) for a, b in evs) / 1e3
 
@@ -711,8 +747,7 @@ def run_e2e(S, steps, flush, graph=True, ws=1):
         run = capture(fn).replay if graph else fn
         barrier(ws)
         ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
-        if flush:
-            head_start()
+        head_start()
         for k in range(steps + 3):
             if flush:
                 flush()
