@@ -44,11 +44,46 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const DecodeAr
     mbar_init(&bar, 1);
     mbar_init_fence();
   }
+  // cum[b], the tiles of sequence b and cum[B]: from the lengths before the wait when this
+  // call's partial pass launched this kernel (the partial pass's rule: a length outside
+  // [max(1, nq), max_seq_len] counts as no tile), else from the header that pass wrote.
+  __shared__ int red[2][kCombineWarps];
+  __shared__ int nt_b;
+  int cb = 0, nt = 0, ctot = 0;
+  if (a.combine_after_partial) {
+    int before = 0, total = 0;
+    for (int i = tid; i < a.B; i += kCombineThreads) {
+      const int T = a.seq_lens[i];
+      const int t = T >= a.nq && T >= 1 && T <= a.max_seq_len ? (T + kBlockTokens - 1) / kBlockTokens : 0;
+      total += t;
+      if (i < b) before += t;
+      if (i == b) nt_b = t;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      before += __shfl_xor_sync(kFullMask, before, o);
+      total += __shfl_xor_sync(kFullMask, total, o);
+    }
+    if (lane == 0) {
+      red[0][warp] = before;
+      red[1][warp] = total;
+    }
+    __syncthreads();
+    for (int w = 0; w < kCombineWarps; ++w) {
+      cb += red[0][w];
+      ctot += red[1][w];
+    }
+    nt = nt_b;
+  }
   griddep_wait();
   griddep_launch_dependents();
-  const int* cum = reinterpret_cast<const int*>(a.part);
   const float* recs = a.part + header_bytes(a.B) / 4;
-  const int nt = cum[b + 1] - cum[b];
+  if (!a.combine_after_partial) {
+    const int* hdr = reinterpret_cast<const int*>(a.part);
+    cb = hdr[b];
+    nt = hdr[b + 1] - cb;
+    ctot = hdr[a.B];
+  }
   // sub-record hh of a record: query q0 + hh / Rh of the pass, head hh % Rh of group g
   const int Rh = a.H / a.G;
   auto out_row = [&](int hh) {
@@ -59,10 +94,10 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const DecodeAr
     for (int i = tid; i < R * DV; i += kCombineThreads) out_row(i / DV)[i % DV] = 0.f;
     return;
   }
-  const long long U = static_cast<long long>(a.G) * cum[a.B];
+  const long long U = static_cast<long long>(a.G) * ctot;
   const long long NG = a.n_groups;
   const int C = a.group_warps;
-  const long long s = static_cast<long long>(g) * cum[a.B] + cum[b];  // first unit of (g, b)
+  const long long s = static_cast<long long>(g) * ctot + cb;  // first unit of (g, b)
   const long long c0 = range_of(s, U, NG);
   const int nrec = static_cast<int>(range_of(s + nt - 1, U, NG) - c0 + 1) * C;
   const long long f = segment_of(g, b, a.B);

@@ -404,13 +404,17 @@ __global__ void __launch_bounds__(mma_max_threads(DV, NQ), 1) decode_mma_kernel(
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmv)) : "memory");
     if (SEPK) asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmk)) : "memory");
   }
-  // Everything below may read what earlier work in the stream wrote.
-  griddep_wait();
-  // The block table (and, for the fused step, the key maps) into L2 while the lengths are
-  // scanned: the first copies wait on table reads, and the cache stream of the previous call
-  // has evicted them.  (Both are device memory; the step's own inputs may be host memory.)
+  // The lengths, the block table (and, for the fused step, the key maps) into L2 while this
+  // kernel still waits for the earlier work in the stream: the scan and the first copies wait
+  // on them, and the cache stream of the previous call has evicted them.  A prefetch returns no
+  // data, and L2 keeps the lines coherent with any write that earlier work still makes, so it
+  // may go out before the wait.  (All three are device memory; the step's own inputs may be
+  // host memory.)
+  warm_l2(a.seq_lens, static_cast<long long>(a.B) * 4);
   warm_l2(a.block_table, static_cast<long long>(a.B) * a.max_blocks * 4);
   if constexpr (FUSED) warm_l2(a.M, static_cast<long long>(a.H) * DV * DV * 4);
+  // Everything below may read what earlier work in the stream wrote.
+  griddep_wait();
   build_prefix<kMmaMaxThreads>(a, cum, lens_s);  // ends with __syncthreads: the barriers are set up
   griddep_launch_dependents();
 

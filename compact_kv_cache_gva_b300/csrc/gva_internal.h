@@ -71,6 +71,12 @@ struct DecodeArgs {
   // the shared memory the ring leaves over (spare_smem bytes) when they fit, here otherwise.
   float* qstage;
   int spare_smem;
+  // Combine pass launched right after this call's partial pass (its programmatic dependent):
+  // every write that preceded the partial pass, the lengths included, is complete when the
+  // combine starts, so it may form its prefix sums from seq_lens before its own wait instead of
+  // reading the header after it (set for batches of up to 256 sequences: each combine CTA
+  // reads all B lengths).
+  int combine_after_partial;
 };
 
 // Floats of one fused-step query stage (a multiple of 4, so every stage is 16-byte aligned).
