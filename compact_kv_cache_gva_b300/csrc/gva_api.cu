@@ -182,10 +182,6 @@ int step_form(const gva_ctx* ctx, int B, const gva::Plan& plan) {
       // kernel does that work faster.
       const gva_dims& d = ctx->dims;
       const long long map_bytes = 4ll * (d.H / d.G) * d.d_v * d.d_n;
-      // the fp8 cache at d_v = 64 runs eight consumers and no spare warp, so its fused kernel
-      // appends from the consumers: slower than the separate kernels (long-context: 95.8 us
-      // against 93.7 us a step)
-      if (d.cache_dtype == GVA_FP8_E4M3 && d.d_v == 64) return 0;
       return step_fusable(ctx, plan) && map_bytes <= kStepAutoMapBytes &&
                      static_cast<long long>(B) * d.G <= kStepAutoSegmentsPerRange * plan.n_groups
                  ? 1

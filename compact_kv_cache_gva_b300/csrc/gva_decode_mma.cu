@@ -107,11 +107,12 @@ bool mma_shape(const gva_dims& d, bool sep_k, int B, int nqp, int* pairs, int* s
   auto depth = [&](int p) { return std::min(avail / (p * stage), kMaxStages / p); };
   // Several queries per pass double the consumers' work per tile: as many pairs as fit (four
   // rather than three at d_v = 128: the ragged batch's two-query decode 690 us against 817 us).
-  // The fp8 cache's consumers do more work per byte than the bf16 ones: at d_v = 64 eight
-  // consumers, two per copy warp (mma_consumers_per_copy_warp), fill the 384 threads (the
-  // long-context step: 6 pairs 119 us, 4 pairs 155 us); at d_v = 128 three pairs.
+  // The fp8 cache's consumers do more work per byte than the bf16 ones: at d_v = 64 twelve
+  // self-fed consumers fill the 384 threads (mma_self_fed; the long-context partial pass: 4
+  // pairs 120 us, 6 pairs 108.6 us, 8 consumers with 4 copy warps 84.0 us, 12 self-fed
+  // 82.0 us, and the fused pass 90.4 -> 84.5 us); at d_v = 128 three pairs.
   const int P = nqp > 1 ? (d.d_v == 64 ? 8 : mma_max_threads(d.d_v, nqp) / 64)
-                : f8    ? (d.d_v == 64 ? 8 : 3)
+                : f8    ? (d.d_v == 64 ? 12 : 3)
                         : std::min(stage <= 11 * 1024 ? 4 : stage <= 12 * 1024 ? 6 : 3,
                                    mma_max_threads(d.d_v, nqp) / 64);
   const int D = depth(P);

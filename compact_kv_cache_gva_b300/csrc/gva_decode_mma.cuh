@@ -60,20 +60,22 @@ constexpr int kMmaMaxThreads = 64 * kMmaMaxPairs;  // consumer warps + as many c
 __host__ __device__ constexpr int mma_max_threads(int dv, int nq) { return dv == 64 && nq == 1 ? 384 : 256; }
 // (query, head) column pairs a multi-query pass may hold: 16 at d_v = 64, 8 at d_v = 128.
 __host__ __device__ constexpr int mma_max_column_pairs(int dv) { return dv == 64 ? 16 : 8; }
-// Consumers a copy warp fills: one (warp pairs), or more where a CTA wants more consumers than
+// Consumers a copy warp fills: one (warp pairs), or two where a CTA wants more consumers than
 // pairs fit (a copy warp issues a tile in a small fraction of the time a consumer computes
-// one): the fp8 value cache at d_v = 64, whose small tiles make its consumers what limits (8
-// consumers and 4 copy warps fill the 384 threads), the bf16 cache at d_v = 64, d_r = 32
-// (6 consumers and 3 copy warps, which leaves the fused step a patcher and two helpers).
+// one): the bf16 cache at d_v = 64, d_r = 32 (6 consumers and 3 copy warps, which leaves the
+// fused step a patcher and two helpers).  The fp8 instances at d_v = 64 are self-fed (below).
 __host__ __device__ constexpr int mma_consumers_per_copy_warp(int dv, int dr, bool f8) {
-  return dv == 64 && (f8 || dr == 32) ? 2 : 1;
+  return dv == 64 && dr == 32 && !f8 ? 2 : 1;
 }
 // The passes of a multi-query call at d_v = 64 (and a call's single-query remainder pass, which
 // shares their plan) have no copy warps: 8 consumers, two per sub-partition so that one
 // computes while the other waits on its dependent products, each issuing the copies of its own
 // ring.  A tile costs them over ten times longer to compute than its copies take to issue, and
 // one copy warp for seven consumers left them waiting for tiles.
-__host__ __device__ constexpr bool mma_self_fed(int dv, bool multi) { return dv == 64 && multi; }
+// The fp8 value cache at d_v = 64 does the same with twelve consumers: its small tiles make
+// the consumers' instructions the limit, and the copy warps' issue slots serve them better as
+// a third consumer per sub-partition.
+__host__ __device__ constexpr bool mma_self_fed(int dv, bool multi, bool f8) { return dv == 64 && (multi || f8); }
 constexpr int kSubTileBytes = kBlockTokens * 128;  // one [64 tokens][64 columns] bf16 swizzled box
 
 // ---- PTX wrappers ------------------------------------------------------------------------
@@ -332,8 +334,8 @@ inline int ring_fixed_bytes(int B) { return 1024 + kCtrlBytes + cum_bytes(B); }
 //
 // A FUSED launch adds E = (threads of the instance)/32 - P - P/CPC prologue warps that help
 // form the queries; the first of them then stays as the patcher warp, the others exit.  (The
-// fp8 instances at d_v = 64, 8 consumers and 4 copy warps, have none to spare: their
-// consumers append themselves.)
+// fp8 instances at d_v = 64, twelve self-fed consumers, have none to spare: their consumers
+// append themselves.)
 //
 // F8 instances read the fp8 value cache: the value tile is E4M3 codes (a tensor copy of
 // 64 x DV bytes) plus its 64 scale exponents (a bulk copy), converted to f16 in registers for
@@ -369,7 +371,7 @@ __global__ void __launch_bounds__(mma_max_threads(DV, NQ), 1) decode_mma_kernel(
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const int P = a.group_warps;  // consumer warps
-  constexpr bool kSelfFed = mma_self_fed(DV, CAUSAL);
+  constexpr bool kSelfFed = mma_self_fed(DV, CAUSAL, F8);
   const int PC = kSelfFed ? 0 : P / CPC;  // copy warps; blockDim.x == 32 * (P + PC), plus the prologue warps of a fused launch
   const int D = a.n_stages;     // ring slots per pair
   const int N = P * D;
@@ -725,6 +727,25 @@ __global__ void __launch_bounds__(mma_max_threads(DV, NQ), 1) decode_mma_kernel(
   }
 
   // ------------------------------------------------------------------ consumer warps
+  // Self-fed consumer: its units are k = warp + P*i (i < n_own), unit i in slot i % D.  Lanes
+  // hold the block ids of units [f0, f0 + 32) and of the next 32 (looked up a batch ahead); the
+  // first D units' copies go out first (ahead of a fused launch's prologue), unit i + D's once
+  // unit i is done.
+  static_assert(!(kSelfFed && kPatcher), "self-fed consumers append the new token themselves");
+  int n_own = 0, f0 = 0, i_own = 0;
+  int fb = -1, fg = 0, fv = 0, xb = -1, xg = 0, xv = 0;
+  if constexpr (kSelfFed) {
+    n_own = n > warp ? (n - warp + P - 1) / P : 0;
+    lookup(warp, P, n_own, 0, fb, fg, fv);
+    lookup(warp, P, n_own, 32, xb, xg, xv);
+    const int first = min(D, n_own);
+    for (int j = 0; j < first; ++j) {
+      const int bj = __shfl_sync(kFullMask, fb, j);
+      const int gj = __shfl_sync(kFullMask, fg, j);
+      const int vj = __shfl_sync(kFullMask, fv, j);
+      if (lane == 0) issue(warp * D + j, bj, gj, vj);
+    }
+  }
   if constexpr (FUSED) {
     const int E = static_cast<int>(blockDim.x / 32) - P - PC;
     absorb_segments(warp, P + E);
@@ -737,23 +758,6 @@ __global__ void __launch_bounds__(mma_max_threads(DV, NQ), 1) decode_mma_kernel(
   constexpr int rec_floats = DV + 4;
   UnitCursor cc = cursor_at(u0 + k, cum, a.B, a.G);
   int slot = 0, ph = 0;  // ring slot and phase parity of this warp's next unit
-  // Self-fed consumer: its units are k = warp + P*i (i < n_own), unit i in slot i % D.  Lanes
-  // hold the block ids of units [f0, f0 + 32) and of the next 32 (looked up a batch ahead); the
-  // first D units' copies go out before the query is loaded, unit i + D's once unit i is done.
-  int n_own = 0, f0 = 0, i_own = 0;
-  int fb = -1, fg = 0, fv = 0, xb = -1, xg = 0, xv = 0;
-  if constexpr (kSelfFed) {
-    n_own = (n - warp + P - 1) / P;
-    lookup(warp, P, n_own, 0, fb, fg, fv);
-    lookup(warp, P, n_own, 32, xb, xg, xv);
-    const int first = min(D, n_own);
-    for (int j = 0; j < first; ++j) {
-      const int bj = __shfl_sync(kFullMask, fb, j);
-      const int gj = __shfl_sync(kFullMask, fg, j);
-      const int vj = __shfl_sync(kFullMask, fv, j);
-      if (lane == 0) issue(warp * D + j, bj, gj, vj);
-    }
-  }
 
   // query fragments (B operand of the score product) of the current (b, g), pre-scaled by
   // scale*log2(e); column n = 2*c + part for column pair c = i*R + h (query q0 + i of this
@@ -1291,7 +1295,7 @@ cudaError_t launch_mma_t(const DecodeArgs& a, const CUtensorMap& mv, const CUten
   using L = MmaLayout<DV, DR, SEPK, F8>;
   const int P = a.group_warps, D = a.n_stages;
   constexpr int CPC = mma_consumers_per_copy_warp(DV, DR, F8);
-  const int warps = P + (mma_self_fed(DV, CAUSAL) ? 0 : P / CPC);
+  const int warps = P + (mma_self_fed(DV, CAUSAL, F8) ? 0 : P / CPC);
   if (P < 1 || P % CPC || 32 * warps > mma_max_threads(DV, NQ) || D < 1 || P * D > kMaxStages)
     return cudaErrorInvalidValue;
   if (a.nqp != NQ || (a.nq > 1) != CAUSAL || (a.fused != 0) != FUSED) return cudaErrorInvalidValue;

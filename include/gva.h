@@ -219,9 +219,8 @@ size_t gva_decode_workspace_size_multi(const gva_ctx* ctx, int B, int n_q, int m
 /* Step mode for gva_set_step_mode. */
 typedef enum {
   GVA_STEP_AUTO = 0,     /* fused where it applies, the key maps of a group are small
-                            (R*d_v*d_n*4 <= 64 KB), the batch has at most 8 (group,
-                            sequence) segments per unit range, and the cache is not fp8 at
-                            d_v = 64; else the separate kernels */
+                            (R*d_v*d_n*4 <= 64 KB) and the batch has at most 8 (group,
+                            sequence) segments per unit range; else the separate kernels */
   GVA_STEP_FUSED = 1,    /* fused kernel (GVA_ERR_UNSUPPORTED where it does not apply) */
   GVA_STEP_SEPARATE = 2  /* append, absorb and decode as separate kernels */
 } gva_step_mode;

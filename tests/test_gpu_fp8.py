@@ -267,10 +267,10 @@ def test_fp8_cache_against_the_bf16_cache_of_the_same_values():
 
 
 def test_fp8_step_form_query():
-    """The automatic step mode keeps the fp8 cache at d_v = 64 on the separate kernels (its
-    fused kernel has no spare warp for the append); the fused mode still applies."""
+    """The automatic step mode fuses the fp8 step under the same rule as the bf16 one (small
+    key maps, few segments per range); the separate mode still applies."""
     w = synth.custom(dtype="fp8", B=8, H=16, G=4, d_v=64, d_r=16, T=4096)
     layer = make_layer(w)
-    assert gva.gva_step_is_fused(layer.ctx, w.B, w.max_seq_len) == 0
-    gva.gva_set_step_mode(layer.ctx, gva.GVA_STEP_FUSED)
     assert gva.gva_step_is_fused(layer.ctx, w.B, w.max_seq_len) == 1
+    gva.gva_set_step_mode(layer.ctx, gva.GVA_STEP_SEPARATE)
+    assert gva.gva_step_is_fused(layer.ctx, w.B, w.max_seq_len) == 0
