@@ -88,7 +88,7 @@ bool mma_supported(const gva_dims& d, bool sep_k) {
 // of d_v = 128 use three pairs (four give the same time with half the depth).  D takes the
 // rest of shared memory.
 // Queries per pass: the largest power of two up to 4 whose (query, head) column pairs fit,
-// 16 at d_v = 64 (four n-tiles of hi/lo columns, 251-255 registers at 256 threads; the
+// 16 at d_v = 64 (four n-tiles of hi/lo columns, about 240 registers at 256 threads; the
 // long-context four-query decode in one pass instead of two) and 8 at d_v = 128 (sixteen
 // spilled 508 bytes).
 int mma_max_queries_per_pass(int R, int d_v) {
@@ -105,8 +105,11 @@ bool mma_shape(const gva_dims& d, bool sep_k, int B, int nqp, int* pairs, int* s
   const int stage = op + (sep_k ? 0 : kBlockTokens * d.d_r * 2) + (f8 ? kBlockTokens : 0);
   const int avail = kSmemLimit - ring_fixed_bytes(B);
   auto depth = [&](int p) { return std::min(avail / (p * stage), kMaxStages / p); };
-  // Several queries per pass double the consumers' work per tile: as many pairs as fit (four
-  // rather than three at d_v = 128: the ragged batch's two-query decode 690 us against 817 us).
+  // Several queries per pass double the consumers' work per tile: at d_v = 64 eight self-fed
+  // consumers with two-slot rings (mma_self_fed; the long-context two-query decode 110 us,
+  // against 115 and 128 us with seven or six consumers and three slots, and 120 us with four
+  // warp pairs); at d_v = 128 as many pairs as fit (four rather than three: the ragged batch's
+  // two-query decode 690 us against 817 us).
   // The fp8 cache's consumers do more work per byte than the bf16 ones: at d_v = 64 twelve
   // self-fed consumers fill the 384 threads (mma_self_fed; the long-context partial pass: 4
   // pairs 120 us, 6 pairs 108.6 us, 8 consumers with 4 copy warps 84.0 us, 12 self-fed

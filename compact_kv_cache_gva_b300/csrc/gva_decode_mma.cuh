@@ -20,16 +20,18 @@
 // into the B fragment of the output product (tokens on k).
 //
 // Work split (gva_sched.cuh): one CTA per SM streams a balanced range of (sequence, group,
-// tile) units with a few warp pairs: a copy warp keeps its consumer's private ring of tiles
-// full (TMA), and the consumer warps take the range's tiles round-robin, each writing one
-// partial record per (sequence, group) it touched.  The matching GQA form (a separate key cache, no positional
-// slice) reuses the kernel with the key tile scored instead of the value tile.
+// tile) units with a few consumer warps, each with a private ring of tiles that a copy warp
+// keeps full (TMA) or, in the self-fed instances (multi-query passes and the fp8 cache at
+// d_v = 64), that the consumer refills itself.  The consumers take the range's tiles
+// round-robin, each writing one partial record per (sequence, group) it touched.  The matching
+// GQA form (a separate key cache, no positional slice) reuses the kernel with the key tile
+// scored instead of the value tile.
 //
 // Fused decode step (FUSED instances): the absorption q' = M_h q_c and the rotation of the
 // positional query (the neighbouring step of the decode path) run in the kernel's prologue
 // instead of a kernel of their own.  The consumer warps, and the warps the launch has to spare
-// beside the pairs, compute them for every (group, sequence) segment of the CTA's range while
-// the copy warps fill the rings.  Each output is an fp32 dot product in the absorb kernel's
+// beside them and their copy warps, compute them for every (group, sequence) segment of the
+// CTA's range while the rings fill.  Each output is an fp32 dot product in the absorb kernel's
 // summation order, so the results are bit-identical to it.  The new token of every sequence
 // (the last position of its context) is appended between the copy engine and the consumer:
 // the sequence's last tile lands on a barrier of its own, a patcher warp writes the value row
