@@ -36,11 +36,11 @@ METRIC = "GVA decode-attention cache-read GB/s (% of B300 HBM peak) and context 
 # or the plain one), from the ncu captures summarised in profiles/ (absent where no capture of
 # the current kernel exists).  The ragged batch's figure is the capture of its first 32
 # sequences (73,600 units) scaled to the full batch's 254,224 units.
-TRAFFIC = {("long-context-bf16", "plain"): 570_841_344, ("long-context-bf16", "fused"): 571_154_944,
-           ("long-context-bf16-dr32", "fused"): 604_714_240,
-           ("layer-350m-bf16", "fused"): 71_829_504, ("dr24-bf16", "fused"): 296_206_848,
+TRAFFIC = {("long-context-bf16", "plain"): 570_978_048, ("long-context-bf16", "fused"): 571_264_768,
+           ("long-context-bf16-dr32", "fused"): 604_555_264,
+           ("layer-350m-bf16", "fused"): 71_835_648, ("dr24-bf16", "fused"): 294_979_328,
            ("ragged-paged-bf16", "plain"): 4_271_621_972,
-           ("long-context-fp8", "plain"): 306_742_016, ("long-context-fp8", "fused"): 306_979_840}
+           ("long-context-fp8", "plain"): 306_572_032, ("long-context-fp8", "fused"): 306_774_016}
 L2_BYTES = 126 * 1024 * 1024
 NOMINAL_HBM_GBS = 8000.0  # B300 HBM3e, nominal
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
