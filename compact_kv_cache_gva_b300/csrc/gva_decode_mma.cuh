@@ -95,6 +95,16 @@ __device__ __forceinline__ void tma_load_2d_evict_first(void* dst, const CUtenso
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar)), "l"(pol)
       : "memory");
 }
+// A bulk copy with an L2 evict-last policy: for tiles several CTAs read at about the same time.
+__device__ __forceinline__ void bulk_g2s_evict_last(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::
+          "r"(smem_addr(dst)),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(pol)
+      : "memory");
+}
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y,
                                             uint64_t* bar) {
   asm volatile(
@@ -660,13 +670,21 @@ __global__ void __launch_bounds__(mma_max_threads(DV, NQ), 1) decode_mma_kernel(
   // One thread: the copies of a unit (block bj, group gj, vj tokens to the end) into stage s,
   // completing full[s] (or, for a sequence's last tile in a fused step, landed[s]).
   // The value (or code) tile of a unit is read once: at d_v = 64 its copy carries an L2
-  // evict-first policy (long-context step 97.4 -> 95.1 us, the fp8 step 91.9 -> 90.5 us); at
-  // d_v = 128 the ragged batch's step was 0.9 % slower with it, so those copies keep the default.
+  // evict-first policy (long-context step 97.4 -> 95.1 us, the fp8 step 91.9 -> 90.5 us), and
+  // the positional-key tile, which the G CTAs of a slice read together, an evict-last one
+  // (95.1 -> 94.5 us).  At d_v = 128 the ragged batch's step was 0.9 % slower with evict-first
+  // values, so those copies keep the default policy.
   auto load_tile = [&](void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
     if constexpr (DV == 64)
       tma_load_2d_evict_first(dst, map, x, y, bar);
     else
       tma_load_2d(dst, map, x, y, bar);
+  };
+  auto load_kr = [&](void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    if constexpr (DV == 64)
+      bulk_g2s_evict_last(dst, src, bytes, bar);
+    else
+      bulk_g2s(dst, src, bytes, bar);
   };
   auto issue = [&](int s, int bj, int gj, int vj) {
     nvs[s] = bj >= 0 ? vj : 0;  // published by the arrive below (release)
@@ -690,7 +708,7 @@ __global__ void __launch_bounds__(mma_max_threads(DV, NQ), 1) decode_mma_kernel(
         }
       }
       if (!SEPK && DR > 0)
-        bulk_g2s(krs + s * L::kKrBytes,
+        load_kr(krs + s * L::kKrBytes,
                  static_cast<const __nv_bfloat16*>(a.kr_pool) + static_cast<size_t>(bj) * kBlockTokens * DR,
                  L::kKrBytes, bar);
     } else {
