@@ -36,11 +36,11 @@ METRIC = "GVA decode-attention cache-read GB/s (% of B300 HBM peak) and context 
 # or the plain one), from the ncu captures summarised in profiles/ (absent where no capture of
 # the current kernel exists).  The ragged batch's figure is the capture of its first 32
 # sequences (73,600 units) scaled to the full batch's 254,224 units.
-TRAFFIC = {("long-context-bf16", "plain"): 570_978_048, ("long-context-bf16", "fused"): 571_264_768,
-           ("long-context-bf16-dr32", "fused"): 604_555_264,
-           ("layer-350m-bf16", "fused"): 71_835_648, ("dr24-bf16", "fused"): 294_979_328,
+TRAFFIC = {("long-context-bf16", "plain"): 570_688_256, ("long-context-bf16", "fused"): 571_011_072,
+           ("long-context-bf16-dr32", "fused"): 604_663_040,
+           ("layer-350m-bf16", "fused"): 71_835_904, ("dr24-bf16", "fused"): 295_033_600,
            ("ragged-paged-bf16", "plain"): 4_271_621_972,
-           ("long-context-fp8", "plain"): 306_572_032, ("long-context-fp8", "fused"): 306_774_016}
+           ("long-context-fp8", "plain"): 306_442_752, ("long-context-fp8", "fused"): 306_741_248}
 L2_BYTES = 126 * 1024 * 1024
 NOMINAL_HBM_GBS = 8000.0  # B300 HBM3e, nominal
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
