@@ -180,7 +180,7 @@ gva_status gva_decode_attention(gva_ctx* ctx, int B, const float* q_abs, const f
 /* The two passes of gva_decode_attention as separate calls, for callers that schedule them
  * apart (or time them apart).  gva_decode_attention(...) is exactly gva_decode_partial
  * followed by gva_decode_combine on the same stream.
- *   gva_decode_partial: the split-T pass (the north-star's "split-T flash-decoding kernel");
+ *   gva_decode_partial: the split-T pass (the split-T flash-decoding kernel);
  *     arguments as gva_decode_attention without `out`.  Its results (partial maxima, sums
  *     and weighted value sums, plus the batch's tile prefix sums) stay in the workspace.
  *   gva_decode_combine: merges them into out [B,H,d_v] f32.  It must follow the partial pass
