@@ -1,7 +1,7 @@
 """Builds the fp64 CPU oracle (test infrastructure) into oracle/liboracle.so with gcc.
 
-Building the checker is not using it: the package build step compiles this library so
-that the test suite and the benchmark's CPU-baseline leg can load it.
+The package build step compiles this library (compiling it runs none of it) so that the
+test suite and the benchmark's CPU-baseline leg can load it.
 """
 import os
 import subprocess
