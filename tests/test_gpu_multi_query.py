@@ -214,3 +214,29 @@ def test_multi_query_one_call_step(case):
     want_o = oracle.decode_multi(qa.reshape(w.B, n_q, w.H, w.d_v), qr.reshape(w.B, n_q, w.H, w.d_r), vp, kp, table,
                                  L, G=w.G, d_n=w.d_n)
     assert_bf16(got.cpu().numpy(), want_o, f"one-call step, case {case}")
+
+
+# ------------------------------------------------------------------------------- full-size workloads
+
+@pytest.mark.slow
+@pytest.mark.parametrize("n_q", [2, 4])
+def test_full_size_long_context_multi_query_all_rows(n_q):
+    """The long-context workload (570 MB of cache) with n_q queries per sequence, one pass in the
+    launch configuration the benchmark times: every (b, query, h) row against the oracle, which
+    reads a host copy of the whole cache."""
+    w = synth.WORKLOADS[4]
+    inp, qa, qr = multi_inputs(w, n_q, seed=40 + n_q)
+    out, ctx = run_multi(w, inp, qa, qr)
+    assert gva.gva_get_device_error(ctx) == 0
+    assert_bf16(out.cpu().numpy(), oracle_multi(w, inp, qa, qr), f"long-context, n_q = {n_q}, all rows")
+
+
+@pytest.mark.slow
+def test_full_size_ragged_four_queries_all_rows():
+    """The ragged paged batch (4.26 GB of cache, shuffled blocks, d_v = 128) with four queries per
+    sequence, two passes of two queries: every (b, query, h) row against the oracle."""
+    w = synth.WORKLOADS[5]
+    inp, qa, qr = multi_inputs(w, 4, seed=45)
+    out, ctx = run_multi(w, inp, qa, qr)
+    assert gva.gva_get_device_error(ctx) == 0
+    assert_bf16(out.cpu().numpy(), oracle_multi(w, inp, qa, qr), "ragged batch, n_q = 4, all rows")
