@@ -9,6 +9,8 @@ the separate kernels' arithmetic in the same order, so each case checks:
 Cases cover the kernel's instances (d_v 64/128, d_r 0..32, r = 1..8), the new token at the
 first and the last row of a block, one-token contexts, and ranges that meet many segments.
 """
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -347,3 +349,20 @@ def test_fused_steps_on_two_streams():
         torch.cuda.synchronize()
         assert torch.equal(runs[0][0].out, want[0]) and torch.equal(runs[1][0].out, want[1])
     assert all(layer.device_error() == 0 for layer, _, _ in runs)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("d_r", [0, 8, 32])
+def test_full_size_fused_step_other_positional_widths(d_r):
+    """The long-context workload at the other positional widths the kernel is built for (the
+    d_r sweep: no positional slice, one k8 step, and the six-consumer instance of d_r = 32 with
+    its patcher warp), full size: one call against three, bit for bit, and every (b, h) row
+    against the oracle."""
+    w = dataclasses.replace(synth.WORKLOADS[4], d_r=d_r, name=f"long-context-dr{d_r}")
+    inp, raw, (o1, v1, k1), (o2, v2, k2) = run_both(w, seed=0)
+    assert torch.equal(o1, o2) and torch.equal(v1, v2)
+    if d_r:
+        assert torch.equal(k1, k2)
+    del v1, k1, v2, k2
+    want, _, _ = oracle_step(w, inp, raw)
+    assert_bf16_parity(o2.cpu().numpy(), want, f"{w.name} fused step, all {w.B * w.H} rows")
