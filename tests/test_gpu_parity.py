@@ -403,6 +403,28 @@ def test_gqa_comparison_kernel_matches_oracle():
     assert_parity(out.cpu().numpy(), want, "bf16", "gqa")
 
 
+@pytest.mark.slow
+def test_gqa_comparison_kernel_full_size_all_rows():
+    """The same-build GQA decode at the size the benchmark times it beside GVA (the long-context
+    shape over a 1.07 GB K+V cache): every (b, h) row against the oracle."""
+    w4 = synth.WORKLOADS[4]
+    w = synth.custom(name="long-context-gqa", dtype="bf16", B=w4.B, H=w4.H, G=w4.G, d_v=w4.d_v, d_r=0,
+                     T=w4.T, T_range=w4.T_range, shuffled=w4.shuffled)
+    inp = synth.decode_inputs(w, seed=1, device="cuda", k_pool=True)
+    ctx = gva.gva_create(w.H, w.G, w.d_v, w.d_v, 0, "bf16")
+    out = torch.empty((w.B, w.H, w.d_v), device="cuda")
+    ws = torch.empty(gva.gva_decode_workspace_size(ctx, w.B, w.max_seq_len), dtype=torch.uint8, device="cuda")
+    gva.gqa_decode_attention(ctx, inp.extra["q"], inp.extra["k_pool"], inp.v_pool, inp.block_table, inp.seq_lens,
+                             w.max_seq_len, out, ws)
+    assert gva.gva_get_device_error(ctx) == 0
+    kp, vp = to_np_bits(inp.extra["k_pool"]), to_np_bits(inp.v_pool)
+    q = inp.extra["q"].double().cpu().numpy()
+    table, lens = inp.block_table.cpu().numpy(), inp.seq_lens.cpu().numpy()
+    want = np.stack([np.stack([oracle.gqa_decode_one(q, kp, vp, table, lens, G=w.G, b=b, h=h) for h in range(w.H)])
+                     for b in range(w.B)])
+    assert_parity(out.cpu().numpy(), want, "bf16", f"gqa, long-context shape, all {w.B * w.H} rows")
+
+
 # ------------------------------------------------------------------------------- errors and edges
 
 def test_host_side_errors():
