@@ -70,6 +70,10 @@ CASES = [
     (dict(B=3, H=16, G=4, d_v=64, d_r=24, T_range=(6, 900)), 6, 64 * 4),  # passes of 4 + 2
     (dict(B=3, H=16, G=2, d_v=64, d_r=16, T_range=(2, 700)), 2, 0),      # R=8, d_v=64: one pass of 2
     (dict(B=2, H=16, G=4, d_v=64, d_r=32, T_range=(4, 500)), 4, 0),      # d_r = 32, one pass of 4
+    # prefill scale: sequence 0 is its queries alone (a whole causal prefill), the others decode
+    # 128 (65) new tokens over a longer context
+    (dict(B=3, H=16, G=4, d_v=64, d_r=16, T_range=(130, 700)), 128, 0),   # 32 passes of 4
+    (dict(B=2, H=32, G=8, d_v=128, d_r=24, T_range=(66, 300)), 65, 0),    # d_v = 128: 32 passes of 2 + 1
 ]
 
 
