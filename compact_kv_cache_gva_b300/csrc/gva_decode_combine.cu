@@ -213,8 +213,8 @@ cudaError_t launch_dv(const DecodeArgs& a, cudaLaunchConfig_t& cfg) {
     case 2: return launch_t<DV, 2>(a, cfg);
     case 4: return launch_t<DV, 4>(a, cfg);
     case 8: return launch_t<DV, 8>(a, cfg);
-    case 16:  // several queries per pass at d_v = 64
-      if constexpr (DV == 64) return launch_t<DV, 16>(a, cfg);
+    case 16:  // several queries per pass (d_v = 64 and 128)
+      if constexpr (DV == 64 || DV == 128) return launch_t<DV, 16>(a, cfg);
       return cudaErrorInvalidValue;
     default: return cudaErrorInvalidValue;
   }

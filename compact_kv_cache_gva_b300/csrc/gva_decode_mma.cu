@@ -88,8 +88,9 @@ bool mma_supported(const gva_dims& d, bool sep_k) {
 // of d_v = 128 use three pairs (four give the same time with half the depth).  D takes the
 // rest of shared memory.
 // Queries per pass: the largest power of two up to 4 whose (query, head) column pairs fit,
-// 16 at d_v = 64 (four n-tiles of hi/lo columns, about 240 registers at 256 threads; the
-// long-context four-query decode in one pass instead of two) and 8 at d_v = 128 (sixteen
+// 16 (four n-tiles of hi/lo columns, about 240 registers at 256 threads at d_v = 64; the
+// long-context four-query decode in one pass instead of two; at d_v = 128 with the query
+// operand in shared memory, mma_query_in_smem, since as registers the sixteen pairs
 // spilled 508 bytes).
 int mma_max_queries_per_pass(int R, int d_v) {
   const int cols = mma_max_column_pairs(d_v);
@@ -103,7 +104,7 @@ bool mma_shape(const gva_dims& d, bool sep_k, int B, int nqp, int* pairs, int* s
   if (f8 && (sep_k || nqp > 1)) return false;
   const int op = f8 ? kBlockTokens * d.d_v : (d.d_v / 64) * kSubTileBytes * (sep_k ? 2 : 1);
   const int stage = op + (sep_k ? 0 : kBlockTokens * d.d_r * 2) + (f8 ? kBlockTokens : 0);
-  const int avail = kSmemLimit - ring_fixed_bytes(B);
+  int avail = kSmemLimit - ring_fixed_bytes(B);
   auto depth = [&](int p) { return std::min(avail / (p * stage), kMaxStages / p); };
   // Several queries per pass double the consumers' work per tile: at d_v = 64 eight self-fed
   // consumers with two-slot rings (mma_self_fed; the long-context two-query decode 110 us,
@@ -118,6 +119,8 @@ bool mma_shape(const gva_dims& d, bool sep_k, int B, int nqp, int* pairs, int* s
                 : f8    ? (d.d_v == 64 ? 12 : 3)
                         : std::min(stage <= 11 * 1024 ? 4 : stage <= 12 * 1024 ? 6 : 3,
                                    mma_max_threads(d.d_v, nqp) / 64);
+  // 16-pair passes at d_v = 128 keep each consumer's query operand in shared memory
+  if (!f8 && !sep_k) avail -= P * mma_qop_bytes(d.d_v, d.d_r, (d.H / d.G) * nqp);
   const int D = depth(P);
   if (D < 1) return false;
   *pairs = P;

@@ -60,8 +60,18 @@ constexpr int kMmaMaxThreads = 64 * kMmaMaxPairs;  // consumer warps + as many c
 // warps (two each), 168 with nine to twelve.  Several queries per pass and d_v = 128 hold
 // twice the accumulators and keep eight warps.
 __host__ __device__ constexpr int mma_max_threads(int dv, int nq) { return dv == 64 && nq == 1 ? 384 : 256; }
-// (query, head) column pairs a multi-query pass may hold: 16 at d_v = 64, 8 at d_v = 128.
-__host__ __device__ constexpr int mma_max_column_pairs(int dv) { return dv == 64 ? 16 : 8; }
+// (query, head) column pairs a multi-query pass may hold: 16 (four n-tiles of hi/lo columns).
+__host__ __device__ constexpr int mma_max_column_pairs(int) { return 16; }
+// At d_v = 128 the query operand of a 16-pair pass (72 registers as B fragments) stays in shared
+// memory, one copy per consumer, and each k-step's B fragments are loaded once per tile with
+// ldmatrix, outside the loop over the tile's m-tiles.  Rows: column n = 2c + part (column pair c,
+// bf16 part), its d_v content then d_r positional elements, the row stride an odd number of
+// 16-byte units so that the eight rows of an ldmatrix fall in distinct banks.
+__host__ __device__ constexpr bool mma_query_in_smem(int dv, int rq) { return dv == 128 && rq > 8; }
+__host__ __device__ constexpr int mma_qop_stride(int dv, int dr) { return ((((dv + dr) * 2 + 15) / 16) | 1) * 16; }
+__host__ __device__ constexpr int mma_qop_bytes(int dv, int dr, int rq) {
+  return mma_query_in_smem(dv, rq) ? 8 * ((2 * rq + 7) / 8) * mma_qop_stride(dv, dr) : 0;
+}
 // Consumers a copy warp fills: one (warp pairs), or two where a CTA wants more consumers than
 // pairs fit (a copy warp issues a tile in a small fraction of the time a consumer computes
 // one): the bf16 cache at d_v = 64, d_r = 32 (6 consumers and 3 copy warps, which leaves the
@@ -391,6 +401,10 @@ __global__ void __launch_bounds__(mma_max_threads(DV, NQ), 1) decode_mma_kernel(
   static_assert(!F8 || (NQ == 1 && !CAUSAL && !SEPK), "the fp8 value cache is read by single-query GVA decode");
   constexpr int CPC = mma_consumers_per_copy_warp(DV, DR, F8);
   constexpr int QS = step_stage_floats(R, DV, DR);  // floats of one staged segment (fused step)
+  constexpr bool kQS = mma_query_in_smem(DV, RQ) && !F8 && !SEPK;  // query operand in shared memory
+  constexpr int QST = mma_qop_stride(DV, DR);
+  constexpr int kQopBytes = kQS ? mma_qop_bytes(DV, DR, RQ) : 0;  // one consumer's query operand
+  static_assert(!kQS || (NT == 4 && CAUSAL && !FUSED), "staged query operand: 16-pair multi-query passes");
 
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
@@ -413,7 +427,8 @@ __global__ void __launch_bounds__(mma_max_threads(DV, NQ), 1) decode_mma_kernel(
   unsigned char* tiles = smem + kCtrlBytes;
   unsigned char* krs = tiles + N * L::kOpBytes;
   unsigned char* exs = krs + N * L::kKrBytes;  // fp8 cache: the scale exponents of each stage's tile
-  int* cum = reinterpret_cast<int*>(exs + N * L::kExBytes);
+  unsigned char* qops = exs + N * L::kExBytes;  // 16-pair passes at d_v = 128: each consumer's query operand
+  int* cum = reinterpret_cast<int*>(qops + P * kQopBytes);
   // fused step: the shared memory past the ring, [lengths: B ints][query stages]
   unsigned char* spare = reinterpret_cast<unsigned char*>(cum) + cum_bytes(a.B);
   int* lens_s = FUSED && a.spare_smem >= cum_bytes(a.B) ? reinterpret_cast<int*>(spare) : nullptr;
@@ -804,11 +819,30 @@ __global__ void __launch_bounds__(mma_max_threads(DV, NQ), 1) decode_mma_kernel(
   // query fragments (B operand of the score product) of the current (b, g), pre-scaled by
   // scale*log2(e); column n = 2*c + part for column pair c = i*R + h (query q0 + i of this
   // pass, head h of the group), part 0 = bf16(q), part 1 = bf16 remainder.
-  uint32_t qb[NT][KSV + KSR][2];
-  uint32_t qt[NT];
+  uint32_t qb[kQS ? 1 : NT][kQS ? 1 : KSV + KSR][2];
+  uint32_t qt[kQS ? 1 : NT];
   uint4 vnew = make_uint4(0, 0, 0, 0);  // fused step: a 16-byte piece of the new value row
   uint32_t knew = 0;                    // fused step: a pair of the new rotated positional key
   auto load_q = [&](int b, int g) {
+    if constexpr (kQS) {
+      // operand rows n = 2c + part of this consumer's copy, element pairs (2kp, 2kp + 1)
+      const uint32_t qb0 = smem_addr(qops + warp * kQopBytes);
+      constexpr int KP = (DV + DR) / 2;
+      __syncwarp();  // the previous segment's rows have been read
+      for (int idx = lane; idx < 8 * NT * KP; idx += 32) {
+        const int nr = idx / KP, kp = idx - nr * KP;
+        const int c = nr >> 1, part = nr & 1;
+        uint32_t w = 0;
+        if (c < RQ) {
+          const long long row = (static_cast<long long>(b) * a.nq + a.q0 + c / R) * a.H + g * R + c % R;
+          const int k = 2 * kp;
+          const float* src = k < DV ? a.q_abs + row * DV + k : a.q_rot + row * DR + (k - DV);
+          w = pack_bf16(split_part(src[0] * a.scale_log2, part), split_part(src[1] * a.scale_log2, part));
+        }
+        st_shared_u32(qb0 + nr * QST + 4 * kp, w);
+      }
+      __syncwarp();
+    } else {
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       const int cp = nt * 4 + ((lane >> 2) >> 1), part = (lane >> 2) & 1;
@@ -843,6 +877,7 @@ __global__ void __launch_bounds__(mma_max_threads(DV, NQ), 1) decode_mma_kernel(
         const int k0 = 16 * (KSV + KSR) + 2 * tq;
         qt[nt] = pack_bf16(qv(k0), qv(k0 + 1));
       }
+    }
     }
     if constexpr (FUSED && !kPatcher) {  // the new token's row, in case this warp meets the segment's last tile
       if (lane < DV / 8)
@@ -987,6 +1022,51 @@ __global__ void __launch_bounds__(mma_max_threads(DV, NQ), 1) decode_mma_kernel(
         for (int mt = 0; mt < 4; ++mt)
 #pragma unroll
           for (int e = 0; e < 4; ++e) sc[nt][mt][e] = 0.f;
+      if constexpr (kQS) {
+        // each k-step's B fragments from the staged operand, once per tile: matrices (n +0..7,
+        // k +0..7), (n +0..7, k +8..15), (n +8..15, k +0..7), (n +8..15, k +8..15)
+        const uint32_t qb0 = smem_addr(qops + warp * kQopBytes);
+        const uint32_t qlane = qb0 + (8 * (lane >> 4) + (lane & 7)) * QST + 16 * ((lane >> 3) & 1);
+#pragma unroll
+        for (int ks = 0; ks < KSV + KSR; ++ks) {
+          uint32_t bq[NT][2];
+#pragma unroll
+          for (int np = 0; np < NT / 2; ++np) {
+            uint32_t r4[4];
+            ldsm_x4(qlane + 16 * np * QST + 32 * ks, r4);
+            bq[2 * np][0] = r4[0];
+            bq[2 * np][1] = r4[1];
+            bq[2 * np + 1][0] = r4[2];
+            bq[2 * np + 1][1] = r4[3];
+          }
+#pragma unroll
+          for (int mt = 0; mt < 4; ++mt) {
+            const int row = 16 * mt + ld_row;
+            uint32_t af[4];
+            if (ks < KSV) {
+              const int kc = 2 * ks + ld_kc;
+              ldsm_x4(kbase + (kc >> 3) * kSubTileBytes + row * 128 + (((kc & 7) ^ (row & 7)) << 4), af);
+            } else {
+              ldsm_x4(krbase + row * (2 * DR) + (2 * (ks - KSV) + ld_kc) * 16, af);
+            }
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) mma_16816(sc[nt][mt], af, bq[nt][0], bq[nt][1]);
+          }
+        }
+        if constexpr (KR8) {
+          // the trailing k8 step: one matrix per n-tile (n +8i..+7, k 16(KSV + KSR) .. +7)
+          uint32_t bt[4];
+          ldsm_x4(qb0 + (8 * (lane >> 3) + (lane & 7)) * QST + 32 * (KSV + KSR), bt);
+#pragma unroll
+          for (int mt = 0; mt < 4; ++mt) {
+            const int row = 16 * mt + ld_row;
+            uint32_t a0, a1;
+            ldsm_x2(krbase + row * (2 * DR) + (2 * KSR) * 16, a0, a1);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) mma_1688(sc[nt][mt], a0, a1, bt[nt]);
+          }
+        }
+      } else {
 #pragma unroll
       for (int mt = 0; mt < 4; ++mt) {
         const int row = 16 * mt + ld_row;
@@ -1038,6 +1118,7 @@ __global__ void __launch_bounds__(mma_max_threads(DV, NQ), 1) decode_mma_kernel(
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) mma_1688(sc[nt][mt], a0, a1, qt[nt]);
         }
+      }
       }
 
       // online softmax (log2 domain); thread holds column pair c = nt*4 + tq (query q0 + c/R,
@@ -1341,7 +1422,7 @@ cudaError_t launch_mma_t(const DecodeArgs& a, const CUtensorMap& mv, const CUten
   if (P < 1 || P % CPC || 32 * warps > mma_max_threads(DV, NQ) || D < 1 || P * D > kMaxStages)
     return cudaErrorInvalidValue;
   if (a.nqp != NQ || (a.nq > 1) != CAUSAL || (a.fused != 0) != FUSED) return cudaErrorInvalidValue;
-  const int smem = ring_fixed_bytes(a.B) + P * D * L::kStageBytes;
+  const int smem = ring_fixed_bytes(a.B) + P * D * L::kStageBytes + P * (F8 || SEPK ? 0 : mma_qop_bytes(DV, DR, R * NQ));
   if (smem > kSmemLimit) return cudaErrorInvalidValue;
   // the fused step fills the instance's thread budget with prologue warps, and the shared
   // memory budget with query stages; its patcher warp is the first prologue warp

@@ -206,8 +206,7 @@ gva_status gva_decode_combine(gva_ctx* ctx, int B, int max_seq_len, float* out, 
  *   sets GVA_DEVERR_SEQ_LEN and zeroes that sequence's rows).
  * Tensor-core path only (bf16 caches; GVA_ERR_UNSUPPORTED otherwise when n_q > 1).  The
  * kernel packs R*nqp (query, head) pairs into its MMA columns, nqp = up to 4 queries per
- * pass with R*nqp <= 16 at d_v = 64 and <= 8 at d_v = 128 (R = H/G); more queries take more
- * passes, each reading the cache.
+ * pass with R*nqp <= 16 (R = H/G); more queries take more passes, each reading the cache.
  * n_q == 1 is gva_decode_attention.  Workspace: gva_decode_workspace_size_multi bytes. */
 gva_status gva_decode_attention_multi(gva_ctx* ctx, int B, int n_q, const float* q_abs,
                                       const float* q_rot, const void* v_pool, const void* kr_pool,

@@ -65,7 +65,7 @@ CASES = [
     (dict(B=3, H=4, G=4, d_v=64, d_r=8, T_range=(5, 300)), 5, 64),       # R=1: passes of 4 + 1
     (dict(B=3, H=32, G=8, d_v=128, d_r=24, T_range=(2, 1200)), 2, 0),   # d_v = 128
     (dict(B=2, H=16, G=4, d_v=64, d_r=0, T_range=(2, 400)), 2, 0),       # no positional slice
-    (dict(B=2, H=8, G=1, d_v=128, d_r=32, T_range=(8, 200)), 8, 0),      # R=8: 8 passes of 1
+    (dict(B=2, H=8, G=1, d_v=128, d_r=32, T_range=(8, 200)), 8, 0),      # R=8, d_v=128: 4 passes of 2 (16 pairs)
     (dict(B=4, H=16, G=4, d_v=64, d_r=16, T_range=(4, 3000)), 4, 0),     # R=4, d_v=64: one pass of 4
     (dict(B=3, H=16, G=4, d_v=64, d_r=24, T_range=(6, 900)), 6, 64 * 4),  # passes of 4 + 2
     (dict(B=3, H=16, G=2, d_v=64, d_r=16, T_range=(2, 700)), 2, 0),      # R=8, d_v=64: one pass of 2
@@ -73,7 +73,7 @@ CASES = [
     # prefill scale: sequence 0 is its queries alone (a whole causal prefill), the others decode
     # 128 (65) new tokens over a longer context
     (dict(B=3, H=16, G=4, d_v=64, d_r=16, T_range=(130, 700)), 128, 0),   # 32 passes of 4
-    (dict(B=2, H=32, G=8, d_v=128, d_r=24, T_range=(66, 300)), 65, 0),    # d_v = 128: 32 passes of 2 + 1
+    (dict(B=2, H=32, G=8, d_v=128, d_r=24, T_range=(66, 300)), 65, 0),    # d_v = 128: 16 passes of 4 + 1
 ]
 
 
@@ -238,7 +238,8 @@ def test_full_size_long_context_multi_query_all_rows(n_q):
 @pytest.mark.slow
 def test_full_size_ragged_four_queries_all_rows():
     """The ragged paged batch (4.26 GB of cache, shuffled blocks, d_v = 128) with four queries per
-    sequence, two passes of two queries: every (b, query, h) row against the oracle."""
+    sequence in one pass (16 column pairs, the query operand in shared memory): every
+    (b, query, h) row against the oracle."""
     w = synth.WORKLOADS[5]
     inp, qa, qr = multi_inputs(w, 4, seed=45)
     out, ctx = run_multi(w, inp, qa, qr)
