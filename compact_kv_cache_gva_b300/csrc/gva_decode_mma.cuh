@@ -72,6 +72,13 @@ __host__ __device__ constexpr int mma_qop_stride(int dv, int dr) { return ((((dv
 __host__ __device__ constexpr int mma_qop_bytes(int dv, int dr, int rq) {
   return mma_query_in_smem(dv, rq) ? 8 * ((2 * rq + 7) / 8) * mma_qop_stride(dv, dr) : 0;
 }
+// Those passes also split each tile's 16 pairs between two consumer warps (eight each, with
+// their halves of the operand): eight consumers, two per sub-partition, beside the four copy
+// warps, so that one covers the other's dependent products.  Both write their halves of the
+// ring's one partial record.
+__host__ __device__ constexpr int mma_kernel_threads(int dv, int rq, int nq) {
+  return mma_query_in_smem(dv, rq) ? 384 : mma_max_threads(dv, nq);
+}
 // Consumers a copy warp fills: one (warp pairs), or two where a CTA wants more consumers than
 // pairs fit (a copy warp issues a tile in a small fraction of the time a consumer computes
 // one): the bf16 cache at d_v = 64, d_r = 32 (6 consumers and 3 copy warps, which leaves the
@@ -385,12 +392,17 @@ inline int ring_fixed_bytes(int B) { return 1024 + kCtrlBytes + cum_bytes(B); }
 // Probabilities enter as p_j 2^(e_j - E + 14) (E the largest exponent of the tile's tokens,
 // in f16's normal range) into a per-tile accumulator that is added to o times 2^(E - 14).
 template <int DV, int DR, int R, int NQ, bool CAUSAL, bool SEPK, bool FUSED, bool F8 = false>
-__global__ void __launch_bounds__(mma_max_threads(DV, NQ), 1) decode_mma_kernel(const DecodeArgs a,
+__global__ void __launch_bounds__(mma_kernel_threads(DV, R * NQ, NQ), 1) decode_mma_kernel(const DecodeArgs a,
                                                                        const __grid_constant__ CUtensorMap tmv,
                                                                        const __grid_constant__ CUtensorMap tmk) {
   using L = MmaLayout<DV, DR, SEPK, F8>;
   constexpr int RQ = R * NQ;            // (query, head) column pairs of a group: c = i*R + h
-  constexpr int NT = (2 * RQ + 7) / 8;  // n-tiles of 8 columns (4 column pairs each)
+  // 16-pair passes at d_v = 128: the query operand in shared memory, the pairs split between two
+  // consumer warps per ring (mma_query_in_smem, mma_kernel_threads)
+  constexpr bool kQS = mma_query_in_smem(DV, RQ) && !F8 && !SEPK;
+  constexpr bool kSplit = kQS;
+  constexpr int RQc = kSplit ? RQ / 2 : RQ;  // column pairs one consumer warp computes
+  constexpr int NT = (2 * RQc + 7) / 8;      // its n-tiles of 8 columns (4 column pairs each)
   constexpr int KSV = DV / 16;          // k16 steps over the value (key) columns
   constexpr int KSR = DR / 16;          // k16 steps over the positional columns
   constexpr bool KR8 = (DR % 16) != 0;  // one trailing k8 step
@@ -401,16 +413,16 @@ __global__ void __launch_bounds__(mma_max_threads(DV, NQ), 1) decode_mma_kernel(
   static_assert(!F8 || (NQ == 1 && !CAUSAL && !SEPK), "the fp8 value cache is read by single-query GVA decode");
   constexpr int CPC = mma_consumers_per_copy_warp(DV, DR, F8);
   constexpr int QS = step_stage_floats(R, DV, DR);  // floats of one staged segment (fused step)
-  constexpr bool kQS = mma_query_in_smem(DV, RQ) && !F8 && !SEPK;  // query operand in shared memory
   constexpr int QST = mma_qop_stride(DV, DR);
-  constexpr int kQopBytes = kQS ? mma_qop_bytes(DV, DR, RQ) : 0;  // one consumer's query operand
-  static_assert(!kQS || (NT == 4 && CAUSAL && !FUSED), "staged query operand: 16-pair multi-query passes");
+  constexpr int kQopBytes = kQS ? 8 * NT * QST : 0;  // one consumer warp's query operand
+  static_assert(!kQS || (NT == 2 && CAUSAL && !FUSED), "staged query operand: 16-pair multi-query passes");
 
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const int P = a.group_warps;  // consumer warps
   constexpr bool kSelfFed = mma_self_fed(DV, CAUSAL, F8);
+  const int PW = kSplit ? 2 * P : P;      // consumer warps (two per ring when the pairs are split)
   const int PC = kSelfFed ? 0 : P / CPC;  // copy warps; blockDim.x == 32 * (P + PC), plus the prologue warps of a fused launch
   const int D = a.n_stages;     // ring slots per pair
   const int N = P * D;
@@ -428,7 +440,7 @@ __global__ void __launch_bounds__(mma_max_threads(DV, NQ), 1) decode_mma_kernel(
   unsigned char* krs = tiles + N * L::kOpBytes;
   unsigned char* exs = krs + N * L::kKrBytes;  // fp8 cache: the scale exponents of each stage's tile
   unsigned char* qops = exs + N * L::kExBytes;  // 16-pair passes at d_v = 128: each consumer's query operand
-  int* cum = reinterpret_cast<int*>(qops + P * kQopBytes);
+  int* cum = reinterpret_cast<int*>(qops + PW * kQopBytes);
   // fused step: the shared memory past the ring, [lengths: B ints][query stages]
   unsigned char* spare = reinterpret_cast<unsigned char*>(cum) + cum_bytes(a.B);
   int* lens_s = FUSED && a.spare_smem >= cum_bytes(a.B) ? reinterpret_cast<int*>(spare) : nullptr;
@@ -437,12 +449,12 @@ __global__ void __launch_bounds__(mma_max_threads(DV, NQ), 1) decode_mma_kernel(
   if (threadIdx.x == 0) {
     for (int s = 0; s < N; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+      mbar_init(&empty[s], kSplit ? 2 : 1);  // released by each consumer warp of the ring
       if (kPatcher) mbar_init(&landed[s], 1);
     }
     mbar_init_fence();
   }
-  if (warp == (kSelfFed ? 0 : P) && lane == 0) {
+  if (warp == (kSelfFed ? 0 : PW) && lane == 0) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmv)) : "memory");
     if (SEPK) asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmk)) : "memory");
   }
@@ -730,10 +742,10 @@ __global__ void __launch_bounds__(mma_max_threads(DV, NQ), 1) decode_mma_kernel(
       mbar_arrive(&full[s]);  // completes the phase with no data; the tile is skipped
     }
   };
-  if (!kSelfFed && warp >= P) {
+  if (!kSelfFed && warp >= PW) {
     // copy warp c serves the units k = c + PC*i of the range (i < n_mine): CPC consumers, unit
     // k going to consumer k % P as its (k / P)-th unit
-    const int c = warp - P;
+    const int c = warp - PW;
     const int n_mine = n > c ? (n - c + PC - 1) / PC : 0;
     int blk, grp, nv;
     lookup(c, PC, n_mine, 0, blk, grp, nv);
@@ -808,8 +820,10 @@ __global__ void __launch_bounds__(mma_max_threads(DV, NQ), 1) decode_mma_kernel(
     absorb_segments(warp, P + E);
     named_barrier_sync(kStepBarrier, 32 * (P + E));  // every stage of the range is written
   }
-  const int NC = P;  // consumer warps sharing the range
-  int k = warp;
+  const int NC = P;  // consumers (rings) sharing the range
+  const int ring = kSplit ? warp % P : warp;  // this warp's ring and consumer (record) index
+  const int cp0 = kSplit ? RQc * (warp / P) : 0;  // its first column pair
+  int k = ring;
   if (k >= n) return;
   float* recs = a.part + header_bytes(a.B) / 4;
   constexpr int rec_floats = DV + 4;
@@ -828,12 +842,13 @@ __global__ void __launch_bounds__(mma_max_threads(DV, NQ), 1) decode_mma_kernel(
       // operand rows n = 2c + part of this consumer's copy, element pairs (2kp, 2kp + 1)
       const uint32_t qb0 = smem_addr(qops + warp * kQopBytes);
       constexpr int KP = (DV + DR) / 2;
+      static_assert(kSplit, "the staged operand holds a consumer's half of the pairs");
       __syncwarp();  // the previous segment's rows have been read
       for (int idx = lane; idx < 8 * NT * KP; idx += 32) {
         const int nr = idx / KP, kp = idx - nr * KP;
-        const int c = nr >> 1, part = nr & 1;
+        const int c = (nr >> 1) + cp0, part = nr & 1;
         uint32_t w = 0;
-        if (c < RQ) {
+        if (c < cp0 + RQc) {
           const long long row = (static_cast<long long>(b) * a.nq + a.q0 + c / R) * a.H + g * R + c % R;
           const int k = 2 * kp;
           const float* src = k < DV ? a.q_abs + row * DV + k : a.q_rot + row * DR + (k - DV);
@@ -847,7 +862,7 @@ __global__ void __launch_bounds__(mma_max_threads(DV, NQ), 1) decode_mma_kernel(
     for (int nt = 0; nt < NT; ++nt) {
       const int cp = nt * 4 + ((lane >> 2) >> 1), part = (lane >> 2) & 1;
       const int tq = lane & 3;
-      const bool valid = cp < RQ;
+      const bool valid = cp < RQc;
       const int qi = valid ? cp / R : 0, head = valid ? cp % R : 0;
       const long long row = (static_cast<long long>(b) * a.nq + a.q0 + qi) * a.H + g * R + head;
       const float* qa = FUSED ? stage + (segment_of(g, b, a.B) - f_lo) * QS + head * (DV + DR) : a.q_abs + row * DV;
@@ -914,7 +929,7 @@ __global__ void __launch_bounds__(mma_max_threads(DV, NQ), 1) decode_mma_kernel(
   const int gid = lane >> 2, tq = lane & 3;
   // Partial record of segment f for this warp: per column pair (m, l, 0, 0, o[0..DV)).
   auto flush = [&](long long f) {
-    float* rec = recs + ((static_cast<long long>(blockIdx.x) + f) * NC + warp) * RQ * rec_floats;
+    float* rec = recs + ((static_cast<long long>(blockIdx.x) + f) * NC + ring) * RQ * rec_floats;
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       float lt = l[nt];
@@ -922,8 +937,8 @@ __global__ void __launch_bounds__(mma_max_threads(DV, NQ), 1) decode_mma_kernel(
       lt += __shfl_xor_sync(kFullMask, lt, 8);
       lt += __shfl_xor_sync(kFullMask, lt, 16);
       const int cp = nt * 4 + tq;
-      if (cp < RQ) {
-        float* r = rec + cp * rec_floats;
+      if (cp < RQc) {
+        float* r = rec + (cp + cp0) * rec_floats;
         if (gid == 0) {
           r[0] = m[nt];
           r[1] = lt;
@@ -960,7 +975,7 @@ __global__ void __launch_bounds__(mma_max_threads(DV, NQ), 1) decode_mma_kernel(
   load_q(cc.b, cc.g);
   bool ok = true;
   while (true) {
-    const int s = warp * D + slot;
+    const int s = ring * D + slot;
     const bool got = mbar_wait_bounded(&full[s], ph);
     if (!__all_sync(kFullMask, got)) {
       ok = false;
@@ -1055,8 +1070,8 @@ __global__ void __launch_bounds__(mma_max_threads(DV, NQ), 1) decode_mma_kernel(
         }
         if constexpr (KR8) {
           // the trailing k8 step: one matrix per n-tile (n +8i..+7, k 16(KSV + KSR) .. +7)
-          uint32_t bt[4];
-          ldsm_x4(qb0 + (8 * (lane >> 3) + (lane & 7)) * QST + 32 * (KSV + KSR), bt);
+          uint32_t bt[2];
+          ldsm_x2(qb0 + (8 * ((lane >> 3) & 1) + (lane & 7)) * QST + 32 * (KSV + KSR), bt[0], bt[1]);
 #pragma unroll
           for (int mt = 0; mt < 4; ++mt) {
             const int row = 16 * mt + ld_row;
@@ -1145,7 +1160,7 @@ __global__ void __launch_bounds__(mma_max_threads(DV, NQ), 1) decode_mma_kernel(
           float mx = -INFINITY;
           if constexpr (kMasked) {
             const int cp = nt * 4 + tq;
-            const int lim = min(nv, nrem - (a.nq - 1 - (a.q0 + (cp < RQ ? cp / R : 0))));
+            const int lim = min(nv, nrem - (a.nq - 1 - (a.q0 + (cp < RQc ? (cp + cp0) / R : 0))));
 #pragma unroll
             for (int mt = 0; mt < 4; ++mt) {
               const int j0 = 16 * mt + gid;
@@ -1418,8 +1433,9 @@ cudaError_t launch_mma_t(const DecodeArgs& a, const CUtensorMap& mv, const CUten
   using L = MmaLayout<DV, DR, SEPK, F8>;
   const int P = a.group_warps, D = a.n_stages;
   constexpr int CPC = mma_consumers_per_copy_warp(DV, DR, F8);
-  const int warps = P + (mma_self_fed(DV, CAUSAL, F8) ? 0 : P / CPC);
-  if (P < 1 || P % CPC || 32 * warps > mma_max_threads(DV, NQ) || D < 1 || P * D > kMaxStages)
+  constexpr bool kSplit = mma_query_in_smem(DV, R * NQ) && !F8 && !SEPK;
+  const int warps = (kSplit ? 2 * P : P) + (mma_self_fed(DV, CAUSAL, F8) ? 0 : P / CPC);
+  if (P < 1 || P % CPC || 32 * warps > mma_kernel_threads(DV, R * NQ, NQ) || D < 1 || P * D > kMaxStages)
     return cudaErrorInvalidValue;
   if (a.nqp != NQ || (a.nq > 1) != CAUSAL || (a.fused != 0) != FUSED) return cudaErrorInvalidValue;
   const int smem = ring_fixed_bytes(a.B) + P * D * L::kStageBytes + P * (F8 || SEPK ? 0 : mma_qop_bytes(DV, DR, R * NQ));
