@@ -402,6 +402,15 @@ __global__ void __launch_bounds__(mma_kernel_threads(DV, R * NQ, NQ), 1) decode_
   constexpr bool kQS = mma_query_in_smem(DV, RQ) && !F8 && !SEPK;
   constexpr bool kSplit = kQS;
   constexpr int RQc = kSplit ? RQ / 2 : RQ;  // column pairs one consumer warp computes
+  // 16-pair passes at d_v = 64 put the queries on M: S[pairs x 64 tok] = Q . V^T with the bf16
+  // high parts and remainders of the query as two A operands into one accumulator, and the score
+  // fragment (pairs on rows) serving as the output product's B operand as it stands: no
+  // movmatrix, no adding of high and low score columns, two shuffle levels for a row maximum
+  // (long-context four-query step 186.6 -> 180.3 us; with 8 pairs half of each M = 16 product
+  // was empty and the two-query step went from 109.5 to 115.3 us, so those passes keep the
+  // tokens on M).
+  constexpr bool kQM = DV == 64 && CAUSAL && RQ > 8 && !F8 && !SEPK && !FUSED;
+  constexpr int RH = RQ > 8 ? 2 : 1;  // queries on M: 8-pair row halves that hold pairs
   constexpr int NT = (2 * RQc + 7) / 8;      // its n-tiles of 8 columns (4 column pairs each)
   constexpr int KSV = DV / 16;          // k16 steps over the value (key) columns
   constexpr int KSR = DR / 16;          // k16 steps over the positional columns
@@ -833,12 +842,40 @@ __global__ void __launch_bounds__(mma_kernel_threads(DV, R * NQ, NQ), 1) decode_
   // query fragments (B operand of the score product) of the current (b, g), pre-scaled by
   // scale*log2(e); column n = 2*c + part for column pair c = i*R + h (query q0 + i of this
   // pass, head h of the group), part 0 = bf16(q), part 1 = bf16 remainder.
-  uint32_t qb[kQS ? 1 : NT][kQS ? 1 : KSV + KSR][2];
-  uint32_t qt[kQS ? 1 : NT];
+  uint32_t qb[kQS || kQM ? 1 : NT][kQS || kQM ? 1 : KSV + KSR][2];
+  uint32_t qt[kQS || kQM ? 1 : NT];
+  // queries on M: A fragments of the query (rows: column pairs; content then positional k16
+  // steps, and the trailing k8 step), per bf16 part
+  uint32_t qa[2][kQM ? KSV + KSR : 1][4];
+  uint32_t qat[2][2];
   uint4 vnew = make_uint4(0, 0, 0, 0);  // fused step: a 16-byte piece of the new value row
   uint32_t knew = 0;                    // fused step: a pair of the new rotated positional key
   auto load_q = [&](int b, int g) {
-    if constexpr (kQS) {
+    if constexpr (kQM) {
+      const int lg = lane >> 2, lt4 = lane & 3;
+      auto qv = [&](int c, int kk, int part) -> float {
+        if (c >= RQ) return 0.f;
+        const long long row = (static_cast<long long>(b) * a.nq + a.q0 + c / R) * a.H + g * R + c % R;
+        const float x = kk < DV ? a.q_abs[row * DV + kk] : a.q_rot[row * DR + (kk - DV)];
+        return split_part(x * a.scale_log2, part);
+      };
+#pragma unroll
+      for (int part = 0; part < 2; ++part) {
+#pragma unroll
+        for (int ks = 0; ks < KSV + KSR; ++ks) {
+          const int k0 = 16 * ks + 2 * lt4;
+          qa[part][ks][0] = pack_bf16(qv(lg, k0, part), qv(lg, k0 + 1, part));
+          qa[part][ks][1] = pack_bf16(qv(lg + 8, k0, part), qv(lg + 8, k0 + 1, part));
+          qa[part][ks][2] = pack_bf16(qv(lg, k0 + 8, part), qv(lg, k0 + 9, part));
+          qa[part][ks][3] = pack_bf16(qv(lg + 8, k0 + 8, part), qv(lg + 8, k0 + 9, part));
+        }
+        if constexpr (KR8) {
+          const int k0 = 16 * (KSV + KSR) + 2 * lt4;
+          qat[part][0] = pack_bf16(qv(lg, k0, part), qv(lg, k0 + 1, part));
+          qat[part][1] = pack_bf16(qv(lg + 8, k0, part), qv(lg + 8, k0 + 1, part));
+        }
+      }
+    } else if constexpr (kQS) {
       // operand rows n = 2c + part of this consumer's copy, element pairs (2kp, 2kp + 1)
       const uint32_t qb0 = smem_addr(qops + warp * kQopBytes);
       constexpr int KP = (DV + DR) / 2;
@@ -913,7 +950,20 @@ __global__ void __launch_bounds__(mma_kernel_threads(DV, R * NQ, NQ), 1) decode_
   constexpr int NO = kWide ? NT / 2 : NT;  // accumulator n-tiles
   constexpr bool kFastExp = F8 || kWide;
   float m[NT], l[NT], o[NO][MD][4];
+  float mq[RH], lq[RH], oq[RH][MD][4];  // queries on M: per row half (row gid, gid + 8 of it)
   auto reset_state = [&]() {
+    if constexpr (kQM) {
+#pragma unroll
+      for (int rh = 0; rh < RH; ++rh) {
+        mq[rh] = -INFINITY;
+        lq[rh] = 0.f;
+#pragma unroll
+        for (int md = 0; md < MD; ++md)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) oq[rh][md][e] = 0.f;
+      }
+      return;
+    }
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       m[nt] = -INFINITY;
@@ -930,6 +980,29 @@ __global__ void __launch_bounds__(mma_kernel_threads(DV, R * NQ, NQ), 1) decode_
   // Partial record of segment f for this warp: per column pair (m, l, 0, 0, o[0..DV)).
   auto flush = [&](long long f) {
     float* rec = recs + ((static_cast<long long>(blockIdx.x) + f) * NC + ring) * RQ * rec_floats;
+    if constexpr (kQM) {
+      // pair c = 8 rh + gid: m and l (l summed over the row's four lanes); output column pairs
+      // 8 rh + 2tq (+1), value rows 16 md + gid (+8)
+#pragma unroll
+      for (int rh = 0; rh < RH; ++rh) {
+        float lt = lq[rh];
+        lt += __shfl_xor_sync(kFullMask, lt, 1);
+        lt += __shfl_xor_sync(kFullMask, lt, 2);
+        const int c = 8 * rh + gid;
+        if (tq == 0 && c < RQ) {
+          rec[c * rec_floats] = mq[rh];
+          rec[c * rec_floats + 1] = lt;
+        }
+#pragma unroll
+        for (int md = 0; md < MD; ++md)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int cp = 8 * rh + 2 * tq + (e & 1);
+            if (cp < RQ) rec[cp * rec_floats + 4 + 16 * md + gid + 8 * (e >> 1)] = oq[rh][md][e];
+          }
+      }
+      return;
+    }
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       float lt = l[nt];
@@ -1001,6 +1074,153 @@ __global__ void __launch_bounds__(mma_kernel_threads(DV, R * NQ, NQ), 1) decode_
           __syncwarp();
         }
       }
+      if constexpr (kQM) {
+        // scores S[pairs x 64 tokens]: thread holds rows gid, gid + 8 (e = 0, 1 and 2, 3) and
+        // tokens 8 jb + 2tq (+1) of column block jb
+        float sc[8][4];
+#pragma unroll
+        for (int jb = 0; jb < 8; ++jb)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) sc[jb][e] = 0.f;
+        // content: the value rows as B fragments (tokens on n), two column blocks per load:
+        // matrices (tokens +0..7, chunk 2ks), (+0..7, 2ks + 1), (+8..15, 2ks), (+8..15, 2ks + 1)
+#pragma unroll
+        for (int ks = 0; ks < KSV; ++ks) {
+#pragma unroll
+          for (int jb = 0; jb < 8; jb += 2) {
+            const int tok = 8 * jb + 8 * (lane >> 4) + (lane & 7);
+            const int kc = 2 * ks + ((lane >> 3) & 1);
+            uint32_t bf[4];
+            ldsm_x4(kbase + (kc >> 3) * kSubTileBytes + tok * 128 + (((kc & 7) ^ (tok & 7)) << 4), bf);
+#pragma unroll
+            for (int part = 0; part < 2; ++part) {
+              mma_16816(sc[jb], qa[part][ks], bf[0], bf[1]);
+              mma_16816(sc[jb + 1], qa[part][ks], bf[2], bf[3]);
+            }
+          }
+        }
+        // positional: the k_r rows as B fragments, the same way (plain rows of 2 DR bytes)
+#pragma unroll
+        for (int ks = 0; ks < KSR; ++ks) {
+#pragma unroll
+          for (int jb = 0; jb < 8; jb += 2) {
+            const int tok = 8 * jb + 8 * (lane >> 4) + (lane & 7);
+            uint32_t bf[4];
+            ldsm_x4(krbase + tok * (2 * DR) + (16 * ks + 8 * ((lane >> 3) & 1)) * 2, bf);
+#pragma unroll
+            for (int part = 0; part < 2; ++part) {
+              mma_16816(sc[jb], qa[part][KSV + ks], bf[0], bf[1]);
+              mma_16816(sc[jb + 1], qa[part][KSV + ks], bf[2], bf[3]);
+            }
+          }
+        }
+        if constexpr (KR8) {
+#pragma unroll
+          for (int jb = 0; jb < 8; jb += 4) {
+            const int tok = 8 * jb + 8 * (lane >> 3) + (lane & 7);
+            uint32_t bf[4];
+            ldsm_x4(krbase + tok * (2 * DR) + 32 * KSR, bf);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+              for (int part = 0; part < 2; ++part) mma_1688(sc[jb + i], qat[part][0], qat[part][1], bf[i]);
+          }
+        }
+        // online softmax along each row (column pair c = 8 rh + gid: query q0 + c/R, head c%R):
+        // this thread's tokens, then the row's four lanes.  Query q of nq reads tokens
+        // j < nrem - (nq - 1 - q) of this tile; most tiles are seen whole by every query.
+        float al[RH];
+        auto softmax_qm = [&](auto masked) {
+          constexpr bool kMasked = decltype(masked)::value;
+#pragma unroll
+          for (int rh = 0; rh < RH; ++rh) {
+            const int c = 8 * rh + gid;
+            const int lim = kMasked ? min(nv, nrem - (a.nq - 1 - (a.q0 + (c < RQ ? c / R : 0)))) : kBlockTokens;
+            float mx = -INFINITY;
+#pragma unroll
+            for (int jb = 0; jb < 8; ++jb)
+#pragma unroll
+              for (int e = 0; e < 2; ++e) {
+                if (kMasked && 8 * jb + 2 * tq + e >= lim) sc[jb][2 * rh + e] = -INFINITY;
+                mx = fmaxf(mx, sc[jb][2 * rh + e]);
+              }
+            mx = fmaxf(mx, __shfl_xor_sync(kFullMask, mx, 1));
+            mx = fmaxf(mx, __shfl_xor_sync(kFullMask, mx, 2));
+            const float mn = fmaxf(mq[rh], mx);
+            const bool none = kMasked && mn == -INFINITY;
+            al[rh] = none || mn == mq[rh] ? 1.f : fast_exp2(mq[rh] - mn);
+            mq[rh] = mn;
+            float ps = 0.f;
+#pragma unroll
+            for (int jb = 0; jb < 8; ++jb)
+#pragma unroll
+              for (int e = 0; e < 2; ++e) {
+                const float pv = none ? 0.f : fast_exp2(sc[jb][2 * rh + e] - mn);
+                sc[jb][2 * rh + e] = pv;
+                ps += pv;
+              }
+            lq[rh] = fmaf(lq[rh], al[rh], ps);
+          }
+        };
+        if (nrem - (a.nq - 1 - a.q0) >= kBlockTokens)
+          softmax_qm(std::false_type{});
+        else
+          softmax_qm(std::true_type{});
+        // rescale the accumulators (columns 2tq, 2tq + 1 of a row half: the factors of the rows
+        // that lanes 8tq and 8tq + 4 hold), skipped by the whole warp when no maximum moved
+        bool moved = false;
+#pragma unroll
+        for (int rh = 0; rh < RH; ++rh) moved |= al[rh] != 1.f;
+        if (__any_sync(kFullMask, moved)) {
+#pragma unroll
+          for (int rh = 0; rh < RH; ++rh) {
+            const float a0 = __shfl_sync(kFullMask, al[rh], 8 * tq);
+            const float a1 = __shfl_sync(kFullMask, al[rh], 8 * tq + 4);
+#pragma unroll
+            for (int md = 0; md < MD; ++md) {
+              oq[rh][md][0] *= a0;
+              oq[rh][md][1] *= a1;
+              oq[rh][md][2] *= a0;
+              oq[rh][md][3] *= a1;
+            }
+          }
+        }
+        // output: O^T[d x pairs] += V^T[d x tok] P^T[tok x pairs], the probabilities' bf16 high
+        // parts and remainders as two B operands taken straight from the score fragments
+        // (tokens 2tq, 2tq + 1 of column blocks 2kt and 2kt + 1)
+#pragma unroll
+        for (int kt = 0; kt < 4; ++kt) {
+          uint32_t bh[RH][2], bl[RH][2];
+#pragma unroll
+          for (int rh = 0; rh < RH; ++rh)
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+              const float x0 = sc[2 * kt + h2][2 * rh], x1 = sc[2 * kt + h2][2 * rh + 1];
+              const uint32_t hi = pack2_bf16(x0, x1);
+              bh[rh][h2] = hi;
+              bl[rh][h2] = pack2_bf16(x0 - __uint_as_float(hi << 16), x1 - __uint_as_float(hi & 0xffff0000u));
+            }
+          const int tok = 16 * kt + tr_tok;
+          const int jt = 16 * kt + 2 * tq;  // tokens of this thread's A-fragment halves
+#pragma unroll
+          for (int md = 0; md < MD; ++md) {
+            const int dc = 2 * md + tr_dc;
+            uint32_t af[4];
+            ldsm_x4_trans(vbase + (dc >> 3) * kSubTileBytes + tok * 128 + (((dc & 7) ^ (tok & 7)) << 4), af);
+            if (nv < kBlockTokens) {  // slots past the context may hold anything: zero them
+              af[0] = mask_pair(af[0], jt, nv);
+              af[1] = mask_pair(af[1], jt, nv);
+              af[2] = mask_pair(af[2], jt + 8, nv);
+              af[3] = mask_pair(af[3], jt + 8, nv);
+            }
+#pragma unroll
+            for (int rh = 0; rh < RH; ++rh) {
+              mma_16816(oq[rh][md], af, bh[rh][0], bh[rh][1]);
+              mma_16816(oq[rh][md], af, bl[rh][0], bl[rh][1]);
+            }
+          }
+        }
+      } else {
       // fp8 cache: the scale 2^e of the tokens this thread's score rows hold (16mt + gid and
       // 16mt + gid + 8); E, the largest exponent among the tile's valid tokens, no lower than
       // -112 (so that 2^(14 - E) and 2^(E - 14) are normal floats); and each token's factor
@@ -1364,6 +1584,7 @@ __global__ void __launch_bounds__(mma_kernel_threads(DV, R * NQ, NQ), 1) decode_
             for (int nt = 0; nt < NT; ++nt) mma_16816(o[nt][md], af, pb[nt][kt][0], pb[nt][kt][1]);
           }
         }
+      }
       }
       }
     }
