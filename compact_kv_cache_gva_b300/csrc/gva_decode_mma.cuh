@@ -19,10 +19,17 @@
 // Probabilities never leave registers: movmatrix turns the score fragment (tokens on rows)
 // into the B fragment of the output product (tokens on k).
 //
+// Multi-query passes of 16 (query, head) pairs take two other forms.  At d_v = 64 the queries
+// go on M instead: S[pairs x 64 tok] = [q'_hi ; q'_lo] . V^T, both bf16 parts as A operands into
+// one accumulator, whose fragment (pairs on rows) is the output product's B operand as it stands.
+// At d_v = 128 the query operand stays in shared memory (ldmatrix per k-step), and each tile's
+// pairs are split between two consumer warps that write their halves of one partial record.
+//
 // Work split (gva_sched.cuh): one CTA per SM streams a balanced range of (sequence, group,
 // tile) units with a few consumer warps, each with a private ring of tiles that a copy warp
 // keeps full (TMA) or, in the self-fed instances (multi-query passes and the fp8 cache at
-// d_v = 64), that the consumer refills itself.  The consumers take the range's tiles
+// d_v = 64), that the consumer refills itself; the 16-pair passes at d_v = 128 give each ring
+// two consumers.  The consumers take the range's tiles
 // round-robin, each writing one partial record per (sequence, group) it touched.  The matching
 // GQA form (a separate key cache, no positional slice) reuses the kernel with the key tile
 // scored instead of the value tile.
