@@ -37,6 +37,7 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const DecodeAr
   extern __shared__ __align__(16) float stage[];  // [kRch][R][rs] records of this round
   __shared__ __align__(8) uint64_t bar;
   __shared__ float wgt[S::kRch][R];               // 2^(m_j - M) of the round, 0 for unused
+  __shared__ unsigned char valid[S::kRch];        // has_data of the round's records
   __shared__ float Mrun[R], Lrun[R], scale_old[R];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = blockIdx.x, b = blockIdx.y;
@@ -128,6 +129,9 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const DecodeAr
       mbar_arrive_expect_tx(&bar, bytes);
       bulk_g2s(stage, base + static_cast<size_t>(j0) * R * rs, bytes, &bar);
     }
+    // which of the round's records hold data, once per record (three 64-bit divisions each),
+    // while the copy is in flight; the barrier below publishes them
+    if (tid < n) valid[tid] = has_data(j0 + tid) ? 1 : 0;
     const bool got = mbar_wait_bounded(&bar, phase);
     phase ^= 1;
     if (!__syncthreads_and(got)) {
@@ -138,7 +142,7 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const DecodeAr
     for (int hh = warp; hh < R; hh += kCombineWarps) {
       float mx = -INFINITY;
       for (int j = lane; j < n; j += 32) {
-        if (!has_data(j0 + j)) continue;
+        if (!valid[j]) continue;
         mx = fmaxf(mx, stage[(j * R + hh) * rs]);
       }
 #pragma unroll
@@ -147,7 +151,7 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const DecodeAr
       float ls = 0.f;
       for (int j = lane; j < n; j += 32) {
         const float mj = stage[(j * R + hh) * rs];
-        const bool use = mnew != -INFINITY && has_data(j0 + j) && mj != -INFINITY;
+        const bool use = mnew != -INFINITY && valid[j] && mj != -INFINITY;
         const float wj = use ? exp2f(mj - mnew) : 0.f;
         wgt[j][hh] = wj;
         ls = fmaf(wj, use ? stage[(j * R + hh) * rs + 1] : 0.f, ls);
