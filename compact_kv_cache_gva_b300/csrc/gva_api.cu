@@ -279,6 +279,7 @@ gva_status decode_common(gva_ctx* ctx, bool sep_k, int phases, int B, const floa
     if (combine) {
       // each combine CTA then reads all B lengths: only for batches of up to 256 sequences
       a.combine_after_partial = partial && a.seq_lens && B <= 256 ? 1 : 0;
+      a.combine_big = static_cast<long long>(B) * d.G <= ctx->num_sms ? 1 : 0;
       const cudaError_t e = gva::launch_combine(a, stream);
       if (e != cudaSuccess) return GVA_ERR_CUDA;
     }

@@ -22,11 +22,15 @@ namespace {
 constexpr int kCombineWarps = 8;
 constexpr int kCombineThreads = 32 * kCombineWarps;
 constexpr int kStageBytes = 32 * 1024;  // records staged per round (7 CTAs fit on an SM)
+// records staged per round when the grid has at most one CTA per SM (fewer rounds for segments
+// with many records: many consumer warps per range, or several queries per pass)
+constexpr int kBigStageBytes = 96 * 1024;
 
 template <int DV, int R>
 struct CombineShape {
   static constexpr int kRs = DV + 4;  // floats per head record
   static constexpr int kRch = kStageBytes / (R * kRs * 4) < 64 ? kStageBytes / (R * kRs * 4) : 64;
+  static constexpr int kRchBig = kBigStageBytes / (R * kRs * 4) < 64 ? kBigStageBytes / (R * kRs * 4) : 64;
   static constexpr int kOut = (R * DV + kCombineThreads - 1) / kCombineThreads;  // outputs per thread
 };
 
@@ -36,8 +40,9 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const DecodeAr
   constexpr int rs = S::kRs;
   extern __shared__ __align__(16) float stage[];  // [kRch][R][rs] records of this round
   __shared__ __align__(8) uint64_t bar;
-  __shared__ float wgt[S::kRch][R];               // 2^(m_j - M) of the round, 0 for unused
-  __shared__ unsigned char valid[S::kRch];        // has_data of the round's records
+  __shared__ float wgt[S::kRchBig][R];            // 2^(m_j - M) of the round, 0 for unused
+  __shared__ unsigned char valid[S::kRchBig];     // has_data of the round's records
+  const int rch = a.combine_big ? S::kRchBig : S::kRch;  // records per round
   __shared__ float Mrun[R], Lrun[R], scale_old[R];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = blockIdx.x, b = blockIdx.y;
@@ -121,8 +126,8 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const DecodeAr
   __syncthreads();
 
   uint32_t phase = 0;
-  for (int j0 = 0; j0 < nrec; j0 += S::kRch) {
-    const int n = min(S::kRch, nrec - j0);
+  for (int j0 = 0; j0 < nrec; j0 += rch) {
+    const int n = min(rch, nrec - j0);
     if (tid == 0) {
       fence_proxy_async_smem();  // earlier reads of the stage come before the copy's writes
       const uint32_t bytes = static_cast<uint32_t>(n) * R * rs * 4;
@@ -195,13 +200,14 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const DecodeAr
 template <int DV, int R>
 cudaError_t launch_t(const DecodeArgs& a, cudaLaunchConfig_t& cfg) {
   using S = CombineShape<DV, R>;
-  const int smem = S::kRch * R * S::kRs * 4;
+  const int smem = (a.combine_big ? S::kRchBig : S::kRch) * R * S::kRs * 4;
   static int configured[kMaxDevicesHost] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev >= kMaxDevicesHost || !configured[dev]) {
-    e = cudaFuncSetAttribute(combine_kernel<DV, R>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    e = cudaFuncSetAttribute(combine_kernel<DV, R>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             S::kRchBig * R * S::kRs * 4);
     if (e != cudaSuccess) return e;
     if (dev < kMaxDevicesHost) configured[dev] = 1;
   }

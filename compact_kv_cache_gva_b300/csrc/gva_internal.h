@@ -77,6 +77,9 @@ struct DecodeArgs {
   // reading the header after it (set for batches of up to 256 sequences: each combine CTA
   // reads all B lengths).
   int combine_after_partial;
+  // combine: one CTA per (group, sequence) fits on the SMs at once, so each may stage its
+  // records in the large rounds (kBigStageBytes) instead of the small ones
+  int combine_big;
 };
 
 // Floats of one fused-step query stage (a multiple of 4, so every stage is 16-byte aligned).
