@@ -24,13 +24,15 @@ constexpr int kCombineThreads = 32 * kCombineWarps;
 constexpr int kStageBytes = 32 * 1024;  // records staged per round (7 CTAs fit on an SM)
 // records staged per round when the grid has at most one CTA per SM (fewer rounds for segments
 // with many records: many consumer warps per range, or several queries per pass)
-constexpr int kBigStageBytes = 96 * 1024;
+constexpr int kBigStageBytes = 208 * 1024;
+constexpr int kMaxRch = kCombineThreads;  // records per round: one thread tests each for data
 
 template <int DV, int R>
 struct CombineShape {
   static constexpr int kRs = DV + 4;  // floats per head record
   static constexpr int kRch = kStageBytes / (R * kRs * 4) < 64 ? kStageBytes / (R * kRs * 4) : 64;
-  static constexpr int kRchBig = kBigStageBytes / (R * kRs * 4) < 64 ? kBigStageBytes / (R * kRs * 4) : 64;
+  static constexpr int kRchBig =
+      kBigStageBytes / (R * kRs * 4) < kMaxRch ? kBigStageBytes / (R * kRs * 4) : kMaxRch;
   static constexpr int kOut = (R * DV + kCombineThreads - 1) / kCombineThreads;  // outputs per thread
 };
 
